@@ -1,0 +1,419 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE expert-layer hot path on one or more GPUs (one process per GPU).
+
+Default workload: the decode-shaped W4A16 MXFP4 layer (T=64 tokens, hidden 2880,
+intermediate 2880, 128 experts, top-4, bf16 biases).  One step = bucket padding of the
+token dimension, routing + alignment, grouped GEMM1 + bias + SwiGLU, grouped GEMM2 + bias
+* routing weight, and the top-k combine, through the C ABI.
+
+Prints one JSON line.  value = tokens/s over all ranks with inputs resident in HBM;
+e2e = the same metric with the step's inputs copied from pinned host memory and the
+output copied back inside the timed region; roofline = the dominant kernel's algorithmic
+bytes / its CUDA-event time against the measured HBM copy bandwidth; cpu_baseline = the
+float64 oracle timed on a bounded sample on this host (one thread).
+
+``--impl reference`` times that oracle alone (the reference arm), on rank 0.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer useful TFLOP/s & tokens/s; % of GB300 block-scaled TC / HBM roofline"
+L2_BYTES = 129 * 1024 * 1024
+
+# DRAM traffic (read + write bytes) of one launch of the dominant kernel, from an ncu
+# capture of the same command (summary under profiles/), valid while the kernel source
+# hashes the same; otherwise reported as null.
+TRAFFIC = {}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_mxfp4",
+                    choices=["decode_mxfp4", "decode_bf16", "prefill_mxfp4", "tiny"])
+    ap.add_argument("--m", type=int, default=28, help="tokens for decode_bf16")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--sample-tokens", type=int, default=None, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+DEFAULT_STEPS = {"decode_mxfp4": (2000, 50), "decode_bf16": (4000, 100),
+                 "prefill_mxfp4": (10, 3), "tiny": (4000, 100)}
+ORACLE_SAMPLE = {"decode_mxfp4": 8, "decode_bf16": 28, "prefill_mxfp4": 4, "tiny": 64}
+
+
+def workload(name, m):
+    import synth
+    if name == "decode_mxfp4":
+        return synth.DECODE_MXFP4
+    if name == "decode_bf16":
+        return synth.decode_bf16_workload(m)
+    if name == "prefill_mxfp4":
+        return synth.prefill_workload()
+    return synth.TINY
+
+
+def describe(w, rows):
+    d = {"workload": f"{w.name}: T={w.T} tokens, hidden {w.K}, intermediate {w.I}, "
+                     f"{w.E} experts, top-{w.k}, {w.quant}{', bf16 biases' if w.bias else ''}",
+         "T": w.T, "T_rows": rows, "hidden": w.K, "intermediate": w.I, "experts": w.E,
+         "top_k": w.k, "quant": w.quant, "block_m": 128}
+    return d
+
+
+def useful_flops(w):
+    P = w.T * w.k
+    return 2.0 * P * w.K * 2 * w.I + 2.0 * P * w.I * w.K
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def src_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "mixture_experts_grouped_align_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------------------ oracle
+
+def oracle_sample(name, m, n_tok):
+    """Times the float64 oracle on the first n_tok tokens of the workload (this process
+    was started with one BLAS / OpenMP thread).  Returns seconds."""
+    import synth
+    from oracle import formats, layer, route
+    w = workload(name, m)
+    lay = synth.make_layer(w, T=w.T if name != "prefill_mxfp4" else 4096)
+    W = layer.ExpertWeights(w.quant, lay["w1"], lay["w1_scale"], lay["b1"], lay["w2"],
+                            lay["w2_scale"], lay["b2"])
+    n = min(n_tok, lay["x"].shape[0])
+    t0 = time.perf_counter()
+    x = formats.bf16_decode(lay["x"][:n])
+    ids, wt = route.route(lay["logits"][:n], w.k)
+    layer.moe_layer(x, ids, wt, W)
+    return time.perf_counter() - t0, n
+
+
+def run_oracle_subprocess(name, m, n_tok):
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[v] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", "--workload", name,
+           "--m", str(m), "--sample-tokens", str(n_tok)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    def __init__(self, path):
+        self.path = path
+        self.proc = None
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self, dev_index):
+        if not self.proc:
+            return {"samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9 or parts[0] != str(dev_index):
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for nm, v in zip(names[1:], parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        if not sm:
+            return {"samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ ours
+
+def bench_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_grouped_align_gb300 as moe
+    from mixture_experts_grouped_align_gb300.runner import DeviceLayer
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    moe.build()
+    moe.load()
+    w = workload(args.workload, args.m)
+    steps, warmup = DEFAULT_STEPS[args.workload]
+    steps = args.steps if args.steps is not None else steps
+    warmup = max(3, args.warmup if args.warmup is not None else warmup)
+    lay = synth.make_layer(w)
+
+    def d(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    L = DeviceLayer(w.quant, w.E, w.K, w.I, w.k, d(lay["w1"]), d(lay["w1_scale"]), d(lay["b1"]),
+                    d(lay["w2"]), d(lay["w2_scale"]), d(lay["b2"]), max_rows=w.T, device=dev)
+    T = w.T
+    x = d(lay["x"])
+    lg = d(lay["logits"])
+    y = torch.empty((T, w.K), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # one step to learn the routing (same every step) for the byte counts
+    rows = L.step(x, lg, T, y)
+    torch.cuda.synchronize()
+    if int(L.status[0]) != 0:
+        raise RuntimeError(f"device status {int(L.status[0])}")
+    eoff = L.expert_offsets[:w.E + 1].cpu().numpy()
+    touched = int(np.count_nonzero(np.diff(eoff)))
+    P_rows = rows * w.k
+
+    def wbytes(N, Kin):
+        if w.quant == "mxfp4":
+            return N * Kin // 2 + N * Kin // 32
+        return N * Kin * 2
+    bias_b = (2 * w.I * 2) if w.bias else 0
+    gemm1_bytes = touched * (wbytes(2 * w.I, w.K) + bias_b) + rows * w.K * 2 + P_rows * w.I * 2
+    gemm2_bytes = touched * (wbytes(w.K, w.I) + (w.K * 2 if w.bias else 0)) + P_rows * w.I * 2 + P_rows * w.K * 4
+    step_weight_bytes = touched * (wbytes(2 * w.I, w.K) + wbytes(w.K, w.I))
+
+    def step(evs=None):
+        return L.step(x, lg, T, y, events=evs)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    t_start.record(stream)
+    for i in range(steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ck = clocks.stop(local_rank)
+    ms = t_start.elapsed_time(t_end)
+    g1 = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
+    g2 = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
+    cb = sum(e[2].elapsed_time(e[3]) for e in evs) / steps
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end: pinned host inputs in, output back out, inside the timed region
+    xh = torch.empty_like(x, device="cpu").pin_memory()
+    xh.copy_(x.cpu())
+    lh = torch.empty_like(lg, device="cpu").pin_memory()
+    lh.copy_(lg.cpu())
+    yh = torch.empty_like(y, device="cpu").pin_memory()
+    xd = torch.empty_like(x)
+    ld = torch.empty_like(lg)
+    e2e_steps = max(1, min(steps, 500))
+    for _ in range(3):
+        xd.copy_(xh, non_blocking=True); ld.copy_(lh, non_blocking=True)
+        L.step(xd, ld, T, y); yh.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        xd.copy_(xh, non_blocking=True)
+        ld.copy_(lh, non_blocking=True)
+        L.step(xd, ld, T, y)
+        yh.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return None
+    hbm, bf16, src = peaks()
+    dominant = "gemm1" if g1 >= g2 else "gemm2"
+    dom_bytes, dom_ms = (gemm1_bytes, g1) if dominant == "gemm1" else (gemm2_bytes, g2)
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    key = f"decode_gemm_{dominant}@{w.name}"
+    tr = TRAFFIC.get(key)
+    traffic = tr["bytes"] if tr and tr.get("src") == src_hash("decode_gemm.cu") else None
+    ms_step = ms / steps
+    line = {
+        "metric": METRIC,
+        "value": world * T * steps / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 mma -> f32" if w.quant != "bf16" else "bf16 mma -> f32",
+        "data": "synthetic (seeded PCG64 inputs, random-init weights)",
+        "config": dict(describe(w, rows), l2=f"inputs larger than L2: {step_weight_bytes / 1e9:.2f} GB "
+                                              f"of expert weights streamed per step > 129 MB L2",
+                       parallelism=f"replicas x{world}"),
+        "useful_tflops": world * useful_flops(w) * steps / (ms * 1e-3) / 1e12,
+        "layer_latency_us": ms_step * 1e3,
+        "kernel_ms": {"gemm1_swiglu": g1, "gemm2_weighted": g2, "combine": cb,
+                      "route_align_pad_and_gaps": ms_step - g1 - g2 - cb},
+        "experts_touched": touched,
+        "roofline": {"bound": "hbm", "kernel": f"decode_gemm ({dominant})", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                     "algorithmic_bytes": dom_bytes, "peak_source": f"{src} (hbm_gbs)"},
+        "step_roofline": {"bytes": step_weight_bytes, "achieved_gbs": step_weight_bytes / (ms_step * 1e-3) / 1e9,
+                          "frac": step_weight_bytes / (ms_step * 1e-3) / 1e9 / hbm},
+        "e2e": {"value": world * T * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x.numel() * 2 + lg.numel() * 4,
+                "d2h_bytes_per_step": y.numel() * 2, "steps": e2e_steps},
+        "gpu_launches": steps * launches_per_step(w, rows),
+        "clocks": ck,
+    }
+    return line
+
+
+def launches_per_step(w, rows):
+    n = 3  # GEMM1, GEMM2, combine
+    n += 1  # align (routing fused for rows <= 512)
+    if rows > 512:
+        n += 1
+    if w.quant == "mxfp4":
+        n += 2  # pad x, pad logits
+    return n
+
+
+def cpu_baseline(args):
+    name = args.workload
+    n = args.sample_tokens or ORACLE_SAMPLE[name]
+    r = run_oracle_subprocess(name, args.m, n)
+    return {"value": r["tokens"] / r["seconds"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"float64 oracle on the first {r['tokens']} tokens of the workload "
+                      f"({r['seconds']:.1f} s, one thread)"}
+
+
+def main():
+    args = parse()
+    if args.oracle_sample:
+        s, n = oracle_sample(args.workload, args.m, args.sample_tokens or ORACLE_SAMPLE[args.workload])
+        print(json.dumps({"seconds": s, "tokens": n}))
+        return
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        bench_reference(args)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    line = bench_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            try:
+                line["cpu_baseline"] = cpu_baseline(args)
+            except Exception as e:  # reported, not fatal
+                line["cpu_baseline"] = {"error": str(e)[:300]}
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def bench_reference(args):
+    """The reference arm: the float64 CPU oracle as it stands, one bounded sample per step."""
+    w = workload(args.workload, args.m)
+    steps, warmup = args.steps or 3, max(3, args.warmup or 3)
+    n = 1 if args.workload != "tiny" else 8
+    for _ in range(min(warmup, 1)):
+        run_oracle_subprocess(args.workload, args.m, n)
+    secs, toks = 0.0, 0
+    t_wall = time.perf_counter()
+    for _ in range(steps):
+        r = run_oracle_subprocess(args.workload, args.m, n)
+        secs += r["seconds"]
+        toks += r["tokens"]
+    wall = time.perf_counter() - t_wall
+    v = toks / secs
+    line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+            "warmup": warmup, "ms_per_step": secs / steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": describe(w, w.T), "impl": "reference",
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{n} token(s) of the workload per step (float64 oracle, one "
+                                       f"thread; input generation untimed; wall {wall:.1f} s)"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,228 @@
+/*
+ * moe_gb300.h -- C ABI of the Mixture-of-Experts expert-layer hot path on GB300 (sm_103a).
+ *
+ * The path: top-k routing -> token-to-expert alignment (moe_align) -> geometric
+ * token-dimension bucketing and padding (moe_bucket_pad) -> grouped GEMM1 + bias + SwiGLU ->
+ * grouped GEMM2 + bias * routing weight -> top-k combine (moe_forward); a single grouped
+ * GEMM over given operands (moe_grouped_gemm); and the per-expert weight gradient
+ * (moe_wgrad).
+ *
+ * Sources of the definitions (pull-request pages):
+ *  [BUCKET] "Bound Triton MoE JIT specializations via token-dim bucketing and warmup",
+ *           TensorRT-LLM PR 15311 -- Description; Test Coverage.
+ *  [DECODE] "tune the Nemotron MTP decode row on S5000 with a checked-in recipe",
+ *           torchada PR 115 -- What it does (tiny-M bf16 fused-MoE decode shape).
+ *  [AITER]  "Add MoE GEMM variants and weight-gradient kernel", ROCm aiter PR 5310 --
+ *           Summary; Notes; second review (sentinel handling, E8M0 decoding, bias indexing).
+ *
+ * Conventions for every call
+ *  - All device buffers are owned by the caller.  The library never allocates device
+ *    memory; scratch comes from ctx->workspace (size from the *_workspace_size calls).
+ *  - Work is enqueued on ctx->stream (a cudaStream_t; NULL = the legacy default stream).
+ *    No call synchronises the host with the device.
+ *  - Every device pointer must be 16-byte aligned and every tensor dense row-major with
+ *    exactly the shape stated (a per-expert bias is a contiguous [E, N] array; strided
+ *    biases are not accepted -- the bias-stride defect named in [AITER]'s second review
+ *    is ruled out by contract).
+ *  - Integers that index pairs or weight elements are 64-bit inside the kernels: with
+ *    E = 256 an expert offset times the per-expert weight size exceeds INT32_MAX ([AITER],
+ *    Notes).
+ *  - The return value reports argument and launch errors only.  Errors that depend on
+ *    the data (an expert id outside [0, E), an activation outside the decode path's
+ *    float16 range) are written to the optional device word ctx->dev_status, first error
+ *    wins; the caller reads it after synchronising.  No kernel traps.
+ *  - moe_last_error() returns a thread-local description of the last failed call.
+ *  - The library keeps no state; calls are thread-safe.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t moe_status;
+#define MOE_OK 0
+#define MOE_WARN_PAD_IGNORED 1    /* moe_bucket_pad: padding not allowed for this mode   */
+#define MOE_ERR_INVALID_ARG (-1)  /* null pointer, bad size, misalignment               */
+#define MOE_ERR_UNSUPPORTED (-2)  /* a size or mode this build does not implement       */
+#define MOE_ERR_CAPACITY (-3)     /* an output or workspace buffer is too small         */
+#define MOE_ERR_CUDA (-4)         /* a CUDA launch or runtime error                     */
+/* device status codes (ctx->dev_status) */
+#define MOE_ERR_INVALID_EXPERT (-5) /* a top-k id outside [0, E)                        */
+#define MOE_ERR_RANGE (-6)          /* decode path: |activation| > 65504 (float16 max)   */
+#define MOE_ERR_TIMEOUT (-7)        /* a bounded wait inside a kernel ran out            */
+
+typedef enum {
+  MOE_Q_BF16 = 0,        /* bf16 weights, bf16 activations                              */
+  MOE_Q_MXFP4_W4A16 = 1, /* E2M1 weights, two per byte (even K index in the low nibble),
+                            one E8M0 scale per 32 along K; bf16 activations            */
+  MOE_Q_MXFP8 = 2        /* E4M3 weights and activations, one E8M0 scale per 32 along K */
+} moe_quant;
+
+typedef struct {
+  void* stream;            /* cudaStream_t                                                  */
+  void* workspace;         /* device scratch, caller-owned, 256-byte aligned                */
+  size_t workspace_bytes;  /* its size                                                      */
+  int32_t* dev_status;     /* optional device int32 (set to 0 by the caller); may be NULL   */
+  void** events;           /* optional host array of cudaEvent_t recorded on the stream
+                              around each kernel of a call (profiling); may be NULL.
+                              moe_forward: [0] before GEMM1, [1] after GEMM1, [2] after
+                              GEMM2, [3] after the combine (needs n_events >= 4);
+                              moe_grouped_gemm, moe_wgrad: [0] before, [1] after.      */
+  int32_t n_events;
+} moe_ctx;
+
+/* Thread-local text of the last error returned on this thread ("" if none). */
+const char* moe_last_error(void);
+
+/* ------------------------------------------------------------------------------------ *
+ * Alignment: routing + moe_align_block_size                                             *
+ * ------------------------------------------------------------------------------------ */
+
+/* Capacity of the alignment outputs for num_pairs = T*k pairs:
+ *   cap_tokens = round_up(num_pairs + E*(block_m-1), block_m), cap_blocks = cap_tokens/block_m
+ * -- the most slots any routing can need (each expert's count padded up to whole
+ * blocks). */
+moe_status moe_align_capacity(int64_t num_pairs, int32_t E, int32_t block_m,
+                              int64_t* cap_tokens, int64_t* cap_blocks);
+
+/* Routing and alignment (one call).
+ *
+ * Routing (when logits != NULL): logits [T, E] fp32 -> topk_ids [T, k] int32 (the k largest
+ * logits in descending order; equal logits rank the lower expert id first) and topk_w
+ * [T, k] fp32 = softmax over the k chosen logits, computed in float64 and rounded to
+ * float32.  When logits == NULL, topk_ids is an input and topk_w is not touched (may be
+ * NULL).
+ *
+ * Alignment ([AITER] Summary and second review; [DECODE] What it does): with pair index
+ * p = t*k + j, c_e pairs routed to expert e, P_e = c_e rounded up to block_m and
+ * O_e = sum_{e'<e} P_e':
+ *   sorted_token_ids[cap_tokens]: slots O_e .. O_e+c_e-1 hold expert e's pair indices in
+ *       ascending order; every other slot holds the sentinel T*k;
+ *   expert_ids[cap_tokens/block_m]: block b holds the expert owning slots
+ *       b*block_m .. (b+1)*block_m-1, and -1 for every block at or past
+ *       num_tokens_post_padded/block_m (kernels skip -1 blocks at once);
+ *   num_tokens_post_padded[1] = sum_e P_e;
+ *   expert_offsets[E+1] (may be NULL) = unpadded prefix sums of c_e (differences are the
+ *       per-expert group sizes).
+ * Limits: 1 <= k <= 32, k <= E <= 1024, 1 <= block_m <= 1024, 0 <= T, T*k < 2^31.
+ * cap_tokens must be >= moe_align_capacity() and a multiple of block_m
+ * (MOE_ERR_CAPACITY).  Out-of-range ids set MOE_ERR_INVALID_EXPERT in dev_status and are
+ * left out of the outputs.  Needs no workspace. */
+moe_status moe_align(const float* logits, int32_t* topk_ids, float* topk_w,
+                     int64_t T, int32_t k, int32_t E, int32_t block_m,
+                     int32_t* sorted_token_ids, int64_t cap_tokens,
+                     int32_t* expert_ids, int32_t* num_tokens_post_padded,
+                     int32_t* expert_offsets, const moe_ctx* ctx);
+
+/* ------------------------------------------------------------------------------------ *
+ * Token-dimension bucketing ([BUCKET] Description, Test Coverage)                        *
+ * ------------------------------------------------------------------------------------ */
+
+/* bucket(m) = ceil(m / s) * s with s = max(1, 2^(floor(log2 m) - 3)): eight buckets per
+ * power-of-two octave from 16 on, every m < 16 its own bucket, at most 12.5% padding.
+ * Returns -1 for m < 1. */
+int64_t moe_bucket(int64_t m);
+
+/* Number of buckets <= max_tokens (97 for 20000). */
+int64_t moe_bucket_count(int64_t max_tokens);
+
+/* T_pad = bucket(T) for MOE_Q_MXFP4_W4A16; for every other mode padding is not allowed
+ * (dynamic activation scales would let pad rows change real outputs), *T_pad = T and the
+ * call returns MOE_WARN_PAD_IGNORED.  T == 0 gives T_pad = 0.
+ * Device part (optional): when x_pad != NULL, rows [0, T) of x ([T, row_bytes]) are copied
+ * to x_pad ([T_pad, row_bytes]; x == x_pad skips the copy) and rows [T, T_pad) are zeroed;
+ * likewise logits [T, E] fp32 -> logits_pad [T_pad, E] when logits_pad != NULL (zero pad
+ * logits route pad rows to experts 0..k-1 with weight 1/k).  row_bytes must be a multiple
+ * of 16. */
+moe_status moe_bucket_pad(int64_t T, moe_quant quant, int64_t* T_pad,
+                          const void* x, void* x_pad, int64_t row_bytes,
+                          const float* logits, float* logits_pad, int32_t E,
+                          const moe_ctx* ctx);
+
+/* ------------------------------------------------------------------------------------ *
+ * Forward: grouped GEMM1 + SwiGLU -> grouped GEMM2 -> combine                           *
+ * ------------------------------------------------------------------------------------ */
+
+typedef struct {
+  moe_quant quant;
+  int32_t E, K, I;        /* experts, hidden size, intermediate size                      */
+  const void* w1;         /* [E, 2I, K] (MXFP4: [E, 2I, K/2] bytes); rows 0..I-1 gate,
+                             rows I..2I-1 up                                              */
+  const uint8_t* w1_scale;/* [E, 2I, K/32] E8M0 (NULL for bf16)                           */
+  const void* b1;         /* [E, 2I] bf16 or NULL                                         */
+  const void* w2;         /* [E, K, I] (MXFP4: [E, K, I/2] bytes)                         */
+  const uint8_t* w2_scale;/* [E, K, I/32] E8M0 (NULL for bf16)                            */
+  const void* b2;         /* [E, K] bf16 or NULL                                          */
+} moe_weights;
+
+/* Workspace bytes moe_forward needs for T_rows rows of top-k: h [T_rows*k, I] bf16 and
+ * o [T_rows*k, K] fp32, each 256-byte aligned. */
+size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t I);
+
+/* For every real token t < T_real (the others, e.g. bucket pad rows, are computed and
+ * then sliced off):
+ *   gu = x_t . W1[e]^T + b1[e];  h = silu(gu[:I]) * gu[I:]  (fp32, then bf16 RNE)
+ *   o_tj = w[t,j] * (h . W2[e]^T + b2[e])                    (fp32)
+ *   y_t  = sum_{j=0..k-1} o_tj, in order of j, rounded to bf16 RNE.
+ * x: [T_rows, K] bf16 (BF16 and MXFP4_W4A16 modes).  topk_w [T_rows, k]; the alignment
+ * arrays come from moe_align over T_rows rows with the same block_m and cap_tokens.
+ * y: [T_real, K] bf16.  K and I must be multiples of 32 (and of 16 output rows).
+ * MXFP8 needs a quantiser between the GEMMs and returns MOE_ERR_UNSUPPORTED here; its
+ * GEMMs are available through moe_grouped_gemm.  No pair-count-dependent split of K is
+ * made and every output row depends only on its own input row, so padded and unpadded
+ * calls give bit-identical real rows. */
+moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_scale,
+                       int64_t T_rows, int64_t T_real, int32_t k,
+                       const float* topk_w, const int32_t* sorted_token_ids,
+                       const int32_t* expert_ids, const int32_t* num_tokens_post_padded,
+                       const int32_t* expert_offsets, int32_t block_m, int64_t cap_tokens,
+                       void* y, const moe_ctx* ctx);
+
+/* ------------------------------------------------------------------------------------ *
+ * One grouped GEMM over all experts in a single launch ([AITER] Summary: moe_gemm_mxfp8) *
+ * ------------------------------------------------------------------------------------ */
+
+/* out[p, :] = A[src(p), :] . W[e_p]^T + bias[e_p]   for every pair p < T*k, in bf16 RNE.
+ * A: [T, Kin] (a_per_pair == 0, src = p / k) or [T*k, Kin] (a_per_pair != 0, src = p);
+ *    bf16 for MOE_Q_BF16 / MOE_Q_MXFP4_W4A16, E4M3 bytes + a_scale [rows, Kin/32] E8M0
+ *    for MOE_Q_MXFP8.
+ * W: [E, N, Kin] (MXFP4: [E, N, Kin/2] bytes) + w_scale [E, N, Kin/32]; bias [E, N] bf16
+ *    or NULL.  out: [T*k, N] bf16, indexed by pair.
+ * N must be a multiple of 16 and Kin of 32.  Needs no workspace. */
+moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin,
+                            const void* a, const uint8_t* a_scale, int32_t a_per_pair,
+                            const void* w, const uint8_t* w_scale, const void* bias,
+                            int64_t T, int32_t k,
+                            const int32_t* sorted_token_ids, const int32_t* expert_ids,
+                            const int32_t* num_tokens_post_padded, int32_t block_m,
+                            int64_t cap_tokens, void* out, const moe_ctx* ctx);
+
+/* ------------------------------------------------------------------------------------ *
+ * Weight gradient ([AITER] Summary: moe_wgrad; Tests & Benchmarks)                      *
+ * ------------------------------------------------------------------------------------ */
+
+/* dW[e] = sum over pairs p routed to e of grad[p, :]^T (outer) input[src(p), :], fp32
+ * accumulation, read straight from the alignment outputs (sentinel slots add nothing).
+ * grad: [T*k, N] bf16 indexed by pair; input: [T, Kin] bf16 (input_per_pair == 0,
+ * src = p / k) or [T*k, Kin] (input_per_pair != 0, src = p).  dW: [E, N, Kin] fp32.
+ * mode 0: deterministic -- every dW[e] is written, zeros for experts with no pair, and
+ *         repeated calls give identical bits.
+ * mode 1: accumulate -- the library zeroes dW, then adds token-chunk partial sums with
+ *         atomics (summation order varies between runs).
+ * N and Kin must be multiples of 64.  Needs no workspace. */
+moe_status moe_wgrad(const void* grad, const void* input, int32_t input_per_pair,
+                     int64_t T, int32_t k, int32_t E, int32_t N, int32_t Kin,
+                     const int32_t* sorted_token_ids, const int32_t* expert_ids,
+                     const int32_t* num_tokens_post_padded, int32_t block_m,
+                     int64_t cap_tokens, float* dW, int32_t mode, const moe_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

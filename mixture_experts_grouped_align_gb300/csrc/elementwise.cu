@@ -1,0 +1,102 @@
+// Memory-bound helpers of the path: bucket padding (copy + zero tail), zero fill and the
+// top-k combine.  All are grid-stride loops over 16-byte vectors with grids sized as a
+// multiple of the SM count.
+//
+// Pad and slice: "Bound Triton MoE JIT specializations via token-dim bucketing and
+// warmup" (TensorRT-LLM PR 15311), Description -- zero rows are appended up to the
+// bucket before the grouped GEMMs and removed again before the reduction; the combine
+// below only produces the real rows.
+#include "moe_common.cuh"
+#include "moe_launch.h"
+
+namespace {
+
+int grid_for(int64_t work, int threads) {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  int64_t need = (work + threads - 1) / threads;
+  int64_t cap = (int64_t)sms * 8;
+  return (int)(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+template <typename V>
+__global__ void pad_rows_kernel(const V* __restrict__ src, V* __restrict__ dst, int64_t n_copy,
+                                int64_t n_total) {
+  const V zero{};
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    if (i < n_copy) {
+      if (src) dst[i] = src[i];
+    } else {
+      dst[i] = zero;
+    }
+  }
+}
+
+__global__ void zero_kernel(float4* __restrict__ p, int64_t n4) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// y[t, n] = sum_{j < k} o[t*k + j, n] (j in order), rounded to bf16; 4 columns per thread.
+__global__ void combine_kernel(const float4* __restrict__ o, int64_t T_real, int k, int K4,
+                               uint2* __restrict__ y) {
+  const int64_t n = T_real * K4;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / K4;
+    const int c = (int)(i - t * K4);
+    const float4* src = o + (t * k) * K4 + c;
+    float4 acc = __ldg(src);
+    for (int j = 1; j < k; ++j) {
+      float4 v = __ldg(src + (int64_t)j * K4);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    uint2 out;
+    out.x = (uint32_t)moe::f32_to_bf16_bits(acc.x) | ((uint32_t)moe::f32_to_bf16_bits(acc.y) << 16);
+    out.y = (uint32_t)moe::f32_to_bf16_bits(acc.z) | ((uint32_t)moe::f32_to_bf16_bits(acc.w) << 16);
+    y[i] = out;
+  }
+}
+
+}  // namespace
+
+namespace moe_launch {
+
+cudaError_t pad_rows(const void* src, void* dst, int64_t rows, int64_t rows_pad, int64_t row_bytes,
+                     cudaStream_t stream) {
+  const void* s = (src == dst) ? nullptr : src;
+  if (row_bytes % 16 == 0) {
+    int64_t per = row_bytes / 16;
+    int64_t nt = rows_pad * per;
+    pad_rows_kernel<uint4><<<grid_for(nt, 256), 256, 0, stream>>>(
+        (const uint4*)s, (uint4*)dst, rows * per, nt);
+  } else {
+    int64_t per = row_bytes / 4;
+    int64_t nt = rows_pad * per;
+    pad_rows_kernel<uint32_t><<<grid_for(nt, 256), 256, 0, stream>>>(
+        (const uint32_t*)s, (uint32_t*)dst, rows * per, nt);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t zero_f32(float* p, int64_t n, cudaStream_t stream) {
+  zero_kernel<<<grid_for(n / 4, 256), 256, 0, stream>>>((float4*)p, n / 4);
+  return cudaGetLastError();
+}
+
+cudaError_t combine(const float* o, int64_t T_real, int k, int K, void* y, cudaStream_t stream) {
+  const int K4 = K / 4;
+  const int64_t n = T_real * K4;
+  if (n == 0) return cudaSuccess;
+  combine_kernel<<<grid_for(n, 256), 256, 0, stream>>>((const float4*)o, T_real, k, K4, (uint2*)y);
+  return cudaGetLastError();
+}
+
+}  // namespace moe_launch

@@ -1,0 +1,319 @@
+// The C ABI (include/moe_gb300.h): argument validation, workspace carving and launches.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "moe_common.cuh"
+#include "moe_launch.h"
+
+namespace moe_host {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+}  // namespace moe_host
+
+namespace {
+
+using moe_host::set_error;
+
+#define MOE_REQUIRE(cond, code, ...) \
+  do {                               \
+    if (!(cond)) {                   \
+      set_error(__VA_ARGS__);        \
+      return code;                   \
+    }                                \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status cuda_status(cudaError_t err, const char* what) {
+  if (err == cudaSuccess) return MOE_OK;
+  set_error("%s: %s", what, cudaGetErrorString(err));
+  return MOE_ERR_CUDA;
+}
+
+cudaStream_t stream_of(const moe_ctx* ctx) {
+  return ctx ? static_cast<cudaStream_t>(ctx->stream) : nullptr;
+}
+int32_t* status_of(const moe_ctx* ctx) { return ctx ? ctx->dev_status : nullptr; }
+
+// Records profiling event i of the caller (if it gave at least `need` events).
+void rec(const moe_ctx* ctx, int i, int need) {
+  if (ctx && ctx->events && ctx->n_events >= need && ctx->events[i])
+    cudaEventRecord(static_cast<cudaEvent_t>(ctx->events[i]), stream_of(ctx));
+}
+
+size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
+
+int64_t bucket_of(int64_t m) {
+  if (m < 1) return -1;
+  int lg = 63 - __builtin_clzll((unsigned long long)m);
+  int sh = lg - 3 > 0 ? lg - 3 : 0;
+  int64_t s = (int64_t)1 << sh;
+  return (m + s - 1) / s * s;
+}
+
+moe_status check_align_outputs(int64_t P, int32_t E, int32_t block_m, const int32_t* sorted,
+                               const int32_t* expert_ids, const int32_t* ntpp, int64_t cap_tokens) {
+  MOE_REQUIRE(sorted && expert_ids && ntpp, MOE_ERR_INVALID_ARG, "null alignment pointer");
+  MOE_REQUIRE(aligned16(sorted) && aligned16(expert_ids) && aligned16(ntpp), MOE_ERR_INVALID_ARG,
+              "alignment pointers must be 16-byte aligned");
+  MOE_REQUIRE(block_m >= 1 && block_m <= 1024, MOE_ERR_INVALID_ARG, "block_m must be in [1, 1024]");
+  int64_t need = P + (int64_t)E * (block_m - 1);
+  need = (need + block_m - 1) / block_m * block_m;
+  MOE_REQUIRE(cap_tokens >= need && cap_tokens % block_m == 0, MOE_ERR_CAPACITY,
+              "cap_tokens %lld < required %lld or not a multiple of block_m", (long long)cap_tokens,
+              (long long)need);
+  return MOE_OK;
+}
+
+// Block slots a grouped launch must cover: at most ceil(P / bm) + min(E, P) are used.
+int64_t used_blocks_bound(int64_t P, int32_t E, int32_t bm, int64_t cap_tokens) {
+  int64_t b = (P + bm - 1) / bm + (E < P ? E : P);
+  int64_t cap_blocks = cap_tokens / bm;
+  return b < cap_blocks ? b : cap_blocks;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return moe_host::g_err; }
+
+moe_status moe_align_capacity(int64_t num_pairs, int32_t E, int32_t block_m, int64_t* cap_tokens,
+                              int64_t* cap_blocks) {
+  MOE_REQUIRE(cap_tokens && cap_blocks, MOE_ERR_INVALID_ARG, "null output pointer");
+  MOE_REQUIRE(num_pairs >= 0 && E >= 1 && block_m >= 1, MOE_ERR_INVALID_ARG,
+              "need num_pairs >= 0, E >= 1, block_m >= 1");
+  int64_t c = num_pairs + (int64_t)E * (block_m - 1);
+  c = (c + block_m - 1) / block_m * block_m;
+  *cap_tokens = c;
+  *cap_blocks = c / block_m;
+  return MOE_OK;
+}
+
+moe_status moe_align(const float* logits, int32_t* topk_ids, float* topk_w, int64_t T, int32_t k,
+                     int32_t E, int32_t block_m, int32_t* sorted_token_ids, int64_t cap_tokens,
+                     int32_t* expert_ids, int32_t* num_tokens_post_padded, int32_t* expert_offsets,
+                     const moe_ctx* ctx) {
+  MOE_REQUIRE(T >= 0, MOE_ERR_INVALID_ARG, "T must be >= 0");
+  MOE_REQUIRE(k >= 1 && k <= 32 && E >= k && E <= 1024, MOE_ERR_UNSUPPORTED,
+              "need 1 <= k <= 32 and k <= E <= 1024 (k=%d, E=%d)", k, E);
+  MOE_REQUIRE(T * k < ((int64_t)1 << 31), MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
+  MOE_REQUIRE(topk_ids && aligned16(topk_ids), MOE_ERR_INVALID_ARG,
+              "topk_ids must be a 16-byte aligned device pointer");
+  if (logits) {
+    MOE_REQUIRE(topk_w && aligned16(topk_w) && aligned16(logits), MOE_ERR_INVALID_ARG,
+                "routing needs 16-byte aligned logits and topk_w");
+  }
+  MOE_REQUIRE(!expert_offsets || aligned16(expert_offsets), MOE_ERR_INVALID_ARG,
+              "expert_offsets must be 16-byte aligned");
+  moe_status st = check_align_outputs(T * k, E, block_m, sorted_token_ids, expert_ids,
+                                      num_tokens_post_padded, cap_tokens);
+  if (st != MOE_OK) return st;
+  return cuda_status(moe_launch::align(logits, topk_ids, topk_w, T, k, E, block_m, sorted_token_ids,
+                                       cap_tokens, expert_ids, num_tokens_post_padded,
+                                       expert_offsets, status_of(ctx), stream_of(ctx)),
+                     "moe_align");
+}
+
+int64_t moe_bucket(int64_t m) { return bucket_of(m); }
+
+int64_t moe_bucket_count(int64_t max_tokens) {
+  // 1..15 are their own buckets; from 16 on every octave [2^j, 2^(j+1)) holds 8 buckets.
+  int64_t n = 0;
+  for (int64_t b = 1; b <= max_tokens;) {
+    ++n;
+    int64_t nb = bucket_of(b + 1);
+    b = nb;
+  }
+  return n;
+}
+
+moe_status moe_bucket_pad(int64_t T, moe_quant quant, int64_t* T_pad, const void* x, void* x_pad,
+                          int64_t row_bytes, const float* logits, float* logits_pad, int32_t E,
+                          const moe_ctx* ctx) {
+  MOE_REQUIRE(T_pad, MOE_ERR_INVALID_ARG, "T_pad is null");
+  MOE_REQUIRE(T >= 0, MOE_ERR_INVALID_ARG, "T must be >= 0");
+  const bool allowed = (quant == MOE_Q_MXFP4_W4A16);
+  const int64_t tp = (allowed && T > 0) ? bucket_of(T) : T;
+  *T_pad = tp;
+  cudaStream_t s = stream_of(ctx);
+  if (x_pad) {
+    MOE_REQUIRE(x && row_bytes > 0 && row_bytes % 16 == 0 && aligned16(x) && aligned16(x_pad),
+                MOE_ERR_INVALID_ARG, "x / x_pad must be 16-byte aligned with row_bytes % 16 == 0");
+    moe_status st = cuda_status(moe_launch::pad_rows(x, x_pad, T, tp, row_bytes, s), "pad x");
+    if (st != MOE_OK) return st;
+  }
+  if (logits_pad) {
+    MOE_REQUIRE(logits && E >= 1 && aligned16(logits) && aligned16(logits_pad),
+                MOE_ERR_INVALID_ARG, "logits / logits_pad must be 16-byte aligned, E >= 1");
+    moe_status st =
+        cuda_status(moe_launch::pad_rows(logits, logits_pad, T, tp, (int64_t)E * 4, s), "pad logits");
+    if (st != MOE_OK) return st;
+  }
+  if (!allowed) {
+    set_error("token-dimension padding is only allowed for MOE_Q_MXFP4_W4A16");
+    return MOE_WARN_PAD_IGNORED;
+  }
+  return MOE_OK;
+}
+
+size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t I) {
+  if (T_rows < 0 || k < 1 || K < 1 || I < 1) return 0;
+  const int64_t P = T_rows * k;
+  return round256((size_t)P * I * 2) + round256((size_t)P * K * 4);
+}
+
+moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_scale, int64_t T_rows,
+                       int64_t T_real, int32_t k, const float* topk_w,
+                       const int32_t* sorted_token_ids, const int32_t* expert_ids,
+                       const int32_t* num_tokens_post_padded, const int32_t* expert_offsets,
+                       int32_t block_m, int64_t cap_tokens, void* y, const moe_ctx* ctx) {
+  (void)expert_offsets;
+  (void)x_scale;
+  MOE_REQUIRE(W && ctx, MOE_ERR_INVALID_ARG, "null weights or context");
+  MOE_REQUIRE(W->quant == MOE_Q_BF16 || W->quant == MOE_Q_MXFP4_W4A16, MOE_ERR_UNSUPPORTED,
+              "moe_forward supports MOE_Q_BF16 and MOE_Q_MXFP4_W4A16 (MXFP8: moe_grouped_gemm)");
+  const int32_t E = W->E, K = W->K, I = W->I;
+  MOE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= E, MOE_ERR_INVALID_ARG, "bad E or k");
+  MOE_REQUIRE(K >= 32 && I >= 32 && K % 32 == 0 && I % 32 == 0, MOE_ERR_UNSUPPORTED,
+              "K and I must be positive multiples of 32");
+  MOE_REQUIRE(T_rows >= 0 && T_real >= 0 && T_real <= T_rows, MOE_ERR_INVALID_ARG,
+              "need 0 <= T_real <= T_rows");
+  MOE_REQUIRE(T_rows * k < ((int64_t)1 << 31), MOE_ERR_UNSUPPORTED, "T_rows*k must be < 2^31");
+  const bool fp4 = (W->quant == MOE_Q_MXFP4_W4A16);
+  MOE_REQUIRE(W->w1 && W->w2 && x && topk_w && y, MOE_ERR_INVALID_ARG, "null tensor pointer");
+  MOE_REQUIRE(!fp4 || (W->w1_scale && W->w2_scale), MOE_ERR_INVALID_ARG, "MXFP4 needs scales");
+  MOE_REQUIRE(aligned16(W->w1) && aligned16(W->w2) && aligned16(x) && aligned16(topk_w) &&
+                  aligned16(y) && aligned16(W->b1) && aligned16(W->b2) &&
+                  aligned16(W->w1_scale) && aligned16(W->w2_scale),
+              MOE_ERR_INVALID_ARG, "all pointers must be 16-byte aligned");
+  const int64_t P = T_rows * k;
+  moe_status st = check_align_outputs(P, E, block_m, sorted_token_ids, expert_ids,
+                                      num_tokens_post_padded, cap_tokens);
+  if (st != MOE_OK) return st;
+  const size_t need = moe_forward_workspace_size(T_rows, k, K, I);
+  MOE_REQUIRE(ctx->workspace && ctx->workspace_bytes >= need && aligned16(ctx->workspace),
+              MOE_ERR_CAPACITY, "workspace of %zu bytes needed", need);
+  if (T_rows == 0) return MOE_OK;
+
+  uint8_t* ws = static_cast<uint8_t*>(ctx->workspace);
+  void* h = ws;
+  float* o = reinterpret_cast<float*>(ws + round256((size_t)P * I * 2));
+  cudaStream_t s = stream_of(ctx);
+  const int wf = fp4 ? moe_launch::WF_MXFP4 : moe_launch::WF_BF16;
+  const int64_t blocks = used_blocks_bound(P, E, block_m, cap_tokens);
+
+  moe_launch::GroupedGemm g1{};
+  g1.wfmt = wf;
+  g1.epi = moe_launch::EPI_SWIGLU;
+  g1.w = W->w1; g1.w_scale = W->w1_scale; g1.bias = W->b1;
+  g1.act = x; g1.act_scale = nullptr; g1.act_per_pair = 0;
+  g1.Nw = 2 * (int64_t)I; g1.Kin = K; g1.Nout = I; g1.k = k; g1.P = P; g1.E = E;
+  g1.sorted = sorted_token_ids; g1.expert_ids = expert_ids; g1.ntpp = num_tokens_post_padded;
+  g1.bm = block_m; g1.grid_blocks = blocks; g1.topk_w = topk_w; g1.out = h;
+  g1.status = status_of(ctx);
+  MOE_REQUIRE(moe_launch::decode_gemm_smem_bytes(g1) <= 227 * 1024, MOE_ERR_UNSUPPORTED,
+              "K too large for the decode path");
+  rec(ctx, 0, 4);
+  st = cuda_status(moe_launch::decode_gemm(g1, s), "moe_forward GEMM1");
+  if (st != MOE_OK) return st;
+  rec(ctx, 1, 4);
+
+  moe_launch::GroupedGemm g2 = g1;
+  g2.epi = moe_launch::EPI_WEIGHTED_F32;
+  g2.w = W->w2; g2.w_scale = W->w2_scale; g2.bias = W->b2;
+  g2.act = h; g2.act_per_pair = 1;
+  g2.Nw = K; g2.Kin = I; g2.Nout = K; g2.out = o;
+  st = cuda_status(moe_launch::decode_gemm(g2, s), "moe_forward GEMM2");
+  if (st != MOE_OK) return st;
+  rec(ctx, 2, 4);
+  st = cuda_status(moe_launch::combine(o, T_real, k, K, y, s), "moe_forward combine");
+  rec(ctx, 3, 4);
+  return st;
+}
+
+moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin, const void* a,
+                            const uint8_t* a_scale, int32_t a_per_pair, const void* w,
+                            const uint8_t* w_scale, const void* bias, int64_t T, int32_t k,
+                            const int32_t* sorted_token_ids, const int32_t* expert_ids,
+                            const int32_t* num_tokens_post_padded, int32_t block_m,
+                            int64_t cap_tokens, void* out, const moe_ctx* ctx) {
+  MOE_REQUIRE(quant == MOE_Q_BF16 || quant == MOE_Q_MXFP4_W4A16 || quant == MOE_Q_MXFP8,
+              MOE_ERR_INVALID_ARG, "unknown quant mode");
+  MOE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= E && T >= 0, MOE_ERR_INVALID_ARG,
+              "bad E, k or T");
+  MOE_REQUIRE(N >= 16 && N % 16 == 0 && Kin >= 32 && Kin % 32 == 0, MOE_ERR_UNSUPPORTED,
+              "N must be a multiple of 16 and Kin of 32");
+  MOE_REQUIRE(T * k < ((int64_t)1 << 31), MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
+  const bool mx8 = quant == MOE_Q_MXFP8, fp4 = quant == MOE_Q_MXFP4_W4A16;
+  MOE_REQUIRE(a && w && out, MOE_ERR_INVALID_ARG, "null tensor pointer");
+  MOE_REQUIRE(!(mx8 || fp4) || w_scale, MOE_ERR_INVALID_ARG, "MX weights need w_scale");
+  MOE_REQUIRE(!mx8 || a_scale, MOE_ERR_INVALID_ARG, "MXFP8 activations need a_scale");
+  MOE_REQUIRE(aligned16(a) && aligned16(w) && aligned16(out) && aligned16(bias) &&
+                  aligned16(a_scale) && aligned16(w_scale),
+              MOE_ERR_INVALID_ARG, "all pointers must be 16-byte aligned");
+  const int64_t P = T * k;
+  moe_status st = check_align_outputs(P, E, block_m, sorted_token_ids, expert_ids,
+                                      num_tokens_post_padded, cap_tokens);
+  if (st != MOE_OK) return st;
+  if (P == 0) return MOE_OK;
+  moe_launch::GroupedGemm g{};
+  g.wfmt = mx8 ? moe_launch::WF_MXFP8 : (fp4 ? moe_launch::WF_MXFP4 : moe_launch::WF_BF16);
+  g.epi = moe_launch::EPI_PLAIN_BF16;
+  g.w = w; g.w_scale = w_scale; g.bias = bias;
+  g.act = a; g.act_scale = a_scale; g.act_per_pair = a_per_pair ? 1 : 0;
+  g.Nw = N; g.Kin = Kin; g.Nout = N; g.k = k; g.P = P; g.E = E;
+  g.sorted = sorted_token_ids; g.expert_ids = expert_ids; g.ntpp = num_tokens_post_padded;
+  g.bm = block_m; g.grid_blocks = used_blocks_bound(P, E, block_m, cap_tokens);
+  g.topk_w = nullptr; g.out = out; g.status = status_of(ctx);
+  MOE_REQUIRE(moe_launch::decode_gemm_smem_bytes(g) <= 227 * 1024, MOE_ERR_UNSUPPORTED,
+              "Kin too large for the decode path");
+  rec(ctx, 0, 2);
+  st = cuda_status(moe_launch::decode_gemm(g, stream_of(ctx)), "moe_grouped_gemm");
+  rec(ctx, 1, 2);
+  return st;
+}
+
+moe_status moe_wgrad(const void* grad, const void* input, int32_t input_per_pair, int64_t T,
+                     int32_t k, int32_t E, int32_t N, int32_t Kin, const int32_t* sorted_token_ids,
+                     const int32_t* expert_ids, const int32_t* num_tokens_post_padded,
+                     int32_t block_m, int64_t cap_tokens, float* dW, int32_t mode,
+                     const moe_ctx* ctx) {
+  MOE_REQUIRE(mode == 0 || mode == 1, MOE_ERR_INVALID_ARG, "mode must be 0 or 1");
+  MOE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= E && T >= 0, MOE_ERR_INVALID_ARG,
+              "bad E, k or T");
+  MOE_REQUIRE(N >= 64 && N % 64 == 0 && Kin >= 64 && Kin % 64 == 0, MOE_ERR_UNSUPPORTED,
+              "N and Kin must be multiples of 64");
+  MOE_REQUIRE(N / 64 <= 65535 && Kin / 64 <= 65535, MOE_ERR_UNSUPPORTED, "N or Kin too large");
+  MOE_REQUIRE(T * k < ((int64_t)1 << 31), MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
+  MOE_REQUIRE(grad && input && dW, MOE_ERR_INVALID_ARG, "null tensor pointer");
+  MOE_REQUIRE(aligned16(grad) && aligned16(input) && aligned16(dW), MOE_ERR_INVALID_ARG,
+              "all pointers must be 16-byte aligned");
+  const int64_t P = T * k;
+  moe_status st = check_align_outputs(P, E, block_m, sorted_token_ids, expert_ids,
+                                      num_tokens_post_padded, cap_tokens);
+  if (st != MOE_OK) return st;
+  const int64_t cap_blocks = cap_tokens / block_m;
+  MOE_REQUIRE(mode == 0 || cap_blocks <= 65535, MOE_ERR_UNSUPPORTED,
+              "accumulate mode supports at most 65535 block slots");
+  moe_launch::Wgrad g{};
+  g.grad = grad; g.input = input; g.input_per_pair = input_per_pair ? 1 : 0;
+  g.P = P; g.k = k; g.E = E; g.N = N; g.Kin = Kin;
+  g.sorted = sorted_token_ids; g.expert_ids = expert_ids; g.ntpp = num_tokens_post_padded;
+  g.bm = block_m; g.cap_blocks = cap_blocks; g.dW = dW; g.mode = mode;
+  rec(ctx, 0, 2);
+  st = cuda_status(moe_launch::wgrad(g, stream_of(ctx)), "moe_wgrad");
+  rec(ctx, 1, 2);
+  return st;
+}
+
+}  // extern "C"

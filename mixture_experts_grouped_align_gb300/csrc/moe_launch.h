@@ -1,0 +1,69 @@
+// Internal launchers of the MoE kernels (host side; not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe_launch {
+
+// ---- route + align (route_align.cu)
+size_t align_smem_bytes(int E);
+cudaError_t align(const float* logits, int32_t* ids, float* w, int64_t T, int k, int E, int bm,
+                  int32_t* sorted, int64_t cap, int32_t* expert_ids, int32_t* ntpp,
+                  int32_t* expert_offsets, int32_t* status, cudaStream_t stream);
+
+// ---- pad rows (elementwise.cu)
+cudaError_t pad_rows(const void* src, void* dst, int64_t rows, int64_t rows_pad, int64_t row_bytes,
+                     cudaStream_t stream);
+cudaError_t zero_f32(float* p, int64_t n, cudaStream_t stream);
+cudaError_t combine(const float* o, int64_t T_real, int k, int K, void* y, cudaStream_t stream);
+
+// ---- grouped GEMMs on the weight-streaming (decode) path (decode_gemm.cu)
+enum WFmt { WF_BF16 = 0, WF_MXFP4 = 1, WF_MXFP8 = 2 };
+enum Epi { EPI_SWIGLU = 0, EPI_WEIGHTED_F32 = 1, EPI_PLAIN_BF16 = 2 };
+
+struct GroupedGemm {
+  int wfmt;                 // WFmt
+  int epi;                  // Epi
+  const void* w;            // [E, Nw, Kin] in wfmt
+  const uint8_t* w_scale;   // [E, Nw, Kin/32] E8M0 (mx formats)
+  const void* bias;         // [E, Nw] bf16 or null
+  const void* act;          // rows [*, Kin]: bf16 (wfmt bf16/mxfp4) or E4M3 (mxfp8)
+  const uint8_t* act_scale; // [*, Kin/32] (mxfp8)
+  int act_per_pair;         // act row = p (1) or p / k (0)
+  int64_t Nw;               // weight rows per expert (SwiGLU: 2 * Nout)
+  int Kin;                  // reduction length
+  int Nout;                 // output columns
+  int k;                    // top-k
+  int64_t P;                // number of pairs = sentinel value
+  int E;                    // experts (guards the expert ids read from the alignment)
+  const int32_t* sorted;
+  const int32_t* expert_ids;
+  const int32_t* ntpp;
+  int bm;
+  int64_t grid_blocks;      // block slots to launch for
+  const float* topk_w;      // [P] (EPI_WEIGHTED_F32)
+  void* out;                // [P, Nout]: bf16 (SWIGLU, PLAIN) or f32 (WEIGHTED)
+  int32_t* status;
+};
+size_t decode_gemm_smem_bytes(const GroupedGemm& g);
+cudaError_t decode_gemm(const GroupedGemm& g, cudaStream_t stream);
+
+// ---- weight gradient (wgrad.cu)
+struct Wgrad {
+  const void* grad;   // [P, N] bf16
+  const void* input;  // [T or P, Kin] bf16
+  int input_per_pair;
+  int64_t P;
+  int k, E, N, Kin;
+  const int32_t* sorted;
+  const int32_t* expert_ids;
+  const int32_t* ntpp;
+  int bm;
+  int64_t cap_blocks;
+  float* dW;
+  int mode;
+};
+cudaError_t wgrad(const Wgrad& g, cudaStream_t stream);
+
+}  // namespace moe_launch

@@ -1,0 +1,280 @@
+// Top-k routing and token-to-expert alignment (moe_align_block_size) kernels.
+//
+// Definitions: "Add MoE GEMM variants and weight-gradient kernel" (aiter PR 5310),
+// Summary and second review (sorted_token_ids / expert_ids with -1 sentinel blocks);
+// "tune the Nemotron MTP decode row on S5000 with a checked-in recipe" (torchada PR 115),
+// What it does (moe_align_block_size as the native op feeding the fused-MoE kernel).
+//
+// Design: alignment runs in ONE thread block of 32 warps.  Each warp owns a contiguous
+// range of pairs; pass 1 builds a private per-warp histogram in shared memory (no
+// atomics: __match_any_sync groups lanes of equal expert and the group leader adds the
+// group size), pass 2 scans the padded counts over experts and the per-warp counts over
+// warps, pass 3 re-walks each range in order and scatters.  Because warps own ordered
+// ranges and lanes are ranked inside each 32-pair step, the scatter is stable (ascending
+// pair index within an expert) without any order-dependent atomics.  For small T the
+// routing runs in the same block (one launch for the whole decode-size step); larger T
+// routes with a grid of warps first.
+#include "moe_common.cuh"
+#include "moe_launch.h"
+
+#include <limits.h>
+#include <math.h>
+
+namespace {
+
+constexpr int kAlignThreads = 1024;
+constexpr int kAlignWarps = kAlignThreads / 32;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct AlignArgs {
+  const float* logits;
+  int32_t* ids;
+  float* w;
+  int64_t T;
+  int k, E, bm;
+  int32_t* sorted;
+  int64_t cap;
+  int32_t* expert_ids;
+  int32_t* ntpp;
+  int32_t* expert_offsets;
+  int32_t* status;
+  int route_here;
+};
+
+// (value, index) order of the top-k: larger value first, lower index on equal values.
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return bi == INT_MAX || v > bv || (v == bv && i < bi);
+}
+
+// One warp routes one token: k rounds of a warp arg-max over the unchosen logits, then
+// float64 softmax over the chosen ones.  The float64 sum follows numpy's order for a
+// short vector (a running sum below 8 terms, eight interleaved partial sums from 8 on)
+// so that both sides round the same float64 value to float32.
+__device__ void route_token(const float* __restrict__ row, int E, int k,
+                            int32_t* __restrict__ ids_out, float* __restrict__ w_out,
+                            int lane) {
+  uint32_t taken = 0;  // bit i <=> entry lane + 32*i already chosen (E <= 1024)
+  float my_val = 0.f;
+  int my_idx = 0;
+  const int nper = (E + 31) >> 5;
+  for (int j = 0; j < k; ++j) {
+    float best = -INFINITY;
+    int bidx = INT_MAX;
+    for (int i = 0; i < nper; ++i) {
+      int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u)) {
+        float v = row[e];
+        if (better(v, e, best, bidx)) { best = v; bidx = e; }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      float ov = __shfl_xor_sync(kFull, best, off);
+      int oi = __shfl_xor_sync(kFull, bidx, off);
+      if (oi != INT_MAX && better(ov, oi, best, bidx)) { best = ov; bidx = oi; }
+    }
+    if ((bidx & 31) == lane) taken |= 1u << (bidx >> 5);
+    if (lane == j) { my_val = best; my_idx = bidx; }
+  }
+  const double m = (double)__shfl_sync(kFull, my_val, 0);
+  const double ex = lane < k ? exp((double)my_val - m) : 0.0;
+  double s;
+  if (k < 8) {
+    s = 0.0;
+    for (int j = 0; j < k; ++j) s += __shfl_sync(kFull, ex, j);
+  } else {
+    double r[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = __shfl_sync(kFull, ex, i);
+    int j = 8;
+    for (; j + 8 <= k; j += 8) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) r[i] += __shfl_sync(kFull, ex, j + i);
+    }
+    s = ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
+    for (; j < k; ++j) s += __shfl_sync(kFull, ex, j);
+  }
+  if (lane < k) {
+    ids_out[lane] = my_idx;
+    w_out[lane] = __double2float_rn(ex / s);
+  }
+}
+
+__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int64_t T,
+                                                    int E, int k, int32_t* __restrict__ ids,
+                                                    float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  route_token(logits + t * E, E, k, ids + t * k, w + t * k, lane);
+}
+
+// Exclusive scan of v over threads 0..n-1 of the block (n <= 1024); returns the total.
+__device__ int block_excl_scan(int v, int* warp_tot, int* out_total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int y = __shfl_up_sync(kFull, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int t = warp_tot[lane];
+    int xs = t;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int y = __shfl_up_sync(kFull, xs, off);
+      if (lane >= off) xs += y;
+    }
+    warp_tot[lane] = xs - t;  // exclusive prefix of warp totals
+    if (lane == 31) *out_total = xs;
+  }
+  __syncthreads();
+  int r = warp_tot[warp] + x - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(AlignArgs a) {
+  extern __shared__ int smem_i[];
+  const int E = a.E, bm = a.bm, k = a.k;
+  int* hist = smem_i;                     // [32][E]
+  int* poff = hist + kAlignWarps * E;     // [E+1] padded offsets
+  int* cnt = poff + (E + 1);              // [E]
+  int* scratch = cnt + E;                 // [32 + 2]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  if (a.route_here) {
+    for (int64_t t = warp; t < a.T; t += kAlignWarps)
+      route_token(a.logits + t * E, E, k, a.ids + t * k, a.w + t * k, lane);
+  }
+  for (int i = tid; i < kAlignWarps * E; i += kAlignThreads) hist[i] = 0;
+  __syncthreads();
+
+  const int P = (int)(a.T * k);
+  const int chunk = (P + kAlignWarps - 1) / kAlignWarps;
+  const int beg = min(P, warp * chunk), end = min(P, beg + chunk);
+  int* myhist = hist + warp * E;
+
+  // pass 1: per-warp histogram
+  for (int base = beg; base < end; base += 32) {
+    const int p = base + lane;
+    int e = -1;
+    if (p < end) {
+      e = a.ids[p];
+      if (e < 0 || e >= E) {
+        moe::set_status(a.status, MOE_ERR_INVALID_EXPERT);
+        e = -1;
+      }
+    }
+    const int key = e >= 0 ? e : (0x40000000 | lane);
+    const unsigned grp = __match_any_sync(kFull, key);
+    if (e >= 0 && lane == __ffs(grp) - 1) myhist[e] += __popc(grp);
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // pass 2: counts, padded offsets, per-warp bases
+  int c = 0, padded = 0;
+  if (tid < E) {
+    for (int w = 0; w < kAlignWarps; ++w) c += hist[w * E + tid];
+    padded = (c + bm - 1) / bm * bm;
+  }
+  int total_pad, total_cnt;
+  int off_pad = block_excl_scan(tid < E ? padded : 0, scratch, scratch + 32);
+  total_pad = scratch[32];
+  __syncthreads();
+  int off_cnt = block_excl_scan(tid < E ? c : 0, scratch, scratch + 33);
+  total_cnt = scratch[33];
+  if (tid < E) {
+    poff[tid] = off_pad;
+    cnt[tid] = c;
+    int run = off_pad;
+    for (int w = 0; w < kAlignWarps; ++w) {
+      int t = hist[w * E + tid];
+      hist[w * E + tid] = run;
+      run += t;
+    }
+    if (a.expert_offsets) a.expert_offsets[tid] = off_cnt;
+  }
+  if (tid == 0) {
+    poff[E] = total_pad;
+    *a.ntpp = total_pad;
+    if (a.expert_offsets) a.expert_offsets[E] = total_cnt;
+  }
+  __syncthreads();
+
+  // pass 3: stable scatter (each warp walks its own range in order)
+  for (int base = beg; base < end; base += 32) {
+    const int p = base + lane;
+    int e = -1;
+    if (p < end) {
+      e = a.ids[p];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const int key = e >= 0 ? e : (0x40000000 | lane);
+    const unsigned grp = __match_any_sync(kFull, key);
+    if (e >= 0) {
+      const int rank = __popc(grp & ((1u << lane) - 1u));
+      a.sorted[myhist[e] + rank] = p;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(grp) - 1) myhist[e] += __popc(grp);
+    __syncwarp();
+  }
+  // sentinel fill of each expert's padding and of the tail up to the capacity
+  if (tid < E) {
+    for (int s = poff[tid] + cnt[tid]; s < poff[tid + 1]; ++s) a.sorted[s] = P;
+  }
+  for (int64_t s = (int64_t)total_pad + tid; s < a.cap; s += kAlignThreads) a.sorted[s] = P;
+  // per-block expert ids; -1 past the last used block
+  const int64_t cap_blocks = a.cap / bm;
+  for (int64_t b = tid; b < cap_blocks; b += kAlignThreads) {
+    int64_t s = b * bm;
+    int eid = -1;
+    if (s < total_pad) {
+      int lo = 0, hi = E;  // last e with poff[e] <= s
+      while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (poff[mid] <= s) lo = mid; else hi = mid;
+      }
+      eid = lo;
+    }
+    a.expert_ids[b] = eid;
+  }
+}
+
+}  // namespace
+
+namespace moe_launch {
+
+size_t align_smem_bytes(int E) { return sizeof(int) * ((size_t)kAlignWarps * E + 2 * E + 1 + 34); }
+
+cudaError_t align(const float* logits, int32_t* ids, float* w, int64_t T, int k, int E, int bm,
+                  int32_t* sorted, int64_t cap, int32_t* expert_ids, int32_t* ntpp,
+                  int32_t* expert_offsets, int32_t* status, cudaStream_t stream) {
+  AlignArgs a{logits, ids, w, T, k, E, bm, sorted, cap, expert_ids, ntpp, expert_offsets,
+              status, 0};
+  constexpr int64_t kFuseT = 512;
+  if (logits) {
+    if (T <= kFuseT) {
+      a.route_here = 1;
+    } else {
+      const int warps = 8;
+      route_kernel<<<(unsigned)((T + warps - 1) / warps), warps * 32, 0, stream>>>(logits, T, E, k,
+                                                                                 ids, w);
+      cudaError_t err = cudaGetLastError();
+      if (err != cudaSuccess) return err;
+    }
+  }
+  const size_t smem = align_smem_bytes(E);
+  cudaError_t err = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+  if (err != cudaSuccess) return err;
+  align_kernel<<<1, kAlignThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe_launch

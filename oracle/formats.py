@@ -62,11 +62,12 @@ def apply_block_scale(values: np.ndarray, scales) -> np.ndarray:
 
 
 def dequant_mxfp4(packed, scales) -> np.ndarray:
-    return apply_block_scale(e2m1_decode(unpack_e2m1(packed)), scales)
+    # the 16 code values, then a gather: same numbers as decoding each code in place
+    return apply_block_scale(e2m1_decode(np.arange(16))[unpack_e2m1(packed)], scales)
 
 
 def dequant_mxfp8(codes, scales) -> np.ndarray:
-    return apply_block_scale(e4m3_decode(codes), scales)
+    return apply_block_scale(e4m3_decode(np.arange(256))[np.asarray(codes, dtype=np.uint8)], scales)
 
 
 def dequant(fmt: str, data, scales=None) -> np.ndarray:

@@ -1,0 +1,98 @@
+"""The C ABI library loads, exports every symbol its header declares, and its host-side
+logic (bucket math, capacity, workspace sizes, argument validation) is correct.  No GPU:
+no call here launches a kernel."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import mixture_experts_grouped_align_gb300 as moe
+from oracle import align as oalign
+from oracle import bucket as obucket
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe.build()
+    return moe.load()
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w \*]*?\b(moe_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_binding_symbols():
+    assert sorted(declared_functions()) == sorted(moe.EXPORTED_SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_bucket_matches_oracle_exhaustively(lib):
+    got = [moe.moe_bucket(m) for m in range(1, 65537)]
+    want = [obucket.bucket(m) for m in range(1, 65537)]
+    assert got == want
+    assert moe.moe_bucket(0) == -1
+    assert moe.moe_bucket_count(20000) == 97
+    for n in (1, 15, 16, 17, 100, 4096, 20000, 65536):
+        assert moe.moe_bucket_count(n) == len(obucket.bucket_iter(n))
+
+
+def test_bucket_pad_host_math_without_device_buffers(lib):
+    st, tp = moe.moe_bucket_pad(59000, "mxfp4")
+    assert st == 0 and tp == obucket.bucket(59000)
+    st, tp = moe.moe_bucket_pad(59000, "bf16")
+    assert st == moe.MOE_WARN_PAD_IGNORED and tp == 59000
+    st, tp = moe.moe_bucket_pad(17, "mxfp8")
+    assert st == moe.MOE_WARN_PAD_IGNORED and tp == 17
+    st, tp = moe.moe_bucket_pad(0, "mxfp4")
+    assert st == 0 and tp == 0
+
+
+@pytest.mark.parametrize("P,E,bm", [(0, 1, 1), (256, 128, 128), (65536, 256, 128), (7, 5, 16)])
+def test_capacity_matches_oracle(lib, P, E, bm):
+    assert moe.moe_align_capacity(P, E, bm) == oalign.capacity(P, E, bm)
+
+
+def test_workspace_size(lib):
+    n = moe.moe_forward_workspace_size(64, 4, 2880, 2880)
+    P = 256
+    r = lambda v: (v + 255) // 256 * 256
+    assert n == r(P * 2880 * 2) + r(P * 2880 * 4)
+    assert moe.moe_forward_workspace_size(-1, 4, 1, 1) == 0
+
+
+def test_argument_errors_are_reported_without_a_launch(lib):
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_align(None, None, None, 4, 2, 8, 16, None, 64, None, None)
+    assert ei.value.status == -1
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_align(None, 16, None, 4, 40, 8, 16, 16, 64, 16, 16)
+    assert ei.value.status == -2            # k > 32 / k > E
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_align(None, 16, None, 4, 2, 8, 16, 16, 16, 16, 16)
+    assert ei.value.status == -3            # capacity too small
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_forward("mxfp8", 8, 256, 512, 16, 16, None, 16, 16, None, 16, None, 4, 4, 2,
+                        16, 16, 16, 16, None, 16, 256, 16, moe.Ctx(stream=0))
+    assert ei.value.status == -2            # MXFP8 forward needs the quantiser
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_wgrad(16, 16, 0, 4, 2, 8, 100, 64, 16, 16, 16, 16, 256, 16, 0, moe.Ctx(stream=0))
+    assert ei.value.status == -2            # N not a multiple of 64
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_grouped_gemm("bf16", 8, 64, 64, 8, None, 0, 16, None, None, 4, 2, 16, 16, 16, 16,
+                             256, 16, moe.Ctx(stream=0))
+    assert ei.value.status == -1            # misaligned pointer
+    assert "aligned" in lib.moe_last_error().decode()

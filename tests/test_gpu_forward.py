@@ -1,0 +1,118 @@
+"""moe_forward (GEMM1 + bias + SwiGLU -> GEMM2 + bias * routing weight -> combine) on the
+GPU against the float64 oracle; padded vs unpadded real rows bit-identical."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import bucket as obucket
+from oracle import layer as olayer
+from oracle import formats as ofmt
+from oracle import route as oroute
+
+from helpers import assert_close_bf16, bf16_to_np, dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import mixture_experts_grouped_align_gb300 as m
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    m.build()
+    m.load()
+    return m
+
+
+def device_layer(moe, lay, w, max_rows, pad):
+    from mixture_experts_grouped_align_gb300.runner import DeviceLayer
+    return DeviceLayer(w.quant, w.E, w.K, w.I, w.k, dev(lay["w1"]), dev(lay["w1_scale"]),
+                       dev(lay["b1"]), dev(lay["w2"]), dev(lay["w2_scale"]), dev(lay["b2"]),
+                       max_rows=max_rows, pad=pad)
+
+
+def run(moe, L, lay, T):
+    x = dev(lay["x"][:T])
+    lg = dev(lay["logits"][:T])
+    y = torch.empty((max(T, 1), L.K), dtype=torch.bfloat16, device="cuda")
+    L.status.zero_()
+    rows = L.step(x, lg, T, y)
+    torch.cuda.synchronize()
+    assert int(L.status[0]) == 0
+    return y[:T], rows
+
+
+def oracle_y(lay, w, T, tokens=None):
+    W = olayer.ExpertWeights(w.quant, lay["w1"], lay["w1_scale"], lay["b1"], lay["w2"],
+                             lay["w2_scale"], lay["b2"])
+    x = ofmt.bf16_decode(lay["x"][:T])
+    ids, wt = oroute.route(lay["logits"][:T], w.k)
+    return olayer.moe_layer(x, ids, wt, W, tokens)
+
+
+@pytest.mark.parametrize("bias", [False, True])
+def test_tiny_layer_full(moe, bias):
+    w = synth.scaled(synth.TINY, bias=bias)
+    lay = synth.make_layer(w)
+    L = device_layer(moe, lay, w, w.T, pad=True)
+    y, rows = run(moe, L, lay, w.T)
+    assert rows == obucket.bucket(w.T)
+    assert_close_bf16(bf16_to_np(y), oracle_y(lay, w, w.T), what="tiny")
+
+
+def test_decode_mxfp4_full(moe):
+    w = synth.DECODE_MXFP4
+    lay = synth.make_layer(w)
+    L = device_layer(moe, lay, w, w.T, pad=True)
+    y, _ = run(moe, L, lay, w.T)
+    assert_close_bf16(bf16_to_np(y), oracle_y(lay, w, w.T), what="decode_mxfp4")
+
+
+@pytest.mark.parametrize("M", synth.DECODE_BF16_M)
+def test_decode_bf16_tiny_m(moe, M):
+    w = synth.decode_bf16_workload(M)
+    lay = synth.make_layer(w)
+    L = device_layer(moe, lay, w, M, pad=True)
+    y, rows = run(moe, L, lay, M)
+    assert rows == M  # bf16 mode: padding not allowed
+    assert_close_bf16(bf16_to_np(y), oracle_y(lay, w, M), what=f"decode_bf16 M={M}")
+
+
+@pytest.mark.parametrize("T", [1, 17, 300, 1001])
+def test_padded_equals_unpadded_and_oracle(moe, T):
+    """Several tiles and a ragged tail; bucket-padded and unpadded runs give the same bits
+    on every real row."""
+    w = synth.Workload("ragged", T=T, K=256, I=256, E=16, k=4, quant="mxfp4", seed=11,
+                       scale_exp=(-6, -2), bias=True)
+    lay = synth.make_layer(w)
+    Lp = device_layer(moe, lay, w, T, pad=True)
+    Lu = device_layer(moe, lay, w, T, pad=False)
+    yp, rows_p = run(moe, Lp, lay, T)
+    yu, rows_u = run(moe, Lu, lay, T)
+    assert rows_p == obucket.bucket(T) and rows_u == T
+    assert torch.equal(yp.view(torch.int16), yu.view(torch.int16))
+    assert_close_bf16(bf16_to_np(yp), oracle_y(lay, w, T), what=f"ragged T={T}")
+
+
+def test_prefill_full_size_padded_vs_unpadded_and_sampled_oracle(moe):
+    w = synth.prefill_workload()
+    lay = synth.make_layer(w)
+    T = w.T
+    Lp = device_layer(moe, lay, w, T, pad=True)
+    yp, rows = run(moe, Lp, lay, T)
+    assert rows == obucket.bucket(T) and rows > T
+    del Lp
+    Lu = device_layer(moe, lay, w, T, pad=False)
+    yu, _ = run(moe, Lu, lay, T)
+    del Lu
+    assert torch.equal(yp.view(torch.int16), yu.view(torch.int16))
+    # sampled rows: tokens whose k experts all lie in a 12-expert subset (so that the
+    # oracle decodes only those experts), plus the first and last tokens' own experts
+    ids, _ = oroute.route(lay["logits"], w.k)
+    rng = np.random.default_rng(0)
+    subset = rng.choice(w.E, 12, replace=False)
+    inside = np.flatnonzero(np.isin(ids, subset).all(axis=1))
+    toks = np.concatenate([inside[:24], [0, T - 1]])
+    yo = oracle_y(lay, w, T, tokens=toks)
+    assert_close_bf16(bf16_to_np(yp)[toks], yo, what="prefill sampled rows")

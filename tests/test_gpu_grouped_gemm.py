@@ -1,0 +1,129 @@
+"""moe_grouped_gemm (one launch over all experts, optional per-expert bias) on the GPU
+against the float64 oracle, for MXFP8 (block-scaled E4M3 operands), MXFP4 and bf16."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import align as oalign
+from oracle import formats as ofmt
+from oracle import layer as olayer
+
+from helpers import assert_close_bf16, bf16_to_np, dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+BM = 128
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import mixture_experts_grouped_align_gb300 as m
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    m.build()
+    m.load()
+    return m
+
+
+def align_dev(moe, ids, E, bm=BM):
+    T, k = ids.shape
+    cap, capb = moe.moe_align_capacity(T * k, E, bm)
+    d = "cuda"
+    tid = torch.from_numpy(ids.astype(np.int32)).to(d)
+    srt = torch.empty(cap, dtype=torch.int32, device=d)
+    eid = torch.empty(capb, dtype=torch.int32, device=d)
+    ntpp = torch.empty(4, dtype=torch.int32, device=d)
+    moe.moe_align(None, tid, None, T, k, E, bm, srt, cap, eid, ntpp, None)
+    return srt, eid, ntpp, cap
+
+
+def gemm_dev(moe, quant, E, N, Kin, a, a_scale, per_pair, w, w_scale, bias, ids, bm=BM):
+    T, k = ids.shape
+    srt, eid, ntpp, cap = align_dev(moe, ids, E, bm)
+    out = torch.full((T * k, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(4, dtype=torch.int32, device="cuda")
+    moe.moe_grouped_gemm(quant, E, N, Kin, a, a_scale, per_pair, w, w_scale, bias, T, k, srt, eid,
+                         ntpp, bm, cap, out, moe.Ctx(dev_status=st))
+    torch.cuda.synchronize()
+    assert int(st[0]) == 0
+    return out
+
+
+def random_ids(rng, T, E, k, empty=()):
+    allowed = np.array([e for e in range(E) if e not in set(empty)])
+    return np.stack([rng.choice(allowed, k, replace=False) for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("per_pair", [False, True])
+@pytest.mark.parametrize("bias", [False, True])
+def test_mxfp8_small(moe, per_pair, bias):
+    rng = np.random.default_rng(3)
+    T, E, k, N, Kin = 203, 12, 3, 96, 320
+    ids = random_ids(rng, T, E, k, empty=(5,))
+    rows = T * k if per_pair else T
+    a_c, a_s = synth.mx_quantise_e4m3(rng.standard_normal((rows, Kin)).astype(np.float32))
+    w_c, w_s = synth.mx_quantise_e4m3((rng.standard_normal((E, N, Kin)) * 0.05).astype(np.float32))
+    b = synth.to_bf16_bits(rng.standard_normal((E, N)) * 0.1) if bias else None
+    out = gemm_dev(moe, "mxfp8", E, N, Kin, dev(a_c), dev(a_s), per_pair, dev(w_c), dev(w_s),
+                   dev(b), ids)
+    A = ofmt.dequant_mxfp8(a_c, a_s)
+    Wd = lambda e: (ofmt.dequant_mxfp8(w_c[e], w_s[e]), None if b is None else ofmt.bf16_decode(b[e]))
+    ref = olayer.grouped_gemm(A, ids, Wd, per_pair)
+    assert_close_bf16(bf16_to_np(out), ref, what="mxfp8 small")
+
+
+@pytest.mark.parametrize("quant", ["mxfp4", "bf16"])
+def test_w4a16_and_bf16_small(moe, quant):
+    rng = np.random.default_rng(4)
+    T, E, k, N, Kin = 77, 9, 2, 48, 256
+    ids = random_ids(rng, T, E, k)
+    a = synth.to_bf16_bits(rng.standard_normal((T, Kin)))
+    if quant == "mxfp4":
+        w, ws = synth.gen_mxfp4_weight(rng, E, N, Kin, (-5, 0))
+    else:
+        w, ws = synth.gen_bf16_weight(rng, E, N, Kin, 0.05), None
+    b = synth.to_bf16_bits(rng.standard_normal((E, N)) * 0.1)
+    out = gemm_dev(moe, quant, E, N, Kin, dev(a), None, False, dev(w), dev(ws), dev(b), ids)
+    Wd = lambda e: (ofmt.dequant(quant, w[e], None if ws is None else ws[e]), ofmt.bf16_decode(b[e]))
+    ref = olayer.grouped_gemm(ofmt.bf16_decode(a), ids, Wd, False)
+    assert_close_bf16(bf16_to_np(out), ref, what=quant)
+
+
+def test_mxfp8_constant_roundtrip(moe):
+    """Constant codes and scales: every output is Kin * a * w * 2^(sa + sw) exactly."""
+    T, E, k, N, Kin = 16, 4, 2, 32, 128
+    ids = np.array([[t % E, (t + 1) % E] for t in range(T)], dtype=np.int32)
+    a_c = np.full((T, Kin), 0x38, np.uint8)          # E4M3 1.0
+    a_s = np.full((T, Kin // 32), 127 - 2, np.uint8)
+    w_c = np.full((E, N, Kin), 0xB4, np.uint8)        # E4M3 -0.75
+    w_s = np.full((E, N, Kin // 32), 127 + 1, np.uint8)
+    out = gemm_dev(moe, "mxfp8", E, N, Kin, dev(a_c), dev(a_s), False, dev(w_c), dev(w_s), None, ids)
+    want = Kin * 1.0 * -0.75 * 2.0 ** (-2 + 1)
+    assert np.all(bf16_to_np(out) == want)
+
+
+def test_mxfp8_full_size_sampled(moe):
+    """The 256-expert, hidden 7168 / intermediate 2048, top-8, T=8192 grouped GEMMs with Zipf
+    routing; operands drawn on the device; sampled pairs of a few experts checked."""
+    g = synth.make_mxfp8_gemm_wgrad(device="cuda")
+    T, E, K, I, k = g["T"], g["E"], g["K"], g["I"], g["k"]
+    ids = g["topk_ids"]
+    out1 = gemm_dev(moe, "mxfp8", E, 2 * I, K, g["x_codes"], g["x_scale"], False, g["w1"],
+                    g["w1_scale"], None, ids)
+    out2 = gemm_dev(moe, "mxfp8", E, K, I, g["a2_codes"], g["a2_scale"], True, g["w2"],
+                    g["w2_scale"], None, ids)
+    flat = ids.reshape(-1)
+    cnt = np.bincount(flat, minlength=E)
+    rng = np.random.default_rng(1)
+    experts = [int(np.argmax(cnt)), int(np.argsort(cnt)[E // 2])] + \
+        [int(e) for e in rng.choice(np.flatnonzero(cnt), 2, replace=False)]
+    for e in experts:
+        pairs = np.flatnonzero(flat == e)
+        pairs = pairs[rng.choice(pairs.size, min(16, pairs.size), replace=False)]
+        W1 = ofmt.dequant_mxfp8(g["w1"][e].cpu().numpy(), g["w1_scale"][e].cpu().numpy())
+        X = ofmt.dequant_mxfp8(g["x_codes"][pairs // k].cpu().numpy(), g["x_scale"][pairs // k].cpu().numpy())
+        assert_close_bf16(bf16_to_np(out1[pairs]), X @ W1.T, what=f"gemm1 expert {e}")
+        W2 = ofmt.dequant_mxfp8(g["w2"][e].cpu().numpy(), g["w2_scale"][e].cpu().numpy())
+        A2 = ofmt.dequant_mxfp8(g["a2_codes"][pairs].cpu().numpy(), g["a2_scale"][pairs].cpu().numpy())
+        assert_close_bf16(bf16_to_np(out2[pairs]), A2 @ W2.T, what=f"gemm2 expert {e}")
+    assert np.all(cnt[g["cold"]] == 0)

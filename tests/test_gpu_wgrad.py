@@ -1,0 +1,132 @@
+"""moe_wgrad on the GPU against the float64 oracle (deterministic and accumulate modes)."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import formats as ofmt
+from oracle import wgrad as owgrad
+
+from helpers import dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+BM = 128
+REL = 1e-5  # float32 accumulation of exact bf16 products
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import mixture_experts_grouped_align_gb300 as m
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    m.build()
+    m.load()
+    return m
+
+
+def align_dev(moe, ids, E, bm=BM):
+    T, k = ids.shape
+    cap, capb = moe.moe_align_capacity(T * k, E, bm)
+    d = "cuda"
+    tid = torch.from_numpy(ids.astype(np.int32)).to(d)
+    srt = torch.empty(cap, dtype=torch.int32, device=d)
+    eid = torch.empty(capb, dtype=torch.int32, device=d)
+    ntpp = torch.empty(4, dtype=torch.int32, device=d)
+    moe.moe_align(None, tid, None, T, k, E, bm, srt, cap, eid, ntpp, None)
+    return srt, eid, ntpp, cap
+
+
+def wgrad_dev(moe, grad, inp, per_pair, ids, E, N, Kin, mode, bm=BM, fill=np.nan):
+    T, k = ids.shape
+    srt, eid, ntpp, cap = align_dev(moe, ids, E, bm)
+    dW = torch.full((E, N, Kin), fill, dtype=torch.float32, device="cuda")
+    moe.moe_wgrad(grad, inp, per_pair, T, k, E, N, Kin, srt, eid, ntpp, bm, cap, dW, mode)
+    torch.cuda.synchronize()
+    return dW
+
+
+def rel_err(a, b):
+    return np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("per_pair", [False, True])
+@pytest.mark.parametrize("bm", [128, 16])
+def test_wgrad_small(moe, mode, per_pair, bm):
+    rng = np.random.default_rng(7)
+    T, E, k, N, Kin = 150, 6, 2, 128, 192
+    ids = np.stack([rng.choice(E - 1, k, replace=False) for _ in range(T)]).astype(np.int32)  # E-1 empty
+    g = synth.to_bf16_bits(rng.standard_normal((T * k, N)))
+    x = synth.to_bf16_bits(rng.standard_normal((T * k if per_pair else T, Kin)))
+    dW = wgrad_dev(moe, dev(g), dev(x), per_pair, ids, E, N, Kin, mode, bm=bm).cpu().numpy()
+    ref = owgrad.moe_wgrad(ofmt.bf16_decode(g), ofmt.bf16_decode(x), ids, E, per_pair)
+    assert rel_err(dW, ref) <= REL
+    assert np.all(dW[E - 1] == 0)                   # empty expert written as zeros
+
+
+def test_wgrad_deterministic_repeatable_and_constant(moe):
+    rng = np.random.default_rng(8)
+    T, E, k, N, Kin = 500, 8, 2, 64, 64
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    g = dev(synth.to_bf16_bits(rng.standard_normal((T * k, N))))
+    x = dev(synth.to_bf16_bits(rng.standard_normal((T, Kin))))
+    a = wgrad_dev(moe, g, x, False, ids, E, N, Kin, 0)
+    b = wgrad_dev(moe, g, x, False, ids, E, N, Kin, 0)
+    assert torch.equal(a, b)
+    # analytic constant-input check: grad = 0.5, input = -3 -> dW[e] = n_e * -1.5
+    gc = torch.full((T * k, N), 0.5, dtype=torch.bfloat16, device="cuda")
+    xc = torch.full((T, Kin), -3.0, dtype=torch.bfloat16, device="cuda")
+    c = wgrad_dev(moe, gc, xc, False, ids, E, N, Kin, 0).cpu().numpy()
+    cnt = np.bincount(ids.reshape(-1), minlength=E)
+    for e in range(E):
+        assert np.all(c[e] == cnt[e] * -1.5)
+
+
+def test_wgrad_sentinel_rows_never_read(moe):
+    """NaN rows directly after grad and input: sentinel slots must not touch them."""
+    rng = np.random.default_rng(9)
+    T, E, k, N, Kin = 40, 5, 2, 64, 128
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    g = torch.full((T * k + 64, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    x = torch.full((T + 64, Kin), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gv = synth.to_bf16_bits(rng.standard_normal((T * k, N)))
+    xv = synth.to_bf16_bits(rng.standard_normal((T, Kin)))
+    g[:T * k] = dev(gv)
+    x[:T] = dev(xv)
+    for mode in (0, 1):
+        dW = wgrad_dev(moe, g, x, False, ids, E, N, Kin, mode).cpu().numpy()
+        assert np.all(np.isfinite(dW))
+        ref = owgrad.moe_wgrad(ofmt.bf16_decode(gv), ofmt.bf16_decode(xv), ids, E, False)
+        assert rel_err(dW, ref) <= REL
+
+
+def test_wgrad_full_size_sampled(moe):
+    """dW1 [256, 4096, 7168] and dW2 [256, 7168, 2048] of the MXFP8 training workload:
+    every element of a few experts' sampled rows/columns against the oracle; cold experts
+    are exactly zero."""
+    g = synth.make_mxfp8_gemm_wgrad(device="cuda")
+    T, E, K, I, k = g["T"], g["E"], g["K"], g["I"], g["k"]
+    ids = g["topk_ids"]
+    flat = ids.reshape(-1)
+    cnt = np.bincount(flat, minlength=E)
+    rng = np.random.default_rng(2)
+    experts = [int(np.argmax(cnt)), int(g["cold"][0]), int(rng.choice(np.flatnonzero(cnt)))]
+    for (grad, inp, per_pair, N, Kin) in [(g["grad1"], g["x_bf16"], False, 2 * I, K),
+                                          (g["grad2"], g["h_bf16"], True, K, I)]:
+        for mode in (0, 1):
+            dW = wgrad_dev(moe, grad, inp, per_pair, ids, E, N, Kin, mode)
+            for e in experts:
+                pairs = np.flatnonzero(flat == e)
+                rows = rng.choice(N, 8, replace=False)
+                cols = rng.choice(Kin, 64, replace=False)
+                got = dW[e][rows][:, cols].cpu().numpy()
+                if pairs.size == 0:
+                    assert np.all(got == 0)
+                    continue
+                gs = ofmt.bf16_decode(grad[pairs][:, rows].cpu().view(torch.int16).numpy().view(np.uint16))
+                src = pairs if per_pair else pairs // k
+                xs = ofmt.bf16_decode(inp[src][:, cols].cpu().view(torch.int16).numpy().view(np.uint16))
+                ref = gs.T @ xs
+                assert rel_err(got, ref) <= REL, (e, mode)
+            del dW
+            torch.cuda.empty_cache()
