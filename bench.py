@@ -159,9 +159,13 @@ class ClockSampler:
         sm, mx, reasons = [], None, set()
         names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9 or parts[0] != str(dev_index):
+            rows = [[p.strip() for p in line.split(",")] for line in f]
+        rows = [r for r in rows if len(r) >= 9]
+        idx = {r[0] for r in rows}
+        want = str(dev_index) if str(dev_index) in idx else (sorted(idx)[0] if idx else None)
+        if True:
+            for parts in rows:
+                if parts[0] != want:
                     continue
                 try:
                     sm.append(float(parts[1]))
@@ -238,6 +242,10 @@ def bench_ours(args, rank, world, local_rank):
         step()
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for es in evs:  # torch creates the CUDA event on its first record
+        for e in es:
+            e.record(stream)
+    torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")

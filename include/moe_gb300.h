@@ -53,7 +53,7 @@ typedef int32_t moe_status;
 #define MOE_ERR_CUDA (-4)         /* a CUDA launch or runtime error                     */
 /* device status codes (ctx->dev_status) */
 #define MOE_ERR_INVALID_EXPERT (-5) /* a top-k id outside [0, E)                        */
-#define MOE_ERR_RANGE (-6)          /* decode path: |activation| > 65504 (float16 max)   */
+#define MOE_ERR_RANGE (-6)          /* an activation or h value beyond float16's 65504   */
 #define MOE_ERR_TIMEOUT (-7)        /* a bounded wait inside a kernel ran out            */
 
 typedef enum {
@@ -160,13 +160,14 @@ typedef struct {
   const void* b2;         /* [E, K] bf16 or NULL                                          */
 } moe_weights;
 
-/* Workspace bytes moe_forward needs for T_rows rows of top-k: h [T_rows*k, I] bf16 and
+/* Workspace bytes moe_forward needs for T_rows rows of top-k: h [T_rows*k, I] f16 and
  * o [T_rows*k, K] fp32, each 256-byte aligned. */
 size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t I);
 
 /* For every real token t < T_real (the others, e.g. bucket pad rows, are computed and
  * then sliced off):
- *   gu = x_t . W1[e]^T + b1[e];  h = silu(gu[:I]) * gu[I:]  (fp32, then bf16 RNE)
+ *   gu = x_t . W1[e]^T + b1[e];  h = silu(gu[:I]) * gu[I:]  (fp32, then f16 RNE;
+ *                                                      |h| > 65504 sets MOE_ERR_RANGE)
  *   o_tj = w[t,j] * (h . W2[e]^T + b2[e])                    (fp32)
  *   y_t  = sum_{j=0..k-1} o_tj, in order of j, rounded to bf16 RNE.
  * x: [T_rows, K] bf16 (BF16 and MXFP4_W4A16 modes).  topk_w [T_rows, k]; the alignment

@@ -183,13 +183,24 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gemm_kernel(GroupedGemm a)
           } else {
             const uint4 raw = *reinterpret_cast<const uint4*>(
                 static_cast<const uint16_t*>(a.act) + arow * Kin + kb0 * 32 + c * 8);
-            if (WF == WF_BF16) {
-              v = raw;
-            } else {
-              v.x = moe::bf16x2_to_f16x2(raw.x, &bad);
-              v.y = moe::bf16x2_to_f16x2(raw.y, &bad);
-              v.z = moe::bf16x2_to_f16x2(raw.z, &bad);
-              v.w = moe::bf16x2_to_f16x2(raw.w, &bad);
+            if (WF == WF_BF16) {  // bf16 MMA operand
+              if (a.act_fmt == ACT_F16) {
+                v.x = moe::f16x2_to_bf16x2(raw.x);
+                v.y = moe::f16x2_to_bf16x2(raw.y);
+                v.z = moe::f16x2_to_bf16x2(raw.z);
+                v.w = moe::f16x2_to_bf16x2(raw.w);
+              } else {
+                v = raw;
+              }
+            } else {              // f16 MMA operand
+              if (a.act_fmt == ACT_F16) {
+                v = raw;
+              } else {
+                v.x = moe::bf16x2_to_f16x2(raw.x, &bad);
+                v.y = moe::bf16x2_to_f16x2(raw.y, &bad);
+                v.z = moe::bf16x2_to_f16x2(raw.z, &bad);
+                v.w = moe::bf16x2_to_f16x2(raw.w, &bad);
+              }
             }
           }
         }
@@ -298,8 +309,10 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gemm_kernel(GroupedGemm a)
             gt += moe::bf16_bits_to_f32(bias[e * a.Nw + n]);
             up += moe::bf16_bits_to_f32(bias[e * a.Nw + a.Nout + n]);
           }
-          static_cast<uint16_t*>(a.out)[(int64_t)p * a.Nout + n] =
-              moe::f32_to_bf16_bits(moe::silu(gt) * up);
+          // h is kept as float16 (11-bit significand); an overflow is reported
+          const __half hv = __float2half_rn(moe::silu(gt) * up);
+          if (__hisinf(hv) || __hisnan(hv)) bad = true;
+          static_cast<__half*>(a.out)[(int64_t)p * a.Nout + n] = hv;
         } else if (EPI == EPI_WEIGHTED_F32) {
           float o = v[0][i];
           if (bias) o += moe::bf16_bits_to_f32(bias[e * a.Nw + n]);

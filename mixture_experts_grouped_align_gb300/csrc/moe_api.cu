@@ -216,7 +216,7 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
   g1.wfmt = wf;
   g1.epi = moe_launch::EPI_SWIGLU;
   g1.w = W->w1; g1.w_scale = W->w1_scale; g1.bias = W->b1;
-  g1.act = x; g1.act_scale = nullptr; g1.act_per_pair = 0;
+  g1.act = x; g1.act_fmt = moe_launch::ACT_BF16; g1.act_scale = nullptr; g1.act_per_pair = 0;
   g1.Nw = 2 * (int64_t)I; g1.Kin = K; g1.Nout = I; g1.k = k; g1.P = P; g1.E = E;
   g1.sorted = sorted_token_ids; g1.expert_ids = expert_ids; g1.ntpp = num_tokens_post_padded;
   g1.bm = block_m; g1.grid_blocks = blocks; g1.topk_w = topk_w; g1.out = h;
@@ -231,7 +231,7 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
   moe_launch::GroupedGemm g2 = g1;
   g2.epi = moe_launch::EPI_WEIGHTED_F32;
   g2.w = W->w2; g2.w_scale = W->w2_scale; g2.bias = W->b2;
-  g2.act = h; g2.act_per_pair = 1;
+  g2.act = h; g2.act_fmt = moe_launch::ACT_F16; g2.act_per_pair = 1;
   g2.Nw = K; g2.Kin = I; g2.Nout = K; g2.out = o;
   st = cuda_status(moe_launch::decode_gemm(g2, s), "moe_forward GEMM2");
   if (st != MOE_OK) return st;
@@ -270,7 +270,7 @@ moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin, 
   g.wfmt = mx8 ? moe_launch::WF_MXFP8 : (fp4 ? moe_launch::WF_MXFP4 : moe_launch::WF_BF16);
   g.epi = moe_launch::EPI_PLAIN_BF16;
   g.w = w; g.w_scale = w_scale; g.bias = bias;
-  g.act = a; g.act_scale = a_scale; g.act_per_pair = a_per_pair ? 1 : 0;
+  g.act = a; g.act_fmt = moe_launch::ACT_BF16; g.act_scale = a_scale; g.act_per_pair = a_per_pair ? 1 : 0;
   g.Nw = N; g.Kin = Kin; g.Nout = N; g.k = k; g.P = P; g.E = E;
   g.sorted = sorted_token_ids; g.expert_ids = expert_ids; g.ntpp = num_tokens_post_padded;
   g.bm = block_m; g.grid_blocks = used_blocks_bound(P, E, block_m, cap_tokens);

@@ -51,6 +51,13 @@ MOE_DEV uint32_t bf16x2_to_f16x2(uint32_t v, bool* bad) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// f16x2 -> bf16x2 (round to nearest even).
+MOE_DEV uint32_t f16x2_to_bf16x2(uint32_t v) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+  __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
 MOE_DEV float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
 MOE_DEV uint16_t f32_to_bf16_bits(float f) {

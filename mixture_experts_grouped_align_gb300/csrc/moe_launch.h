@@ -21,6 +21,7 @@ cudaError_t combine(const float* o, int64_t T_real, int k, int K, void* y, cudaS
 // ---- grouped GEMMs on the weight-streaming (decode) path (decode_gemm.cu)
 enum WFmt { WF_BF16 = 0, WF_MXFP4 = 1, WF_MXFP8 = 2 };
 enum Epi { EPI_SWIGLU = 0, EPI_WEIGHTED_F32 = 1, EPI_PLAIN_BF16 = 2 };
+enum ActFmt { ACT_BF16 = 0, ACT_F16 = 1 };
 
 struct GroupedGemm {
   int wfmt;                 // WFmt
@@ -28,7 +29,8 @@ struct GroupedGemm {
   const void* w;            // [E, Nw, Kin] in wfmt
   const uint8_t* w_scale;   // [E, Nw, Kin/32] E8M0 (mx formats)
   const void* bias;         // [E, Nw] bf16 or null
-  const void* act;          // rows [*, Kin]: bf16 (wfmt bf16/mxfp4) or E4M3 (mxfp8)
+  const void* act;          // rows [*, Kin]: bf16, f16 (act_fmt) or E4M3 (wfmt mxfp8)
+  int act_fmt;              // ActFmt of 16-bit activations
   const uint8_t* act_scale; // [*, Kin/32] (mxfp8)
   int act_per_pair;         // act row = p (1) or p / k (0)
   int64_t Nw;               // weight rows per expert (SwiGLU: 2 * Nout)
@@ -43,7 +45,7 @@ struct GroupedGemm {
   int bm;
   int64_t grid_blocks;      // block slots to launch for
   const float* topk_w;      // [P] (EPI_WEIGHTED_F32)
-  void* out;                // [P, Nout]: bf16 (SWIGLU, PLAIN) or f32 (WEIGHTED)
+  void* out;                // [P, Nout]: f16 (SWIGLU), bf16 (PLAIN) or f32 (WEIGHTED)
   int32_t* status;
 };
 size_t decode_gemm_smem_bytes(const GroupedGemm& g);
