@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--workload", default="decode_mxfp4",
                     choices=["decode_mxfp4", "decode_bf16", "prefill_mxfp4", "tiny"])
     ap.add_argument("--m", type=int, default=28, help="tokens for decode_bf16")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the token count (smaller cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-tokens", type=int, default=None, help=argparse.SUPPRESS)
@@ -197,6 +199,9 @@ def bench_ours(args, rank, world, local_rank):
     moe.build()
     moe.load()
     w = workload(args.workload, args.m)
+    if args.tokens:
+        import dataclasses
+        w = dataclasses.replace(w, T=args.tokens, name=f"{w.name}_T{args.tokens}")
     steps, warmup = DEFAULT_STEPS[args.workload]
     steps = args.steps if args.steps is not None else steps
     warmup = max(3, args.warmup if args.warmup is not None else warmup)
@@ -308,10 +313,26 @@ def bench_ours(args, rank, world, local_rank):
     hbm, bf16, src = peaks()
     dominant = "gemm1" if g1 >= g2 else "gemm2"
     dom_bytes, dom_ms = (gemm1_bytes, g1) if dominant == "gemm1" else (gemm2_bytes, g2)
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    key = f"decode_gemm_{dominant}@{w.name}"
+    tensor_path = rows > 256  # row counts above the bucket value 256 run the tcgen05 kernels
+    kernel_file = "prefill_gemm.cu" if tensor_path else "decode_gemm.cu"
+    kernel_name = ("prefill_gemm" if tensor_path else "decode_gemm") + f" ({dominant})"
+    key = f"{kernel_file}:{dominant}@{w.name}"
     tr = TRAFFIC.get(key)
-    traffic = tr["bytes"] if tr and tr.get("src") == src_hash("decode_gemm.cu") else None
+    traffic = tr["bytes"] if tr and tr.get("src") == src_hash(kernel_file) else None
+    if tensor_path:
+        # useful (unpadded) flops of the dominant GEMM against the dense f16/bf16 peak
+        # (f16 and bf16 tensor rates are equal)
+        P_real = w.T * w.k
+        dom_flops = 2.0 * P_real * w.K * 2 * w.I if dominant == "gemm1" else 2.0 * P_real * w.I * w.K
+        achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": kernel_name, "achieved": achieved, "peak": bf16,
+                    "unit": "TFLOP/s", "frac": achieved / bf16, "traffic": traffic,
+                    "algorithmic_flops": dom_flops, "peak_source": f"{src} (bf16_tflops)"}
+    else:
+        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": achieved, "peak": hbm,
+                    "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                    "algorithmic_bytes": dom_bytes, "peak_source": f"{src} (hbm_gbs)"}
     ms_step = ms / steps
     line = {
         "metric": METRIC,
@@ -324,7 +345,7 @@ def bench_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16 mma -> f32" if w.quant != "bf16" else "bf16 mma -> f32",
+        "dtype": ("f16 tcgen05 mma -> f32" if tensor_path else "f16 mma -> f32") if w.quant != "bf16" else "bf16 mma -> f32",
         "data": "synthetic (seeded PCG64 inputs, random-init weights)",
         "config": dict(describe(w, rows), l2=f"inputs larger than L2: {step_weight_bytes / 1e9:.2f} GB "
                                               f"of expert weights streamed per step > 129 MB L2",
@@ -334,9 +355,7 @@ def bench_ours(args, rank, world, local_rank):
         "kernel_ms": {"gemm1_swiglu": g1, "gemm2_weighted": g2, "combine": cb,
                       "route_align_pad_and_gaps": ms_step - g1 - g2 - cb},
         "experts_touched": touched,
-        "roofline": {"bound": "hbm", "kernel": f"decode_gemm ({dominant})", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
-                     "algorithmic_bytes": dom_bytes, "peak_source": f"{src} (hbm_gbs)"},
+        "roofline": roofline,
         "step_roofline": {"bytes": step_weight_bytes, "achieved_gbs": step_weight_bytes / (ms_step * 1e-3) / 1e9,
                           "frac": step_weight_bytes / (ms_step * 1e-3) / 1e9 / hbm},
         "e2e": {"value": world * T * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
@@ -351,6 +370,8 @@ def bench_ours(args, rank, world, local_rank):
 def launches_per_step(w, rows):
     n = 3  # GEMM1, GEMM2, combine
     n += 1  # align (routing fused for rows <= 512)
+    if w.quant == "mxfp4":
+        n += 1  # x -> f16
     if rows > 512:
         n += 1
     if w.quant == "mxfp4":

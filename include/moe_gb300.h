@@ -160,14 +160,16 @@ typedef struct {
   const void* b2;         /* [E, K] bf16 or NULL                                          */
 } moe_weights;
 
-/* Workspace bytes moe_forward needs for T_rows rows of top-k: h [T_rows*k, I] f16 and
- * o [T_rows*k, K] fp32, each 256-byte aligned. */
+/* Workspace bytes moe_forward needs for T_rows rows of top-k: h [T_rows*k, I] (f16 for
+ * MXFP4 weights, bf16 for bf16 weights), o [T_rows*k, K] fp32 and x as f16 [T_rows, K],
+ * each 256-byte aligned. */
 size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t I);
 
 /* For every real token t < T_real (the others, e.g. bucket pad rows, are computed and
  * then sliced off):
- *   gu = x_t . W1[e]^T + b1[e];  h = silu(gu[:I]) * gu[I:]  (fp32, then f16 RNE;
- *                                                      |h| > 65504 sets MOE_ERR_RANGE)
+ *   gu = x_t . W1[e]^T + b1[e];  h = silu(gu[:I]) * gu[I:]  (fp32, then stored as the
+ *        MMA operand type of GEMM2: f16 RNE for MXFP4 weights -- |h| or |x| > 65504 sets
+ *        MOE_ERR_RANGE -- and bf16 RNE for bf16 weights)
  *   o_tj = w[t,j] * (h . W2[e]^T + b2[e])                    (fp32)
  *   y_t  = sum_{j=0..k-1} o_tj, in order of j, rounded to bf16 RNE.
  * x: [T_rows, K] bf16 (BF16 and MXFP4_W4A16 modes).  topk_w [T_rows, k]; the alignment

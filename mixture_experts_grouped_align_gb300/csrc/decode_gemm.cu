@@ -36,22 +36,45 @@ constexpr int kTok = 8;     // tokens per tile (MMA N)
 constexpr int kRows = 16;   // output rows per block (MMA M)
 constexpr unsigned kFull = 0xffffffffu;
 
-// Activation rows in shared memory use a stride of S 16-bit elements with S = 32 mod 64,
-// so that the 8-lane phases of a 16-byte shared load (two token rows) hit disjoint banks.
-__host__ __device__ inline int xs_stride(int Kin) { return (Kin % 64 == 32) ? Kin : Kin + 32; }
-
-struct Smem {
-  int wsc, xs, xsc, red, total;  // byte offsets
+// Weight streaming: each warp copies its K quarter of the block's weight rows through a
+// ring of R shared-memory stages with cp.async (16-byte chunks, no register cost for
+// the bytes in flight); stage = D scale blocks of every row.  Row stride RS is padded so
+// that the lanes' shared loads of one block hit 32 distinct banks.
+template <int WF>
+struct Pipe;
+template <>
+struct Pipe<WF_MXFP4> {  // 16 B per 32-element block; lane reads 4 B (8 codes)
+  static constexpr int BPB = 16, D = 4, R = 3, RS = 80;
+};
+template <>
+struct Pipe<WF_MXFP8> {  // 32 B per block; lane reads 8 B
+  static constexpr int BPB = 32, D = 2, R = 4, RS = 96;
+};
+template <>
+struct Pipe<WF_BF16> {   // 64 B per block; lane reads 16 B
+  static constexpr int BPB = 64, D = 2, R = 4, RS = 192;
 };
 
-__host__ __device__ inline Smem smem_layout(int nmat, int Kin, bool act_scaled) {
-  const int nkb = Kin / 32;
+struct Smem {
+  int ring, wsc, red, total;  // byte offsets
+  int ring_warp, sw;          // bytes of one warp's ring; floats per scale row
+};
+
+template <int WF>
+__host__ __device__ inline Smem smem_layout(int nmat, int Kin) {
+  using PP = Pipe<WF>;
   Smem s;
+  const int nrows = nmat * kRows;
+  const bool mx = (WF != WF_BF16);
+  // one ring slot: weight rows | 2 scale words per row | decoded scales (D per row)
+  const int slot = nrows * PP::RS + (mx ? nrows * 2 * 4 + nrows * PP::D * 4 : 0);
+  s.ring_warp = PP::R * slot;
+  s.sw = 0;
+  (void)Kin;
   int off = 0;
-  s.wsc = off;  off += ((nmat * kRows * nkb + 15) / 16) * 16;          // weight scale bytes
-  s.xs = off;   off += kTok * xs_stride(Kin) * 2;                       // activations, 16-bit
-  s.xsc = off;  off += act_scaled ? ((kTok * nkb + 15) / 16) * 16 : 0;  // activation scales
-  s.red = off;  off += kWarps * nmat * 4 * 32 * 4;                      // cross-warp partials
+  s.ring = off;  off += kWarps * s.ring_warp;
+  s.wsc = off;
+  s.red = off;   off += 2 * kWarps * nmat * 4 * 32 * 4;  // double-buffered cross-warp partials
   s.total = off;
   return s;
 }
@@ -61,10 +84,7 @@ struct Fmt;
 template <>
 struct Fmt<WF_MXFP4> {
   using W = uint32_t;  // 8 codes of one row: physical K 8q..8q+7 of a 32-block
-  static constexpr int kUnroll = 8;
-  static __device__ __forceinline__ W load(const uint8_t* row, int kb, int q) {
-    return moe::ldg_nc_u32(row + kb * 16 + q * 4);
-  }
+  static __device__ __forceinline__ W lds(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
   // half 0: elements 0..3 of the lane's 8 -> (pair 0,1), (pair 2,3); half 1: elements 4..7
   static __device__ __forceinline__ void pairs(W w, int half, uint32_t& p0, uint32_t& p1) {
     p0 = moe::e2m1x2_to_f16x2((w >> (16 * half)) & 0xffu);
@@ -74,10 +94,7 @@ struct Fmt<WF_MXFP4> {
 template <>
 struct Fmt<WF_MXFP8> {
   using W = uint2;
-  static constexpr int kUnroll = 4;
-  static __device__ __forceinline__ W load(const uint8_t* row, int kb, int q) {
-    return moe::ldg_nc_u64(row + kb * 32 + q * 8);
-  }
+  static __device__ __forceinline__ W lds(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
   static __device__ __forceinline__ void pairs(W w, int half, uint32_t& p0, uint32_t& p1) {
     const uint32_t v = half ? w.y : w.x;
     p0 = moe::e4m3x2_to_f16x2(v & 0xffffu);
@@ -87,10 +104,7 @@ struct Fmt<WF_MXFP8> {
 template <>
 struct Fmt<WF_BF16> {
   using W = uint4;
-  static constexpr int kUnroll = 4;
-  static __device__ __forceinline__ W load(const uint8_t* row, int kb, int q) {
-    return moe::ldg_nc_u128(row + kb * 64 + q * 16);
-  }
+  static __device__ __forceinline__ W lds(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
   static __device__ __forceinline__ void pairs(W w, int half, uint32_t& p0, uint32_t& p1) {
     p0 = half ? w.z : w.x;
     p1 = half ? w.w : w.y;
@@ -102,240 +116,412 @@ __host__ __device__ inline int64_t wrow_bytes(int Kin) {
   return WF == WF_MXFP4 ? Kin / 2 : (WF == WF_MXFP8 ? Kin : (int64_t)Kin * 2);
 }
 
-template <int WF, int EPI>
-__global__ void __launch_bounds__(kWarps * 32) decode_gemm_kernel(GroupedGemm a) {
-  constexpr int NMAT = (EPI == EPI_SWIGLU) ? 2 : 1;
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// Work units are (alignment block, 16-row tile) pairs, block-major; a thread block owns
+// a contiguous run of the units that num_tokens_post_padded makes live, so that each
+// warp streams its weight K-slice through the ring without draining between units.
+struct Unit {
+  int64_t blk, e;
+  int rt, nsub;
+};
+
+__device__ __forceinline__ Unit load_unit(const GroupedGemm& a, int64_t u, int row_tiles) {
+  Unit x;
+  x.blk = u / row_tiles;
+  x.rt = (int)(u - x.blk * row_tiles);
+  x.e = a.expert_ids[x.blk];
+  // real pairs form a prefix of every block: count them, 8 tokens per sub-tile
+  int cnt = 0;
+  const int lane = threadIdx.x & 31;
+  for (int s0 = 0; s0 < a.bm; s0 += 32) {
+    const int s = s0 + lane;
+    const bool v = s < a.bm && a.sorted[x.blk * a.bm + s] < a.P;
+    cnt += __popc(__ballot_sync(0xffffffffu, v));
+  }
+  x.nsub = (x.e >= 0 && x.e < a.E) ? (cnt + kTok - 1) / kTok : 0;
+  return x;
+}
+
+__device__ __forceinline__ int64_t unit_row(const GroupedGemm& a, const Unit& x, int r) {
+  return x.e * a.Nw + ((r >= kRows) ? a.Nout : 0) + (int64_t)x.rt * kRows + (r & (kRows - 1));
+}
+
+// Two E2M1 codes per byte of w -> four f16x2 (exact hardware conversions).
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t& o2,
+                                              uint32_t& o3) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+      : "r"(w));
+}
+
+// E8M0 byte -> float bits: 2^(s-127); 0x00 -> 2^-127 (subnormal), 0xFF -> NaN.
+__device__ __forceinline__ float e8m0_fast(uint32_t s) {
+  uint32_t b = s << 23;
+  b = (s == 0u) ? 0x00400000u : b;
+  b = (s == 255u) ? 0x7fc00000u : b;
+  return __uint_as_float(b);
+}
+
+template <int WF>
+struct Lane;  // per-format lane mapping of the ring copies
+template <>
+struct Lane<WF_MXFP4> {  // 4 chunks per lane: rows lane/4 + 8i, block lane%4
+  static constexpr int NPL = 4;
+  static __device__ __forceinline__ int row(int lane, int i) { return (lane >> 2) + 8 * i; }
+  static __device__ __forceinline__ int blk(int lane) { return lane & 3; }
+  static __device__ __forceinline__ int sub(int lane) { return 0; }
+};
+template <>
+struct Lane<WF_MXFP8> {  // rows lane/4 + 8i, block (lane%4)/2, 16-byte half lane%2
+  static constexpr int NPL = 4;
+  static __device__ __forceinline__ int row(int lane, int i) { return (lane >> 2) + 8 * i; }
+  static __device__ __forceinline__ int blk(int lane) { return (lane & 3) >> 1; }
+  static __device__ __forceinline__ int sub(int lane) { return lane & 1; }
+};
+template <>
+struct Lane<WF_BF16> {   // rows lane/8 + 4i, block (lane%8)/4, 16-byte quarter lane%4
+  static constexpr int NPL = 8;
+  static __device__ __forceinline__ int row(int lane, int i) { return (lane >> 3) + 4 * i; }
+  static __device__ __forceinline__ int blk(int lane) { return (lane & 7) >> 2; }
+  static __device__ __forceinline__ int sub(int lane) { return lane & 3; }
+};
+
+template <int WF, int NMAT>
+__host__ __device__ constexpr int ring_slot_bytes() {
+  constexpr int NROWS = NMAT * kRows;
+  return NROWS * Pipe<WF>::RS + ((WF != WF_BF16) ? NROWS * 2 * 4 + NROWS * Pipe<WF>::D * 4 : 0);
+}
+
+// Issue side of the ring: the unit being copied and this lane's row addresses in it.
+template <int WF, int NMAT>
+struct Issuer {
+  static constexpr int NPL = Lane<WF>::NPL * NMAT / 2;  // rows per lane (chunks / 32)
+  int64_t iu, u_end;
+  Unit ix;
+  int isub, ist;
+  uint32_t issued;
+  const uint8_t* wrow[NPL];   // weight row start of this lane's rows
+  int64_t srow[2];            // scale row offsets of this lane's two scale words (MX)
+
+  __device__ __forceinline__ void bind(const GroupedGemm& a, int64_t rb, int lane) {
+    const uint8_t* wb = static_cast<const uint8_t*>(a.w);
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) wrow[i] = wb + unit_row(a, ix, Lane<WF>::row(lane, i)) * rb;
+    const int nkb = a.Kin / 32;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) srow[i] = unit_row(a, ix, (lane >> 1) + 16 * i) * nkb;
+  }
+};
+
+template <int WF, int NMAT>
+__device__ __forceinline__ void issue_next(const GroupedGemm& a, Issuer<WF, NMAT>& c, uint32_t ring_s,
+                                           int64_t rb, int kb0, int kb1, int nst, int row_tiles,
+                                           int lane) {
+  using PP = Pipe<WF>;
+  using LN = Lane<WF>;
+  constexpr int NROWS = NMAT * kRows;
   constexpr bool MX = (WF != WF_BF16);
-  constexpr bool ACT_SCALED = (WF == WF_MXFP8);
+  constexpr int SLOT = ring_slot_bytes<WF, NMAT>();
+  if (c.iu < c.u_end) {
+    const int kbs = kb0 + c.ist * PP::D;
+    const uint32_t slot = ring_s + (c.issued % PP::R) * SLOT;
+    const int j = LN::blk(lane), sub = LN::sub(lane);
+    if (kbs + j < kb1) {
+#pragma unroll
+      for (int i = 0; i < Issuer<WF, NMAT>::NPL; ++i)
+        cp_async16(slot + LN::row(lane, i) * PP::RS + j * PP::BPB + sub * 16,
+                   c.wrow[i] + (int64_t)(kbs + j) * PP::BPB + sub * 16);
+    }
+    if (MX) {  // the two 4-byte words that hold this stage's scale bytes of every row
+      const int wi = lane & 1;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int r = (lane >> 1) + 16 * i;
+        if (r < NROWS) {
+          const int64_t wa = ((c.srow[i] + kbs) & ~int64_t(3)) + 4 * wi;
+          if (wa < c.srow[i] + kb1) cp_async4(slot + NROWS * PP::RS + (r * 2 + wi) * 4, a.w_scale + wa);
+        }
+      }
+    }
+    if (++c.ist == nst) {
+      c.ist = 0;
+      if (++c.isub == c.ix.nsub) {
+        c.isub = 0;
+        do {
+          ++c.iu;
+          if (c.iu < c.u_end) c.ix = load_unit(a, c.iu, row_tiles);
+        } while (c.iu < c.u_end && c.ix.nsub == 0);
+        if (c.iu < c.u_end) c.bind(a, rb, lane);
+      }
+    }
+  }
+  cp_async_commit();
+  ++c.issued;
+}
+
+template <int WF, int EPI>
+__global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm a) {
+  constexpr int NMAT = (EPI == EPI_SWIGLU) ? 2 : 1;
+  constexpr int NROWS = NMAT * kRows;
+  constexpr bool MX = (WF != WF_BF16);
+  constexpr bool ACT_E4M3 = (WF == WF_MXFP8);
   using F = Fmt<WF>;
   using W = typename F::W;
-  constexpr int U = F::kUnroll;
+  using PP = Pipe<WF>;
+  constexpr int SLOT = ring_slot_bytes<WF, NMAT>();
 
   extern __shared__ __align__(16) uint8_t smem[];
-  const Smem L = smem_layout(NMAT, a.Kin, ACT_SCALED);
-  uint8_t* wsc = smem + L.wsc;
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.xs);
-  uint8_t* xsc = smem + L.xsc;
+  const Smem L = smem_layout<WF>(NMAT, a.Kin);
   float* red = reinterpret_cast<float*>(smem + L.red);
-
-  const int row_tiles = a.Nout / kRows;
-  const int64_t blk = blockIdx.x / row_tiles;
-  const int rt = blockIdx.x - (int)(blk * row_tiles);
-  // sentinel / unused block slots leave before touching weights, scales or bias
-  if (blk * a.bm >= *a.ntpp) return;
-  const int64_t e = a.expert_ids[blk];
-  if (e < 0) return;
-  if (e >= a.E) {
-    if (threadIdx.x == 0 && blockIdx.x % row_tiles == 0) moe::set_status(a.status, MOE_ERR_INVALID_EXPERT);
-    return;
-  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
-  const int Kin = a.Kin, nkb = Kin / 32, S = xs_stride(Kin);
+  const int Kin = a.Kin, nkb = Kin / 32;
   const int kb0 = warp * nkb / kWarps, kb1 = (warp + 1) * nkb / kWarps, nb = kb1 - kb0;
+  const int nst = (nb + PP::D - 1) / PP::D;
   const int64_t rb = wrow_bytes<WF>(Kin);
-  const uint8_t* wbase = static_cast<const uint8_t*>(a.w);
+  uint8_t* ring = smem + L.ring + warp * L.ring_warp;
+  const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
 
-  auto wrow = [&](int m, int i) -> int64_t {  // matrix m (0 gate/main, 1 up), tile row i
-    return e * a.Nw + (m ? a.Nout : 0) + (int64_t)rt * kRows + i;
-  };
-  if (MX) {  // this warp's K slice of the block's weight scales
-    for (int idx = lane; idx < NMAT * kRows * nb; idx += 32) {
-      const int r = idx / nb, c = idx - r * nb;
-      wsc[r * nkb + kb0 + c] = a.w_scale[wrow(r / kRows, r % kRows) * nkb + kb0 + c];
-    }
-  }
-  const uint8_t* rowp[NMAT][2];
-#pragma unroll
-  for (int m = 0; m < NMAT; ++m) {
-    rowp[m][0] = wbase + wrow(m, g) * rb;
-    rowp[m][1] = wbase + wrow(m, g + 8) * rb;
-  }
+  // this block's run of live units
+  const int row_tiles = a.Nout / kRows;
+  const int64_t n_units = ((int64_t)*a.ntpp / a.bm) * row_tiles;
+  const int64_t per = (n_units + gridDim.x - 1) / gridDim.x;
+  const int64_t u_begin = blockIdx.x * per;
+  const int64_t u_end = u_begin + per < n_units ? u_begin + per : n_units;
+  if (u_begin >= u_end) return;
 
-  const int64_t slot0 = blk * a.bm;
+  Issuer<WF, NMAT> cur;
+  cur.iu = u_begin;
+  cur.u_end = u_end;
+  cur.ix = load_unit(a, cur.iu, row_tiles);
+  cur.isub = 0;
+  cur.ist = 0;
+  cur.issued = 0;
+  while (cur.ix.nsub == 0 && ++cur.iu < u_end) cur.ix = load_unit(a, cur.iu, row_tiles);
+  if (cur.iu < u_end) cur.bind(a, rb, lane);
+#pragma unroll 1
+  for (int s = 0; s < PP::R - 1; ++s) issue_next<WF, NMAT>(a, cur, ring_s, rb, kb0, kb1, nst, row_tiles, lane);
+
   bool bad = false;
-  for (int st = 0; st < a.bm; st += kTok) {
-    int pr = (int)a.P;
-    if (lane < kTok && st + lane < a.bm) pr = a.sorted[slot0 + st + lane];
-    int ptok[kTok];
+  uint32_t consumed = 0, red_buf = 0;
+  for (int64_t cu = u_begin; cu < u_end; ++cu) {
+    const Unit cx = load_unit(a, cu, row_tiles);
+    if (cx.nsub == 0) continue;
+    // scale-byte offsets of the rows this lane decodes (rows lane/D + (32/D) i)
+    uint32_t soff = 0;
+    if (MX) {
 #pragma unroll
-    for (int j = 0; j < kTok; ++j) ptok[j] = __shfl_sync(kFull, pr, j);
-    if (ptok[0] >= a.P) break;  // uniform over the block: all warps read the same slots
-
-    // stage this warp's K slice of the tile's activations as 16-bit values
-    __syncwarp();
-#pragma unroll
-    for (int j = 0; j < kTok; ++j) {
-      const bool valid = ptok[j] < a.P;
-      const int64_t arow = a.act_per_pair ? (int64_t)ptok[j] : (int64_t)(ptok[j] / a.k);
-      uint16_t* dst = xs + j * S + kb0 * 32;
-      for (int c = lane; c < nb * 4; c += 32) {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) {
-          if (WF == WF_MXFP8) {
-            const uint2 raw = *reinterpret_cast<const uint2*>(
-                static_cast<const uint8_t*>(a.act) + arow * Kin + kb0 * 32 + c * 8);
-            v.x = moe::e4m3x2_to_f16x2(raw.x & 0xffffu);
-            v.y = moe::e4m3x2_to_f16x2(raw.x >> 16);
-            v.z = moe::e4m3x2_to_f16x2(raw.y & 0xffffu);
-            v.w = moe::e4m3x2_to_f16x2(raw.y >> 16);
-          } else {
-            const uint4 raw = *reinterpret_cast<const uint4*>(
-                static_cast<const uint16_t*>(a.act) + arow * Kin + kb0 * 32 + c * 8);
-            if (WF == WF_BF16) {  // bf16 MMA operand
-              if (a.act_fmt == ACT_F16) {
-                v.x = moe::f16x2_to_bf16x2(raw.x);
-                v.y = moe::f16x2_to_bf16x2(raw.y);
-                v.z = moe::f16x2_to_bf16x2(raw.z);
-                v.w = moe::f16x2_to_bf16x2(raw.w);
-              } else {
-                v = raw;
-              }
-            } else {              // f16 MMA operand
-              if (a.act_fmt == ACT_F16) {
-                v = raw;
-              } else {
-                v.x = moe::bf16x2_to_f16x2(raw.x, &bad);
-                v.y = moe::bf16x2_to_f16x2(raw.y, &bad);
-                v.z = moe::bf16x2_to_f16x2(raw.z, &bad);
-                v.w = moe::bf16x2_to_f16x2(raw.w, &bad);
-              }
-            }
-          }
-        }
-        *reinterpret_cast<uint4*>(dst + c * 8) = v;
-      }
-      if (ACT_SCALED) {
-        for (int c = lane; c < nb; c += 32)
-          xsc[j * nkb + kb0 + c] = valid ? a.act_scale[arow * nkb + kb0 + c] : (uint8_t)127;
+      for (int i = 0; i < NROWS * PP::D / 32; ++i) {
+        const int r = lane / PP::D + (32 / PP::D) * i;
+        soff |= (uint32_t)((unit_row(a, cx, r) * nkb) & 3) << (8 * i);
       }
     }
-    __syncwarp();
+    for (int csub = 0; csub < cx.nsub; ++csub) {
+      const int64_t slot0 = cx.blk * a.bm + csub * kTok;
+      int pr = (int)a.P;
+      if (lane < kTok && csub * kTok + lane < a.bm) pr = a.sorted[slot0 + lane];
+      const int p0 = __shfl_sync(kFull, pr, 0);
+      int pg = __shfl_sync(kFull, pr, g);  // invalid token columns read token 0's row
+      if (pg >= a.P) pg = p0;
+      const int64_t arow = a.act_per_pair ? (int64_t)pg : (int64_t)(pg / a.k);
+      const uint16_t* act16 = static_cast<const uint16_t*>(a.act) + arow * Kin + q * 8;
+      const uint8_t* actq = static_cast<const uint8_t*>(a.act) + arow * Kin + q * 8;
+      int pc0 = __shfl_sync(kFull, pr, 2 * q), pc1 = __shfl_sync(kFull, pr, 2 * q + 1);
+      if (pc0 >= a.P) pc0 = p0;
+      if (pc1 >= a.P) pc1 = p0;
+      const int64_t crow0 = a.act_per_pair ? (int64_t)pc0 : (int64_t)(pc0 / a.k);
+      const int64_t crow1 = a.act_per_pair ? (int64_t)pc1 : (int64_t)(pc1 / a.k);
 
-    float acc[NMAT][4];
-#pragma unroll
-    for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
-
-    for (int kb = kb0; kb < kb1; kb += U) {
-      W wr[U][NMAT][2];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (kb + u < kb1) {
-#pragma unroll
-          for (int m = 0; m < NMAT; ++m) {
-            wr[u][m][0] = F::load(rowp[m][0], kb + u, q);
-            wr[u][m][1] = F::load(rowp[m][1], kb + u, q);
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int kk = kb + u;
-        if (kk < kb1) {
-          const uint4 xv = *reinterpret_cast<const uint4*>(xs + g * S + kk * 32 + q * 8);
-          float xsc0 = 1.f, xsc1 = 1.f;
-          if (ACT_SCALED) {
-            xsc0 = moe::e8m0_to_f32(xsc[(2 * q) * nkb + kk]);
-            xsc1 = moe::e8m0_to_f32(xsc[(2 * q + 1) * nkb + kk]);
-          }
-#pragma unroll
-          for (int m = 0; m < NMAT; ++m) {
-            uint32_t A[4];
-            if (MX) {
-              const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-              float t[4];
-              F::pairs(wr[u][m][0], 0, A[0], A[2]);
-              F::pairs(wr[u][m][1], 0, A[1], A[3]);
-              moe::mma_f16(t, A, xv.x, xv.y, zero);
-              F::pairs(wr[u][m][0], 1, A[0], A[2]);
-              F::pairs(wr[u][m][1], 1, A[1], A[3]);
-              moe::mma_f16(t, A, xv.z, xv.w, t);
-              const float s0 = moe::e8m0_to_f32(wsc[(m * kRows + g) * nkb + kk]);
-              const float s1 = moe::e8m0_to_f32(wsc[(m * kRows + g + 8) * nkb + kk]);
-              if (ACT_SCALED) {
-                acc[m][0] = fmaf(t[0] * s0, xsc0, acc[m][0]);
-                acc[m][1] = fmaf(t[1] * s0, xsc1, acc[m][1]);
-                acc[m][2] = fmaf(t[2] * s1, xsc0, acc[m][2]);
-                acc[m][3] = fmaf(t[3] * s1, xsc1, acc[m][3]);
-              } else {
-                acc[m][0] = fmaf(t[0], s0, acc[m][0]);
-                acc[m][1] = fmaf(t[1], s0, acc[m][1]);
-                acc[m][2] = fmaf(t[2], s1, acc[m][2]);
-                acc[m][3] = fmaf(t[3], s1, acc[m][3]);
-              }
-            } else {
-              F::pairs(wr[u][m][0], 0, A[0], A[2]);
-              F::pairs(wr[u][m][1], 0, A[1], A[3]);
-              moe::mma_bf16(acc[m], A, xv.x, xv.y, acc[m]);
-              F::pairs(wr[u][m][0], 1, A[0], A[2]);
-              F::pairs(wr[u][m][1], 1, A[1], A[3]);
-              moe::mma_bf16(acc[m], A, xv.z, xv.w, acc[m]);
-            }
-          }
-        }
-      }
-    }
-
-    // fixed-order sum over the four K quarters, then the epilogue (warp 0)
-#pragma unroll
-    for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) red[((warp * NMAT + m) * 4 + i) * 32 + lane] = acc[m][i];
-    __syncthreads();
-    if (warp == 0) {
-      float v[NMAT][4];
+      float acc[NMAT][4];
 #pragma unroll
       for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float s = red[((0 * NMAT + m) * 4 + i) * 32 + lane];
+        for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
+
+      for (int st = 0; st < nst; ++st) {
+        issue_next<WF, NMAT>(a, cur, ring_s, rb, kb0, kb1, nst, row_tiles, lane);
+        cp_async_wait<PP::R - 1>();
+        __syncwarp();
+        const uint8_t* slot = ring + (consumed % PP::R) * SLOT;
+        float* sf = reinterpret_cast<float*>(ring + (consumed % PP::R) * SLOT + NROWS * PP::RS + NROWS * 8);
+        const int kbs = kb0 + st * PP::D;
+        if (MX) {  // decode this stage's scale bytes (row r, block j) to floats
+          const uint32_t* words = reinterpret_cast<const uint32_t*>(slot + NROWS * PP::RS);
 #pragma unroll
-          for (int w = 1; w < kWarps; ++w) s += red[((w * NMAT + m) * 4 + i) * 32 + lane];
-          v[m][i] = s;
-        }
-      const int pc[2] = {__shfl_sync(kFull, pr, 2 * q), __shfl_sync(kFull, pr, 2 * q + 1)};
-      const uint16_t* bias = static_cast<const uint16_t*>(a.bias);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int p = pc[i & 1];
-        if (p >= a.P) continue;
-        const int n = rt * kRows + g + ((i >> 1) << 3);
-        if (EPI == EPI_SWIGLU) {
-          float gt = v[0][i], up = v[NMAT - 1][i];
-          if (bias) {
-            gt += moe::bf16_bits_to_f32(bias[e * a.Nw + n]);
-            up += moe::bf16_bits_to_f32(bias[e * a.Nw + a.Nout + n]);
+          for (int i = 0; i < NROWS * PP::D / 32; ++i) {
+            const int r = lane / PP::D + (32 / PP::D) * i, j = lane % PP::D;
+            const uint2 w2 = *reinterpret_cast<const uint2*>(words + 2 * r);
+            const uint32_t off = (((soff >> (8 * i)) & 3u) + (uint32_t)kbs) & 3u;
+            const uint32_t byte = __byte_perm(w2.x, w2.y, off + j) & 0xffu;
+            sf[r * PP::D + j] = e8m0_fast(byte);
           }
-          // h is kept as float16 (11-bit significand); an overflow is reported
-          const __half hv = __float2half_rn(moe::silu(gt) * up);
-          if (__hisinf(hv) || __hisnan(hv)) bad = true;
-          static_cast<__half*>(a.out)[(int64_t)p * a.Nout + n] = hv;
-        } else if (EPI == EPI_WEIGHTED_F32) {
-          float o = v[0][i];
-          if (bias) o += moe::bf16_bits_to_f32(bias[e * a.Nw + n]);
-          static_cast<float*>(a.out)[(int64_t)p * a.Nout + n] = o * a.topk_w[p];
-        } else {
-          float o = v[0][i];
-          if (bias) o += moe::bf16_bits_to_f32(bias[e * a.Nw + n]);
-          static_cast<uint16_t*>(a.out)[(int64_t)p * a.Nout + n] = moe::f32_to_bf16_bits(o);
+          __syncwarp();
+        }
+#pragma unroll
+        for (int j = 0; j < PP::D; ++j) {
+          const int kk = kbs + j;
+          if (kk < kb1) {
+            uint4 xv;
+            if (ACT_E4M3) {
+              const uint2 raw = *reinterpret_cast<const uint2*>(actq + kk * 32);
+              xv.x = moe::e4m3x2_to_f16x2(raw.x & 0xffffu);
+              xv.y = moe::e4m3x2_to_f16x2(raw.x >> 16);
+              xv.z = moe::e4m3x2_to_f16x2(raw.y & 0xffffu);
+              xv.w = moe::e4m3x2_to_f16x2(raw.y >> 16);
+            } else {
+              xv = *reinterpret_cast<const uint4*>(act16 + kk * 32);
+              if (MX && a.act_fmt == ACT_BF16) {  // bf16 activations for the f16 MMA
+                xv.x = moe::bf16x2_to_f16x2(xv.x, &bad);
+                xv.y = moe::bf16x2_to_f16x2(xv.y, &bad);
+                xv.z = moe::bf16x2_to_f16x2(xv.z, &bad);
+                xv.w = moe::bf16x2_to_f16x2(xv.w, &bad);
+              } else if (!MX && a.act_fmt == ACT_F16) {
+                xv.x = moe::f16x2_to_bf16x2(xv.x);
+                xv.y = moe::f16x2_to_bf16x2(xv.y);
+                xv.z = moe::f16x2_to_bf16x2(xv.z);
+                xv.w = moe::f16x2_to_bf16x2(xv.w);
+              }
+            }
+            float xs0 = 1.f, xs1 = 1.f;
+            if (ACT_E4M3) {
+              xs0 = moe::e8m0_to_f32(a.act_scale[crow0 * nkb + kk]);
+              xs1 = moe::e8m0_to_f32(a.act_scale[crow1 * nkb + kk]);
+            }
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) {
+              const uint8_t* r0 = slot + (m * kRows + g) * PP::RS + j * PP::BPB + q * (PP::BPB / 4);
+              const W w0 = F::lds(r0);
+              const W w1 = F::lds(r0 + 8 * PP::RS);
+              uint32_t A1[4], A2[4];
+              if constexpr (WF == WF_MXFP4) {
+                e2m1x8_to_f16(w0, A1[0], A1[2], A2[0], A2[2]);
+                e2m1x8_to_f16(w1, A1[1], A1[3], A2[1], A2[3]);
+              } else {
+                F::pairs(w0, 0, A1[0], A1[2]);
+                F::pairs(w1, 0, A1[1], A1[3]);
+                F::pairs(w0, 1, A2[0], A2[2]);
+                F::pairs(w1, 1, A2[1], A2[3]);
+              }
+              if (MX) {
+                const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+                float t[4];
+                moe::mma_f16(t, A1, xv.x, xv.y, zero);
+                moe::mma_f16(t, A2, xv.z, xv.w, t);
+                const float s0 = sf[(m * kRows + g) * PP::D + j];
+                const float s1 = sf[(m * kRows + g + 8) * PP::D + j];
+                if (ACT_E4M3) {
+                  acc[m][0] = fmaf(t[0] * s0, xs0, acc[m][0]);
+                  acc[m][1] = fmaf(t[1] * s0, xs1, acc[m][1]);
+                  acc[m][2] = fmaf(t[2] * s1, xs0, acc[m][2]);
+                  acc[m][3] = fmaf(t[3] * s1, xs1, acc[m][3]);
+                } else {
+                  acc[m][0] = fmaf(t[0], s0, acc[m][0]);
+                  acc[m][1] = fmaf(t[1], s0, acc[m][1]);
+                  acc[m][2] = fmaf(t[2], s1, acc[m][2]);
+                  acc[m][3] = fmaf(t[3], s1, acc[m][3]);
+                }
+              } else {
+                moe::mma_bf16(acc[m], A1, xv.x, xv.y, acc[m]);
+                moe::mma_bf16(acc[m], A2, xv.z, xv.w, acc[m]);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        ++consumed;
+      }
+
+      // fixed-order sum over the four K quarters (double-buffered partials), epilogue
+      float* rb_ = red + red_buf * (kWarps * NMAT * 4 * 32);
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rb_[((warp * NMAT + m) * 4 + i) * 32 + lane] = acc[m][i];
+      __syncthreads();
+      if (warp == 0) {
+        float v[NMAT][4];
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float s = rb_[((0 * NMAT + m) * 4 + i) * 32 + lane];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) s += rb_[((w * NMAT + m) * 4 + i) * 32 + lane];
+            v[m][i] = s;
+          }
+        const int pcol0 = __shfl_sync(kFull, pr, 2 * q), pcol1 = __shfl_sync(kFull, pr, 2 * q + 1);
+        const uint16_t* bias = static_cast<const uint16_t*>(a.bias);
+        const int64_t e = cx.e;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int p = (i & 1) ? pcol1 : pcol0;
+          if (p >= a.P) continue;
+          const int n = cx.rt * kRows + g + ((i >> 1) << 3);
+          if (EPI == EPI_SWIGLU) {
+            float gt = v[0][i], up = v[NMAT - 1][i];
+            if (bias) {
+              gt += moe::bf16_bits_to_f32(bias[e * a.Nw + n]);
+              up += moe::bf16_bits_to_f32(bias[e * a.Nw + a.Nout + n]);
+            }
+            const float hval = moe::silu(gt) * up;
+            if (MX) {  // f16 for the f16 MMA of GEMM2; an overflow is reported
+              const __half hv = __float2half_rn(hval);
+              if (__hisinf(hv) || __hisnan(hv)) bad = true;
+              static_cast<__half*>(a.out)[(int64_t)p * a.Nout + n] = hv;
+            } else {   // bf16 for the bf16 MMA of GEMM2
+              static_cast<uint16_t*>(a.out)[(int64_t)p * a.Nout + n] = moe::f32_to_bf16_bits(hval);
+            }
+          } else if (EPI == EPI_WEIGHTED_F32) {
+            float o = v[0][i];
+            if (bias) o += moe::bf16_bits_to_f32(bias[e * a.Nw + n]);
+            static_cast<float*>(a.out)[(int64_t)p * a.Nout + n] = o * a.topk_w[p];
+          } else {
+            float o = v[0][i];
+            if (bias) o += moe::bf16_bits_to_f32(bias[e * a.Nw + n]);
+            static_cast<uint16_t*>(a.out)[(int64_t)p * a.Nout + n] = moe::f32_to_bf16_bits(o);
+          }
         }
       }
+      red_buf ^= 1;
     }
-    __syncthreads();
   }
+  cp_async_wait<0>();
   if (bad) moe::set_status(a.status, MOE_ERR_RANGE);
 }
 
 template <int WF, int EPI>
 cudaError_t launch_t(const GroupedGemm& g, cudaStream_t stream) {
-  const Smem L = smem_layout(EPI == EPI_SWIGLU ? 2 : 1, g.Kin, WF == WF_MXFP8);
+  const Smem L = smem_layout<WF>(EPI == EPI_SWIGLU ? 2 : 1, g.Kin);
   cudaError_t err = cudaFuncSetAttribute(decode_gemm_kernel<WF, EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
-  const int64_t grid = g.grid_blocks * (g.Nout / kRows);
+  // enough resident blocks to keep every SM streaming; each owns a run of live units
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_gemm_kernel<WF, EPI>, kWarps * 32, L.total);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) per_sm = 1;
+  int64_t grid = (int64_t)sms * per_sm;
+  const int64_t units = g.grid_blocks * (g.Nout / kRows);
+  if (units < grid) grid = units;
   if (grid <= 0) return cudaSuccess;
   decode_gemm_kernel<WF, EPI><<<(unsigned)grid, kWarps * 32, L.total, stream>>>(g);
   return cudaGetLastError();
@@ -346,7 +532,10 @@ cudaError_t launch_t(const GroupedGemm& g, cudaStream_t stream) {
 namespace moe_launch {
 
 size_t decode_gemm_smem_bytes(const GroupedGemm& g) {
-  return smem_layout(g.epi == EPI_SWIGLU ? 2 : 1, g.Kin, g.wfmt == WF_MXFP8).total;
+  const int nmat = g.epi == EPI_SWIGLU ? 2 : 1;
+  if (g.wfmt == WF_MXFP4) return smem_layout<WF_MXFP4>(nmat, g.Kin).total;
+  if (g.wfmt == WF_MXFP8) return smem_layout<WF_MXFP8>(nmat, g.Kin).total;
+  return smem_layout<WF_BF16>(nmat, g.Kin).total;
 }
 
 cudaError_t decode_gemm(const GroupedGemm& g, cudaStream_t stream) {

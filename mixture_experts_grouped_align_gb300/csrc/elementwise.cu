@@ -65,9 +65,32 @@ __global__ void combine_kernel(const float4* __restrict__ o, int64_t T_real, int
   }
 }
 
+// y = f16(x) for bf16 x, 8 elements per thread; |x| > 65504 is reported.
+__global__ void bf16_to_f16_kernel(const uint4* __restrict__ x, uint4* __restrict__ y, int64_t n8,
+                                   int32_t* status) {
+  bool bad = false;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    uint4 v = __ldg(x + i);
+    v.x = moe::bf16x2_to_f16x2(v.x, &bad);
+    v.y = moe::bf16x2_to_f16x2(v.y, &bad);
+    v.z = moe::bf16x2_to_f16x2(v.z, &bad);
+    v.w = moe::bf16x2_to_f16x2(v.w, &bad);
+    y[i] = v;
+  }
+  if (bad) moe::set_status(status, MOE_ERR_RANGE);
+}
+
 }  // namespace
 
 namespace moe_launch {
+
+cudaError_t bf16_to_f16(const void* x, void* y, int64_t n, int32_t* status, cudaStream_t stream) {
+  const int64_t n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  bf16_to_f16_kernel<<<grid_for(n8, 256), 256, 0, stream>>>((const uint4*)x, (uint4*)y, n8, status);
+  return cudaGetLastError();
+}
 
 cudaError_t pad_rows(const void* src, void* dst, int64_t rows, int64_t rows_pad, int64_t row_bytes,
                      cudaStream_t stream) {

@@ -169,7 +169,7 @@ moe_status moe_bucket_pad(int64_t T, moe_quant quant, int64_t* T_pad, const void
 size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t I) {
   if (T_rows < 0 || k < 1 || K < 1 || I < 1) return 0;
   const int64_t P = T_rows * k;
-  return round256((size_t)P * I * 2) + round256((size_t)P * K * 4);
+  return round256((size_t)P * I * 2) + round256((size_t)P * K * 4) + round256((size_t)T_rows * K * 2);
 }
 
 moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_scale, int64_t T_rows,
@@ -208,6 +208,7 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
   uint8_t* ws = static_cast<uint8_t*>(ctx->workspace);
   void* h = ws;
   float* o = reinterpret_cast<float*>(ws + round256((size_t)P * I * 2));
+  void* x16 = ws + round256((size_t)P * I * 2) + round256((size_t)P * K * 4);
   cudaStream_t s = stream_of(ctx);
   const int wf = fp4 ? moe_launch::WF_MXFP4 : moe_launch::WF_BF16;
   const int64_t blocks = used_blocks_bound(P, E, block_m, cap_tokens);
@@ -216,7 +217,9 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
   g1.wfmt = wf;
   g1.epi = moe_launch::EPI_SWIGLU;
   g1.w = W->w1; g1.w_scale = W->w1_scale; g1.bias = W->b1;
-  g1.act = x; g1.act_fmt = moe_launch::ACT_BF16; g1.act_scale = nullptr; g1.act_per_pair = 0;
+  g1.act = fp4 ? x16 : x;  // the f16 MMA of the MXFP4 path reads x converted once to f16
+  g1.act_fmt = fp4 ? moe_launch::ACT_F16 : moe_launch::ACT_BF16;
+  g1.act_scale = nullptr; g1.act_per_pair = 0;
   g1.Nw = 2 * (int64_t)I; g1.Kin = K; g1.Nout = I; g1.k = k; g1.P = P; g1.E = E;
   g1.sorted = sorted_token_ids; g1.expert_ids = expert_ids; g1.ntpp = num_tokens_post_padded;
   g1.bm = block_m; g1.grid_blocks = blocks; g1.topk_w = topk_w; g1.out = h;
@@ -224,16 +227,20 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
   MOE_REQUIRE(moe_launch::decode_gemm_smem_bytes(g1) <= 227 * 1024, MOE_ERR_UNSUPPORTED,
               "K too large for the decode path");
   rec(ctx, 0, 4);
-  st = cuda_status(moe_launch::decode_gemm(g1, s), "moe_forward GEMM1");
+  if (fp4) {
+    st = cuda_status(moe_launch::bf16_to_f16(x, x16, T_rows * K, status_of(ctx), s), "moe_forward x");
+    if (st != MOE_OK) return st;
+  }
+  st = cuda_status(moe_launch::grouped_gemm(g1, T_rows, s), "moe_forward GEMM1");
   if (st != MOE_OK) return st;
   rec(ctx, 1, 4);
 
   moe_launch::GroupedGemm g2 = g1;
   g2.epi = moe_launch::EPI_WEIGHTED_F32;
   g2.w = W->w2; g2.w_scale = W->w2_scale; g2.bias = W->b2;
-  g2.act = h; g2.act_fmt = moe_launch::ACT_F16; g2.act_per_pair = 1;
+  g2.act = h; g2.act_fmt = fp4 ? moe_launch::ACT_F16 : moe_launch::ACT_BF16; g2.act_per_pair = 1;
   g2.Nw = K; g2.Kin = I; g2.Nout = K; g2.out = o;
-  st = cuda_status(moe_launch::decode_gemm(g2, s), "moe_forward GEMM2");
+  st = cuda_status(moe_launch::grouped_gemm(g2, T_rows, s), "moe_forward GEMM2");
   if (st != MOE_OK) return st;
   rec(ctx, 2, 4);
   st = cuda_status(moe_launch::combine(o, T_real, k, K, y, s), "moe_forward combine");
@@ -278,7 +285,7 @@ moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin, 
   MOE_REQUIRE(moe_launch::decode_gemm_smem_bytes(g) <= 227 * 1024, MOE_ERR_UNSUPPORTED,
               "Kin too large for the decode path");
   rec(ctx, 0, 2);
-  st = cuda_status(moe_launch::decode_gemm(g, stream_of(ctx)), "moe_grouped_gemm");
+  st = cuda_status(moe_launch::grouped_gemm(g, T, stream_of(ctx)), "moe_grouped_gemm");
   rec(ctx, 1, 2);
   return st;
 }

@@ -17,6 +17,7 @@ cudaError_t pad_rows(const void* src, void* dst, int64_t rows, int64_t rows_pad,
                      cudaStream_t stream);
 cudaError_t zero_f32(float* p, int64_t n, cudaStream_t stream);
 cudaError_t combine(const float* o, int64_t T_real, int k, int K, void* y, cudaStream_t stream);
+cudaError_t bf16_to_f16(const void* x, void* y, int64_t n, int32_t* status, cudaStream_t stream);
 
 // ---- grouped GEMMs on the weight-streaming (decode) path (decode_gemm.cu)
 enum WFmt { WF_BF16 = 0, WF_MXFP4 = 1, WF_MXFP8 = 2 };
@@ -50,6 +51,19 @@ struct GroupedGemm {
 };
 size_t decode_gemm_smem_bytes(const GroupedGemm& g);
 cudaError_t decode_gemm(const GroupedGemm& g, cudaStream_t stream);
+
+// ---- grouped GEMMs on the tensor-memory (prefill) path (prefill_gemm.cu)
+int prefill_tile_n(const GroupedGemm& g);
+bool prefill_supported(const GroupedGemm& g);
+cudaError_t prefill_gemm(const GroupedGemm& g, cudaStream_t stream);
+
+// Row counts above this bucket value use the tensor-memory path.  A bucket value (a
+// fixed point of the bucket map) keeps a batch and its bucket-padded copy on the same
+// side of the threshold, so both run the same kernel.
+constexpr int64_t kPrefillRowsAbove = 256;
+
+// Runs one grouped GEMM on the path its row count and shape select.
+cudaError_t grouped_gemm(const GroupedGemm& g, int64_t rows, cudaStream_t stream);
 
 // ---- weight gradient (wgrad.cu)
 struct Wgrad {

@@ -70,7 +70,7 @@ def test_workspace_size(lib):
     n = moe.moe_forward_workspace_size(64, 4, 2880, 2880)
     P = 256
     r = lambda v: (v + 255) // 256 * 256
-    assert n == r(P * 2880 * 2) + r(P * 2880 * 4)
+    assert n == r(P * 2880 * 2) + r(P * 2880 * 4) + r(64 * 2880 * 2)
     assert moe.moe_forward_workspace_size(-1, 4, 1, 1) == 0
 
 

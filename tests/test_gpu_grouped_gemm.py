@@ -54,11 +54,12 @@ def random_ids(rng, T, E, k, empty=()):
     return np.stack([rng.choice(allowed, k, replace=False) for _ in range(T)]).astype(np.int32)
 
 
+@pytest.mark.parametrize("T", [203, 600])   # weight-streaming path / tensor-memory path
 @pytest.mark.parametrize("per_pair", [False, True])
 @pytest.mark.parametrize("bias", [False, True])
-def test_mxfp8_small(moe, per_pair, bias):
+def test_mxfp8_small(moe, T, per_pair, bias):
     rng = np.random.default_rng(3)
-    T, E, k, N, Kin = 203, 12, 3, 96, 320
+    E, k, N, Kin = 12, 3, 96, 320
     ids = random_ids(rng, T, E, k, empty=(5,))
     rows = T * k if per_pair else T
     a_c, a_s = synth.mx_quantise_e4m3(rng.standard_normal((rows, Kin)).astype(np.float32))
@@ -72,10 +73,11 @@ def test_mxfp8_small(moe, per_pair, bias):
     assert_close_bf16(bf16_to_np(out), ref, what="mxfp8 small")
 
 
+@pytest.mark.parametrize("T", [77, 700])
 @pytest.mark.parametrize("quant", ["mxfp4", "bf16"])
-def test_w4a16_and_bf16_small(moe, quant):
+def test_w4a16_and_bf16_small(moe, T, quant):
     rng = np.random.default_rng(4)
-    T, E, k, N, Kin = 77, 9, 2, 48, 256
+    E, k, N, Kin = 9, 2, 64, 256
     ids = random_ids(rng, T, E, k)
     a = synth.to_bf16_bits(rng.standard_normal((T, Kin)))
     if quant == "mxfp4":
