@@ -186,6 +186,37 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
                        const int32_t* expert_offsets, int32_t block_m, int64_t cap_tokens,
                        void* y, const moe_ctx* ctx);
 
+/* Size of the fixed device scratch array used by moe_forward_no_alloc (8 MiB). */
+#define MOE_NO_ALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/* moe_forward without a caller workspace; the pages have no counterpart to this call.
+ *
+ * For callers that cannot call cudaMalloc: code embedded in a host program that owns
+ * every device allocation (it hands the plug-in its input and output buffers only), or
+ * threads that must not enter the CUDA allocator, which can synchronise the device and
+ * fail under memory pressure.  Arguments and results are exactly those of moe_forward;
+ * ctx->workspace and ctx->workspace_bytes are ignored.  The scratch (h, o and the f16
+ * copy of x) lives in a file-scope device array of MOE_NO_ALLOC_SCRATCH_BYTES inside
+ * the library; every GPU that loads the library holds it until the process exits.
+ *  - A call whose moe_forward_workspace_size exceeds the array returns MOE_ERR_CAPACITY
+ *    (e.g. the 64-token, 2880/2880, top-4 layer needs about 4.8 MB and fits).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call before any
+ *    stream capture.
+ *  - Every call shares the one array, which keeps the last call's contents.  Nothing in
+ *    it has to start at zero: each call writes every scratch element it reads.  Calls
+ *    that can overlap on the GPU (other streams, other host threads) race on the array:
+ *    serialise them.
+ *  - The call itself allocates no memory (no cudaMalloc, cudaFree or allocating library
+ *    routine). */
+moe_status moe_forward_no_alloc(const moe_weights* W, const void* x, const uint8_t* x_scale,
+                                int64_t T_rows, int64_t T_real, int32_t k,
+                                const float* topk_w, const int32_t* sorted_token_ids,
+                                const int32_t* expert_ids,
+                                const int32_t* num_tokens_post_padded,
+                                const int32_t* expert_offsets, int32_t block_m,
+                                int64_t cap_tokens, void* y, const moe_ctx* ctx);
+
 /* ------------------------------------------------------------------------------------ *
  * One grouped GEMM over all experts in a single launch ([AITER] Summary: moe_gemm_mxfp8) *
  * ------------------------------------------------------------------------------------ */

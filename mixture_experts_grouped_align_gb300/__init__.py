@@ -19,7 +19,7 @@ from .build import LIB, build  # noqa: F401
 __all__ = [
     "MoeError", "load", "Ctx", "QUANT", "moe_align_capacity", "moe_align", "moe_bucket",
     "moe_bucket_count", "moe_bucket_pad", "moe_forward_workspace_size", "moe_forward",
-    "moe_grouped_gemm", "moe_wgrad", "EXPORTED_SYMBOLS",
+    "moe_forward_no_alloc", "moe_grouped_gemm", "moe_wgrad", "EXPORTED_SYMBOLS",
 ]
 
 MOE_OK = 0
@@ -31,8 +31,8 @@ QUANT = {"bf16": 0, "mxfp4": 1, "mxfp8": 2}
 
 EXPORTED_SYMBOLS = [
     "moe_last_error", "moe_align_capacity", "moe_align", "moe_bucket", "moe_bucket_count",
-    "moe_bucket_pad", "moe_forward_workspace_size", "moe_forward", "moe_grouped_gemm",
-    "moe_wgrad",
+    "moe_bucket_pad", "moe_forward_workspace_size", "moe_forward", "moe_forward_no_alloc",
+    "moe_grouped_gemm", "moe_wgrad",
 ]
 
 
@@ -78,6 +78,7 @@ def load(path: str | None = None):
         "moe_bucket_pad": (I32, [I64, ctypes.c_int, P, P, P, I64, P, P, I32, P]),
         "moe_forward_workspace_size": (SZ, [I64, I32, I32, I32]),
         "moe_forward": (I32, [P, P, P, I64, I64, I32, P, P, P, P, P, I32, I64, P, P]),
+        "moe_forward_no_alloc": (I32, [P, P, P, I64, I64, I32, P, P, P, P, P, I32, I64, P, P]),
         "moe_grouped_gemm": (I32, [ctypes.c_int, I32, I32, I32, P, P, I32, P, P, P, I64, I32,
                                    P, P, P, I32, I64, P, P]),
         "moe_wgrad": (I32, [P, P, I32, I64, I32, I32, I32, I32, P, P, P, I32, I64, P, I32, P]),
@@ -184,6 +185,18 @@ def moe_forward(quant, E, K, I, w1, w1_scale, b1, w2, w2_scale, b2, x, x_scale, 
                                      _ptr(topk_w), _ptr(sorted_token_ids), _ptr(expert_ids),
                                      _ptr(num_tokens_post_padded), _ptr(expert_offsets), block_m,
                                      cap_tokens, _ptr(y), _ctx(ctx)))
+
+
+def moe_forward_no_alloc(quant, E, K, I, w1, w1_scale, b1, w2, w2_scale, b2, x, x_scale, T_rows,
+                         T_real, k, topk_w, sorted_token_ids, expert_ids, num_tokens_post_padded,
+                         expert_offsets, block_m, cap_tokens, y, ctx=None):
+    """moe_forward with its scratch in the library's fixed device array (no workspace)."""
+    q = QUANT[quant] if isinstance(quant, str) else quant
+    W = _Weights(q, E, K, I, _ptr(w1), _ptr(w1_scale), _ptr(b1), _ptr(w2), _ptr(w2_scale), _ptr(b2))
+    return _check(load().moe_forward_no_alloc(
+        ctypes.byref(W), _ptr(x), _ptr(x_scale), T_rows, T_real, k, _ptr(topk_w),
+        _ptr(sorted_token_ids), _ptr(expert_ids), _ptr(num_tokens_post_padded),
+        _ptr(expert_offsets), block_m, cap_tokens, _ptr(y), _ctx(ctx)))
 
 
 def moe_grouped_gemm(quant, E, N, Kin, a, a_scale, a_per_pair, w, w_scale, bias, T, k,
