@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_mxfp4",
-                    choices=["decode_mxfp4", "decode_bf16", "prefill_mxfp4", "tiny"])
+                    choices=["decode_mxfp4", "decode_bf16", "prefill_mxfp4", "tiny", "mxfp8_wgrad"])
     ap.add_argument("--m", type=int, default=28, help="tokens for decode_bf16")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the token count (smaller cases for profiling)")
@@ -53,8 +53,9 @@ def parse():
 
 
 DEFAULT_STEPS = {"decode_mxfp4": (2000, 50), "decode_bf16": (4000, 100),
-                 "prefill_mxfp4": (10, 3), "tiny": (4000, 100)}
-ORACLE_SAMPLE = {"decode_mxfp4": 8, "decode_bf16": 28, "prefill_mxfp4": 4, "tiny": 64}
+                 "prefill_mxfp4": (10, 3), "tiny": (4000, 100), "mxfp8_wgrad": (3, 3)}
+ORACLE_SAMPLE = {"decode_mxfp4": 8, "decode_bf16": 28, "prefill_mxfp4": 4, "tiny": 64,
+                 "mxfp8_wgrad": 512}
 
 
 def workload(name, m):
@@ -101,9 +102,42 @@ def src_hash(*names):
 
 # ------------------------------------------------------------------------------ oracle
 
+def oracle_sample_mxfp8(n_tok):
+    """The oracle on a bounded sample of the MXFP8 GEMM + wgrad workload: n_tok tokens of
+    top-8 routing over 2 experts' worth of freshly drawn weights (same shapes and
+    recipe), both grouped GEMMs and both weight gradients of those experts."""
+    import numpy as np
+    import synth
+    from oracle import formats, layer, wgrad
+    w = synth.MXFP8_WGRAD
+    rng = np.random.default_rng(4)
+    E, K, I, k = 2, w.K, w.I, 1
+    T = n_tok
+    ids = (np.arange(T) % E).astype(np.int32)[:, None]
+    xc, xs = synth.mx_quantise_e4m3(rng.standard_normal((T, K)).astype(np.float32))
+    ac, as_ = synth.mx_quantise_e4m3(rng.standard_normal((T, I)).astype(np.float32))
+    w1c, w1s = synth.mx_quantise_e4m3((rng.standard_normal((E, 2 * I, K)) * 0.02).astype(np.float32))
+    w2c, w2s = synth.mx_quantise_e4m3((rng.standard_normal((E, K, I)) * 0.02).astype(np.float32))
+    g1 = synth.to_bf16_bits(rng.standard_normal((T, 2 * I)).astype(np.float32))
+    g2 = synth.to_bf16_bits(rng.standard_normal((T, K)).astype(np.float32))
+    xb = synth.to_bf16_bits(rng.standard_normal((T, K)).astype(np.float32))
+    hb = synth.to_bf16_bits(rng.standard_normal((T, I)).astype(np.float32))
+    t0 = time.perf_counter()
+    A1 = formats.dequant_mxfp8(xc, xs)
+    A2 = formats.dequant_mxfp8(ac, as_)
+    layer.grouped_gemm(A1, ids, lambda e: (formats.dequant_mxfp8(w1c[e], w1s[e]), None), False)
+    layer.grouped_gemm(A2, ids, lambda e: (formats.dequant_mxfp8(w2c[e], w2s[e]), None), True)
+    wgrad.moe_wgrad(formats.bf16_decode(g1), formats.bf16_decode(xb), ids, E, False)
+    wgrad.moe_wgrad(formats.bf16_decode(g2), formats.bf16_decode(hb), ids, E, True)
+    # the full workload has 8 pairs per token
+    return time.perf_counter() - t0, T / 8.0
+
+
 def oracle_sample(name, m, n_tok):
     """Times the float64 oracle on the first n_tok tokens of the workload (this process
     was started with one BLAS / OpenMP thread).  Returns seconds."""
+    if name == "mxfp8_wgrad":
+        return oracle_sample_mxfp8(n_tok)
     import synth
     from oracle import formats, layer, route
     w = workload(name, m)
@@ -367,6 +401,146 @@ def bench_ours(args, rank, world, local_rank):
     return line
 
 
+def bench_mxfp8_wgrad(args, rank, world, local_rank):
+    """256 experts, hidden 7168, intermediate 2048, top-8, T=8192, Zipf routing: MXFP8
+    grouped GEMM1 (per token, K=7168 -> 4096) and GEMM2 (per pair, K=2048 -> 7168), then
+    the deterministic weight gradients dW1 [256, 4096, 7168] and dW2 [256, 7168, 2048]."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_grouped_align_gb300 as moe
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    moe.build()
+    moe.load()
+    steps, warmup = DEFAULT_STEPS["mxfp8_wgrad"]
+    steps = args.steps if args.steps is not None else steps
+    warmup = max(3, args.warmup if args.warmup is not None else warmup)
+    kw = {} if not args.tokens else {"T": args.tokens}
+    g = synth.make_mxfp8_gemm_wgrad(device=dev, **kw)
+    T, E, K, I, k, P = g["T"], g["E"], g["K"], g["I"], g["k"], g["P"]
+    bm = 128
+    cap, capb = moe.moe_align_capacity(P, E, bm)
+    ids = torch.from_numpy(g["topk_ids"]).to(dev)
+    srt = torch.empty(cap, dtype=torch.int32, device=dev)
+    eid = torch.empty(capb, dtype=torch.int32, device=dev)
+    ntpp = torch.empty(4, dtype=torch.int32, device=dev)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+    moe.moe_align(None, ids, None, T, k, E, bm, srt, cap, eid, ntpp, None, moe.Ctx(dev_status=status))
+    out1 = torch.empty((P, 2 * I), dtype=torch.bfloat16, device=dev)
+    out2 = torch.empty((P, K), dtype=torch.bfloat16, device=dev)
+    dW1 = torch.empty((E, 2 * I, K), dtype=torch.float32, device=dev)
+    dW2 = torch.empty((E, K, I), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def ev():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        return e
+
+    def step(evs=None):
+        c = [moe.Ctx(dev_status=status, events=None if evs is None else evs[i]) for i in range(4)]
+        moe.moe_grouped_gemm("mxfp8", E, 2 * I, K, g["x_codes"], g["x_scale"], 0, g["w1"], g["w1_scale"],
+                             None, T, k, srt, eid, ntpp, bm, cap, out1, c[0])
+        moe.moe_grouped_gemm("mxfp8", E, K, I, g["a2_codes"], g["a2_scale"], 1, g["w2"], g["w2_scale"],
+                             None, T, k, srt, eid, ntpp, bm, cap, out2, c[1])
+        moe.moe_wgrad(g["grad1"], g["x_bf16"], 0, T, k, E, 2 * I, K, srt, eid, ntpp, bm, cap, dW1, 0, c[2])
+        moe.moe_wgrad(g["grad2"], g["h_bf16"], 1, T, k, E, K, I, srt, eid, ntpp, bm, cap, dW2, 0, c[3])
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status[0]) != 0:
+        raise RuntimeError(f"device status {int(status[0])}")
+    evs = [[[ev(), ev()] for _ in range(4)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ck = clocks.stop(local_rank)
+    ms = t0.elapsed_time(t1)
+    kms = [sum(e[j][0].elapsed_time(e[j][1]) for e in evs) / steps for j in range(4)]
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    # end to end: the step's activations and output gradients from pinned host memory,
+    # the GEMM outputs back to the host; weights and dW stay resident
+    ins = ["x_codes", "x_scale", "a2_codes", "a2_scale", "grad1", "grad2", "x_bf16", "h_bf16"]
+    host = {n: torch.empty_like(g[n], device="cpu").pin_memory() for n in ins}
+    for n in ins:
+        host[n].copy_(g[n].cpu())
+    o1h = torch.empty_like(out1, device="cpu").pin_memory()
+    o2h = torch.empty_like(out2, device="cpu").pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(steps, 3))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for n in ins:
+            g[n].copy_(host[n], non_blocking=True)
+        step()
+        o1h.copy_(out1, non_blocking=True)
+        o2h.copy_(out2, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if rank != 0:
+        return None
+    hbm, bf16, src = peaks()
+    f_gemm1 = 2.0 * P * K * 2 * I
+    f_gemm2 = 2.0 * P * I * K
+    names = ["gemm1_mxfp8", "gemm2_mxfp8", "wgrad_dW1", "wgrad_dW2"]
+    dw_bytes = [None, None, E * 2 * I * K * 4 + P * 2 * I * 2 + T * K * 2, E * K * I * 4 + P * K * 2 + P * I * 2]
+    dom = int(np.argmax(kms))
+    if dom >= 2:
+        achieved = dw_bytes[dom] / (kms[dom] * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": f"wgrad ({names[dom]})", "achieved": achieved, "peak": hbm,
+                    "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                    "algorithmic_bytes": dw_bytes[dom], "peak_source": f"{src} (hbm_gbs)"}
+    else:
+        fl = f_gemm1 if dom == 0 else f_gemm2
+        achieved = fl / (kms[dom] * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": f"prefill_gemm ({names[dom]})", "achieved": achieved,
+                    "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16, "traffic": None,
+                    "algorithmic_flops": fl, "peak_source": f"{src} (bf16_tflops; f16 operands)"}
+    h2d = sum(host[n].numel() * host[n].element_size() for n in ins)
+    line = {
+        "metric": METRIC, "value": world * T * steps / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16/bf16 tcgen05 mma -> f32",
+        "data": "synthetic (seeded inputs drawn on the device, random-init weights)",
+        "config": {"workload": f"mxfp8_wgrad: T={T} tokens, hidden {K}, intermediate {I}, {E} experts, "
+                               f"top-{k}, Zipf(1.1) routing, MXFP8 GEMM1+GEMM2, dW1+dW2 fp32",
+                   "T": T, "experts": E, "hidden": K, "intermediate": I, "top_k": k, "block_m": bm,
+                   "l2": "inputs larger than L2: 11.3 GB of MXFP8 weights and 45 GB of dW per step",
+                   "parallelism": f"replicas x{world}"},
+        "useful_tflops": world * 2 * (f_gemm1 + f_gemm2) * steps / (ms * 1e-3) / 1e12,
+        "kernel_ms": dict(zip(names, kms)),
+        "roofline": roofline,
+        "e2e": {"value": world * T * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out1.numel() * 2 + out2.numel() * 2,
+                "steps": e2e_steps},
+        "gpu_launches": steps * 4,
+        "clocks": ck,
+    }
+    return line
+
+
 def launches_per_step(w, rows):
     n = 3  # GEMM1, GEMM2, combine
     n += 1  # align (routing fused for rows <= 512)
@@ -383,9 +557,15 @@ def cpu_baseline(args):
     name = args.workload
     n = args.sample_tokens or ORACLE_SAMPLE[name]
     r = run_oracle_subprocess(name, args.m, n)
+    if name == "mxfp8_wgrad":
+        what = (f"float64 oracle: both MXFP8 grouped GEMMs and both weight gradients for {n} "
+                f"token-expert pairs of 2 experts ({r['tokens']:g} tokens at top-8; "
+                f"{r['seconds']:.1f} s, one thread)")
+    else:
+        what = (f"float64 oracle on the first {r['tokens']} tokens of the workload "
+                f"({r['seconds']:.1f} s, one thread)")
     return {"value": r["tokens"] / r["seconds"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"float64 oracle on the first {r['tokens']} tokens of the workload "
-                      f"({r['seconds']:.1f} s, one thread)"}
+            "sample": what}
 
 
 def main():
@@ -405,7 +585,10 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    line = bench_ours(args, rank, world, local_rank)
+    if args.workload == "mxfp8_wgrad":
+        line = bench_mxfp8_wgrad(args, rank, world, local_rank)
+    else:
+        line = bench_ours(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
             try:

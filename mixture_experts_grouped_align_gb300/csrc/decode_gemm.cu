@@ -134,10 +134,18 @@ struct Unit {
   int rt, nsub;
 };
 
-__device__ __forceinline__ Unit load_unit(const GroupedGemm& a, int64_t u, int row_tiles) {
+// Unit u; the block's expert and sub-tile count are reused from `prev` when it is in the
+// same block (consecutive units mostly are), so the alignment arrays are read once per block.
+__device__ __forceinline__ Unit load_unit(const GroupedGemm& a, int64_t u, int row_tiles,
+                                          const Unit& prev) {
   Unit x;
   x.blk = u / row_tiles;
   x.rt = (int)(u - x.blk * row_tiles);
+  if (x.blk == prev.blk) {
+    x.e = prev.e;
+    x.nsub = prev.nsub;
+    return x;
+  }
   x.e = a.expert_ids[x.blk];
   // real pairs form a prefix of every block: count them, 8 tokens per sub-tile
   int cnt = 0;
@@ -153,16 +161,6 @@ __device__ __forceinline__ Unit load_unit(const GroupedGemm& a, int64_t u, int r
 
 __device__ __forceinline__ int64_t unit_row(const GroupedGemm& a, const Unit& x, int r) {
   return x.e * a.Nw + ((r >= kRows) ? a.Nout : 0) + (int64_t)x.rt * kRows + (r & (kRows - 1));
-}
-
-// Two E2M1 codes per byte of w -> four f16x2 (exact hardware conversions).
-__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t& o2,
-                                              uint32_t& o3) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
-      : "r"(w));
 }
 
 // E8M0 byte -> float bits: 2^(s-127); 0x00 -> 2^-127 (subnormal), 0xFF -> NaN.
@@ -260,7 +258,7 @@ __device__ __forceinline__ void issue_next(const GroupedGemm& a, Issuer<WF, NMAT
         c.isub = 0;
         do {
           ++c.iu;
-          if (c.iu < c.u_end) c.ix = load_unit(a, c.iu, row_tiles);
+          if (c.iu < c.u_end) c.ix = load_unit(a, c.iu, row_tiles, c.ix);
         } while (c.iu < c.u_end && c.ix.nsub == 0);
         if (c.iu < c.u_end) c.bind(a, rb, lane);
       }
@@ -305,19 +303,25 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
   Issuer<WF, NMAT> cur;
   cur.iu = u_begin;
   cur.u_end = u_end;
-  cur.ix = load_unit(a, cur.iu, row_tiles);
+  Unit none;
+  none.blk = -1;
+  none.e = -1;
+  none.rt = 0;
+  none.nsub = 0;
+  cur.ix = load_unit(a, cur.iu, row_tiles, none);
   cur.isub = 0;
   cur.ist = 0;
   cur.issued = 0;
-  while (cur.ix.nsub == 0 && ++cur.iu < u_end) cur.ix = load_unit(a, cur.iu, row_tiles);
+  while (cur.ix.nsub == 0 && ++cur.iu < u_end) cur.ix = load_unit(a, cur.iu, row_tiles, cur.ix);
   if (cur.iu < u_end) cur.bind(a, rb, lane);
 #pragma unroll 1
   for (int s = 0; s < PP::R - 1; ++s) issue_next<WF, NMAT>(a, cur, ring_s, rb, kb0, kb1, nst, row_tiles, lane);
 
   bool bad = false;
   uint32_t consumed = 0, red_buf = 0;
+  Unit cx = none;
   for (int64_t cu = u_begin; cu < u_end; ++cu) {
-    const Unit cx = load_unit(a, cu, row_tiles);
+    cx = load_unit(a, cu, row_tiles, cx);
     if (cx.nsub == 0) continue;
     // scale-byte offsets of the rows this lane decodes (rows lane/D + (32/D) i)
     uint32_t soff = 0;
@@ -406,8 +410,8 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
               const W w1 = F::lds(r0 + 8 * PP::RS);
               uint32_t A1[4], A2[4];
               if constexpr (WF == WF_MXFP4) {
-                e2m1x8_to_f16(w0, A1[0], A1[2], A2[0], A2[2]);
-                e2m1x8_to_f16(w1, A1[1], A1[3], A2[1], A2[3]);
+                moe::e2m1x8_to_f16x2(w0, A1[0], A1[2], A2[0], A2[2]);
+                moe::e2m1x8_to_f16x2(w1, A1[1], A1[3], A2[1], A2[3]);
               } else {
                 F::pairs(w0, 0, A1[0], A1[2]);
                 F::pairs(w1, 0, A1[1], A1[3]);

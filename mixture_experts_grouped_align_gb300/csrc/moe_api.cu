@@ -316,7 +316,7 @@ moe_status moe_wgrad(const void* grad, const void* input, int32_t input_per_pair
   g.grad = grad; g.input = input; g.input_per_pair = input_per_pair ? 1 : 0;
   g.P = P; g.k = k; g.E = E; g.N = N; g.Kin = Kin;
   g.sorted = sorted_token_ids; g.expert_ids = expert_ids; g.ntpp = num_tokens_post_padded;
-  g.bm = block_m; g.cap_blocks = cap_blocks; g.dW = dW; g.mode = mode;
+  g.bm = block_m; g.cap_blocks = cap_blocks; g.dW = dW; g.mode = mode; g.status = status_of(ctx);
   rec(ctx, 0, 2);
   st = cuda_status(moe_launch::wgrad(g, stream_of(ctx)), "moe_wgrad");
   rec(ctx, 1, 2);

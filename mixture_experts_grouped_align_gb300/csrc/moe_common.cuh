@@ -33,6 +33,24 @@ MOE_DEV uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   return out;
 }
 
+// Eight E2M1 codes (two per byte, low nibble first) -> four f16x2, exact (hardware
+// conversions; the byte unpack costs nothing extra).
+MOE_DEV void e2m1x8_to_f16x2(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t& o2, uint32_t& o3) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+      : "r"(w));
+}
+
+// Four E4M3 codes -> two f16x2, exact.
+MOE_DEV void e4m3x4_to_f16x2(uint32_t w, uint32_t& o0, uint32_t& o1) {
+  asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, h0;\n\tcvt.rn.f16x2.e4m3x2 %1, h1;\n\t}"
+      : "=r"(o0), "=r"(o1)
+      : "r"(w));
+}
+
 // Two E4M3 codes (low byte = first element) -> f16x2, exact (hardware conversion).
 MOE_DEV uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   uint32_t out;

@@ -79,7 +79,12 @@ struct Wgrad {
   int64_t cap_blocks;
   float* dW;
   int mode;
+  int32_t* status;
 };
 cudaError_t wgrad(const Wgrad& g, cudaStream_t stream);
+
+// ---- weight gradient on the tensor-memory path (wgrad_tc.cu)
+int wgrad_tc_tile(const Wgrad& g);
+cudaError_t wgrad_tc(const Wgrad& g, cudaStream_t stream);
 
 }  // namespace moe_launch

@@ -43,23 +43,35 @@ constexpr int kTmemCols = 512;
 constexpr int kSmemLimit = 227 * 1024;
 
 struct PLayout {
-  int a, b, braw, araw, slot, nslots, bars, total;
+  // raw ring: what the producers copy (the f16 A tile in its final layout, or raw E4M3
+  // A) plus the raw weight bytes; decoded ring: the decoded B tile (and decoded A).
+  int raw_a, raw_b, raw_slot, nraw;
+  int dec_b, dec_a, dec_slot, ndec;
+  int raw_base, dec_base, bars, total;
 };
 
-// Per-slot shared layout (bytes): A tile 128 x 128 B | B tile BN x 128 B | raw weight
-// bytes of the stage | raw E4M3 activation bytes (MXFP8 A only).
+constexpr int kLag = 3;  // stages between a stage's copies and its decode (nraw >= kLag + 1)
+
 __host__ __device__ inline PLayout playout(int wf, bool a_e4m3, int BN) {
   PLayout L;
-  L.a = 0;
-  L.b = kBM * 128;
-  L.braw = L.b + BN * 128;
-  const int braw_bytes = (wf == WF_MXFP4) ? BN * 32 : BN * 64;
-  L.araw = L.braw + braw_bytes;
-  const int araw_bytes = a_e4m3 ? kBM * 64 : 0;
-  L.slot = ((L.araw + araw_bytes) + 1023) / 1024 * 1024;
-  int n = (kSmemLimit - 1024 - 256) / L.slot;
-  L.nslots = n > 4 ? 4 : n;
-  L.bars = L.nslots * L.slot;
+  const int braw_row = (wf == WF_MXFP4) ? 32 : 64;
+  L.raw_a = 0;
+  L.raw_b = a_e4m3 ? kBM * 64 : kBM * 128;
+  L.raw_slot = ((L.raw_b + BN * braw_row) + 1023) / 1024 * 1024;
+  L.dec_b = 0;
+  L.dec_a = BN * 128;
+  L.dec_slot = ((L.dec_a + (a_e4m3 ? kBM * 128 : 0)) + 1023) / 1024 * 1024;
+  const int budget = kSmemLimit - 1024 - 256;
+  L.ndec = 3;
+  L.nraw = (budget - L.ndec * L.dec_slot) / L.raw_slot;
+  if (L.nraw < kLag + 1) {
+    L.ndec = 2;
+    L.nraw = (budget - L.ndec * L.dec_slot) / L.raw_slot;
+  }
+  if (L.nraw > 8) L.nraw = 8;
+  L.dec_base = 0;
+  L.raw_base = L.ndec * L.dec_slot;
+  L.bars = L.raw_base + L.nraw * L.raw_slot;
   L.total = L.bars + 256 + 1024;  // barriers, TMEM address, flags; 1024 B alignment slack
   return L;
 }
@@ -84,41 +96,44 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t v, __half2 s) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Decodes one (row, 32-element half-stage) unit of raw MX weight bytes in shared memory
-// into 4 f16 chunks of the swizzled B (or A) tile.
+// f16x2 holding 2^(s-127) in both halves (exact for the scales the f16 path accepts).
+__device__ __forceinline__ __half2 scale_h2(uint32_t scale_byte) {
+  return __float2half2_rn(moe::e8m0_to_f32(scale_byte));
+}
+
+// Decodes one (row, 32-element half-stage) unit of raw MX bytes in shared memory into
+// the 4 f16 chunks of the swizzled tile whose byte offsets (within the slot) are dst[].
 template <int FMT>
-__device__ __forceinline__ void dequant_unit(const uint8_t* raw, uint8_t* tile, int row, int half,
+__device__ __forceinline__ void dequant_unit(const uint8_t* raw, uint8_t* slot, const uint32_t (&dst)[4],
                                              uint32_t scale_byte, bool& bad) {
   const int se = (int)scale_byte - 127;
-  const float sf = moe::e8m0_to_f32(scale_byte);
-  const __half2 s2 = __float2half2_rn(sf);
-  uint32_t out[16];
-  uint32_t any = 0;
+  const __half2 s2 = scale_h2(scale_byte);
   if (FMT == WF_MXFP4) {
     const uint4 w = *reinterpret_cast<const uint4*>(raw);
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-    any = w.x | w.y | w.z | w.w;
+    if ((w.x | w.y | w.z | w.w) && (se < -23 || se > 13)) bad = true;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) out[i * 4 + b] = hmul2_u32(moe::e2m1x2_to_f16x2((ws[i] >> (8 * b)) & 0xffu), s2);
-    if (any && (se < -23 || se > 13)) bad = true;
+    for (int q = 0; q < 4; ++q) {  // chunk q = elements 8q..8q+7 = raw word q
+      uint32_t o0, o1, o2, o3;
+      moe::e2m1x8_to_f16x2(ws[q], o0, o1, o2, o3);
+      *reinterpret_cast<uint4*>(slot + dst[q]) =
+          make_uint4(hmul2_u32(o0, s2), hmul2_u32(o1, s2), hmul2_u32(o2, s2), hmul2_u32(o3, s2));
+    }
   } else {
     const uint4 w0 = *reinterpret_cast<const uint4*>(raw);
     const uint4 w1 = *reinterpret_cast<const uint4*>(raw + 16);
     const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    any = w0.x | w0.y | w0.z | w0.w | w1.x | w1.y | w1.z | w1.w;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      out[i * 2] = hmul2_u32(moe::e4m3x2_to_f16x2(ws[i] & 0xffffu), s2);
-      out[i * 2 + 1] = hmul2_u32(moe::e4m3x2_to_f16x2(ws[i] >> 16), s2);
-    }
+    const uint32_t any = w0.x | w0.y | w0.z | w0.w | w1.x | w1.y | w1.z | w1.w;
     if ((any & 0x7f7f7f7fu) && (se < -15 || se > 7)) bad = true;
-  }
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
-    *reinterpret_cast<uint4*>(tile + tc::sw128_offset(row, half * 4 + q)) =
-        make_uint4(out[q * 4], out[q * 4 + 1], out[q * 4 + 2], out[q * 4 + 3]);
+    for (int q = 0; q < 4; ++q) {  // chunk q = elements 8q..8q+7 = raw words 2q, 2q+1
+      uint32_t o0, o1, o2, o3;
+      moe::e4m3x4_to_f16x2(ws[2 * q], o0, o1);
+      moe::e4m3x4_to_f16x2(ws[2 * q + 1], o2, o3);
+      *reinterpret_cast<uint4*>(slot + dst[q]) =
+          make_uint4(hmul2_u32(o0, s2), hmul2_u32(o1, s2), hmul2_u32(o2, s2), hmul2_u32(o3, s2));
+    }
+  }
 }
 
 // Tile index -> (block slot, N tile); false for a tile no role works on.
@@ -137,10 +152,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(PArgs pa) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const PLayout L = playout(WF, A_E4M3, pa.BN);
-  const int S = L.nslots;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* empty = full + 4;
-  uint64_t* tfull = empty + 4;
+  const int NR = L.nraw, ND = L.ndec;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);  // [ND] decoded stage ready
+  uint64_t* dec_empty = full + 3;                                // [ND]
+  uint64_t* raw_empty = dec_empty + 3;                           // [NR]
+  uint64_t* tfull = raw_empty + 8;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* taddr_s = reinterpret_cast<uint32_t*>(drain + 1);
@@ -148,10 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(PArgs pa) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < ND; ++s) {
       tc::mbar_init(&full[s], kNumProd / 32);
-      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&dec_empty[s], 1);
     }
+    for (int s = 0; s < NR; ++s) tc::mbar_init(&raw_empty[s], 1);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&tfull[i], 1);
       tc::mbar_init(&tempty[i], 4);
@@ -176,146 +193,155 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(PArgs pa) {
 
   if (warp >= 8) {
     // ------------------------------------------------------------------ producers
+    // Each thread owns fixed pieces of every stage: A chunks (rows pt/8 + 32i, chunk
+    // pt%8) for f16 activations, or the A decode unit (row pt/2, half pt%2) for E4M3
+    // activations, and the B decode units u = pt + 256i (row u/2, half u%2).  Stage s is
+    // copied into raw slot s % NR and decoded kLag stages later into decoded slot s % ND,
+    // so kLag stages of copies are in flight while the MMA works on decoded stages.
     const int pt = tid - kProd0;
     const int64_t rb = (WF == WF_MXFP4) ? Kin / 2 : Kin;  // raw weight row bytes
-    const int braw_row = (WF == WF_MXFP4) ? 32 : 64;     // raw bytes per row per stage
+    constexpr int kBrawRow = (WF == WF_MXFP4) ? 32 : 64;   // raw bytes per row per stage
+    constexpr int kBrawHalf = kBrawRow / 2;
     const uint8_t* wbase = static_cast<const uint8_t*>(a.w);
+    uint32_t a_off[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a_off[i] = L.raw_a + tc::sw128_offset((pt >> 3) + 32 * i, pt & 7);
+    const int ra = pt >> 1, ha = pt & 1;  // E4M3 A decode unit
+    uint32_t a_dst[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) a_dst[q] = L.dec_a + tc::sw128_offset(ra, ha * 4 + q);
+    const uint32_t a_raw = L.raw_a + ra * 64 + ha * 32;
+    uint32_t b_dst[2][4], b_raw[2];
+    bool bvalid[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int u = pt + 256 * i, r = u >> 1, h = u & 1;
+      bvalid[i] = r < BN;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) b_dst[i][q] = L.dec_b + tc::sw128_offset(r, h * 4 + q);
+      b_raw[i] = L.raw_b + r * kBrawRow + h * kBrawHalf;
+    }
+    // stages whose copies are in flight, oldest first
+    uint32_t pend_st[kLag];
+    uint32_t pend_sb[kLag][2], pend_sa[kLag];
+    bool pend_va[kLag];
+    int npend = 0;
     uint32_t it = 0;
-    bool pending = false;
-    int prev_slot = 0;
-    uint32_t sc_b[2] = {0, 0}, sc_a = 0;  // scale bytes of the pending stage
-    bool va = false;                      // the pending stage's A unit row is a real pair
+    auto finish_oldest = [&]() {  // decode + hand over pend[0], shift the queue
+      const uint32_t d = pend_st[0];
+      const int ds = d % ND;
+      if (!tc::mbar_wait(&dec_empty[ds], ((d / ND) & 1) ^ 1)) {
+        moe::set_status(a.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      const uint8_t* rs = smem + L.raw_base + (d % NR) * L.raw_slot;
+      uint8_t* dst = smem + L.dec_base + ds * L.dec_slot;
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        if (bvalid[i]) dequant_unit<WF>(rs + b_raw[i], dst, b_dst[i], pend_sb[0][i], bad);
+      if (A_E4M3 && pend_va[0]) dequant_unit<WF_MXFP8>(rs + a_raw, dst, a_dst, pend_sa[0], bad);
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&full[ds]);
+#pragma unroll
+      for (int j = 0; j + 1 < kLag; ++j) {
+        pend_st[j] = pend_st[j + 1];
+        pend_sb[j][0] = pend_sb[j + 1][0];
+        pend_sb[j][1] = pend_sb[j + 1][1];
+        pend_sa[j] = pend_sa[j + 1];
+        pend_va[j] = pend_va[j + 1];
+      }
+      --npend;
+    };
     for (int64_t t = blockIdx.x; t < pa.tiles && !*abort_flag; t += gridDim.x) {
       int64_t blk, e;
       int nt;
       if (!tile_info(pa, t, ntpp, blk, nt, e)) continue;
-      // this thread's 4 A rows (f16 A) / its A unit row (E4M3 A)
-      int64_t arow[4];
-      bool avalid[4];
+      // global pointers of this tile
+      const uint16_t* aptr[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int r = (pt >> 3) + 32 * i;
-        const int p = a.sorted[blk * a.bm + r];
-        avalid[i] = p < a.P;
-        arow[i] = avalid[i] ? (a.act_per_pair ? (int64_t)p : (int64_t)(p / a.k)) : 0;
+        const int p = A_E4M3 ? (int)a.P : a.sorted[blk * a.bm + (pt >> 3) + 32 * i];
+        aptr[i] = nullptr;
+        if (p < a.P) {
+          const int64_t ar = a.act_per_pair ? (int64_t)p : (int64_t)(p / a.k);
+          aptr[i] = static_cast<const uint16_t*>(a.act) + ar * Kin + (pt & 7) * 8;
+        }
       }
-      // B units (row, half): unit u = pt + 256 * i, row = u >> 1, half = u & 1
-      int64_t brow[2];
-      bool bvalid[2];
+      const uint8_t* a8 = nullptr;   // E4M3 A unit row
+      const uint8_t* as8 = nullptr;  // its scale row
+      if (A_E4M3) {
+        const int p = a.sorted[blk * a.bm + ra];
+        if (p < a.P) {
+          const int64_t ar = a.act_per_pair ? (int64_t)p : (int64_t)(p / a.k);
+          a8 = static_cast<const uint8_t*>(a.act) + ar * Kin + ha * 32;
+          as8 = a.act_scale + ar * nkb + ha;
+        }
+      }
+      const uint8_t* bptr[2];
+      const uint8_t* sptr[2];
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        const int u = pt + 256 * i;
-        const int r = u >> 1;
-        bvalid[i] = r < BN;
+        const int u = pt + 256 * i, r = u >> 1, h = u & 1;
         int64_t n;
         if (EPI == EPI_SWIGLU)
           n = (r < pa.half) ? (int64_t)nt * pa.half + r : (int64_t)a.Nout + (int64_t)nt * pa.half + (r - pa.half);
         else
           n = (int64_t)nt * BN + r;
-        brow[i] = e * a.Nw + n;
+        const int64_t brow = e * a.Nw + n;
+        bptr[i] = wbase + brow * rb + h * kBrawHalf;
+        sptr[i] = a.w_scale + brow * nkb + h;
       }
-      for (int kc = 0; kc < nk; ++kc) {
-        const int slot = it % S;
-        if (!tc::mbar_wait(&empty[slot], ((it / S) & 1) ^ 1)) {
+      for (int kc = 0; kc < nk && !*abort_flag; ++kc) {
+        const int rsl = it % NR;
+        if (!tc::mbar_wait(&raw_empty[rsl], ((it / NR) & 1) ^ 1)) {
           moe::set_status(a.status, MOE_ERR_TIMEOUT);
           *abort_flag = 1;
           break;
         }
-        const uint32_t sl_s = smem_s + slot * L.slot;
-        // A rows
+        const uint32_t sl_s = smem_s + L.raw_base + rsl * L.raw_slot;
         if (!A_E4M3) {
-          const uint16_t* act = static_cast<const uint16_t*>(a.act);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = (pt >> 3) + 32 * i, c = pt & 7;
-            if (avalid[i])
-              cp_async16(sl_s + L.a + tc::sw128_offset(r, c), act + arow[i] * Kin + kc * kBK + c * 8);
-          }
-        } else {
-          // raw A of this thread's own decode unit (row pt/2, half pt%2): 32 B, so that
-          // the thread that decodes the bytes is the one whose cp.async wait covers them
-          const uint8_t* act = static_cast<const uint8_t*>(a.act);
-          const int r = pt >> 1, h = pt & 1;
-          const int p = a.sorted[blk * a.bm + r];
-          if (p < a.P) {
-            const int64_t ar = a.act_per_pair ? (int64_t)p : (int64_t)(p / a.k);
-            const uint8_t* src = act + ar * Kin + kc * kBK + h * 32;
-            cp_async16(sl_s + L.araw + r * 64 + h * 32, src);
-            cp_async16(sl_s + L.araw + r * 64 + h * 32 + 16, src + 16);
-          }
+          for (int i = 0; i < 4; ++i)
+            if (aptr[i]) cp_async16(sl_s + a_off[i], aptr[i] + kc * kBK);
+        } else if (a8) {
+          // raw A of this thread's own decode unit: the thread that decodes the bytes is
+          // the one whose cp.async wait covers them
+          cp_async16(sl_s + a_raw, a8 + kc * kBK);
+          cp_async16(sl_s + a_raw + 16, a8 + kc * kBK + 16);
         }
-        // raw B bytes of this thread's own decode units (row u/2, half u%2)
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int u = pt + 256 * i;
-          const int r = u >> 1, h = u & 1;
-          if (r < BN) {
-            const uint8_t* src = wbase + brow[i] * rb + (int64_t)kc * braw_row + h * (braw_row / 2);
-            const uint32_t dst = sl_s + L.braw + r * braw_row + h * (braw_row / 2);
-            cp_async16(dst, src);
-            if (braw_row / 2 > 16) cp_async16(dst + 16, src + 16);
+        for (int i = 0; i < 2; ++i) {  // raw B bytes of this thread's own decode units
+          if (bvalid[i]) {
+            cp_async16(sl_s + b_raw[i], bptr[i] + (int64_t)kc * kBrawRow);
+            if (kBrawHalf > 16) cp_async16(sl_s + b_raw[i] + 16, bptr[i] + (int64_t)kc * kBrawRow + 16);
           }
         }
         cp_async_commit();
-        // scale bytes of this stage (used one iteration later)
-        uint32_t nsc_b[2] = {0, 0}, nsc_a = 0;
-        bool nva = false;
+        uint32_t nsc_b[2] = {0, 0}, nsc_a = 0;  // scale bytes, used when the stage is decoded
 #pragma unroll
         for (int i = 0; i < 2; ++i)
-          if (bvalid[i]) nsc_b[i] = a.w_scale[brow[i] * nkb + 2 * kc + ((pt + 256 * i) & 1)];
-        if (A_E4M3) {
-          const int r = pt >> 1, h = pt & 1;
-          const int p = a.sorted[blk * a.bm + r];
-          if (p < a.P) {
-            const int64_t ar = a.act_per_pair ? (int64_t)p : (int64_t)(p / a.k);
-            nsc_a = a.act_scale[ar * nkb + 2 * kc + h];
-            nva = true;
-          }
+          if (bvalid[i]) nsc_b[i] = sptr[i][2 * kc];
+        if (A_E4M3 && as8) nsc_a = as8[2 * kc];
+        if (npend == kLag) {  // the oldest stage's copies have landed: decode, hand over
+          cp_async_wait<kLag>();
+          finish_oldest();
         }
-        if (pending) {  // decode the previous stage, then hand it to the MMA
-          cp_async_wait<1>();
-          uint8_t* ps = smem + prev_slot * L.slot;
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int u = pt + 256 * i;
-            const int r = u >> 1, h = u & 1;
-            if (r < BN) dequant_unit<WF>(ps + L.braw + r * braw_row + h * (braw_row / 2), ps + L.b, r, h, sc_b[i], bad);
+        for (int j = 0; j < kLag; ++j)
+          if (j == npend) {
+            pend_st[j] = it;
+            pend_sb[j][0] = nsc_b[0];
+            pend_sb[j][1] = nsc_b[1];
+            pend_sa[j] = nsc_a;
+            pend_va[j] = A_E4M3 && (a8 != nullptr);
           }
-          if (A_E4M3 && va) {
-            const int r = pt >> 1, h = pt & 1;
-            dequant_unit<WF_MXFP8>(ps + L.araw + r * 64 + h * 32, ps + L.a, r, h, sc_a, bad);
-          }
-          tc::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&full[prev_slot]);
-        }
-        va = nva;
-        pending = true;
-        prev_slot = slot;
-        sc_b[0] = nsc_b[0];
-        sc_b[1] = nsc_b[1];
-        sc_a = nsc_a;
+        ++npend;
         ++it;
       }
     }
-    if (pending) {
-      cp_async_wait<0>();
-      uint8_t* ps = smem + prev_slot * L.slot;
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int u = pt + 256 * i;
-        const int r = u >> 1, h = u & 1;
-        if (r < BN) dequant_unit<WF>(ps + L.braw + r * braw_row + h * (braw_row / 2), ps + L.b, r, h, sc_b[i], bad);
-      }
-      if (A_E4M3 && va) {
-        const int r = pt >> 1, h = pt & 1;
-        dequant_unit<WF_MXFP8>(ps + L.araw + r * 64 + h * 32, ps + L.a, r, h, sc_a, bad);
-      }
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&full[prev_slot]);
-    }
     cp_async_wait<0>();
+    while (npend > 0) finish_oldest();
   } else if (warp == 0) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -335,21 +361,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(PArgs pa) {
         const uint32_t d_tmem = taddr + acc * 256;
         bool ok = true;
         for (int kc = 0; kc < nk; ++kc) {
-          const int slot = it % S;
-          if (!tc::mbar_wait(&full[slot], (it / S) & 1)) {
+          const int ds = it % ND, rsl = it % NR;
+          if (!tc::mbar_wait(&full[ds], (it / ND) & 1)) {
             moe::set_status(a.status, MOE_ERR_TIMEOUT);
             *abort_flag = 1;
             ok = false;
             break;
           }
           tc::tc_fence_after();
-          const uint32_t a_s = smem_s + slot * L.slot + L.a;
-          const uint32_t b_s = smem_s + slot * L.slot + L.b;
+          const uint32_t dec_s = smem_s + L.dec_base + ds * L.dec_slot;
+          const uint32_t a_s = A_E4M3 ? dec_s + L.dec_a : smem_s + L.raw_base + rsl * L.raw_slot + L.raw_a;
+          const uint32_t b_s = dec_s + L.dec_b;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             tc::mma_f16_ss(d_tmem, tc::sdesc_sw128(a_s + kk * 32), tc::sdesc_sw128(b_s + kk * 32), idesc,
                            (kc | kk) != 0);
-          tc::mma_commit(&empty[slot]);
+          tc::mma_commit(&raw_empty[rsl]);
+          tc::mma_commit(&dec_empty[ds]);
           ++it;
         }
         if (!ok) break;

@@ -46,13 +46,11 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return bi == INT_MAX || v > bv || (v == bv && i < bi);
 }
 
-// One warp routes one token: k rounds of a warp arg-max over the unchosen logits, then
-// float64 softmax over the chosen ones.  The float64 sum follows numpy's order for a
-// short vector (a running sum below 8 terms, eight interleaved partial sums from 8 on)
-// so that both sides round the same float64 value to float32.
-__device__ void route_token(const float* __restrict__ row, int E, int k,
-                            int32_t* __restrict__ ids_out, float* __restrict__ w_out,
-                            int lane) {
+// One warp selects one token's top-k: k rounds of a warp arg-max over the unchosen
+// logits.  Lane j < k writes the j-th id and, for now, the chosen logit itself into the
+// weight slot (the softmax replaces it).
+__device__ void select_topk(const float* __restrict__ row, int E, int k,
+                            int32_t* __restrict__ ids_out, float* __restrict__ w_out, int lane) {
   uint32_t taken = 0;  // bit i <=> entry lane + 32*i already chosen (E <= 1024)
   float my_val = 0.f;
   int my_idx = 0;
@@ -76,37 +74,58 @@ __device__ void route_token(const float* __restrict__ row, int E, int k,
     if ((bidx & 31) == lane) taken |= 1u << (bidx >> 5);
     if (lane == j) { my_val = best; my_idx = bidx; }
   }
-  const double m = (double)__shfl_sync(kFull, my_val, 0);
-  const double ex = lane < k ? exp((double)my_val - m) : 0.0;
+  if (lane < k) {
+    ids_out[lane] = my_idx;
+    w_out[lane] = my_val;
+  }
+}
+
+// One lane turns one token's k chosen logits (descending, in w[0..k)) into routing
+// weights: softmax over them in float64, rounded to float32.  The float64 sum follows
+// numpy's order for a short vector (a running sum below 8 terms, eight interleaved
+// partial sums from 8 on) so that both sides round the same float64 value.  A lane per
+// token keeps the (slow) float64 work on all 32 lanes of each instruction.
+__device__ void softmax_topk(float* __restrict__ w, int k) {
+  const double m = (double)w[0];
+  double ex[32];
+  for (int j = 0; j < k; ++j) ex[j] = exp((double)w[j] - m);
   double s;
   if (k < 8) {
     s = 0.0;
-    for (int j = 0; j < k; ++j) s += __shfl_sync(kFull, ex, j);
+    for (int j = 0; j < k; ++j) s += ex[j];
   } else {
     double r[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) r[i] = __shfl_sync(kFull, ex, i);
+    for (int i = 0; i < 8; ++i) r[i] = ex[i];
     int j = 8;
-    for (; j + 8 <= k; j += 8) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) r[i] += __shfl_sync(kFull, ex, j + i);
-    }
+    for (; j + 8 <= k; j += 8)
+      for (int i = 0; i < 8; ++i) r[i] += ex[j + i];
     s = ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
-    for (; j < k; ++j) s += __shfl_sync(kFull, ex, j);
+    for (; j < k; ++j) s += ex[j];
   }
-  if (lane < k) {
-    ids_out[lane] = my_idx;
-    w_out[lane] = __double2float_rn(ex / s);
+  for (int j = 0; j < k; ++j) w[j] = __double2float_rn(ex[j] / s);
+}
+
+// Routes tokens t0 .. t0 + n - 1 (n <= blockDim.x) with the whole thread block: a warp
+// per token selects the top-k, then (after a block barrier) a thread per token computes
+// its softmax, so both phases use every warp of the block.
+__device__ void route_block(const float* __restrict__ logits, int64_t t0, int n, int E, int k,
+                            int32_t* __restrict__ ids, float* __restrict__ w) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int i = warp; i < n; i += nw) {
+    const int64_t t = t0 + i;
+    select_topk(logits + t * E, E, k, ids + t * k, w + t * k, lane);
   }
+  __syncthreads();
+  if ((int)threadIdx.x < n) softmax_topk(w + (t0 + threadIdx.x) * k, k);
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int64_t T,
                                                     int E, int k, int32_t* __restrict__ ids,
                                                     float* __restrict__ w) {
-  const int lane = threadIdx.x & 31;
-  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  route_token(logits + t * E, E, k, ids + t * k, w + t * k, lane);
+  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x;
+  const int n = (int)((T - t0) < (int64_t)blockDim.x ? (T - t0) : (int64_t)blockDim.x);
+  route_block(logits, t0, n, E, k, ids, w);
 }
 
 // Exclusive scan of v over threads 0..n-1 of the block (n <= 1024); returns the total.
@@ -146,10 +165,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(AlignArgs a) {
   int* scratch = cnt + E;                 // [32 + 2]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  if (a.route_here) {
-    for (int64_t t = warp; t < a.T; t += kAlignWarps)
-      route_token(a.logits + t * E, E, k, a.ids + t * k, a.w + t * k, lane);
-  }
+  if (a.route_here) route_block(a.logits, 0, (int)a.T, E, k, a.ids, a.w);  // T <= 512
   for (int i = tid; i < kAlignWarps * E; i += kAlignThreads) hist[i] = 0;
   __syncthreads();
 
@@ -262,9 +278,9 @@ cudaError_t align(const float* logits, int32_t* ids, float* w, int64_t T, int k,
     if (T <= kFuseT) {
       a.route_here = 1;
     } else {
-      const int warps = 8;
-      route_kernel<<<(unsigned)((T + warps - 1) / warps), warps * 32, 0, stream>>>(logits, T, E, k,
-                                                                                 ids, w);
+      const int64_t tok_per_block = 256;  // 8 warps; 32 tokens per warp, a thread per token
+      route_kernel<<<(unsigned)((T + tok_per_block - 1) / tok_per_block), 256, 0, stream>>>(
+          logits, T, E, k, ids, w);
       cudaError_t err = cudaGetLastError();
       if (err != cudaSuccess) return err;
     }

@@ -111,6 +111,19 @@ MOE_DEV uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
+// Descriptor of an MN-major operand tile in 128-byte swizzle atoms (64 MN elements x 8
+// K rows, 1024 B each): leading byte offset = distance between atoms along MN, stride
+// byte offset = distance between 8-row groups along K.
+MOE_DEV uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma.kind::f16: f32 accumulator, A and B both f16
 // (ab_fmt 0) or both bf16 (ab_fmt 1), both K-major, N >> 3 in bits 17-22, M >> 4 in bits
 // 24-28.

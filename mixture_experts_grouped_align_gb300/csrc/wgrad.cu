@@ -171,6 +171,7 @@ namespace moe_launch {
 
 cudaError_t wgrad(const Wgrad& g, cudaStream_t stream) {
   dim3 block(kThreads);
+  if (g.mode == 0 && wgrad_tc_tile(g) > 0) return wgrad_tc(g, stream);
   if (g.mode == 0) {
     dim3 grid(g.Kin / kTN, g.N / kTM, g.E);
     wgrad_kernel<false><<<grid, block, 0, stream>>>(g);

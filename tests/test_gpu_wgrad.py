@@ -64,9 +64,10 @@ def test_wgrad_small(moe, mode, per_pair, bm):
     assert np.all(dW[E - 1] == 0)                   # empty expert written as zeros
 
 
-def test_wgrad_deterministic_repeatable_and_constant(moe):
+@pytest.mark.parametrize("N,Kin", [(64, 64), (128, 320)])   # mma.sync path / tcgen05 path
+def test_wgrad_deterministic_repeatable_and_constant(moe, N, Kin):
     rng = np.random.default_rng(8)
-    T, E, k, N, Kin = 500, 8, 2, 64, 64
+    T, E, k = 500, 8, 2
     ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
     g = dev(synth.to_bf16_bits(rng.standard_normal((T * k, N))))
     x = dev(synth.to_bf16_bits(rng.standard_normal((T, Kin))))
@@ -82,10 +83,11 @@ def test_wgrad_deterministic_repeatable_and_constant(moe):
         assert np.all(c[e] == cnt[e] * -1.5)
 
 
-def test_wgrad_sentinel_rows_never_read(moe):
+@pytest.mark.parametrize("N", [64, 128])
+def test_wgrad_sentinel_rows_never_read(moe, N):
     """NaN rows directly after grad and input: sentinel slots must not touch them."""
     rng = np.random.default_rng(9)
-    T, E, k, N, Kin = 40, 5, 2, 64, 128
+    T, E, k, Kin = 40, 5, 2, 128
     ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
     g = torch.full((T * k + 64, N), float("nan"), dtype=torch.bfloat16, device="cuda")
     x = torch.full((T + 64, Kin), float("nan"), dtype=torch.bfloat16, device="cuda")
