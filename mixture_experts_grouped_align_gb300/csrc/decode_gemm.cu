@@ -38,8 +38,9 @@ constexpr unsigned kFull = 0xffffffffu;
 
 // Weight streaming: each warp copies its K quarter of the block's weight rows through a
 // ring of R shared-memory stages with cp.async (16-byte chunks, no register cost for
-// the bytes in flight); stage = D scale blocks of every row.  Row stride RS is padded so
-// that the lanes' shared loads of one block hit 32 distinct banks.
+// the bytes in flight); stage = D scale blocks of every row, plus the same K range of
+// the tile's token rows.  Row strides are padded so that the lanes' shared loads of one
+// block hit distinct banks.
 template <int WF>
 struct Pipe;
 template <>
@@ -52,7 +53,7 @@ struct Pipe<WF_MXFP8> {  // 32 B per block; lane reads 8 B
 };
 template <>
 struct Pipe<WF_BF16> {   // 64 B per block; lane reads 16 B
-  static constexpr int BPB = 64, D = 2, R = 4, RS = 192;
+  static constexpr int BPB = 64, D = 2, R = 3, RS = 192;
 };
 
 struct Smem {
@@ -60,15 +61,31 @@ struct Smem {
   int ring_warp, sw;          // bytes of one warp's ring; floats per scale row
 };
 
+// Token rows in a ring slot: D blocks of 32 activations (E4M3 for MXFP8 weights, else 16
+// bits), row stride padded by 16 bytes.
+template <int WF>
+__host__ __device__ constexpr int act_block_bytes() { return WF == WF_MXFP8 ? 32 : 64; }
+template <int WF>
+__host__ __device__ constexpr int act_row_stride() { return Pipe<WF>::D * act_block_bytes<WF>() + 16; }
+
+// One ring slot: weight rows | 2 scale words per row | decoded scales (D per row) | token rows.
+__host__ __device__ constexpr int slot_bytes(int WF, int nrows, int RS, int D) {
+  return nrows * RS + ((WF != WF_BF16) ? nrows * 2 * 4 + nrows * D * 4 : 0);
+}
+template <int WF>
+__host__ __device__ constexpr int act_offset(int nmat) {
+  return slot_bytes(WF, nmat * kRows, Pipe<WF>::RS, Pipe<WF>::D);
+}
+template <int WF>
+__host__ __device__ constexpr int ring_slot_total(int nmat) {
+  return act_offset<WF>(nmat) + kTok * act_row_stride<WF>();
+}
+
 template <int WF>
 __host__ __device__ inline Smem smem_layout(int nmat, int Kin) {
   using PP = Pipe<WF>;
   Smem s;
-  const int nrows = nmat * kRows;
-  const bool mx = (WF != WF_BF16);
-  // one ring slot: weight rows | 2 scale words per row | decoded scales (D per row)
-  const int slot = nrows * PP::RS + (mx ? nrows * 2 * 4 + nrows * PP::D * 4 : 0);
-  s.ring_warp = PP::R * slot;
+  s.ring_warp = PP::R * ring_slot_total<WF>(nmat);
   s.sw = 0;
   (void)Kin;
   int off = 0;
@@ -197,20 +214,32 @@ struct Lane<WF_BF16> {   // rows lane/8 + 4i, block (lane%8)/4, 16-byte quarter 
 
 template <int WF, int NMAT>
 __host__ __device__ constexpr int ring_slot_bytes() {
-  constexpr int NROWS = NMAT * kRows;
-  return NROWS * Pipe<WF>::RS + ((WF != WF_BF16) ? NROWS * 2 * 4 + NROWS * Pipe<WF>::D * 4 : 0);
+  return ring_slot_total<WF>(NMAT);
 }
+
+// Token-row copies of one stage: chunk c = lane + 32 i is token c / (D * CPB), block
+// (c / CPB) % D, 16-byte piece c % CPB of that block.
+template <int WF>
+struct ActCopy {
+  static constexpr int CPB = act_block_bytes<WF>() / 16;
+  static constexpr int PER_TOK = Pipe<WF>::D * CPB;
+  static constexpr int N = (kTok * PER_TOK + 31) / 32;  // chunks per lane
+};
 
 // Issue side of the ring: the unit being copied and this lane's row addresses in it.
 template <int WF, int NMAT>
 struct Issuer {
   static constexpr int NPL = Lane<WF>::NPL * NMAT / 2;  // rows per lane (chunks / 32)
+  static constexpr int NACT = ActCopy<WF>::N;
   int64_t iu, u_end;
   Unit ix;
   int isub, ist;
   uint32_t issued;
   const uint8_t* wrow[NPL];   // weight row start of this lane's rows
   int64_t srow[2];            // scale row offsets of this lane's two scale words (MX)
+  const uint8_t* arow[NACT];  // token row start (plus block / piece offset) of this lane's chunks
+  int64_t act_blk;            // (block, sub-tile) the token rows were bound for
+  int act_sub;
 
   __device__ __forceinline__ void bind(const GroupedGemm& a, int64_t rb, int lane) {
     const uint8_t* wb = static_cast<const uint8_t*>(a.w);
@@ -220,6 +249,31 @@ struct Issuer {
 #pragma unroll
     for (int i = 0; i < 2; ++i) srow[i] = unit_row(a, ix, (lane >> 1) + 16 * i) * nkb;
   }
+
+  // Token rows of sub-tile isub of the current unit's block (read once per block and
+  // sub-tile: consecutive units of a block share them).
+  __device__ __forceinline__ void bind_act(const GroupedGemm& a, int lane) {
+    if (ix.blk == act_blk && isub == act_sub) return;
+    act_blk = ix.blk;
+    act_sub = isub;
+    using AC = ActCopy<WF>;
+    const int s = isub * kTok + lane;
+    int p = (int)a.P;
+    if (lane < kTok && s < a.bm) p = a.sorted[ix.blk * a.bm + s];
+    const int64_t abytes = (WF == WF_MXFP8) ? 1 : 2;
+#pragma unroll
+    for (int i = 0; i < NACT; ++i) {
+      const int c = lane + 32 * i;
+      const int t = c / AC::PER_TOK, rem = c % AC::PER_TOK;
+      const int pt = __shfl_sync(0xffffffffu, p, t & (kTok - 1));
+      arow[i] = nullptr;
+      if (t < kTok && pt < a.P) {
+        const int64_t r = a.act_per_pair ? (int64_t)pt : (int64_t)(pt / a.k);
+        arow[i] = static_cast<const uint8_t*>(a.act) + r * a.Kin * abytes +
+                  (rem / AC::CPB) * act_block_bytes<WF>() + (rem % AC::CPB) * 16;
+      }
+    }
+  }
 };
 
 template <int WF, int NMAT>
@@ -228,9 +282,11 @@ __device__ __forceinline__ void issue_next(const GroupedGemm& a, Issuer<WF, NMAT
                                            int lane) {
   using PP = Pipe<WF>;
   using LN = Lane<WF>;
+  using AC = ActCopy<WF>;
   constexpr int NROWS = NMAT * kRows;
   constexpr bool MX = (WF != WF_BF16);
   constexpr int SLOT = ring_slot_bytes<WF, NMAT>();
+  constexpr int AOFF = act_offset<WF>(NMAT);
   if (c.iu < c.u_end) {
     const int kbs = kb0 + c.ist * PP::D;
     const uint32_t slot = ring_s + (c.issued % PP::R) * SLOT;
@@ -252,6 +308,15 @@ __device__ __forceinline__ void issue_next(const GroupedGemm& a, Issuer<WF, NMAT
         }
       }
     }
+#pragma unroll
+    for (int i = 0; i < Issuer<WF, NMAT>::NACT; ++i) {  // this stage's K range of the token rows
+      const int ci = lane + 32 * i;
+      const int t = ci / AC::PER_TOK, rem = ci % AC::PER_TOK;
+      if (c.arow[i] != nullptr && kbs + rem / AC::CPB < kb1)
+        cp_async16(slot + AOFF + t * act_row_stride<WF>() + (rem / AC::CPB) * act_block_bytes<WF>() +
+                       (rem % AC::CPB) * 16,
+                   c.arow[i] + (int64_t)kbs * act_block_bytes<WF>());
+    }
     if (++c.ist == nst) {
       c.ist = 0;
       if (++c.isub == c.ix.nsub) {
@@ -262,6 +327,7 @@ __device__ __forceinline__ void issue_next(const GroupedGemm& a, Issuer<WF, NMAT
         } while (c.iu < c.u_end && c.ix.nsub == 0);
         if (c.iu < c.u_end) c.bind(a, rb, lane);
       }
+      if (c.iu < c.u_end) c.bind_act(a, lane);
     }
   }
   cp_async_commit();
@@ -278,6 +344,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
   using W = typename F::W;
   using PP = Pipe<WF>;
   constexpr int SLOT = ring_slot_bytes<WF, NMAT>();
+  constexpr int AOFF = act_offset<WF>(NMAT);
 
   extern __shared__ __align__(16) uint8_t smem[];
   const Smem L = smem_layout<WF>(NMAT, a.Kin);
@@ -312,8 +379,13 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
   cur.isub = 0;
   cur.ist = 0;
   cur.issued = 0;
+  cur.act_blk = -1;
+  cur.act_sub = 0;
   while (cur.ix.nsub == 0 && ++cur.iu < u_end) cur.ix = load_unit(a, cur.iu, row_tiles, cur.ix);
-  if (cur.iu < u_end) cur.bind(a, rb, lane);
+  if (cur.iu < u_end) {
+    cur.bind(a, rb, lane);
+    cur.bind_act(a, lane);
+  }
 #pragma unroll 1
   for (int s = 0; s < PP::R - 1; ++s) issue_next<WF, NMAT>(a, cur, ring_s, rb, kb0, kb1, nst, row_tiles, lane);
 
@@ -337,11 +409,10 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
       int pr = (int)a.P;
       if (lane < kTok && csub * kTok + lane < a.bm) pr = a.sorted[slot0 + lane];
       const int p0 = __shfl_sync(kFull, pr, 0);
-      int pg = __shfl_sync(kFull, pr, g);  // invalid token columns read token 0's row
-      if (pg >= a.P) pg = p0;
-      const int64_t arow = a.act_per_pair ? (int64_t)pg : (int64_t)(pg / a.k);
-      const uint16_t* act16 = static_cast<const uint16_t*>(a.act) + arow * Kin + q * 8;
-      const uint8_t* actq = static_cast<const uint8_t*>(a.act) + arow * Kin + q * 8;
+      // token column g: its row is in the ring when valid; an invalid column holds stale
+      // bytes, which only reach that column's outputs (never stored, never flagged)
+      const bool gvalid = __shfl_sync(kFull, pr, g) < a.P;
+      bool xbad = false;
       int pc0 = __shfl_sync(kFull, pr, 2 * q), pc1 = __shfl_sync(kFull, pr, 2 * q + 1);
       if (pc0 >= a.P) pc0 = p0;
       if (pc1 >= a.P) pc1 = p0;
@@ -361,6 +432,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
         const uint8_t* slot = ring + (consumed % PP::R) * SLOT;
         float* sf = reinterpret_cast<float*>(ring + (consumed % PP::R) * SLOT + NROWS * PP::RS + NROWS * 8);
         const int kbs = kb0 + st * PP::D;
+        const uint8_t* xs = slot + AOFF + g * act_row_stride<WF>() + q * (act_block_bytes<WF>() / 4);
         if (MX) {  // decode this stage's scale bytes (row r, block j) to floats
           const uint32_t* words = reinterpret_cast<const uint32_t*>(slot + NROWS * PP::RS);
 #pragma unroll
@@ -379,18 +451,18 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
           if (kk < kb1) {
             uint4 xv;
             if (ACT_E4M3) {
-              const uint2 raw = *reinterpret_cast<const uint2*>(actq + kk * 32);
+              const uint2 raw = *reinterpret_cast<const uint2*>(xs + j * act_block_bytes<WF>());
               xv.x = moe::e4m3x2_to_f16x2(raw.x & 0xffffu);
               xv.y = moe::e4m3x2_to_f16x2(raw.x >> 16);
               xv.z = moe::e4m3x2_to_f16x2(raw.y & 0xffffu);
               xv.w = moe::e4m3x2_to_f16x2(raw.y >> 16);
             } else {
-              xv = *reinterpret_cast<const uint4*>(act16 + kk * 32);
+              xv = *reinterpret_cast<const uint4*>(xs + j * act_block_bytes<WF>());
               if (MX && a.act_fmt == ACT_BF16) {  // bf16 activations for the f16 MMA
-                xv.x = moe::bf16x2_to_f16x2(xv.x, &bad);
-                xv.y = moe::bf16x2_to_f16x2(xv.y, &bad);
-                xv.z = moe::bf16x2_to_f16x2(xv.z, &bad);
-                xv.w = moe::bf16x2_to_f16x2(xv.w, &bad);
+                xv.x = moe::bf16x2_to_f16x2(xv.x, &xbad);
+                xv.y = moe::bf16x2_to_f16x2(xv.y, &xbad);
+                xv.z = moe::bf16x2_to_f16x2(xv.z, &xbad);
+                xv.w = moe::bf16x2_to_f16x2(xv.w, &xbad);
               } else if (!MX && a.act_fmt == ACT_F16) {
                 xv.x = moe::f16x2_to_bf16x2(xv.x);
                 xv.y = moe::f16x2_to_bf16x2(xv.y);
@@ -446,6 +518,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
         __syncwarp();
         ++consumed;
       }
+      if (xbad && gvalid) bad = true;
 
       // fixed-order sum over the four K quarters (double-buffered partials), epilogue
       float* rb_ = red + red_buf * (kWarps * NMAT * 4 * 32);
