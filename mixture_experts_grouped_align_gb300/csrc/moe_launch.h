@@ -57,6 +57,10 @@ int prefill_tile_n(const GroupedGemm& g);
 bool prefill_supported(const GroupedGemm& g);
 cudaError_t prefill_gemm(const GroupedGemm& g, cudaStream_t stream);
 
+// ---- MXFP8 grouped GEMM on the block-scaled tensor-core MMA (mx8_gemm.cu)
+bool mx8_supported(const GroupedGemm& g);
+cudaError_t mx8_gemm(const GroupedGemm& g, cudaStream_t stream);
+
 // Row counts above this bucket value use the tensor-memory path.  A bucket value (a
 // fixed point of the bucket map) keeps a batch and its bucket-padded copy on the same
 // side of the threshold, so both run the same kernel.

@@ -1,0 +1,362 @@
+// Grouped expert GEMM on MXFP8 operands with the block-scaled tensor-core MMA.
+//
+// out[p, n] = bf16( sum_k A[row(p), k] * sa[row(p), k / 32] * W[e, n, k] * sw[e, n, k / 32]
+//                   + bias[e, n] ): E4M3 activations and weights, one E8M0 scale per 32
+// K elements of every activation row and weight row ("Add MoE GEMM variants and
+// weight-gradient kernel", aiter PR 5310, Summary: single-launch MXFP8 grouped GEMM with
+// E8M0 microscales and per-expert bias).  tcgen05.mma kind::mxf8f6f4 takes the E4M3 codes
+// straight from shared memory and the E8M0 scales from tensor memory, so nothing is
+// decoded: the products of codes and power-of-two scales are exact and accumulate in f32.
+//
+// Per thread block (one per SM, 512 threads), persistent over (alignment block, N tile):
+//   warp 0      allocates the 512 TMEM columns (a 128 x BN f32 accumulator in columns
+//               0..255, the scale factors of the stages in 256..511) and, on one lane,
+//               issues the MMAs (M = 128, N = BN, K = 32) of each 128-wide K stage;
+//   warps 8-15  copy each stage with cp.async: 128 gathered activation rows and BN
+//               weight rows of 128 bytes into 128-byte-swizzled K-major tiles, and the
+//               stage's scale words; two stages later they write the scale words into
+//               TMEM (warps 8-11 the activation scales, 12-15 the weight scales) and
+//               hand the stage to the MMA;
+//   warps 4-7   drain the accumulator (one TMEM lane = one tile row), add the bias and
+//               store bf16 rows at their pair index.
+// Tiles past num_tokens_post_padded or of the -1 sentinel are skipped by every role before
+// anything is read (second review of the same page).  Expert offsets are 64-bit (Notes).
+// Every mbarrier wait is bounded; one that runs out sets MOE_ERR_TIMEOUT, every role leaves
+// its loop, the MMA lane drains its own work and the TMEM is freed.
+//
+// Scale factors in TMEM (32-bit words, one byte per 32-element K block; the MMA of the
+// stage's K block j selects byte j): the MMA reads the word of A row m at lane m, column
+// m / 32 of the stage's A region (the word is written to all four columns of lane m), and
+// the word of B row n in column n / 32 of the B region at lane n % 32 (written to that
+// lane of every 32-lane quarter).
+#include "moe_common.cuh"
+#include "moe_launch.h"
+#include "tcgen05.cuh"
+
+namespace {
+
+using namespace moe_launch;
+
+constexpr int kThreads = 512;
+constexpr int kBM = 128, kBK = 128;        // tile rows, K elements (bytes) per stage
+constexpr int kProd0 = 256, kNumProd = 256;
+constexpr int kEpiWarp0 = 4;
+constexpr int kTmemCols = 512;
+constexpr int kSfCol0 = 256;               // first TMEM column of the scale regions
+constexpr int kStages = 4;
+constexpr int kLag = 2;                    // stages between a stage's copies and its hand-over
+
+// One stage slot: A tile | B tile | A scale words (one per row) | B scale words (one copy
+// per 32-lane quarter: 4 x 32 lanes x BN/32).
+struct MLayout {
+  int a, b, sfa, sfb, slot, bars, total;
+};
+
+__host__ __device__ inline MLayout mlayout(int BN) {
+  MLayout L;
+  L.a = 0;
+  L.b = kBM * kBK;
+  L.sfa = L.b + BN * kBK;
+  L.sfb = L.sfa + kBM * 4;
+  L.slot = (L.sfb + 4 * 32 * (BN / 32) * 4 + 1023) / 1024 * 1024;
+  L.bars = kStages * L.slot;
+  L.total = L.bars + 256 + 1024;
+  return L;
+}
+
+// TMEM columns of a stage's scale words: A (4 columns at +0), B (BN / 32 <= 8 columns at +8).
+__device__ __forceinline__ uint32_t sfa_col(int s) { return kSfCol0 + 16 * s; }
+__device__ __forceinline__ uint32_t sfb_col(int s) { return kSfCol0 + 16 * s + 8; }
+
+struct MArgs {
+  GroupedGemm g;
+  int BN;
+  int n_tiles;
+  int64_t tiles;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ bool tile_info(const MArgs& ma, int64_t t, int ntpp, int64_t& blk, int& nt,
+                                          int64_t& e) {
+  blk = t / ma.n_tiles;
+  nt = (int)(t - blk * ma.n_tiles);
+  if (blk * ma.g.bm >= ntpp) return false;
+  e = ma.g.expert_ids[blk];
+  return e >= 0 && e < ma.g.E;
+}
+
+__device__ __forceinline__ int64_t act_row(const GroupedGemm& a, int p) {
+  return a.act_per_pair ? (int64_t)p : (int64_t)(p / a.k);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(MArgs ma) {
+  const GroupedGemm& a = ma.g;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int BN = ma.BN, NBW = BN / 32;  // B scale words per lane
+  const MLayout L = mlayout(BN);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tempty + 1;
+  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(taddr_s + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full[s], kNumProd / 32);
+      tc::mbar_init(&empty[s], 1);
+    }
+    tc::mbar_init(tfull, 1);
+    tc::mbar_init(tempty, 4);
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::mbar_fence_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(taddr_s, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t taddr = *taddr_s;
+  const int ntpp = *a.ntpp;
+  const int Kin = a.Kin, nk = Kin / kBK, nkb = Kin / 32;
+  const uint32_t smem_s = tc::smem_addr(smem);
+
+  if (warp >= 8) {
+    // ------------------------------------------------------------------ producers
+    const int pt = tid - kProd0, wp = pt >> 5, q = wp & 3;
+    const int c16 = pt & 7, r0 = pt >> 3;  // 16-byte chunk and first row of this thread's copies
+    const uint8_t* wbase = static_cast<const uint8_t*>(a.w);
+    const uint8_t* abase = static_cast<const uint8_t*>(a.act);
+    uint32_t it = 0;
+    int npend = 0;
+    // hand stage h over to the MMA: its copies (this thread's own) have landed
+    auto hand_over = [&](uint32_t h) {
+      const int hs = (int)(h % kStages);
+      const uint8_t* sl = smem + hs * L.slot;
+      tc::fence_proxy_async_smem();
+      if (wp < 4) {
+        const uint32_t wv = *reinterpret_cast<const uint32_t*>(sl + L.sfa + (q * 32 + lane) * 4);
+        tc::tmem_st4(taddr + ((uint32_t)(q * 32) << 16) + sfa_col(hs), wv, wv, wv, wv);
+      } else {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(sl + L.sfb) + (q * 32 + lane) * NBW;
+        uint32_t v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = j < NBW ? src[j] : 0u;
+        tc::tmem_st8(taddr + ((uint32_t)(q * 32) << 16) + sfb_col(hs), v);
+      }
+      tc::tmem_st_wait();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&full[hs]);
+    };
+    for (int64_t t = blockIdx.x; t < ma.tiles && !*abort_flag; t += gridDim.x) {
+      int64_t blk, e;
+      int nt;
+      if (!tile_info(ma, t, ntpp, blk, nt, e)) continue;
+      const uint8_t* aptr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int p = a.sorted[blk * a.bm + r0 + 32 * i];
+        aptr[i] = p < a.P ? abase + act_row(a, p) * Kin + c16 * 16 : nullptr;
+      }
+      const int64_t brow0 = e * a.Nw + (int64_t)nt * BN;
+      const uint8_t* bptr = wbase + (brow0 + r0) * Kin + c16 * 16;
+      const uint8_t* sfsrc = nullptr;  // A: this lane's row; B: row lane (+ 32 j)
+      if (wp < 4) {
+        const int p = a.sorted[blk * a.bm + q * 32 + lane];
+        if (p < a.P) sfsrc = a.act_scale + act_row(a, p) * nkb;
+      } else {
+        sfsrc = a.w_scale + (brow0 + lane) * nkb;
+      }
+      for (int kc = 0; kc < nk; ++kc) {
+        const int s = (int)(it % kStages);
+        if (!tc::mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1)) {
+          moe::set_status(a.status, MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        const uint32_t sl = smem_s + s * L.slot;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (aptr[i]) cp_async16(sl + L.a + tc::sw128_offset(r0 + 32 * i, c16), aptr[i] + kc * kBK);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < NBW)
+            cp_async16(sl + L.b + tc::sw128_offset(r0 + 32 * i, c16), bptr + (int64_t)(32 * i) * Kin + kc * kBK);
+        if (wp < 4) {
+          if (sfsrc) cp_async4(sl + L.sfa + (q * 32 + lane) * 4, sfsrc + kc * 4);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (j < NBW)
+              cp_async4(sl + L.sfb + ((q * 32 + lane) * NBW + j) * 4, sfsrc + (int64_t)(32 * j) * nkb + kc * 4);
+        }
+        cp_async_commit();
+        ++it;
+        if (++npend > kLag) {
+          cp_async_wait<kLag>();
+          hand_over(it - 1 - kLag);
+          --npend;
+        }
+      }
+    }
+    cp_async_wait<0>();
+    while (npend > 0) {
+      hand_over(it - npend);
+      --npend;
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t idesc[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) idesc[j] = tc::idesc_mx8(kBM, BN, j, j);
+      uint32_t it = 0, acc_it = 0;
+      for (int64_t t = blockIdx.x; t < ma.tiles && !*abort_flag; t += gridDim.x) {
+        int64_t blk, e;
+        int nt;
+        if (!tile_info(ma, t, ntpp, blk, nt, e)) continue;
+        if (!tc::mbar_wait(tempty, (acc_it & 1) ^ 1)) {
+          moe::set_status(a.status, MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc::tc_fence_after();
+        bool ok = true;
+        for (int kc = 0; kc < nk; ++kc) {
+          const int s = (int)(it % kStages);
+          if (!tc::mbar_wait(&full[s], (it / kStages) & 1)) {
+            moe::set_status(a.status, MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t sl = smem_s + s * L.slot;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tc::mma_mx8_ss(taddr, tc::sdesc_sw128(sl + L.a + j * 32), tc::sdesc_sw128(sl + L.b + j * 32), idesc[j],
+                           taddr + sfa_col(s), taddr + sfb_col(s), (kc | j) != 0);
+          tc::mma_commit(&empty[s]);
+          ++it;
+        }
+        if (!ok) break;
+        tc::mma_commit(tfull);
+        ++acc_it;
+      }
+      tc::mma_commit(drain);
+      if (!tc::mbar_wait(drain, 0)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int quarter = warp - kEpiWarp0;
+    const int r = quarter * 32 + lane;
+    const uint16_t* bias = static_cast<const uint16_t*>(a.bias);
+    uint32_t acc_it = 0;
+    for (int64_t t = blockIdx.x; t < ma.tiles && !*abort_flag; t += gridDim.x) {
+      int64_t blk, e;
+      int nt;
+      if (!tile_info(ma, t, ntpp, blk, nt, e)) continue;
+      if (!tc::mbar_wait(tfull, acc_it & 1)) {
+        moe::set_status(a.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      tc::tc_fence_after();
+      const int p = a.sorted[blk * a.bm + r];
+      const bool valid = p < a.P;
+      const int n0 = nt * BN;
+      const uint32_t tb = taddr + ((uint32_t)(quarter * 32) << 16);
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        tc::tmem_ld32(tb + c0, v);
+        tc::tmem_ld_wait();
+        if (valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float o0 = __uint_as_float(v[2 * j]), o1 = __uint_as_float(v[2 * j + 1]);
+            if (bias) {
+              o0 += moe::bf16_bits_to_f32(bias[e * a.Nw + n0 + c0 + 2 * j]);
+              o1 += moe::bf16_bits_to_f32(bias[e * a.Nw + n0 + c0 + 2 * j + 1]);
+            }
+            pk[j] = (uint32_t)moe::f32_to_bf16_bits(o0) | ((uint32_t)moe::f32_to_bf16_bits(o1) << 16);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + (int64_t)p * a.Nout + n0 + c0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tempty);
+      ++acc_it;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(taddr, kTmemCols);
+  }
+}
+
+int sm_count_mx8() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+}  // namespace
+
+namespace moe_launch {
+
+bool mx8_supported(const GroupedGemm& g) {
+  if (g.wfmt != WF_MXFP8 || g.epi != EPI_PLAIN_BF16 || g.act_scale == nullptr) return false;
+  if (g.bm != kBM || g.Kin <= 0 || g.Kin % kBK != 0) return false;
+  if (g.Nout % 128 != 0) return false;
+  // 16-byte copies of activation and weight rows, 4-byte copies of scale words
+  const uintptr_t al16 = reinterpret_cast<uintptr_t>(g.act) | reinterpret_cast<uintptr_t>(g.w);
+  const uintptr_t al4 = reinterpret_cast<uintptr_t>(g.act_scale) | reinterpret_cast<uintptr_t>(g.w_scale);
+  return (al16 & 15) == 0 && (al4 & 3) == 0;
+}
+
+cudaError_t mx8_gemm(const GroupedGemm& g, cudaStream_t stream) {
+  if (!mx8_supported(g)) return cudaErrorInvalidValue;
+  MArgs ma;
+  ma.g = g;
+  ma.BN = (g.Nout % 256 == 0) ? 256 : 128;
+  ma.n_tiles = g.Nout / ma.BN;
+  ma.tiles = g.grid_blocks * ma.n_tiles;
+  const MLayout L = mlayout(ma.BN);
+  cudaError_t err = cudaFuncSetAttribute(mx8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  if (err != cudaSuccess) return err;
+  int64_t grid = sm_count_mx8();
+  if (ma.tiles < grid) grid = ma.tiles;
+  if (grid <= 0) return cudaSuccess;
+  mx8_gemm_kernel<<<(unsigned)grid, kThreads, L.total, stream>>>(ma);
+  return cudaGetLastError();
+}
+
+}  // namespace moe_launch

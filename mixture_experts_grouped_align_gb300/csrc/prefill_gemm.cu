@@ -548,6 +548,7 @@ cudaError_t prefill_gemm(const GroupedGemm& g, cudaStream_t stream) {
 }
 
 cudaError_t grouped_gemm(const GroupedGemm& g, int64_t rows, cudaStream_t stream) {
+  if (rows > kPrefillRowsAbove && mx8_supported(g)) return mx8_gemm(g, stream);
   if (rows > kPrefillRowsAbove && prefill_supported(g)) return prefill_gemm(g, stream);
   return decode_gemm(g, stream);
 }

@@ -94,6 +94,21 @@ MOE_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 MOE_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Registers -> TMEM: thread i writes lane i of the warp's 32-lane quarter, columns c..c+3
+// (x4) or c..c+7 (x8) from r[0..].
+MOE_DEV void tmem_st4(uint32_t taddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r0),
+               "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+MOE_DEV void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+// Waits until this thread's tcgen05.st writes have completed.
+MOE_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // ---------------------------------------------------------------- MMA
 
 // Shared-memory matrix descriptor of a K-major operand tile stored in 128-byte swizzle
@@ -145,6 +160,33 @@ MOE_DEV void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint3
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale: E4M3 A and B, both
+// K-major, f32 accumulator, UE8M0 scale factors; the scale-factor ids pick the byte of
+// the 32-bit TMEM scale words this MMA uses (B in bits 4-5, A in bits 29-30), N >> 3 in
+// bits 17-22, scale type UE8M0 in bit 23, M >> 4 in bits 24-28.
+MOE_DEV uint32_t idesc_mx8(int M, int N, uint32_t sf_id_a, uint32_t sf_id_b) {
+  uint32_t d = 0;
+  d |= (sf_id_b & 3u) << 4;
+  d |= (uint32_t)(N >> 3) << 17;
+  d |= 1u << 23;
+  d |= (uint32_t)(M >> 4) << 24;
+  d |= (sf_id_a & 3u) << 29;
+  return d;
+}
+
+// D[tmem] (+)= (A . SFA)[smem] . (B . SFB)[smem]^T with one E8M0 scale per 32 K elements
+// of every A row and B row, read from TMEM; issued by one thread.
+MOE_DEV void mma_mx8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t sfa_tmem,
+                        uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
 

@@ -129,3 +129,63 @@ def test_mxfp8_full_size_sampled(moe):
         A2 = ofmt.dequant_mxfp8(g["a2_codes"][pairs].cpu().numpy(), g["a2_scale"][pairs].cpu().numpy())
         assert_close_bf16(bf16_to_np(out2[pairs]), A2 @ W2.T, what=f"gemm2 expert {e}")
     assert np.all(cnt[g["cold"]] == 0)
+
+
+@pytest.mark.parametrize("N", [256, 384])          # N tile 256 / N tile 128
+@pytest.mark.parametrize("per_pair", [False, True])
+@pytest.mark.parametrize("bias", [False, True])
+def test_mxfp8_block_scaled(moe, N, per_pair, bias):
+    """Rows above the threshold, K a multiple of 128 and N of 128: the block-scaled MMA path.
+    Ragged experts (two empty) over several 128-row tiles, three K stages."""
+    rng = np.random.default_rng(13)
+    T, E, k, Kin = 700, 12, 3, 384
+    ids = random_ids(rng, T, E, k, empty=(5, 9))
+    rows = T * k if per_pair else T
+    a_c, a_s = synth.mx_quantise_e4m3(rng.standard_normal((rows, Kin)).astype(np.float32))
+    w_c, w_s = synth.mx_quantise_e4m3((rng.standard_normal((E, N, Kin)) * 0.05).astype(np.float32))
+    b = synth.to_bf16_bits(rng.standard_normal((E, N)) * 0.1) if bias else None
+    out = gemm_dev(moe, "mxfp8", E, N, Kin, dev(a_c), dev(a_s), per_pair, dev(w_c), dev(w_s),
+                   dev(b), ids)
+    A = ofmt.dequant_mxfp8(a_c, a_s)
+    Wd = lambda e: (ofmt.dequant_mxfp8(w_c[e], w_s[e]), None if b is None else ofmt.bf16_decode(b[e]))
+    ref = olayer.grouped_gemm(A, ids, Wd, per_pair)
+    assert_close_bf16(bf16_to_np(out), ref, what=f"mxfp8 block-scaled N={N}")
+
+
+def test_mxfp8_block_scaled_constant_roundtrip(moe):
+    """Constant codes and scales on the block-scaled path: every output is exactly
+    Kin * a * w * 2^(sa + sw)."""
+    T, E, k, N, Kin = 300, 4, 2, 256, 256
+    ids = np.array([[t % E, (t + 1) % E] for t in range(T)], dtype=np.int32)
+    a_c = np.full((T, Kin), 0x38, np.uint8)          # E4M3 1.0
+    a_s = np.full((T, Kin // 32), 127 - 3, np.uint8)
+    w_c = np.full((E, N, Kin), 0xB4, np.uint8)        # E4M3 -0.75
+    w_s = np.full((E, N, Kin // 32), 127 + 2, np.uint8)
+    out = gemm_dev(moe, "mxfp8", E, N, Kin, dev(a_c), dev(a_s), False, dev(w_c), dev(w_s), None, ids)
+    want = Kin * 1.0 * -0.75 * 2.0 ** (-3 + 2)
+    assert np.all(bf16_to_np(out) == want)
+
+
+def test_mxfp8_block_scaled_scale_edges(moe):
+    """E8M0 edge codes on the block-scaled path (the edge decoding of the second review on
+    the aiter MoE GEMM page): 0x00 is 2^-127 -- here every weight scale of K block 2 is 0x00
+    and every activation scale of that block is 2^125, so the block still weighs 2^-2 -- and
+    0xFF is NaN, which must reach exactly the outputs whose dot product uses that block."""
+    rng = np.random.default_rng(17)
+    T, E, k, N, Kin = 300, 4, 2, 128, 256
+    ids = random_ids(rng, T, E, k)
+    a_c, a_s = synth.mx_quantise_e4m3(rng.standard_normal((T, Kin)).astype(np.float32))
+    w_c, w_s = synth.mx_quantise_e4m3((rng.standard_normal((E, N, Kin)) * 0.05).astype(np.float32))
+    a_s[:, 2] = 127 + 125
+    w_s[:, :, 2] = 0x00
+    w_s[2, 3:5, 1] = 0xFF
+    out = bf16_to_np(gemm_dev(moe, "mxfp8", E, N, Kin, dev(a_c), dev(a_s), False, dev(w_c), dev(w_s),
+                              None, ids))
+    A = ofmt.dequant_mxfp8(a_c, a_s)
+    Wd = lambda e: (ofmt.dequant_mxfp8(w_c[e], w_s[e]), None)
+    ref = olayer.grouped_gemm(A, ids, Wd, False)
+    nan_ref = np.isnan(ref)
+    assert nan_ref.any()
+    assert np.array_equal(np.isnan(out), nan_ref)
+    keep = ~nan_ref.any(axis=1)
+    assert_close_bf16(out[keep], ref[keep], what="mxfp8 scale edges")
