@@ -32,7 +32,10 @@ L2_BYTES = 129 * 1024 * 1024
 # DRAM traffic (read + write bytes) of one launch of the dominant kernel, from an ncu
 # capture of the same command (summary under profiles/), valid while the kernel source
 # hashes the same; otherwise reported as null.
-TRAFFIC = {}
+TRAFFIC = {
+    "decode_gemm.cu:gemm1@decode_mxfp4": {  # profiles/decode_gemm_decode_mxfp4_T64.md
+        "src": "978915d2a01efc1e", "bytes": 998010112 + 4668416},
+}
 
 
 def parse():
