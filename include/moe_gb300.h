@@ -160,10 +160,12 @@ typedef struct {
   const void* b2;         /* [E, K] bf16 or NULL                                          */
 } moe_weights;
 
-/* Workspace bytes moe_forward needs for T_rows rows of top-k: h [T_rows*k, I] (f16 for
- * MXFP4 weights, bf16 for bf16 weights), o [T_rows*k, K] fp32 and x as f16 [T_rows, K],
- * each 256-byte aligned. */
-size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t I);
+/* Workspace bytes moe_forward needs for T_rows rows of top-k with an alignment of
+ * cap_tokens slots (moe_align_capacity): h [rows_h, I] (f16 for MXFP4 weights, bf16 for bf16
+ * weights), o [T_rows*k, K] fp32 and x as f16 [rows_x, K], each 256-byte aligned.  rows_h =
+ * T_rows*k and rows_x = T_rows up to 256 rows; above that h and x may be kept in
+ * alignment-slot order and rows_h = rows_x = cap_tokens.  Returns 0 for a negative argument. */
+size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t I, int64_t cap_tokens);
 
 /* For every real token t < T_real (the others, e.g. bucket pad rows, are computed and
  * then sliced off):

@@ -76,7 +76,7 @@ def load(path: str | None = None):
         "moe_bucket": (I64, [I64]),
         "moe_bucket_count": (I64, [I64]),
         "moe_bucket_pad": (I32, [I64, ctypes.c_int, P, P, P, I64, P, P, I32, P]),
-        "moe_forward_workspace_size": (SZ, [I64, I32, I32, I32]),
+        "moe_forward_workspace_size": (SZ, [I64, I32, I32, I32, I64]),
         "moe_forward": (I32, [P, P, P, I64, I64, I32, P, P, P, P, P, I32, I64, P, P]),
         "moe_forward_no_alloc": (I32, [P, P, P, I64, I64, I32, P, P, P, P, P, I32, I64, P, P]),
         "moe_grouped_gemm": (I32, [ctypes.c_int, I32, I32, I32, P, P, I32, P, P, P, I64, I32,
@@ -172,8 +172,8 @@ def moe_bucket_pad(T, quant, x=None, x_pad=None, row_bytes=0, logits=None, logit
     return st, tp.value
 
 
-def moe_forward_workspace_size(T_rows, k, K, I) -> int:
-    return load().moe_forward_workspace_size(T_rows, k, K, I)
+def moe_forward_workspace_size(T_rows, k, K, I, cap_tokens) -> int:
+    return load().moe_forward_workspace_size(T_rows, k, K, I, cap_tokens)
 
 
 def moe_forward(quant, E, K, I, w1, w1_scale, b1, w2, w2_scale, b2, x, x_scale, T_rows, T_real, k,

@@ -81,9 +81,43 @@ __global__ void bf16_to_f16_kernel(const uint4* __restrict__ x, uint4* __restric
   if (bad) moe::set_status(status, MOE_ERR_RANGE);
 }
 
+// y[s] = f16(x[sorted[s] / k]) for the alignment slots s < num_tokens_post_padded (a slot of
+// the sentinel gets zeros), 8 elements per thread: the token rows in slot order, so that a
+// block of 128 slots is 128 consecutive rows.  |x| > 65504 of a real row is reported.
+__global__ void gather_rows_f16_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted,
+                                       const int32_t* __restrict__ ntpp, int64_t P, int k, int64_t per,
+                                       int64_t n8, uint4* __restrict__ y, int32_t* status) {
+  const int64_t lim = (int64_t)*ntpp * per;
+  bool bad = false;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8 && i < lim;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t s = i / per, c = i - s * per;
+    const int p = __ldg(sorted + s);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (p < P) {
+      v = __ldg(x + (int64_t)(p / k) * per + c);
+      v.x = moe::bf16x2_to_f16x2(v.x, &bad);
+      v.y = moe::bf16x2_to_f16x2(v.y, &bad);
+      v.z = moe::bf16x2_to_f16x2(v.z, &bad);
+      v.w = moe::bf16x2_to_f16x2(v.w, &bad);
+    }
+    y[i] = v;
+  }
+  if (bad) moe::set_status(status, MOE_ERR_RANGE);
+}
+
 }  // namespace
 
 namespace moe_launch {
+
+cudaError_t gather_rows_f16(const void* x, const int32_t* sorted, const int32_t* ntpp, int64_t P, int k,
+                            int64_t K, int64_t slots, void* y, int32_t* status, cudaStream_t stream) {
+  const int64_t per = K / 8, n8 = slots * per;
+  if (n8 == 0) return cudaSuccess;
+  gather_rows_f16_kernel<<<grid_for(n8, 256), 256, 0, stream>>>((const uint4*)x, sorted, ntpp, P, k, per, n8,
+                                                                 (uint4*)y, status);
+  return cudaGetLastError();
+}
 
 cudaError_t bf16_to_f16(const void* x, void* y, int64_t n, int32_t* status, cudaStream_t stream) {
   const int64_t n8 = n / 8;

@@ -166,10 +166,23 @@ moe_status moe_bucket_pad(int64_t T, moe_quant quant, int64_t* T_pad, const void
   return MOE_OK;
 }
 
-size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t I) {
-  if (T_rows < 0 || k < 1 || K < 1 || I < 1) return 0;
+// Scratch of moe_forward: h ([rows_h, I], 16-bit), o ([P, K] fp32) and the f16 copy of x
+// ([rows_x, K]).  Above the tensor-memory threshold h and x may be kept in alignment-slot
+// order, with one row per slot of the capacity.
+static void forward_scratch_rows(int64_t T_rows, int32_t k, int64_t cap_tokens, int64_t* rows_h,
+                                 int64_t* rows_x) {
   const int64_t P = T_rows * k;
-  return round256((size_t)P * I * 2) + round256((size_t)P * K * 4) + round256((size_t)T_rows * K * 2);
+  const bool slots = T_rows > moe_launch::kPrefillRowsAbove && cap_tokens > P;
+  *rows_h = slots ? cap_tokens : P;
+  *rows_x = slots ? cap_tokens : T_rows;
+}
+
+size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t I, int64_t cap_tokens) {
+  if (T_rows < 0 || k < 1 || K < 1 || I < 1 || cap_tokens < 0) return 0;
+  const int64_t P = T_rows * k;
+  int64_t rows_h, rows_x;
+  forward_scratch_rows(T_rows, k, cap_tokens, &rows_h, &rows_x);
+  return round256((size_t)rows_h * I * 2) + round256((size_t)P * K * 4) + round256((size_t)rows_x * K * 2);
 }
 
 moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_scale, int64_t T_rows,
@@ -200,15 +213,17 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
   moe_status st = check_align_outputs(P, E, block_m, sorted_token_ids, expert_ids,
                                       num_tokens_post_padded, cap_tokens);
   if (st != MOE_OK) return st;
-  const size_t need = moe_forward_workspace_size(T_rows, k, K, I);
+  const size_t need = moe_forward_workspace_size(T_rows, k, K, I, cap_tokens);
   MOE_REQUIRE(ctx->workspace && ctx->workspace_bytes >= need && aligned16(ctx->workspace),
               MOE_ERR_CAPACITY, "workspace of %zu bytes needed", need);
   if (T_rows == 0) return MOE_OK;
 
+  int64_t rows_h, rows_x;
+  forward_scratch_rows(T_rows, k, cap_tokens, &rows_h, &rows_x);
   uint8_t* ws = static_cast<uint8_t*>(ctx->workspace);
   void* h = ws;
-  float* o = reinterpret_cast<float*>(ws + round256((size_t)P * I * 2));
-  void* x16 = ws + round256((size_t)P * I * 2) + round256((size_t)P * K * 4);
+  float* o = reinterpret_cast<float*>(ws + round256((size_t)rows_h * I * 2));
+  void* x16 = ws + round256((size_t)rows_h * I * 2) + round256((size_t)P * K * 4);
   cudaStream_t s = stream_of(ctx);
   const int wf = fp4 ? moe_launch::WF_MXFP4 : moe_launch::WF_BF16;
   const int64_t blocks = used_blocks_bound(P, E, block_m, cap_tokens);
@@ -226,20 +241,35 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
   g1.status = status_of(ctx);
   MOE_REQUIRE(moe_launch::decode_gemm_smem_bytes(g1) <= 227 * 1024, MOE_ERR_UNSUPPORTED,
               "K too large for the decode path");
+  moe_launch::GroupedGemm g2 = g1;
+  g2.epi = moe_launch::EPI_WEIGHTED_F32;
+  g2.w = W->w2; g2.w_scale = W->w2_scale; g2.bias = W->b2;
+  g2.act = h; g2.act_fmt = fp4 ? moe_launch::ACT_F16 : moe_launch::ACT_BF16; g2.act_per_pair = 1;
+  g2.Nw = K; g2.Kin = I; g2.Nout = K; g2.out = o;
+  // Above the threshold the MXFP4 path keeps x and h in alignment-slot order: a block of 128
+  // slots is then 128 consecutive rows, which the tensor-memory kernel loads as one box.
+  if (fp4 && rows_x == rows_h && rows_h > P) {
+    moe_launch::GroupedGemm s1 = g1, s2 = g2;
+    s1.act_by_slot = 1; s1.out_by_slot = 1;
+    s2.act_by_slot = 1;
+    if (blocks * block_m <= rows_h && moe_launch::ts_supported(s1) && moe_launch::ts_supported(s2)) {
+      g1 = s1;
+      g2 = s2;
+    }
+  }
   rec(ctx, 0, 4);
-  if (fp4) {
+  if (fp4 && g1.act_by_slot) {
+    st = cuda_status(moe_launch::gather_rows_f16(x, sorted_token_ids, num_tokens_post_padded, P, k, K,
+                                                 blocks * block_m, x16, status_of(ctx), s),
+                     "moe_forward x");
+    if (st != MOE_OK) return st;
+  } else if (fp4) {
     st = cuda_status(moe_launch::bf16_to_f16(x, x16, T_rows * K, status_of(ctx), s), "moe_forward x");
     if (st != MOE_OK) return st;
   }
   st = cuda_status(moe_launch::grouped_gemm(g1, T_rows, s), "moe_forward GEMM1");
   if (st != MOE_OK) return st;
   rec(ctx, 1, 4);
-
-  moe_launch::GroupedGemm g2 = g1;
-  g2.epi = moe_launch::EPI_WEIGHTED_F32;
-  g2.w = W->w2; g2.w_scale = W->w2_scale; g2.bias = W->b2;
-  g2.act = h; g2.act_fmt = fp4 ? moe_launch::ACT_F16 : moe_launch::ACT_BF16; g2.act_per_pair = 1;
-  g2.Nw = K; g2.Kin = I; g2.Nout = K; g2.out = o;
   st = cuda_status(moe_launch::grouped_gemm(g2, T_rows, s), "moe_forward GEMM2");
   if (st != MOE_OK) return st;
   rec(ctx, 2, 4);

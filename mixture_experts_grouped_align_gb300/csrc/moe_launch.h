@@ -18,6 +18,9 @@ cudaError_t pad_rows(const void* src, void* dst, int64_t rows, int64_t rows_pad,
 cudaError_t zero_f32(float* p, int64_t n, cudaStream_t stream);
 cudaError_t combine(const float* o, int64_t T_real, int k, int K, void* y, cudaStream_t stream);
 cudaError_t bf16_to_f16(const void* x, void* y, int64_t n, int32_t* status, cudaStream_t stream);
+// Token rows of bf16 x gathered into alignment-slot order as f16 ([slots, K]).
+cudaError_t gather_rows_f16(const void* x, const int32_t* sorted, const int32_t* ntpp, int64_t P, int k,
+                            int64_t K, int64_t slots, void* y, int32_t* status, cudaStream_t stream);
 
 // ---- grouped GEMMs on the weight-streaming (decode) path (decode_gemm.cu)
 enum WFmt { WF_BF16 = 0, WF_MXFP4 = 1, WF_MXFP8 = 2 };
@@ -34,6 +37,8 @@ struct GroupedGemm {
   int act_fmt;              // ActFmt of 16-bit activations
   const uint8_t* act_scale; // [*, Kin/32] (mxfp8)
   int act_per_pair;         // act row = p (1) or p / k (0)
+  int act_by_slot;          // 1: act row = alignment slot (rows already in sorted order)
+  int out_by_slot;          // 1: output row = alignment slot instead of the pair p
   int64_t Nw;               // weight rows per expert (SwiGLU: 2 * Nout)
   int Kin;                  // reduction length
   int Nout;                 // output columns
@@ -56,6 +61,10 @@ cudaError_t decode_gemm(const GroupedGemm& g, cudaStream_t stream);
 int prefill_tile_n(const GroupedGemm& g);
 bool prefill_supported(const GroupedGemm& g);
 cudaError_t prefill_gemm(const GroupedGemm& g, cudaStream_t stream);
+
+// ---- W4A16 grouped GEMM with the decoded weights in tensor memory (prefill_ts.cu)
+bool ts_supported(const GroupedGemm& g);
+cudaError_t prefill_ts(const GroupedGemm& g, cudaStream_t stream);
 
 // ---- MXFP8 grouped GEMM on the block-scaled tensor-core MMA (mx8_gemm.cu)
 bool mx8_supported(const GroupedGemm& g);

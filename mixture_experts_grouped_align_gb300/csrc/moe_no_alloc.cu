@@ -64,7 +64,7 @@ extern "C" moe_status moe_forward_no_alloc(
     moe_host::set_error("moe_forward_no_alloc: null weights");
     return MOE_ERR_INVALID_ARG;
   }
-  const size_t need = moe_forward_workspace_size(T_rows, k, W->K, W->I);
+  const size_t need = moe_forward_workspace_size(T_rows, k, W->K, W->I, cap_tokens);
   if (need == 0 || need > kNoAllocScratchBytes) {
     moe_host::set_error(
         "moe_forward_no_alloc: the call needs %zu bytes of scratch; the fixed array holds %zu "

@@ -12,11 +12,12 @@
 //   warp 0      allocates the 512 TMEM columns (a 128 x BN f32 accumulator in columns
 //               0..255, the scale factors of the stages in 256..511) and, on one lane,
 //               issues the MMAs (M = 128, N = BN, K = 32) of each 128-wide K stage;
-//   warps 8-15  copy each stage with cp.async: 128 gathered activation rows and BN
-//               weight rows of 128 bytes into 128-byte-swizzled K-major tiles, and the
-//               stage's scale words; two stages later they write the scale words into
-//               TMEM (warps 8-11 the activation scales, 12-15 the weight scales) and
-//               hand the stage to the MMA;
+//   warps 8-15  copy each stage: one thread loads the BN weight rows of 128 bytes with a
+//               TMA box into a 128-byte-swizzled K-major tile (completing on the stage's
+//               barrier); all copy the 128 gathered activation rows into the same layout
+//               and the stage's scale words with cp.async; two stages later they write the
+//               scale words into TMEM (warps 8-11 the activation scales, 12-15 the weight
+//               scales) and hand the stage to the MMA;
 //   warps 4-7   drain the accumulator (one TMEM lane = one tile row), add the bias and
 //               store bf16 rows at their pair index.
 // Tiles past num_tokens_post_padded or of the -1 sentinel are skipped by every role before
@@ -32,6 +33,7 @@
 #include "moe_common.cuh"
 #include "moe_launch.h"
 #include "tcgen05.cuh"
+#include "tma.cuh"
 
 namespace {
 
@@ -98,7 +100,7 @@ __device__ __forceinline__ int64_t act_row(const GroupedGemm& a, int p) {
   return a.act_per_pair ? (int64_t)p : (int64_t)(p / a.k);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(MArgs ma) {
+__global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, MArgs ma) {
   const GroupedGemm& a = ma.g;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -115,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(MArgs ma) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&full[s], kNumProd / 32);
+      tc::mbar_init(&full[s], kNumProd / 32 + 1);  // producer warps + the weight box
       tc::mbar_init(&empty[s], 1);
     }
     tc::mbar_init(tfull, 1);
@@ -140,8 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(MArgs ma) {
     // ------------------------------------------------------------------ producers
     const int pt = tid - kProd0, wp = pt >> 5, q = wp & 3;
     const int c16 = pt & 7, r0 = pt >> 3;  // 16-byte chunk and first row of this thread's copies
-    const uint8_t* wbase = static_cast<const uint8_t*>(a.w);
     const uint8_t* abase = static_cast<const uint8_t*>(a.act);
+    if (pt == 0) tma::prefetch_map(&tmap_w);
     uint32_t it = 0;
     int npend = 0;
     // hand stage h over to the MMA: its copies (this thread's own) have landed
@@ -175,7 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(MArgs ma) {
         aptr[i] = p < a.P ? abase + act_row(a, p) * Kin + c16 * 16 : nullptr;
       }
       const int64_t brow0 = e * a.Nw + (int64_t)nt * BN;
-      const uint8_t* bptr = wbase + (brow0 + r0) * Kin + c16 * 16;
       const uint8_t* sfsrc = nullptr;  // A: this lane's row; B: row lane (+ 32 j)
       if (wp < 4) {
         const int p = a.sorted[blk * a.bm + q * 32 + lane];
@@ -184,6 +185,13 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(MArgs ma) {
         sfsrc = a.w_scale + (brow0 + lane) * nkb;
       }
       for (int kc = 0; kc < nk; ++kc) {
+        // hand the oldest stage over before waiting for a free slot, so that the MMA has two
+        // stages queued while this one's copies fly
+        if (npend == kLag) {
+          cp_async_wait<kLag - 1>();
+          hand_over(it - kLag);
+          --npend;
+        }
         const int s = (int)(it % kStages);
         if (!tc::mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1)) {
           moe::set_status(a.status, MOE_ERR_TIMEOUT);
@@ -191,13 +199,13 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(MArgs ma) {
           break;
         }
         const uint32_t sl = smem_s + s * L.slot;
+        if (pt == 0) {
+          tma::mbar_arrive_expect_tx(&full[s], (uint32_t)(BN * kBK));
+          tma::load_2d(sl + L.b, &tmap_w, kc * kBK, (int32_t)brow0, &full[s]);
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           if (aptr[i]) cp_async16(sl + L.a + tc::sw128_offset(r0 + 32 * i, c16), aptr[i] + kc * kBK);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (i < NBW)
-            cp_async16(sl + L.b + tc::sw128_offset(r0 + 32 * i, c16), bptr + (int64_t)(32 * i) * Kin + kc * kBK);
         if (wp < 4) {
           if (sfsrc) cp_async4(sl + L.sfa + (q * 32 + lane) * 4, sfsrc + kc * 4);
         } else {
@@ -208,11 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(MArgs ma) {
         }
         cp_async_commit();
         ++it;
-        if (++npend > kLag) {
-          cp_async_wait<kLag>();
-          hand_over(it - 1 - kLag);
-          --npend;
-        }
+        ++npend;
       }
     }
     cp_async_wait<0>();
@@ -336,6 +340,7 @@ bool mx8_supported(const GroupedGemm& g) {
   if (g.wfmt != WF_MXFP8 || g.epi != EPI_PLAIN_BF16 || g.act_scale == nullptr) return false;
   if (g.bm != kBM || g.Kin <= 0 || g.Kin % kBK != 0) return false;
   if (g.Nout % 128 != 0) return false;
+  if ((int64_t)g.E * g.Nw >= ((int64_t)1 << 31)) return false;  // TMA row coordinates are 32-bit
   // 16-byte copies of activation and weight rows, 4-byte copies of scale words
   const uintptr_t al16 = reinterpret_cast<uintptr_t>(g.act) | reinterpret_cast<uintptr_t>(g.w);
   const uintptr_t al4 = reinterpret_cast<uintptr_t>(g.act_scale) | reinterpret_cast<uintptr_t>(g.w_scale);
@@ -349,13 +354,17 @@ cudaError_t mx8_gemm(const GroupedGemm& g, cudaStream_t stream) {
   ma.BN = (g.Nout % 256 == 0) ? 256 : 128;
   ma.n_tiles = g.Nout / ma.BN;
   ma.tiles = g.grid_blocks * ma.n_tiles;
+  // weights as E * Nw rows of Kin bytes; boxes of 128 bytes x BN rows in the 128-byte swizzle
+  CUtensorMap tmap;
+  if (!tma::encode_2d_u8(&tmap, g.w, (uint64_t)g.Kin, (uint64_t)g.E * g.Nw, (uint64_t)g.Kin, kBK, ma.BN, true))
+    return cudaErrorInvalidValue;
   const MLayout L = mlayout(ma.BN);
   cudaError_t err = cudaFuncSetAttribute(mx8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
   int64_t grid = sm_count_mx8();
   if (ma.tiles < grid) grid = ma.tiles;
   if (grid <= 0) return cudaSuccess;
-  mx8_gemm_kernel<<<(unsigned)grid, kThreads, L.total, stream>>>(ma);
+  mx8_gemm_kernel<<<(unsigned)grid, kThreads, L.total, stream>>>(tmap, ma);
   return cudaGetLastError();
 }
 

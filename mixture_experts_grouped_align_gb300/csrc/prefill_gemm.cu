@@ -548,6 +548,9 @@ cudaError_t prefill_gemm(const GroupedGemm& g, cudaStream_t stream) {
 }
 
 cudaError_t grouped_gemm(const GroupedGemm& g, int64_t rows, cudaStream_t stream) {
+  if (g.act_by_slot || g.out_by_slot)  // slot-ordered rows: only the tensor-memory W4A16 kernel
+    return ts_supported(g) ? prefill_ts(g, stream) : cudaErrorInvalidValue;
+  if (rows > kPrefillRowsAbove && ts_supported(g)) return prefill_ts(g, stream);
   if (rows > kPrefillRowsAbove && mx8_supported(g)) return mx8_gemm(g, stream);
   if (rows > kPrefillRowsAbove && prefill_supported(g)) return prefill_gemm(g, stream);
   return decode_gemm(g, stream);

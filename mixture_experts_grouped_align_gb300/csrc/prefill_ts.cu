@@ -1,0 +1,587 @@
+// Grouped expert GEMM for W4A16 prefill shapes with the weights as the tensor-memory
+// operand of tcgen05.mma.
+//
+// D[f, t] = sum_k W[e, f, k] * x[row(t), k] over one alignment block of 128 pairs t and 128
+// output features f of the block's expert e ("Add MoE GEMM variants and weight-gradient
+// kernel", aiter PR 5310, Summary: all expert GEMMs in one launch; "Bound Triton MoE JIT
+// specializations via token-dim bucketing and warmup", TensorRT-LLM PR 15311, Description:
+// the W4A16 MXFP4 path, E2M1 weights with one E8M0 scale per 32 K elements, 16-bit
+// activations).  Tiles past num_tokens_post_padded or of the -1 sentinel are skipped by every
+// role before anything is read (second review of the aiter page); expert offsets are 64-bit.
+//
+// Why this shape.  The weights must be decoded (E2M1 codes times the block scale, to f16)
+// before an f16 MMA can use them.  Writing the decoded weights to shared memory and reading
+// them back as an MMA operand costs more shared-memory bandwidth than the MMA leaves free;
+// decoded into tensor memory they cost none: tcgen05.mma reads its A operand (M = 128
+// weight rows x K) straight from TMEM and only the token tile B (N = 128 rows x K) from
+// shared memory.  SwiGLU pairs gate row f and up row f in the same TMEM lane: the two
+// matrices are two MMAs into two accumulators G and U.
+//
+// Per thread block (one per SM, 512 threads), persistent over (alignment block, feature tile):
+//   warp 0      allocates the 512 TMEM columns (accumulators in 0..255: G | U for SwiGLU,
+//               two alternating 128-column accumulators otherwise; decoded weight stages in
+//               256..511) and, on one lane, issues the MMAs (M = 128, N = 128, K = 16);
+//   warp 1      loads each 64-wide K stage with TMA: the 128 token rows (f16, gathered four
+//               rows per instruction into a 128-byte-swizzled K-major tile) and the raw E2M1
+//               bytes of the stage's weight rows;
+//   warps 8-15  decode: one thread per weight row (= TMEM lane) turns the stage's codes into
+//               f16 (hardware conversion, times the block's E8M0 scale) and writes them into
+//               the stage's TMEM columns with tcgen05.st;
+//   warps 4-7   drain the accumulators (one TMEM lane = one feature, one column = one pair)
+//               and run the fused epilogue: bias + SwiGLU -> h (f16), bias * routing weight
+//               -> o (fp32), or bias -> out (bf16), stored at the pair's row.
+// Every mbarrier wait is bounded; one that runs out sets MOE_ERR_TIMEOUT, every role leaves
+// its loop, the MMA lane drains its own work and the TMEM is freed.
+//
+// f16 operands: a decoded weight is exact when its scale is within 2^-23..2^13; a block with
+// nonzero codes outside that range sets MOE_ERR_RANGE.  Each output depends on its own token
+// row only and K is always reduced in the same order, so padded and unpadded batches give
+// identical real rows.
+#include "moe_common.cuh"
+#include "moe_launch.h"
+#include "tcgen05.cuh"
+#include "tma.cuh"
+
+namespace {
+
+using namespace moe_launch;
+
+constexpr int kThreads = 512;
+constexpr int kTM = 128;    // weight rows (features) per tile: MMA M
+constexpr int kTN = 128;    // pairs per tile (one alignment block): MMA N
+constexpr int kBK = 64;     // K elements per stage
+// Shared-memory stages (token tile + raw codes) and TMEM stages (decoded weights) form two
+// rings: copies may run further ahead of the MMA than the TMEM columns allow decoding to.
+__host__ __device__ constexpr int smem_stages(int nmat) { return nmat == 2 ? 6 : 8; }
+__host__ __device__ constexpr int tmem_stages(int nmat) { return nmat == 2 ? 4 : 8; }
+constexpr int kEpiWarp0 = 4, kDecWarp0 = 8;
+constexpr int kTmemCols = 512;
+constexpr int kAcol0 = 256;  // first TMEM column of the decoded weight stages
+constexpr int kMaxKin = 4096;
+
+struct TArgs {
+  GroupedGemm g;
+  int nmat;          // 2 for SwiGLU (gate and up rows), else 1
+  int m_tiles;       // feature tiles per block: ceil(Nout / 128)
+  int64_t tiles;     // block slots * m_tiles
+  int scw;           // 32-bit words of one thread's scale-row buffer
+};
+
+// Shared memory: stages [B tile 16 KB | raw weight rows nmat x 4 KB] | scale rows
+// [2 tiles][256 decoder threads][scw words] | barriers.
+struct TLayout {
+  int slot, raw, sc, bars, total;
+};
+
+__host__ __device__ inline TLayout tlayout(int nmat, int scw) {
+  TLayout L;
+  L.raw = kTN * 128;
+  L.slot = L.raw + nmat * kTM * (kBK / 2);
+  L.sc = smem_stages(nmat) * L.slot;
+  L.bars = L.sc + 2 * 256 * scw * 4;
+  L.total = L.bars + 512 + 1024;
+  return L;
+}
+
+__device__ __forceinline__ bool tile_info(const TArgs& ta, int64_t t, int ntpp, int64_t& blk, int& mt,
+                                          int64_t& e) {
+  blk = t / ta.m_tiles;
+  mt = (int)(t - blk * ta.m_tiles);
+  if (blk * ta.g.bm >= ntpp) return false;
+  e = ta.g.expert_ids[blk];
+  return e >= 0 && e < ta.g.E;
+}
+
+// First tile of this block's sequence at or after t that some role works on (or >= tiles).
+__device__ __forceinline__ int64_t next_tile(const TArgs& ta, int64_t t, int ntpp) {
+  int64_t blk, e;
+  int mt;
+  while (t < ta.tiles && !tile_info(ta, t, ntpp, blk, mt, e)) t += gridDim.x;
+  return t;
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// TMA gather of four 128-byte rows (rows y0..y3 of the tensor, bytes x..x+127) to dst.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y0,
+                                            int32_t y1, int32_t y2, int32_t y3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(tc::smem_addr(bar))
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] . B[smem]^T (kind::f16), issued by one thread.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t v, __half2 s) {
+  __half2 h = __hmul2(*reinterpret_cast<__half2*>(&v), s);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// TMEM column of stage s, matrix m, in the decoded-weight region.
+__device__ __forceinline__ uint32_t a_col(int s, int m, int nmat) { return kAcol0 + s * 32 * nmat + 32 * m; }
+
+// Weight row of feature f (tile row) of matrix m of expert e.
+__device__ __forceinline__ int64_t weight_row(const GroupedGemm& a, int64_t e, int m, int64_t f) {
+  return e * a.Nw + (int64_t)m * a.Nout + f;
+}
+
+// f16x2 holding 2^(s-127) in both halves: NaN for 0xFF; the exponent clamped to the f16
+// range (a block whose nonzero codes need a scale outside 2^-23..2^13 is reported, and all-zero
+// codes stay zero under any finite scale).
+__device__ __forceinline__ __half2 scale_h2(uint32_t sb) {
+  if (sb == 255u) return __half2half2(__ushort_as_half((unsigned short)0x7e00u));
+  int se = (int)sb - 127;
+  se = se < -24 ? -24 : (se > 15 ? 15 : se);
+  const unsigned short bits = se >= -14 ? (unsigned short)((se + 15) << 10) : (unsigned short)(1u << (se + 24));
+  return __half2half2(__ushort_as_half(bits));
+}
+
+// 16 E2M1 codes of one 32-element block (16 bytes, low nibble first) -> 16 f16x2 words scaled.
+__device__ __forceinline__ void decode_block(const uint4 w, uint32_t sb, uint32_t* out, bool& bad) {
+  const int se = (int)sb - 127;
+  if ((w.x | w.y | w.z | w.w) && sb != 255u && (se < -23 || se > 13)) bad = true;
+  const __half2 s2 = scale_h2(sb);
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t o0, o1, o2, o3;
+    moe::e2m1x8_to_f16x2(ws[q], o0, o1, o2, o3);
+    out[4 * q + 0] = hmul2_u32(o0, s2);
+    out[4 * q + 1] = hmul2_u32(o1, s2);
+    out[4 * q + 2] = hmul2_u32(o2, s2);
+    out[4 * q + 3] = hmul2_u32(o3, s2);
+  }
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_ts_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+                      TArgs ta) {
+  constexpr int NMAT = (EPI == EPI_SWIGLU) ? 2 : 1;
+  constexpr int NACC = (EPI == EPI_SWIGLU) ? 1 : 2;  // accumulator sets: G | U, or two alternating
+  const GroupedGemm& a = ta.g;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const TLayout L = tlayout(NMAT, ta.scw);
+  constexpr int S1 = smem_stages(NMAT), S2 = tmem_stages(NMAT);
+  uint64_t* ld_full = reinterpret_cast<uint64_t*>(smem + L.bars);  // [S1] token tile + raw codes landed
+  uint64_t* empty = ld_full + S1;                                   // [S1] shared stage consumed by the MMA
+  uint64_t* a_full = empty + S1;                                    // [S2] decoded weights in TMEM
+  uint64_t* a_empty = a_full + S2;                                  // [S2] TMEM stage consumed by the MMA
+  uint64_t* tfull = a_empty + S2;                                   // [2]
+  uint64_t* tempty = tfull + 2;                                     // [2]
+  uint64_t* drain = tempty + 2;
+  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(taddr_s + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < S1; ++s) {
+      tc::mbar_init(&ld_full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < S2; ++s) {
+      tc::mbar_init(&a_full[s], 8);
+      tc::mbar_init(&a_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&tfull[i], 1);
+      tc::mbar_init(&tempty[i], 4);
+    }
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::mbar_fence_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(taddr_s, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t taddr = *taddr_s;
+  const int ntpp = *a.ntpp;
+  const int Kin = a.Kin, nk = Kin / kBK, nkb = Kin / 32;
+  const uint32_t smem_s = tc::smem_addr(smem);
+  bool bad = false;
+
+  if (warp == 1) {
+    // ------------------------------------------------------------------ TMA loads
+    if (lane == 0) {
+      tma::prefetch_map(&tmap_x);
+      tma::prefetch_map(&tmap_w);
+    }
+    const int64_t rows_total = a.act_per_pair ? a.P : a.P / a.k;
+    const uint32_t stage_bytes = kTN * 128 + NMAT * kTM * (kBK / 2);
+    uint32_t it = 0;
+    for (int64_t t = blockIdx.x; t < ta.tiles && !*abort_flag; t += gridDim.x) {
+      int64_t blk, e;
+      int mt;
+      if (!tile_info(ta, t, ntpp, blk, mt, e)) continue;
+      // token rows of slots 4 lane .. 4 lane + 3 (this lane's gather); an empty slot reads
+      // past the end of the activations (zeros).  Rows already in slot order need no gather.
+      int32_t y[4] = {0, 0, 0, 0};
+      if (!a.act_by_slot) {
+        const int4 p4 = *reinterpret_cast<const int4*>(a.sorted + blk * a.bm + 4 * lane);
+        const int pv[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          y[j] = (int32_t)(pv[j] < a.P ? (a.act_per_pair ? (int64_t)pv[j] : (int64_t)(pv[j] / a.k)) : rows_total);
+      }
+      const int64_t f0 = (int64_t)mt * kTM;
+      bool ok = true;
+      for (int kc = 0; kc < nk; ++kc) {
+        const int s = (int)(it % S1);
+        if (lane == 0) ok = tc::mbar_wait(&empty[s], ((it / S1) & 1) ^ 1);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const uint32_t sl = smem_s + s * L.slot;
+        if (lane == 0) tma::mbar_arrive_expect_tx(&ld_full[s], stage_bytes);
+        __syncwarp();
+        if (a.act_by_slot) {  // the block's 128 slot rows: one box
+          if (lane == 0) tma::load_2d(sl, &tmap_x, kc * 128, (int32_t)(blk * a.bm), &ld_full[s]);
+        } else {  // rows 4 lane .. 4 lane + 3 of the token tile: every lane issues its own gather
+          tma_gather4(sl + lane * 512, &tmap_x, kc * 128, y[0], y[1], y[2], y[3], &ld_full[s]);
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int m = 0; m < NMAT; ++m)
+            tma::load_2d(sl + L.raw + m * kTM * (kBK / 2), &tmap_w, kc * (kBK / 2), (int32_t)weight_row(a, e, m, f0),
+                         &ld_full[s]);
+        }
+        ++it;
+      }
+      if (!ok) {
+        if (lane == 0) moe::set_status(a.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+    }
+  } else if (warp >= kDecWarp0) {
+    // ------------------------------------------------------------------ decoders
+    const int dj = warp - kDecWarp0, q = dj & 3, part = dj >> 2;
+    const int m = NMAT == 2 ? part : 0;   // matrix (SwiGLU: gate, up)
+    const int kh = NMAT == 2 ? 0 : part;  // K half of the stage (single matrix)
+    const int r = 32 * q + lane;          // tile row = TMEM lane
+    const int scw = ta.scw;
+    uint32_t* scb = reinterpret_cast<uint32_t*>(smem + L.sc) + (dj * 32 + lane) * scw;
+    const uint32_t scb_s = smem_s + L.sc + (uint32_t)((dj * 32 + lane) * scw * 4);
+    const uint32_t buf_words = 256u * (uint32_t)scw;
+    // this thread's scale row of tile (mt, e) into buffer `buf`; one copy group
+    auto issue_scales = [&](int mt, int64_t e, int buf) {
+      const int64_t f = (int64_t)mt * kTM + r;
+      if (f < a.Nout) {
+        const int64_t off = weight_row(a, e, m, f) * nkb;
+        const int64_t w0 = off & ~int64_t(3);
+        const int nw = (int)((((off + nkb + 3) & ~int64_t(3)) - w0) >> 2);
+        for (int i = 0; i < nw; ++i) cp_async4(scb_s + (buf * buf_words + i) * 4, a.w_scale + w0 + 4 * i);
+      }
+      cp_async_commit();
+    };
+    uint32_t it = 0;
+    int buf = 0;
+    int64_t t = next_tile(ta, blockIdx.x, ntpp);
+    int64_t blk = 0, e = 0;
+    int mt = 0;
+    if (t < ta.tiles) {
+      tile_info(ta, t, ntpp, blk, mt, e);
+      issue_scales(mt, e, 0);
+    }
+    while (t < ta.tiles && !*abort_flag) {
+      // the next tile in this block's sequence: its expert id is read now and its scale
+      // rows are requested after the first stage, off the critical path
+      const int64_t tn = t + gridDim.x;
+      const int64_t blk_n = tn / ta.m_tiles;
+      const int mt_n = (int)(tn - blk_n * ta.m_tiles);
+      const bool live_n = tn < ta.tiles && blk_n * a.bm < ntpp;
+      const int64_t e_n = live_n ? (int64_t)a.expert_ids[blk_n] : -1;
+      bool issued_n = false;
+      const int64_t f = (int64_t)mt * kTM + r;
+      const bool valid = f < a.Nout;
+      bool ok = true;
+      for (int kc = 0; kc < nk; ++kc) {
+        if (kc == 1 || (kc == 0 && nk == 1)) {  // this tile's scales landed; request the next tile's
+          if (e_n >= 0 && e_n < a.E) {
+            issue_scales(mt_n, e_n, buf ^ 1);
+            cp_async_wait<1>();
+            issued_n = true;
+          } else {
+            cp_async_wait<0>();
+          }
+        }
+        if (kc == 0 && nk > 1) cp_async_wait<0>();
+        const uint8_t* sc = reinterpret_cast<const uint8_t*>(scb + buf * buf_words) +
+                            (valid ? (int)((weight_row(a, e, m, f) * nkb) & 3) : 0);
+        const int s = (int)(it % S1), s2 = (int)(it % S2);
+        if (!tc::mbar_wait(&ld_full[s], (it / S1) & 1) || !tc::mbar_wait(&a_empty[s2], ((it / S2) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();  // the MMA that read this TMEM stage before has completed
+        const uint8_t* raw = smem + s * L.slot + L.raw + m * kTM * (kBK / 2) + r * (kBK / 2);
+        const uint32_t dst = taddr + ((uint32_t)(32 * q) << 16) + a_col(s2, m, NMAT);
+        if (NMAT == 2) {
+          uint32_t v[32];
+          const uint4 w0 = *reinterpret_cast<const uint4*>(raw);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(raw + 16);
+          decode_block(w0, valid ? sc[2 * kc] : 127u, v, bad);
+          decode_block(w1, valid ? sc[2 * kc + 1] : 127u, v + 16, bad);
+          tmem_st16(dst, v);
+          tmem_st16(dst + 16, v + 16);
+        } else {
+          uint32_t v[16];
+          const uint4 w = *reinterpret_cast<const uint4*>(raw + kh * 16);
+          decode_block(w, valid ? sc[2 * kc + kh] : 127u, v, bad);
+          tmem_st16(dst + kh * 16, v);
+        }
+        tc::tmem_st_wait();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&a_full[s2]);
+        ++it;
+      }
+      if (!ok) {
+        moe::set_status(a.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      buf ^= 1;
+      if (issued_n) {
+        t = tn;
+        blk = blk_n;
+        mt = mt_n;
+        e = e_n;
+      } else {  // no live next tile, or an expert id the roles skip: search on
+        t = next_tile(ta, tn, ntpp);
+        if (t < ta.tiles) {
+          tile_info(ta, t, ntpp, blk, mt, e);
+          issue_scales(mt, e, buf);
+        }
+      }
+    }
+    cp_async_wait<0>();
+  } else if (warp == 0) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_f16(kTM, kTN, 0);
+      uint32_t it = 0, acc_it = 0;
+      for (int64_t t = blockIdx.x; t < ta.tiles && !*abort_flag; t += gridDim.x) {
+        int64_t blk, e;
+        int mt;
+        if (!tile_info(ta, t, ntpp, blk, mt, e)) continue;
+        const int acc = NACC == 2 ? (int)(acc_it & 1) : 0;
+        if (!tc::mbar_wait(&tempty[acc], ((acc_it / NACC) & 1) ^ 1)) {
+          moe::set_status(a.status, MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc::tc_fence_after();
+        bool ok = true;
+        for (int kc = 0; kc < nk; ++kc) {
+          const int s = (int)(it % S1), s2 = (int)(it % S2);
+          if (!tc::mbar_wait(&ld_full[s], (it / S1) & 1) || !tc::mbar_wait(&a_full[s2], (it / S2) & 1)) {
+            moe::set_status(a.status, MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t bs = smem_s + s * L.slot;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t bd = tc::sdesc_sw128(bs + kk * 32);
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m)
+              mma_ts(taddr + (NMAT == 2 ? m * 128 : acc * 128), taddr + a_col(s2, m, NMAT) + kk * 8, bd, idesc,
+                     (kc | kk) != 0);
+          }
+          tc::mma_commit(&empty[s]);
+          tc::mma_commit(&a_empty[s2]);
+          ++it;
+        }
+        if (!ok) break;
+        tc::mma_commit(&tfull[acc]);
+        ++acc_it;
+      }
+      tc::mma_commit(drain);
+      if (!tc::mbar_wait(drain, 0)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp - kEpiWarp0;
+    const uint16_t* bias = static_cast<const uint16_t*>(a.bias);
+    uint32_t acc_it = 0;
+    for (int64_t t = blockIdx.x; t < ta.tiles && !*abort_flag; t += gridDim.x) {
+      int64_t blk, e;
+      int mt;
+      if (!tile_info(ta, t, ntpp, blk, mt, e)) continue;
+      const int acc = NACC == 2 ? (int)(acc_it & 1) : 0;
+      int pls[kTN / 32];  // pair of token column 32 i + lane, read while the MMAs run
+      float wls[kTN / 32];
+#pragma unroll
+      for (int i = 0; i < kTN / 32; ++i) pls[i] = a.sorted[blk * a.bm + 32 * i + lane];
+      const int64_t slot0 = blk * a.bm;
+#pragma unroll
+      for (int i = 0; i < kTN / 32; ++i)
+        wls[i] = (EPI == EPI_WEIGHTED_F32 && pls[i] < a.P) ? a.topk_w[pls[i]] : 1.f;
+      if (!tc::mbar_wait(&tfull[acc], (acc_it / NACC) & 1)) {
+        moe::set_status(a.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      tc::tc_fence_after();
+      const int64_t f = (int64_t)mt * kTM + 32 * q + lane;  // this lane's feature
+      const bool fvalid = f < a.Nout;
+      float b0 = 0.f, b1 = 0.f;
+      if (bias && fvalid) {
+        b0 = moe::bf16_bits_to_f32(bias[e * a.Nw + f]);
+        if (EPI == EPI_SWIGLU) b1 = moe::bf16_bits_to_f32(bias[e * a.Nw + a.Nout + f]);
+      }
+      const uint32_t tb = taddr + ((uint32_t)(32 * q) << 16);
+#pragma unroll
+      for (int c0 = 0; c0 < kTN; c0 += 32) {
+        const int pl = pls[c0 / 32];
+        uint32_t v0[32];
+        tc::tmem_ld32(tb + (NMAT == 2 ? 0 : acc * 128) + c0, v0);
+        if (EPI == EPI_SWIGLU) {
+          uint32_t v1[32];
+          tc::tmem_ld32(tb + 128 + c0, v1);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int p = __shfl_sync(0xffffffffu, pl, j);
+            if (p < a.P && fvalid) {
+              const float gt = __uint_as_float(v0[j]) + b0, up = __uint_as_float(v1[j]) + b1;
+              const __half hv = __float2half_rn(moe::silu(gt) * up);
+              if (__hisinf(hv) || __hisnan(hv)) bad = true;
+              const int64_t row = a.out_by_slot ? slot0 + c0 + j : (int64_t)p;
+              static_cast<__half*>(a.out)[row * a.Nout + f] = hv;
+            }
+          }
+        } else {
+          tc::tmem_ld_wait();
+          const float wl = wls[c0 / 32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int p = __shfl_sync(0xffffffffu, pl, j);
+            const float wp = __shfl_sync(0xffffffffu, wl, j);
+            if (p < a.P && fvalid) {
+              const float o = __uint_as_float(v0[j]) + b0;
+              const int64_t row = a.out_by_slot ? slot0 + c0 + j : (int64_t)p;
+              if (EPI == EPI_WEIGHTED_F32)
+                static_cast<float*>(a.out)[row * a.Nout + f] = o * wp;
+              else
+                static_cast<uint16_t*>(a.out)[row * a.Nout + f] = moe::f32_to_bf16_bits(o);
+            }
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+      ++acc_it;
+    }
+  }
+  if (bad) moe::set_status(a.status, MOE_ERR_RANGE);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(taddr, kTmemCols);
+  }
+}
+
+int sm_count_ts() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+int scale_words(int Kin) { return (Kin / 32 + 3) / 4 + 1; }
+
+template <int EPI>
+cudaError_t launch_ts(const TArgs& ta, const CUtensorMap& mx, const CUtensorMap& mw, cudaStream_t stream) {
+  const TLayout L = tlayout(EPI == EPI_SWIGLU ? 2 : 1, ta.scw);
+  cudaError_t err = cudaFuncSetAttribute(prefill_ts_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  if (err != cudaSuccess) return err;
+  int64_t grid = sm_count_ts();
+  if (ta.tiles < grid) grid = ta.tiles;
+  if (grid <= 0) return cudaSuccess;
+  prefill_ts_kernel<EPI><<<(unsigned)grid, kThreads, L.total, stream>>>(mx, mw, ta);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace moe_launch {
+
+bool ts_supported(const GroupedGemm& g) {
+  if (g.wfmt != WF_MXFP4 || g.act_fmt != ACT_F16) return false;
+  if (g.epi != EPI_SWIGLU && g.epi != EPI_WEIGHTED_F32 && g.epi != EPI_PLAIN_BF16) return false;
+  if (g.bm != kTN || g.Kin <= 0 || g.Kin % kBK != 0 || g.Kin > kMaxKin) return false;
+  const int64_t rows_total = g.act_by_slot ? g.grid_blocks * g.bm : (g.act_per_pair ? g.P : g.P / g.k);
+  if (rows_total >= ((int64_t)1 << 31) - 1 || (int64_t)g.E * g.Nw >= ((int64_t)1 << 31)) return false;
+  // the decoders copy each scale row in whole 32-bit words: the scale array must end on one
+  if ((g.Nw * (int64_t)(g.Kin / 32)) % 4 != 0) return false;
+  // TMA sources 16-byte aligned; 4-byte copies of the scale words
+  const uintptr_t al16 = reinterpret_cast<uintptr_t>(g.act) | reinterpret_cast<uintptr_t>(g.w);
+  if ((al16 & 15) != 0 || (reinterpret_cast<uintptr_t>(g.w_scale) & 3) != 0) return false;
+  return tlayout(g.epi == EPI_SWIGLU ? 2 : 1, scale_words(g.Kin)).total <= 227 * 1024;
+}
+
+cudaError_t prefill_ts(const GroupedGemm& g, cudaStream_t stream) {
+  if (!ts_supported(g)) return cudaErrorInvalidValue;
+  TArgs ta;
+  ta.g = g;
+  ta.nmat = g.epi == EPI_SWIGLU ? 2 : 1;
+  ta.m_tiles = (g.Nout + kTM - 1) / kTM;
+  ta.tiles = g.grid_blocks * ta.m_tiles;
+  ta.scw = scale_words(g.Kin);
+  const int64_t rows_total = g.act_by_slot ? g.grid_blocks * g.bm : (g.act_per_pair ? g.P : g.P / g.k);
+  // token rows of Kin f16 in 128-byte swizzle: 128 slot rows per box when the rows are in
+  // slot order, else gathered one row at a time; weight rows of Kin / 2 bytes of E2M1 codes
+  // (boxes of one stage's 32 bytes x 128 rows)
+  CUtensorMap mx, mw;
+  if (!tma::encode_2d_u8(&mx, g.act, (uint64_t)g.Kin * 2, (uint64_t)rows_total, (uint64_t)g.Kin * 2, 128,
+                         g.act_by_slot ? kTN : 1, true))
+    return cudaErrorInvalidValue;
+  if (!tma::encode_2d_u8(&mw, g.w, (uint64_t)g.Kin / 2, (uint64_t)g.E * g.Nw, (uint64_t)g.Kin / 2, kBK / 2, kTM,
+                         false))
+    return cudaErrorInvalidValue;
+  if (g.epi == EPI_SWIGLU) return launch_ts<EPI_SWIGLU>(ta, mx, mw, stream);
+  if (g.epi == EPI_WEIGHTED_F32) return launch_ts<EPI_WEIGHTED_F32>(ta, mx, mw, stream);
+  return launch_ts<EPI_PLAIN_BF16>(ta, mx, mw, stream);
+}
+
+}  // namespace moe_launch

@@ -48,21 +48,29 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 
 // One warp selects one token's top-k: k rounds of a warp arg-max over the unchosen
 // logits.  Lane j < k writes the j-th id and, for now, the chosen logit itself into the
-// weight slot (the softmax replaces it).
+// weight slot (the softmax replaces it).  The row is read once into registers (lane holds
+// entries lane + 32 i); NPER is the compile-time bound on E / 32.
+template <int NPER>
 __device__ void select_topk(const float* __restrict__ row, int E, int k,
                             int32_t* __restrict__ ids_out, float* __restrict__ w_out, int lane) {
-  uint32_t taken = 0;  // bit i <=> entry lane + 32*i already chosen (E <= 1024)
+  float v[NPER];
+#pragma unroll
+  for (int i = 0; i < NPER; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? row[e] : -INFINITY;
+  }
+  uint32_t taken = 0;  // bit i <=> entry lane + 32*i already chosen
   float my_val = 0.f;
   int my_idx = 0;
-  const int nper = (E + 31) >> 5;
   for (int j = 0; j < k; ++j) {
     float best = -INFINITY;
     int bidx = INT_MAX;
-    for (int i = 0; i < nper; ++i) {
-      int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u)) {
-        float v = row[e];
-        if (better(v, e, best, bidx)) { best = v; bidx = e; }
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && better(v[i], e, best, bidx)) {
+        best = v[i];
+        bidx = e;
       }
     }
 #pragma unroll
@@ -78,6 +86,14 @@ __device__ void select_topk(const float* __restrict__ row, int E, int k,
     ids_out[lane] = my_idx;
     w_out[lane] = my_val;
   }
+}
+
+__device__ void select_topk_any(const float* __restrict__ row, int E, int k, int32_t* __restrict__ ids_out,
+                                float* __restrict__ w_out, int lane) {
+  if (E <= 64) select_topk<2>(row, E, k, ids_out, w_out, lane);
+  else if (E <= 128) select_topk<4>(row, E, k, ids_out, w_out, lane);
+  else if (E <= 256) select_topk<8>(row, E, k, ids_out, w_out, lane);
+  else select_topk<32>(row, E, k, ids_out, w_out, lane);
 }
 
 // One lane turns one token's k chosen logits (descending, in w[0..k)) into routing
@@ -113,7 +129,7 @@ __device__ void route_block(const float* __restrict__ logits, int64_t t0, int n,
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   for (int i = warp; i < n; i += nw) {
     const int64_t t = t0 + i;
-    select_topk(logits + t * E, E, k, ids + t * k, w + t * k, lane);
+    select_topk_any(logits + t * E, E, k, ids + t * k, w + t * k, lane);
   }
   __syncthreads();
   if ((int)threadIdx.x < n) softmax_topk(w + (t0 + threadIdx.x) * k, k);
@@ -240,11 +256,21 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(AlignArgs a) {
     if (e >= 0 && lane == __ffs(grp) - 1) myhist[e] += __popc(grp);
     __syncwarp();
   }
-  // sentinel fill of each expert's padding and of the tail up to the capacity
-  if (tid < E) {
-    for (int s = poff[tid] + cnt[tid]; s < poff[tid + 1]; ++s) a.sorted[s] = P;
+  // sentinel fill of each expert's padding and of the tail up to the capacity: consecutive
+  // threads take consecutive slots (coalesced stores); a slot below the padded total is
+  // padding when it lies past its expert's pairs
+  for (int64_t s = tid; s < a.cap; s += kAlignThreads) {
+    bool pad = s >= total_pad;
+    if (!pad) {
+      int lo = 0, hi = E;  // last e with poff[e] <= s
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (poff[mid] <= s) lo = mid; else hi = mid;
+      }
+      pad = s >= (int64_t)poff[lo] + cnt[lo];
+    }
+    if (pad) a.sorted[s] = P;
   }
-  for (int64_t s = (int64_t)total_pad + tid; s < a.cap; s += kAlignThreads) a.sorted[s] = P;
   // per-block expert ids; -1 past the last used block
   const int64_t cap_blocks = a.cap / bm;
   for (int64_t b = tid; b < cap_blocks; b += kAlignThreads) {

@@ -39,7 +39,7 @@ class DeviceLayer:
         self.expert_offsets = torch.empty(E + 1 + (-(E + 1)) % 4, dtype=torch.int32, device=dev)
         self.x_pad = torch.zeros((rows, K), dtype=torch.bfloat16, device=dev)
         self.logits_pad = torch.zeros((rows, E), dtype=torch.float32, device=dev)
-        self.ws_bytes = moe_forward_workspace_size(rows, k, K, I)
+        self.ws_bytes = moe_forward_workspace_size(rows, k, K, I, self.cap)
         self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         self.status = torch.zeros(4, dtype=torch.int32, device=dev)
         self._ctx_cache = {}

@@ -67,11 +67,15 @@ def test_capacity_matches_oracle(lib, P, E, bm):
 
 
 def test_workspace_size(lib):
-    n = moe.moe_forward_workspace_size(64, 4, 2880, 2880)
-    P = 256
     r = lambda v: (v + 255) // 256 * 256
+    cap, _ = moe.moe_align_capacity(256, 128, 128)
+    n = moe.moe_forward_workspace_size(64, 4, 2880, 2880, cap)
+    P = 256  # up to 256 rows: h and x in pair / token order
     assert n == r(P * 2880 * 2) + r(P * 2880 * 4) + r(64 * 2880 * 2)
-    assert moe.moe_forward_workspace_size(-1, 4, 1, 1) == 0
+    cap, _ = moe.moe_align_capacity(4 * 1000, 128, 128)
+    n = moe.moe_forward_workspace_size(1000, 4, 2880, 2880, cap)
+    assert n == r(cap * 2880 * 2) + r(4000 * 2880 * 4) + r(cap * 2880 * 2)  # slot order
+    assert moe.moe_forward_workspace_size(-1, 4, 1, 1, 0) == 0
 
 
 def test_argument_errors_are_reported_without_a_launch(lib):
