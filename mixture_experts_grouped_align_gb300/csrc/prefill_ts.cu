@@ -52,33 +52,37 @@ constexpr int kTN = 128;    // pairs per tile (one alignment block): MMA N
 constexpr int kBK = 64;     // K elements per stage
 // Shared-memory stages (token tile + raw codes) and TMEM stages (decoded weights) form two
 // rings: copies may run further ahead of the MMA than the TMEM columns allow decoding to.
-__host__ __device__ constexpr int smem_stages(int nmat) { return nmat == 2 ? 6 : 8; }
+__host__ __device__ constexpr int smem_stages(int nmat) { return nmat == 2 ? 5 : 10; }
 __host__ __device__ constexpr int tmem_stages(int nmat) { return nmat == 2 ? 4 : 8; }
 constexpr int kEpiWarp0 = 4, kDecWarp0 = 8;
 constexpr int kTmemCols = 512;
 constexpr int kAcol0 = 256;  // first TMEM column of the decoded weight stages
 constexpr int kMaxKin = 4096;
+// The raw codes of a weight row are loaded 128 bytes (four K stages) per TMA box, into a
+// ring of their own.
+constexpr int kGroup = 4;
+constexpr int kRawSlots = 3;
 
 struct TArgs {
   GroupedGemm g;
   int nmat;          // 2 for SwiGLU (gate and up rows), else 1
   int m_tiles;       // feature tiles per block: ceil(Nout / 128)
   int64_t tiles;     // block slots * m_tiles
-  int scw;           // 32-bit words of one thread's scale-row buffer
 };
 
-// Shared memory: stages [B tile 16 KB | raw weight rows nmat x 4 KB] | scale rows
-// [2 tiles][256 decoder threads][scw words] | barriers.
+// Shared memory: token-tile stages (16 KB each) | raw-code slots (nmat x 128 rows x 128 B,
+// 128-byte swizzle) | SwiGLU output staging (128 slots x 128 f16) | barriers.
 struct TLayout {
-  int slot, raw, sc, bars, total;
+  int slot, raw, raw_slot, stg, bars, total;
 };
 
-__host__ __device__ inline TLayout tlayout(int nmat, int scw) {
+__host__ __device__ inline TLayout tlayout(int nmat) {
   TLayout L;
-  L.raw = kTN * 128;
-  L.slot = L.raw + nmat * kTM * (kBK / 2);
-  L.sc = smem_stages(nmat) * L.slot;
-  L.bars = L.sc + 2 * 256 * scw * 4;
+  L.slot = kTN * 128;
+  L.raw = smem_stages(nmat) * L.slot;
+  L.raw_slot = nmat * kTM * 128;
+  L.stg = L.raw + kRawSlots * L.raw_slot;
+  L.bars = L.stg + (nmat == 2 ? kTN * kTM * 2 : 0);
   L.total = L.bars + 512 + 1024;
   return L;
 }
@@ -99,13 +103,6 @@ __device__ __forceinline__ int64_t next_tile(const TArgs& ta, int64_t t, int ntp
   while (t < ta.tiles && !tile_info(ta, t, ntpp, blk, mt, e)) t += gridDim.x;
   return t;
 }
-
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 // TMA gather of four 128-byte rows (rows y0..y3 of the tensor, bytes x..x+127) to dst.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y0,
@@ -181,22 +178,25 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_ts_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-                      TArgs ta) {
+                      const __grid_constant__ CUtensorMap tmap_h, TArgs ta) {
   constexpr int NMAT = (EPI == EPI_SWIGLU) ? 2 : 1;
   constexpr int NACC = (EPI == EPI_SWIGLU) ? 1 : 2;  // accumulator sets: G | U, or two alternating
   const GroupedGemm& a = ta.g;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const TLayout L = tlayout(NMAT, ta.scw);
+  const TLayout L = tlayout(NMAT);
   constexpr int S1 = smem_stages(NMAT), S2 = tmem_stages(NMAT);
   uint64_t* ld_full = reinterpret_cast<uint64_t*>(smem + L.bars);  // [S1] token tile + raw codes landed
   uint64_t* empty = ld_full + S1;                                   // [S1] shared stage consumed by the MMA
   uint64_t* a_full = empty + S1;                                    // [S2] decoded weights in TMEM
   uint64_t* a_empty = a_full + S2;                                  // [S2] TMEM stage consumed by the MMA
-  uint64_t* tfull = a_empty + S2;                                   // [2]
+  uint64_t* raw_full = a_empty + S2;                                // [kRawSlots] raw codes landed
+  uint64_t* raw_empty = raw_full + kRawSlots;                       // [kRawSlots] decoded by all
+  uint64_t* tfull = raw_empty + kRawSlots;                          // [2]
   uint64_t* tempty = tfull + 2;                                     // [2]
   uint64_t* drain = tempty + 2;
-  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* epi_bar = drain + 1;  // the four epilogue warps meet here (bounded, unlike bar.sync)
+  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(epi_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(taddr_s + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -209,11 +209,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&a_full[s], 8);
       tc::mbar_init(&a_empty[s], 1);
     }
+    for (int s = 0; s < kRawSlots; ++s) {
+      tc::mbar_init(&raw_full[s], 1);
+      tc::mbar_init(&raw_empty[s], 8);
+    }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&tfull[i], 1);
       tc::mbar_init(&tempty[i], 4);
     }
     tc::mbar_init(drain, 1);
+    tc::mbar_init(epi_bar, 4);
     *abort_flag = 0;
     tc::mbar_fence_init();
   }
@@ -237,8 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma::prefetch_map(&tmap_w);
     }
     const int64_t rows_total = a.act_per_pair ? a.P : a.P / a.k;
-    const uint32_t stage_bytes = kTN * 128 + NMAT * kTM * (kBK / 2);
-    uint32_t it = 0;
+    const uint32_t stage_bytes = kTN * 128;
+    const uint32_t raw_bytes = NMAT * kTM * 128;
+    uint32_t it = 0, gi = 0;
     for (int64_t t = blockIdx.x; t < ta.tiles && !*abort_flag; t += gridDim.x) {
       int64_t blk, e;
       int mt;
@@ -256,6 +262,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t f0 = (int64_t)mt * kTM;
       bool ok = true;
       for (int kc = 0; kc < nk; ++kc) {
+        if (kc % kGroup == 0) {  // raw codes of stages kc .. kc + 3: 128 bytes of every row
+          const int rs = (int)(gi % kRawSlots);
+          if (lane == 0) ok = tc::mbar_wait(&raw_empty[rs], ((gi / kRawSlots) & 1) ^ 1);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (lane == 0) {
+            const uint32_t rsl = smem_s + L.raw + rs * L.raw_slot;
+            tma::mbar_arrive_expect_tx(&raw_full[rs], raw_bytes);
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m)
+              tma::load_2d(rsl + m * kTM * 128, &tmap_w, (kc / kGroup) * 128, (int32_t)weight_row(a, e, m, f0),
+                           &raw_full[rs]);
+          }
+          ++gi;
+        }
         const int s = (int)(it % S1);
         if (lane == 0) ok = tc::mbar_wait(&empty[s], ((it / S1) & 1) ^ 1);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -267,12 +288,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) tma::load_2d(sl, &tmap_x, kc * 128, (int32_t)(blk * a.bm), &ld_full[s]);
         } else {  // rows 4 lane .. 4 lane + 3 of the token tile: every lane issues its own gather
           tma_gather4(sl + lane * 512, &tmap_x, kc * 128, y[0], y[1], y[2], y[3], &ld_full[s]);
-        }
-        if (lane == 0) {
-#pragma unroll
-          for (int m = 0; m < NMAT; ++m)
-            tma::load_2d(sl + L.raw + m * kTM * (kBK / 2), &tmap_w, kc * (kBK / 2), (int32_t)weight_row(a, e, m, f0),
-                         &ld_full[s]);
         }
         ++it;
       }
@@ -288,81 +303,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int m = NMAT == 2 ? part : 0;   // matrix (SwiGLU: gate, up)
     const int kh = NMAT == 2 ? 0 : part;  // K half of the stage (single matrix)
     const int r = 32 * q + lane;          // tile row = TMEM lane
-    const int scw = ta.scw;
-    uint32_t* scb = reinterpret_cast<uint32_t*>(smem + L.sc) + (dj * 32 + lane) * scw;
-    const uint32_t scb_s = smem_s + L.sc + (uint32_t)((dj * 32 + lane) * scw * 4);
-    const uint32_t buf_words = 256u * (uint32_t)scw;
-    // this thread's scale row of tile (mt, e) into buffer `buf`; one copy group
-    auto issue_scales = [&](int mt, int64_t e, int buf) {
+    const int ngroups = (nk + kGroup - 1) / kGroup;
+    // The eight E8M0 bytes of this row's K group g (blocks 8g .. 8g + 7), read from global
+    // memory one group ahead into registers; 127 (scale 1) for a row past the features.
+    auto load_scales = [&](int64_t e, int mt, int g, uint32_t (&w)[2]) {
+      w[0] = w[1] = 0x7f7f7f7fu;
       const int64_t f = (int64_t)mt * kTM + r;
-      if (f < a.Nout) {
-        const int64_t off = weight_row(a, e, m, f) * nkb;
-        const int64_t w0 = off & ~int64_t(3);
-        const int nw = (int)((((off + nkb + 3) & ~int64_t(3)) - w0) >> 2);
-        for (int i = 0; i < nw; ++i) cp_async4(scb_s + (buf * buf_words + i) * 4, a.w_scale + w0 + 4 * i);
-      }
-      cp_async_commit();
+      if (f >= a.Nout) return;
+      const uint8_t* src = a.w_scale + weight_row(a, e, m, f) * nkb + 8 * g;
+      uint32_t v[2] = {0u, 0u};
+#pragma unroll
+      for (int bb = 0; bb < 8; ++bb)
+        if (8 * g + bb < nkb) v[bb >> 2] |= (uint32_t)__ldg(src + bb) << (8 * (bb & 3));
+      w[0] = v[0];
+      w[1] = v[1];
     };
-    uint32_t it = 0;
-    int buf = 0;
+    uint32_t it = 0, gi = 0;
     int64_t t = next_tile(ta, blockIdx.x, ntpp);
     int64_t blk = 0, e = 0;
     int mt = 0;
+    uint32_t sc_next[2] = {0x7f7f7f7fu, 0x7f7f7f7fu};
     if (t < ta.tiles) {
       tile_info(ta, t, ntpp, blk, mt, e);
-      issue_scales(mt, e, 0);
+      load_scales(e, mt, 0, sc_next);
     }
     while (t < ta.tiles && !*abort_flag) {
-      // the next tile in this block's sequence: its expert id is read now and its scale
-      // rows are requested after the first stage, off the critical path
+      // the next tile in this block's sequence, read now for the scale prefetch of its first group
       const int64_t tn = t + gridDim.x;
       const int64_t blk_n = tn / ta.m_tiles;
       const int mt_n = (int)(tn - blk_n * ta.m_tiles);
       const bool live_n = tn < ta.tiles && blk_n * a.bm < ntpp;
       const int64_t e_n = live_n ? (int64_t)a.expert_ids[blk_n] : -1;
-      bool issued_n = false;
-      const int64_t f = (int64_t)mt * kTM + r;
-      const bool valid = f < a.Nout;
+      const bool next_ok = e_n >= 0 && e_n < a.E;
       bool ok = true;
+      uint32_t sc0 = 0u, sc1 = 0u;
+      int rs = 0;
       for (int kc = 0; kc < nk; ++kc) {
-        if (kc == 1 || (kc == 0 && nk == 1)) {  // this tile's scales landed; request the next tile's
-          if (e_n >= 0 && e_n < a.E) {
-            issue_scales(mt_n, e_n, buf ^ 1);
-            cp_async_wait<1>();
-            issued_n = true;
-          } else {
-            cp_async_wait<0>();
+        const int kg = kc % kGroup, g = kc / kGroup;
+        if (kg == 0) {  // a new group of raw codes: its scales are the prefetched ones
+          rs = (int)(gi % kRawSlots);
+          sc0 = sc_next[0];
+          sc1 = sc_next[1];
+          if (g + 1 < ngroups) load_scales(e, mt, g + 1, sc_next);
+          else if (next_ok) load_scales(e_n, mt_n, 0, sc_next);
+          if (!tc::mbar_wait(&raw_full[rs], (gi / kRawSlots) & 1)) {
+            ok = false;
+            break;
           }
         }
-        if (kc == 0 && nk > 1) cp_async_wait<0>();
-        const uint8_t* sc = reinterpret_cast<const uint8_t*>(scb + buf * buf_words) +
-                            (valid ? (int)((weight_row(a, e, m, f) * nkb) & 3) : 0);
-        const int s = (int)(it % S1), s2 = (int)(it % S2);
-        if (!tc::mbar_wait(&ld_full[s], (it / S1) & 1) || !tc::mbar_wait(&a_empty[s2], ((it / S2) & 1) ^ 1)) {
+        const int s2 = (int)(it % S2);
+        if (!tc::mbar_wait(&a_empty[s2], ((it / S2) & 1) ^ 1)) {
           ok = false;
           break;
         }
         tc::tc_fence_after();  // the MMA that read this TMEM stage before has completed
-        const uint8_t* raw = smem + s * L.slot + L.raw + m * kTM * (kBK / 2) + r * (kBK / 2);
+        // row r of the slot, bytes 32 kg + 16 h of the row, in the 128-byte swizzle
+        const uint8_t* rowp = smem + L.raw + rs * L.raw_slot + m * kTM * 128 + r * 128;
         const uint32_t dst = taddr + ((uint32_t)(32 * q) << 16) + a_col(s2, m, NMAT);
+        const uint32_t scw = (kg >> 1) ? sc1 : sc0;  // scale bytes of blocks 2 kg, 2 kg + 1
+        const int sh = 16 * (kg & 1);
         if (NMAT == 2) {
           uint32_t v[32];
-          const uint4 w0 = *reinterpret_cast<const uint4*>(raw);
-          const uint4 w1 = *reinterpret_cast<const uint4*>(raw + 16);
-          decode_block(w0, valid ? sc[2 * kc] : 127u, v, bad);
-          decode_block(w1, valid ? sc[2 * kc + 1] : 127u, v + 16, bad);
+          const uint4 w0 = *reinterpret_cast<const uint4*>(rowp + (((2 * kg) ^ (r & 7)) << 4));
+          const uint4 w1 = *reinterpret_cast<const uint4*>(rowp + (((2 * kg + 1) ^ (r & 7)) << 4));
+          decode_block(w0, (scw >> sh) & 0xffu, v, bad);
+          decode_block(w1, (scw >> (sh + 8)) & 0xffu, v + 16, bad);
           tmem_st16(dst, v);
           tmem_st16(dst + 16, v + 16);
         } else {
           uint32_t v[16];
-          const uint4 w = *reinterpret_cast<const uint4*>(raw + kh * 16);
-          decode_block(w, valid ? sc[2 * kc + kh] : 127u, v, bad);
+          const uint4 w = *reinterpret_cast<const uint4*>(rowp + (((2 * kg + kh) ^ (r & 7)) << 4));
+          decode_block(w, (scw >> (sh + 8 * kh)) & 0xffu, v, bad);
           tmem_st16(dst + kh * 16, v);
         }
         tc::tmem_st_wait();
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&a_full[s2]);
+        if (kg == kGroup - 1 || kc == nk - 1) {  // this group's raw codes are decoded
+          if (lane == 0) tc::mbar_arrive(&raw_empty[rs]);
+          ++gi;
+        }
         ++it;
       }
       if (!ok) {
@@ -370,8 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
         break;
       }
-      buf ^= 1;
-      if (issued_n) {
+      if (next_ok) {
         t = tn;
         blk = blk_n;
         mt = mt_n;
@@ -380,11 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         t = next_tile(ta, tn, ntpp);
         if (t < ta.tiles) {
           tile_info(ta, t, ntpp, blk, mt, e);
-          issue_scales(mt, e, buf);
+          load_scales(e, mt, 0, sc_next);
         }
       }
     }
-    cp_async_wait<0>();
   } else if (warp == 0) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -436,7 +455,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ epilogue
     const int q = warp - kEpiWarp0;
     const uint16_t* bias = static_cast<const uint16_t*>(a.bias);
-    uint32_t acc_it = 0;
+    // SwiGLU into slot-ordered h: the tile goes through shared memory and leaves as one TMA
+    // store, and the accumulators are released before the last chunk is computed
+    const bool staged = (EPI == EPI_SWIGLU) && a.out_by_slot;
+    __half* stg = reinterpret_cast<__half*>(smem + L.stg);
+    const uint32_t stg_s = smem_s + L.stg;
+    uint32_t acc_it = 0, eb_it = 0;
+    // all four epilogue warps reach this point (a wait that runs out aborts the kernel)
+    auto epi_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(epi_bar);
+      const bool ok = tc::mbar_wait(epi_bar, eb_it & 1);
+      ++eb_it;
+      if (!ok) {
+        moe::set_status(a.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      return ok;
+    };
     for (int64_t t = blockIdx.x; t < ta.tiles && !*abort_flag; t += gridDim.x) {
       int64_t blk, e;
       int mt;
@@ -464,6 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (EPI == EPI_SWIGLU) b1 = moe::bf16_bits_to_f32(bias[e * a.Nw + a.Nout + f]);
       }
       const uint32_t tb = taddr + ((uint32_t)(32 * q) << 16);
+      if (staged) {  // the previous tile's store has finished reading the staging buffer
+        if (q == 0 && lane == 0) tma::bulk_wait_read_all();
+        if (!epi_sync()) break;
+      }
 #pragma unroll
       for (int c0 = 0; c0 < kTN; c0 += 32) {
         const int pl = pls[c0 / 32];
@@ -473,13 +513,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v1[32];
           tc::tmem_ld32(tb + 128 + c0, v1);
           tc::tmem_ld_wait();
+          if (staged && c0 == kTN - 32) {  // both accumulators drained: the next tile may start
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+          }
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int p = __shfl_sync(0xffffffffu, pl, j);
-            if (p < a.P && fvalid) {
-              const float gt = __uint_as_float(v0[j]) + b0, up = __uint_as_float(v1[j]) + b1;
-              const __half hv = __float2half_rn(moe::silu(gt) * up);
-              if (__hisinf(hv) || __hisnan(hv)) bad = true;
+            const float gt = __uint_as_float(v0[j]) + b0, up = __uint_as_float(v1[j]) + b1;
+            const __half hv = __float2half_rn(moe::silu(gt) * up);
+            if (p < a.P && fvalid && (__hisinf(hv) || __hisnan(hv))) bad = true;
+            if (staged) {
+              stg[(c0 + j) * kTM + 32 * q + lane] = hv;
+            } else if (p < a.P && fvalid) {
               const int64_t row = a.out_by_slot ? slot0 + c0 + j : (int64_t)p;
               static_cast<__half*>(a.out)[row * a.Nout + f] = hv;
             }
@@ -502,11 +549,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+      if (staged) {  // the tile's h rows [slot0, slot0 + 128) x features [f0, f0 + 128)
+        tc::fence_proxy_async_smem();
+        if (!epi_sync()) break;
+        if (q == 0 && lane == 0) {
+          tma::store_2d(&tmap_h, mt * kTM * 2, (int32_t)slot0, stg_s);
+          tma::bulk_commit();
+        }
+      } else {
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+      }
       ++acc_it;
     }
+    if (staged && q == 0 && lane == 0) tma::bulk_wait_all();
   }
   if (bad) moe::set_status(a.status, MOE_ERR_RANGE);
   tc::tc_fence_before();
@@ -528,17 +585,16 @@ int sm_count_ts() {
   return n;
 }
 
-int scale_words(int Kin) { return (Kin / 32 + 3) / 4 + 1; }
-
 template <int EPI>
-cudaError_t launch_ts(const TArgs& ta, const CUtensorMap& mx, const CUtensorMap& mw, cudaStream_t stream) {
-  const TLayout L = tlayout(EPI == EPI_SWIGLU ? 2 : 1, ta.scw);
+cudaError_t launch_ts(const TArgs& ta, const CUtensorMap& mx, const CUtensorMap& mw, const CUtensorMap& mh,
+                      cudaStream_t stream) {
+  const TLayout L = tlayout(EPI == EPI_SWIGLU ? 2 : 1);
   cudaError_t err = cudaFuncSetAttribute(prefill_ts_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
   int64_t grid = sm_count_ts();
   if (ta.tiles < grid) grid = ta.tiles;
   if (grid <= 0) return cudaSuccess;
-  prefill_ts_kernel<EPI><<<(unsigned)grid, kThreads, L.total, stream>>>(mx, mw, ta);
+  prefill_ts_kernel<EPI><<<(unsigned)grid, kThreads, L.total, stream>>>(mx, mw, mh, ta);
   return cudaGetLastError();
 }
 
@@ -552,12 +608,11 @@ bool ts_supported(const GroupedGemm& g) {
   if (g.bm != kTN || g.Kin <= 0 || g.Kin % kBK != 0 || g.Kin > kMaxKin) return false;
   const int64_t rows_total = g.act_by_slot ? g.grid_blocks * g.bm : (g.act_per_pair ? g.P : g.P / g.k);
   if (rows_total >= ((int64_t)1 << 31) - 1 || (int64_t)g.E * g.Nw >= ((int64_t)1 << 31)) return false;
-  // the decoders copy each scale row in whole 32-bit words: the scale array must end on one
-  if ((g.Nw * (int64_t)(g.Kin / 32)) % 4 != 0) return false;
-  // TMA sources 16-byte aligned; 4-byte copies of the scale words
-  const uintptr_t al16 = reinterpret_cast<uintptr_t>(g.act) | reinterpret_cast<uintptr_t>(g.w);
-  if ((al16 & 15) != 0 || (reinterpret_cast<uintptr_t>(g.w_scale) & 3) != 0) return false;
-  return tlayout(g.epi == EPI_SWIGLU ? 2 : 1, scale_words(g.Kin)).total <= 227 * 1024;
+  // TMA sources and destinations 16-byte aligned
+  uintptr_t al16 = reinterpret_cast<uintptr_t>(g.act) | reinterpret_cast<uintptr_t>(g.w);
+  if (g.out_by_slot) al16 |= reinterpret_cast<uintptr_t>(g.out);
+  if ((al16 & 15) != 0) return false;
+  return tlayout(g.epi == EPI_SWIGLU ? 2 : 1).total <= 227 * 1024;
 }
 
 cudaError_t prefill_ts(const GroupedGemm& g, cudaStream_t stream) {
@@ -567,21 +622,26 @@ cudaError_t prefill_ts(const GroupedGemm& g, cudaStream_t stream) {
   ta.nmat = g.epi == EPI_SWIGLU ? 2 : 1;
   ta.m_tiles = (g.Nout + kTM - 1) / kTM;
   ta.tiles = g.grid_blocks * ta.m_tiles;
-  ta.scw = scale_words(g.Kin);
   const int64_t rows_total = g.act_by_slot ? g.grid_blocks * g.bm : (g.act_per_pair ? g.P : g.P / g.k);
   // token rows of Kin f16 in 128-byte swizzle: 128 slot rows per box when the rows are in
   // slot order, else gathered one row at a time; weight rows of Kin / 2 bytes of E2M1 codes
-  // (boxes of one stage's 32 bytes x 128 rows)
+  // (boxes of four stages' 128 bytes x 128 rows, 128-byte swizzle)
   CUtensorMap mx, mw;
   if (!tma::encode_2d_u8(&mx, g.act, (uint64_t)g.Kin * 2, (uint64_t)rows_total, (uint64_t)g.Kin * 2, 128,
                          g.act_by_slot ? kTN : 1, true))
     return cudaErrorInvalidValue;
-  if (!tma::encode_2d_u8(&mw, g.w, (uint64_t)g.Kin / 2, (uint64_t)g.E * g.Nw, (uint64_t)g.Kin / 2, kBK / 2, kTM,
-                         false))
+  if (!tma::encode_2d_u8(&mw, g.w, (uint64_t)g.Kin / 2, (uint64_t)g.E * g.Nw, (uint64_t)g.Kin / 2, 128, kTM,
+                         true))
     return cudaErrorInvalidValue;
-  if (g.epi == EPI_SWIGLU) return launch_ts<EPI_SWIGLU>(ta, mx, mw, stream);
-  if (g.epi == EPI_WEIGHTED_F32) return launch_ts<EPI_WEIGHTED_F32>(ta, mx, mw, stream);
-  return launch_ts<EPI_PLAIN_BF16>(ta, mx, mw, stream);
+  // SwiGLU output in slot order: h rows of Nout f16, stored 128 slots x 128 features per box
+  CUtensorMap mh = mx;
+  if (g.epi == EPI_SWIGLU && g.out_by_slot &&
+      !tma::encode_2d_u8(&mh, g.out, (uint64_t)g.Nout * 2, (uint64_t)(g.grid_blocks * g.bm), (uint64_t)g.Nout * 2,
+                         kTM * 2, kTN, false))
+    return cudaErrorInvalidValue;
+  if (g.epi == EPI_SWIGLU) return launch_ts<EPI_SWIGLU>(ta, mx, mw, mh, stream);
+  if (g.epi == EPI_WEIGHTED_F32) return launch_ts<EPI_WEIGHTED_F32>(ta, mx, mw, mh, stream);
+  return launch_ts<EPI_PLAIN_BF16>(ta, mx, mw, mh, stream);
 }
 
 }  // namespace moe_launch
