@@ -123,7 +123,9 @@ MOE_DEV uint4 ldg_nc_u128(const void* p) {
   return v;
 }
 
-MOE_DEV float silu(float g) { return g / (1.0f + expf(-g)); }
+// silu(g) = g * sigmoid(g) with the hardware exponential and reciprocal (relative error
+// near 1e-6, far below the f16 / bf16 rounding of the value it feeds); 0 for g -> -inf.
+MOE_DEV float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 }  // namespace moe
 

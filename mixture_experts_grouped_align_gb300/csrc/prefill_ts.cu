@@ -17,19 +17,24 @@
 // shared memory.  SwiGLU pairs gate row f and up row f in the same TMEM lane: the two
 // matrices are two MMAs into two accumulators G and U.
 //
-// Per thread block (one per SM, 512 threads), persistent over (alignment block, feature tile):
-//   warp 0      allocates the 512 TMEM columns (accumulators in 0..255: G | U for SwiGLU,
-//               two alternating 128-column accumulators otherwise; decoded weight stages in
-//               256..511) and, on one lane, issues the MMAs (M = 128, N = 128, K = 16);
-//   warp 1      loads each 64-wide K stage with TMA: the 128 token rows (f16, gathered four
-//               rows per instruction into a 128-byte-swizzled K-major tile) and the raw E2M1
-//               bytes of the stage's weight rows;
+// Every tile is two 128-row weight matrices against one token tile of 128 slots: the gate and
+// up rows of 128 features for SwiGLU, else 256 consecutive features; reading the token tile
+// once for both halves its L2 traffic per flop.  Per thread block (one per SM, 640 threads),
+// persistent over (alignment block, feature tile):
+//   warp 0      allocates the 512 TMEM columns (the two 128-column accumulators in 0..255,
+//               the decoded weight stages in 256..511) and, on one lane, issues the MMAs
+//               (M = 128, N = 128, K = 16, two per K step);
+//   warp 1      loads each 64-wide K stage of the token tile with TMA (one box of 128 slot
+//               rows when the rows are in slot order, else gathered four rows per
+//               instruction) and the raw E2M1 codes 128 bytes (four stages) per weight row;
 //   warps 8-15  decode: one thread per weight row (= TMEM lane) turns the stage's codes into
-//               f16 (hardware conversion, times the block's E8M0 scale) and writes them into
-//               the stage's TMEM columns with tcgen05.st;
-//   warps 4-7   drain the accumulators (one TMEM lane = one feature, one column = one pair)
-//               and run the fused epilogue: bias + SwiGLU -> h (f16), bias * routing weight
-//               -> o (fp32), or bias -> out (bf16), stored at the pair's row.
+//               f16 (hardware conversion, times the block's E8M0 scale, read a group ahead)
+//               and writes them into the stage's TMEM columns with tcgen05.st;
+//   warps 4-7 and 16-19 drain the accumulators (one TMEM lane = one feature, one column =
+//               one pair; each group of four takes half of the columns), release them before
+//               computing the last chunk, and run the fused epilogue: bias + SwiGLU -> h
+//               (f16, through a shared staging tile and one TMA store when h is in slot
+//               order), bias * routing weight -> o (fp32), or bias -> out (bf16).
 // Every mbarrier wait is bounded; one that runs out sets MOE_ERR_TIMEOUT, every role leaves
 // its loop, the MMA lane drains its own work and the TMEM is freed.
 //
@@ -46,15 +51,22 @@ namespace {
 
 using namespace moe_launch;
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;
 constexpr int kTM = 128;    // weight rows (features) per tile: MMA M
 constexpr int kTN = 128;    // pairs per tile (one alignment block): MMA N
 constexpr int kBK = 64;     // K elements per stage
 // Shared-memory stages (token tile + raw codes) and TMEM stages (decoded weights) form two
 // rings: copies may run further ahead of the MMA than the TMEM columns allow decoding to.
-__host__ __device__ constexpr int smem_stages(int nmat) { return nmat == 2 ? 5 : 10; }
-__host__ __device__ constexpr int tmem_stages(int nmat) { return nmat == 2 ? 4 : 8; }
-constexpr int kEpiWarp0 = 4, kDecWarp0 = 8;
+// Every tile is two 128-row weight matrices against one token tile: the gate and up rows of
+// 128 features for SwiGLU, else 256 consecutive features.  The token tile is read once for
+// both, which halves its L2 traffic per flop.
+constexpr int kMats = 2;
+__host__ __device__ constexpr int smem_stages(bool swiglu) { return swiglu ? 5 : 7; }
+constexpr int kTmemStages = 4;
+// epilogue warps 4-7 take token columns 0-63, warps 16-19 columns 64-127 (warp % 4 = TMEM
+// lane quarter); decoders are warps 8-15
+constexpr int kEpiWarp0 = 4, kEpiWarp1 = 16, kDecWarp0 = 8;
+constexpr int kEpiCols = kTN / 2;
 constexpr int kTmemCols = 512;
 constexpr int kAcol0 = 256;  // first TMEM column of the decoded weight stages
 constexpr int kMaxKin = 4096;
@@ -65,24 +77,23 @@ constexpr int kRawSlots = 3;
 
 struct TArgs {
   GroupedGemm g;
-  int nmat;          // 2 for SwiGLU (gate and up rows), else 1
-  int m_tiles;       // feature tiles per block: ceil(Nout / 128)
+  int m_tiles;       // feature tiles per block: ceil(Nout / 128) for SwiGLU, else ceil(Nout / 256)
   int64_t tiles;     // block slots * m_tiles
 };
 
-// Shared memory: token-tile stages (16 KB each) | raw-code slots (nmat x 128 rows x 128 B,
+// Shared memory: token-tile stages (16 KB each) | raw-code slots (2 x 128 rows x 128 B,
 // 128-byte swizzle) | SwiGLU output staging (128 slots x 128 f16) | barriers.
 struct TLayout {
   int slot, raw, raw_slot, stg, bars, total;
 };
 
-__host__ __device__ inline TLayout tlayout(int nmat) {
+__host__ __device__ inline TLayout tlayout(bool swiglu) {
   TLayout L;
   L.slot = kTN * 128;
-  L.raw = smem_stages(nmat) * L.slot;
-  L.raw_slot = nmat * kTM * 128;
+  L.raw = smem_stages(swiglu) * L.slot;
+  L.raw_slot = kMats * kTM * 128;
   L.stg = L.raw + kRawSlots * L.raw_slot;
-  L.bars = L.stg + (nmat == 2 ? kTN * kTM * 2 : 0);
+  L.bars = L.stg + (swiglu ? kTN * kTM * 2 : 0);
   L.total = L.bars + 512 + 1024;
   return L;
 }
@@ -131,11 +142,16 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t v, __half2 s) {
 }
 
 // TMEM column of stage s, matrix m, in the decoded-weight region.
-__device__ __forceinline__ uint32_t a_col(int s, int m, int nmat) { return kAcol0 + s * 32 * nmat + 32 * m; }
+__device__ __forceinline__ uint32_t a_col(int s, int m) { return kAcol0 + s * 32 * kMats + 32 * m; }
 
-// Weight row of feature f (tile row) of matrix m of expert e.
-__device__ __forceinline__ int64_t weight_row(const GroupedGemm& a, int64_t e, int m, int64_t f) {
-  return e * a.Nw + (int64_t)m * a.Nout + f;
+// Output feature of row r of matrix m in feature tile mt, and the weight row that holds it.
+template <bool SWIGLU>
+__device__ __forceinline__ int64_t tile_feature(int mt, int m, int r) {
+  return SWIGLU ? (int64_t)mt * kTM + r : (int64_t)mt * (kMats * kTM) + m * kTM + r;
+}
+template <bool SWIGLU>
+__device__ __forceinline__ int64_t tile_wrow(const GroupedGemm& a, int64_t e, int mt, int m, int r) {
+  return e * a.Nw + (SWIGLU ? (int64_t)m * a.Nout : 0) + tile_feature<SWIGLU>(mt, m, r);
 }
 
 // f16x2 holding 2^(s-127) in both halves: NaN for 0xFF; the exponent clamped to the f16
@@ -179,13 +195,12 @@ template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_ts_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                       const __grid_constant__ CUtensorMap tmap_h, TArgs ta) {
-  constexpr int NMAT = (EPI == EPI_SWIGLU) ? 2 : 1;
-  constexpr int NACC = (EPI == EPI_SWIGLU) ? 1 : 2;  // accumulator sets: G | U, or two alternating
+  constexpr bool SW = (EPI == EPI_SWIGLU);
   const GroupedGemm& a = ta.g;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const TLayout L = tlayout(NMAT);
-  constexpr int S1 = smem_stages(NMAT), S2 = tmem_stages(NMAT);
+  const TLayout L = tlayout(SW);
+  constexpr int S1 = smem_stages(SW), S2 = kTmemStages;
   uint64_t* ld_full = reinterpret_cast<uint64_t*>(smem + L.bars);  // [S1] token tile + raw codes landed
   uint64_t* empty = ld_full + S1;                                   // [S1] shared stage consumed by the MMA
   uint64_t* a_full = empty + S1;                                    // [S2] decoded weights in TMEM
@@ -215,10 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&tfull[i], 1);
-      tc::mbar_init(&tempty[i], 4);
+      tc::mbar_init(&tempty[i], 8);
     }
     tc::mbar_init(drain, 1);
-    tc::mbar_init(epi_bar, 4);
+    tc::mbar_init(epi_bar, 8);
     *abort_flag = 0;
     tc::mbar_fence_init();
   }
@@ -243,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int64_t rows_total = a.act_per_pair ? a.P : a.P / a.k;
     const uint32_t stage_bytes = kTN * 128;
-    const uint32_t raw_bytes = NMAT * kTM * 128;
+    const uint32_t raw_bytes = kMats * kTM * 128;
     uint32_t it = 0, gi = 0;
     for (int64_t t = blockIdx.x; t < ta.tiles && !*abort_flag; t += gridDim.x) {
       int64_t blk, e;
@@ -259,7 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 4; ++j)
           y[j] = (int32_t)(pv[j] < a.P ? (a.act_per_pair ? (int64_t)pv[j] : (int64_t)(pv[j] / a.k)) : rows_total);
       }
-      const int64_t f0 = (int64_t)mt * kTM;
       bool ok = true;
       for (int kc = 0; kc < nk; ++kc) {
         if (kc % kGroup == 0) {  // raw codes of stages kc .. kc + 3: 128 bytes of every row
@@ -271,8 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t rsl = smem_s + L.raw + rs * L.raw_slot;
             tma::mbar_arrive_expect_tx(&raw_full[rs], raw_bytes);
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m)
-              tma::load_2d(rsl + m * kTM * 128, &tmap_w, (kc / kGroup) * 128, (int32_t)weight_row(a, e, m, f0),
+            for (int m = 0; m < kMats; ++m)
+              tma::load_2d(rsl + m * kTM * 128, &tmap_w, (kc / kGroup) * 128, (int32_t)tile_wrow<SW>(a, e, mt, m, 0),
                            &raw_full[rs]);
           }
           ++gi;
@@ -297,20 +311,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
     }
-  } else if (warp >= kDecWarp0) {
+  } else if (warp >= kDecWarp0 && warp < kDecWarp0 + 8) {
     // ------------------------------------------------------------------ decoders
     const int dj = warp - kDecWarp0, q = dj & 3, part = dj >> 2;
-    const int m = NMAT == 2 ? part : 0;   // matrix (SwiGLU: gate, up)
-    const int kh = NMAT == 2 ? 0 : part;  // K half of the stage (single matrix)
-    const int r = 32 * q + lane;          // tile row = TMEM lane
+    const int m = part;          // matrix (SwiGLU: gate, up; else the two feature halves)
+    const int r = 32 * q + lane;  // tile row = TMEM lane
     const int ngroups = (nk + kGroup - 1) / kGroup;
     // The eight E8M0 bytes of this row's K group g (blocks 8g .. 8g + 7), read from global
     // memory one group ahead into registers; 127 (scale 1) for a row past the features.
     auto load_scales = [&](int64_t e, int mt, int g, uint32_t (&w)[2]) {
       w[0] = w[1] = 0x7f7f7f7fu;
-      const int64_t f = (int64_t)mt * kTM + r;
-      if (f >= a.Nout) return;
-      const uint8_t* src = a.w_scale + weight_row(a, e, m, f) * nkb + 8 * g;
+      if (tile_feature<SW>(mt, m, r) >= a.Nout) return;
+      const uint8_t* src = a.w_scale + tile_wrow<SW>(a, e, mt, m, r) * nkb + 8 * g;
       uint32_t v[2] = {0u, 0u};
 #pragma unroll
       for (int bb = 0; bb < 8; ++bb)
@@ -359,10 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tc_fence_after();  // the MMA that read this TMEM stage before has completed
         // row r of the slot, bytes 32 kg + 16 h of the row, in the 128-byte swizzle
         const uint8_t* rowp = smem + L.raw + rs * L.raw_slot + m * kTM * 128 + r * 128;
-        const uint32_t dst = taddr + ((uint32_t)(32 * q) << 16) + a_col(s2, m, NMAT);
+        const uint32_t dst = taddr + ((uint32_t)(32 * q) << 16) + a_col(s2, m);
         const uint32_t scw = (kg >> 1) ? sc1 : sc0;  // scale bytes of blocks 2 kg, 2 kg + 1
         const int sh = 16 * (kg & 1);
-        if (NMAT == 2) {
+        {
           uint32_t v[32];
           const uint4 w0 = *reinterpret_cast<const uint4*>(rowp + (((2 * kg) ^ (r & 7)) << 4));
           const uint4 w1 = *reinterpret_cast<const uint4*>(rowp + (((2 * kg + 1) ^ (r & 7)) << 4));
@@ -370,11 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           decode_block(w1, (scw >> (sh + 8)) & 0xffu, v + 16, bad);
           tmem_st16(dst, v);
           tmem_st16(dst + 16, v + 16);
-        } else {
-          uint32_t v[16];
-          const uint4 w = *reinterpret_cast<const uint4*>(rowp + (((2 * kg + kh) ^ (r & 7)) << 4));
-          decode_block(w, (scw >> (sh + 8 * kh)) & 0xffu, v, bad);
-          tmem_st16(dst + kh * 16, v);
         }
         tc::tmem_st_wait();
         tc::tc_fence_before();
@@ -413,8 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t blk, e;
         int mt;
         if (!tile_info(ta, t, ntpp, blk, mt, e)) continue;
-        const int acc = NACC == 2 ? (int)(acc_it & 1) : 0;
-        if (!tc::mbar_wait(&tempty[acc], ((acc_it / NACC) & 1) ^ 1)) {
+        const int acc = 0;  // one accumulator set (two 128-column accumulators)
+        if (!tc::mbar_wait(&tempty[acc], (acc_it & 1) ^ 1)) {
           moe::set_status(a.status, MOE_ERR_TIMEOUT);
           *abort_flag = 1;
           break;
@@ -435,9 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t bd = tc::sdesc_sw128(bs + kk * 32);
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m)
-              mma_ts(taddr + (NMAT == 2 ? m * 128 : acc * 128), taddr + a_col(s2, m, NMAT) + kk * 8, bd, idesc,
-                     (kc | kk) != 0);
+            for (int m = 0; m < kMats; ++m)
+              mma_ts(taddr + m * 128, taddr + a_col(s2, m) + kk * 8, bd, idesc, (kc | kk) != 0);
           }
           tc::mma_commit(&empty[s]);
           tc::mma_commit(&a_empty[s2]);
@@ -451,9 +457,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!tc::mbar_wait(drain, 0)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
     }
     __syncwarp();
-  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
+  } else if ((warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) || warp >= kEpiWarp1) {
     // ------------------------------------------------------------------ epilogue
-    const int q = warp - kEpiWarp0;
+    const int q = warp & 3;
+    const int cbase = warp >= kEpiWarp1 ? kEpiCols : 0;  // this warp's token columns
     const uint16_t* bias = static_cast<const uint16_t*>(a.bias);
     // SwiGLU into slot-ordered h: the tile goes through shared memory and leaves as one TMA
     // store, and the accumulators are released before the last chunk is computed
@@ -477,93 +484,94 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t blk, e;
       int mt;
       if (!tile_info(ta, t, ntpp, blk, mt, e)) continue;
-      const int acc = NACC == 2 ? (int)(acc_it & 1) : 0;
-      int pls[kTN / 32];  // pair of token column 32 i + lane, read while the MMAs run
-      float wls[kTN / 32];
+      const int acc = 0;  // one accumulator set
+      int pls[kEpiCols / 32];  // pair of token column cbase + 32 i + lane, read while the MMAs run
+      float wls[kEpiCols / 32];
 #pragma unroll
-      for (int i = 0; i < kTN / 32; ++i) pls[i] = a.sorted[blk * a.bm + 32 * i + lane];
+      for (int i = 0; i < kEpiCols / 32; ++i) pls[i] = a.sorted[blk * a.bm + cbase + 32 * i + lane];
       const int64_t slot0 = blk * a.bm;
 #pragma unroll
-      for (int i = 0; i < kTN / 32; ++i)
+      for (int i = 0; i < kEpiCols / 32; ++i)
         wls[i] = (EPI == EPI_WEIGHTED_F32 && pls[i] < a.P) ? a.topk_w[pls[i]] : 1.f;
-      if (!tc::mbar_wait(&tfull[acc], (acc_it / NACC) & 1)) {
+      if (!tc::mbar_wait(&tfull[acc], acc_it & 1)) {
         moe::set_status(a.status, MOE_ERR_TIMEOUT);
         *abort_flag = 1;
         break;
       }
       tc::tc_fence_after();
-      const int64_t f = (int64_t)mt * kTM + 32 * q + lane;  // this lane's feature
-      const bool fvalid = f < a.Nout;
+      // this lane's features: SwiGLU gate (accumulator 0) and up (1) of feature fA; otherwise
+      // feature fA in accumulator 0 and fB in accumulator 1
+      const int64_t fA = tile_feature<SW>(mt, 0, 32 * q + lane), fB = tile_feature<SW>(mt, 1, 32 * q + lane);
+      const bool vA = fA < a.Nout, vB = fB < a.Nout;
       float b0 = 0.f, b1 = 0.f;
-      if (bias && fvalid) {
-        b0 = moe::bf16_bits_to_f32(bias[e * a.Nw + f]);
-        if (EPI == EPI_SWIGLU) b1 = moe::bf16_bits_to_f32(bias[e * a.Nw + a.Nout + f]);
+      if (bias) {
+        if (vA) b0 = moe::bf16_bits_to_f32(bias[e * a.Nw + fA]);
+        if (SW && vA) b1 = moe::bf16_bits_to_f32(bias[e * a.Nw + a.Nout + fA]);
+        if (!SW && vB) b1 = moe::bf16_bits_to_f32(bias[e * a.Nw + fB]);
       }
       const uint32_t tb = taddr + ((uint32_t)(32 * q) << 16);
       if (staged) {  // the previous tile's store has finished reading the staging buffer
-        if (q == 0 && lane == 0) tma::bulk_wait_read_all();
+        if (warp == kEpiWarp0 && lane == 0) tma::bulk_wait_read_all();
         if (!epi_sync()) break;
       }
 #pragma unroll
-      for (int c0 = 0; c0 < kTN; c0 += 32) {
-        const int pl = pls[c0 / 32];
-        uint32_t v0[32];
-        tc::tmem_ld32(tb + (NMAT == 2 ? 0 : acc * 128) + c0, v0);
-        if (EPI == EPI_SWIGLU) {
-          uint32_t v1[32];
-          tc::tmem_ld32(tb + 128 + c0, v1);
-          tc::tmem_ld_wait();
-          if (staged && c0 == kTN - 32) {  // both accumulators drained: the next tile may start
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&tempty[acc]);
-          }
+      for (int cc = 0; cc < kEpiCols; cc += 32) {
+        const int c0 = cbase + cc;
+        const int pl = pls[cc / 32];
+        uint32_t v0[32], v1[32];
+        tc::tmem_ld32(tb + c0, v0);
+        tc::tmem_ld32(tb + 128 + c0, v1);
+        tc::tmem_ld_wait();
+        if (cc == kEpiCols - 32) {  // this warp's accumulator columns are drained
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+        }
+        if (SW) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int p = __shfl_sync(0xffffffffu, pl, j);
             const float gt = __uint_as_float(v0[j]) + b0, up = __uint_as_float(v1[j]) + b1;
             const __half hv = __float2half_rn(moe::silu(gt) * up);
-            if (p < a.P && fvalid && (__hisinf(hv) || __hisnan(hv))) bad = true;
+            if (p < a.P && vA && (__hisinf(hv) || __hisnan(hv))) bad = true;
             if (staged) {
               stg[(c0 + j) * kTM + 32 * q + lane] = hv;
-            } else if (p < a.P && fvalid) {
+            } else if (p < a.P && vA) {
               const int64_t row = a.out_by_slot ? slot0 + c0 + j : (int64_t)p;
-              static_cast<__half*>(a.out)[row * a.Nout + f] = hv;
+              static_cast<__half*>(a.out)[row * a.Nout + fA] = hv;
             }
           }
         } else {
-          tc::tmem_ld_wait();
-          const float wl = wls[c0 / 32];
+          const float wl = wls[cc / 32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int p = __shfl_sync(0xffffffffu, pl, j);
             const float wp = __shfl_sync(0xffffffffu, wl, j);
-            if (p < a.P && fvalid) {
-              const float o = __uint_as_float(v0[j]) + b0;
+            if (p < a.P) {
               const int64_t row = a.out_by_slot ? slot0 + c0 + j : (int64_t)p;
-              if (EPI == EPI_WEIGHTED_F32)
-                static_cast<float*>(a.out)[row * a.Nout + f] = o * wp;
-              else
-                static_cast<uint16_t*>(a.out)[row * a.Nout + f] = moe::f32_to_bf16_bits(o);
+              const float o0 = __uint_as_float(v0[j]) + b0, o1 = __uint_as_float(v1[j]) + b1;
+              if (EPI == EPI_WEIGHTED_F32) {
+                if (vA) static_cast<float*>(a.out)[row * a.Nout + fA] = o0 * wp;
+                if (vB) static_cast<float*>(a.out)[row * a.Nout + fB] = o1 * wp;
+              } else {
+                if (vA) static_cast<uint16_t*>(a.out)[row * a.Nout + fA] = moe::f32_to_bf16_bits(o0);
+                if (vB) static_cast<uint16_t*>(a.out)[row * a.Nout + fB] = moe::f32_to_bf16_bits(o1);
+              }
             }
           }
         }
       }
-      if (staged) {  // the tile's h rows [slot0, slot0 + 128) x features [f0, f0 + 128)
+      if (staged) {  // the tile's h rows [slot0, slot0 + 128) x features [mt * 128, + 128)
         tc::fence_proxy_async_smem();
         if (!epi_sync()) break;
-        if (q == 0 && lane == 0) {
+        if (warp == kEpiWarp0 && lane == 0) {
           tma::store_2d(&tmap_h, mt * kTM * 2, (int32_t)slot0, stg_s);
           tma::bulk_commit();
         }
-      } else {
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&tempty[acc]);
       }
       ++acc_it;
     }
-    if (staged && q == 0 && lane == 0) tma::bulk_wait_all();
+    if (staged && warp == kEpiWarp0 && lane == 0) tma::bulk_wait_all();
   }
   if (bad) moe::set_status(a.status, MOE_ERR_RANGE);
   tc::tc_fence_before();
@@ -588,7 +596,7 @@ int sm_count_ts() {
 template <int EPI>
 cudaError_t launch_ts(const TArgs& ta, const CUtensorMap& mx, const CUtensorMap& mw, const CUtensorMap& mh,
                       cudaStream_t stream) {
-  const TLayout L = tlayout(EPI == EPI_SWIGLU ? 2 : 1);
+  const TLayout L = tlayout(EPI == EPI_SWIGLU);
   cudaError_t err = cudaFuncSetAttribute(prefill_ts_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
   int64_t grid = sm_count_ts();
@@ -612,15 +620,15 @@ bool ts_supported(const GroupedGemm& g) {
   uintptr_t al16 = reinterpret_cast<uintptr_t>(g.act) | reinterpret_cast<uintptr_t>(g.w);
   if (g.out_by_slot) al16 |= reinterpret_cast<uintptr_t>(g.out);
   if ((al16 & 15) != 0) return false;
-  return tlayout(g.epi == EPI_SWIGLU ? 2 : 1).total <= 227 * 1024;
+  return tlayout(g.epi == EPI_SWIGLU).total <= 227 * 1024;
 }
 
 cudaError_t prefill_ts(const GroupedGemm& g, cudaStream_t stream) {
   if (!ts_supported(g)) return cudaErrorInvalidValue;
   TArgs ta;
   ta.g = g;
-  ta.nmat = g.epi == EPI_SWIGLU ? 2 : 1;
-  ta.m_tiles = (g.Nout + kTM - 1) / kTM;
+  const int tile_features = g.epi == EPI_SWIGLU ? kTM : kMats * kTM;
+  ta.m_tiles = (g.Nout + tile_features - 1) / tile_features;
   ta.tiles = g.grid_blocks * ta.m_tiles;
   const int64_t rows_total = g.act_by_slot ? g.grid_blocks * g.bm : (g.act_per_pair ? g.P : g.P / g.k);
   // token rows of Kin f16 in 128-byte swizzle: 128 slot rows per box when the rows are in
