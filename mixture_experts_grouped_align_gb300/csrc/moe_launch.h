@@ -57,6 +57,7 @@ struct GroupedGemm {
 size_t decode_gemm_smem_bytes(const GroupedGemm& g);
 cudaError_t decode_gemm(const GroupedGemm& g, cudaStream_t stream);
 
+
 // ---- grouped GEMMs on the tensor-memory (prefill) path (prefill_gemm.cu)
 int prefill_tile_n(const GroupedGemm& g);
 bool prefill_supported(const GroupedGemm& g);
