@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--m", type=int, default=28, help="tokens for decode_bf16")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the token count (smaller cases for profiling)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="experts of the mxfp8_wgrad workload (a smaller case for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-tokens", type=int, default=None, help=argparse.SUPPRESS)
@@ -423,6 +425,8 @@ def bench_mxfp8_wgrad(args, rank, world, local_rank):
     steps = args.steps if args.steps is not None else steps
     warmup = max(3, args.warmup if args.warmup is not None else warmup)
     kw = {} if not args.tokens else {"T": args.tokens}
+    if args.experts:
+        kw["E"] = args.experts
     g = synth.make_mxfp8_gemm_wgrad(device=dev, **kw)
     T, E, K, I, k, P = g["T"], g["E"], g["K"], g["I"], g["k"], g["P"]
     bm = 128
