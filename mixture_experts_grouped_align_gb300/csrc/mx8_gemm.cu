@@ -49,7 +49,7 @@ constexpr int kStages = 4;
 constexpr int kLag = 2;                    // stages between a stage's copies and its hand-over
 
 // One stage slot: A tile | B tile | A scale words (one per row) | B scale words (one copy
-// per 32-lane quarter: 4 x 32 lanes x BN/32).
+// per 32-lane quarter: [4][BN/32][32 lanes], lanes contiguous).
 struct MLayout {
   int a, b, sfa, sfb, slot, bars, total;
 };
@@ -155,10 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
         const uint32_t wv = *reinterpret_cast<const uint32_t*>(sl + L.sfa + (q * 32 + lane) * 4);
         tc::tmem_st4(taddr + ((uint32_t)(q * 32) << 16) + sfa_col(hs), wv, wv, wv, wv);
       } else {
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(sl + L.sfb) + (q * 32 + lane) * NBW;
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(sl + L.sfb) + q * NBW * 32 + lane;
         uint32_t v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = j < NBW ? src[j] : 0u;
+        for (int j = 0; j < 8; ++j) v[j] = j < NBW ? src[j * 32] : 0u;
         tc::tmem_st8(taddr + ((uint32_t)(q * 32) << 16) + sfb_col(hs), v);
       }
       tc::tmem_st_wait();
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             if (j < NBW)
-              cp_async4(sl + L.sfb + ((q * 32 + lane) * NBW + j) * 4, sfsrc + (int64_t)(32 * j) * nkb + kc * 4);
+              cp_async4(sl + L.sfb + ((q * NBW + j) * 32 + lane) * 4, sfsrc + (int64_t)(32 * j) * nkb + kc * 4);
         }
         cp_async_commit();
         ++it;
