@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(PArgs pa) {
                 up += moe::bf16_bits_to_f32(bias[e * a.Nw + a.Nout + n0 + c0 + j]);
               }
               hv[j] = __float2half_rn(moe::silu(gt) * up);
-              if (__hisinf(hv[j]) || __hisnan(hv[j])) bad = true;
+              if (__hisinf(hv[j])) bad = true;
             }
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(a.out) + (int64_t)p * a.Nout + n0 + c0);
 #pragma unroll

@@ -533,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int p = __shfl_sync(0xffffffffu, pl, j);
             const float gt = __uint_as_float(v0[j]) + b0, up = __uint_as_float(v1[j]) + b1;
             const __half hv = __float2half_rn(moe::silu(gt) * up);
-            if (p < a.P && vA && (__hisinf(hv) || __hisnan(hv))) bad = true;
+            if (p < a.P && vA && __hisinf(hv)) bad = true;
             if (staged) {
               stg[(c0 + j) * kTM + 32 * q + lane] = hv;
             } else if (p < a.P && vA) {

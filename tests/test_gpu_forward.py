@@ -131,3 +131,53 @@ def test_both_variants_agree_across_the_threshold(moe):
     a, b = bf16_to_np(y257)[:256], bf16_to_np(y256)
     assert_close_bf16(a, oracle_y(lay, w, 256), what="tensor-memory path")
     assert_close_bf16(b, oracle_y(lay, w, 256), what="weight-streaming path")
+
+
+def _run_status(moe, L, lay, T):
+    x = dev(lay["x"][:T])
+    lg = dev(lay["logits"][:T])
+    y = torch.empty((T, L.K), dtype=torch.bfloat16, device="cuda")
+    L.status.zero_()
+    L.step(x, lg, T, y)
+    torch.cuda.synchronize()
+    return y, int(L.status[0])
+
+
+@pytest.mark.parametrize("T", [64, 300])  # weight-streaming / tensor-memory path
+def test_w4a16_nan_scale_reaches_exactly_its_tokens(moe, T):
+    """An E8M0 0xFF (NaN) scale on one W1 block makes h -- and through GEMM2 every output --
+    NaN for exactly the tokens routed to that expert (the oracle's decoding), and nothing
+    else."""
+    w = synth.Workload("nan_scale", T=T, K=256, I=256, E=16, k=4, quant="mxfp4", seed=21,
+                       scale_exp=(-6, -2), bias=True)
+    lay = synth.make_layer(w)
+    lay["w1_scale"] = lay["w1_scale"].copy()
+    lay["w1_scale"][3, 5, 2] = 0xFF  # expert 3, gate row 5, K block 2
+    L = device_layer(moe, lay, w, T, pad=False)
+    y, st = _run_status(moe, L, lay, T)
+    assert st == 0
+    got = bf16_to_np(y)
+    ref = oracle_y(lay, w, T)
+    nan_rows = np.isnan(ref).any(axis=1)
+    assert nan_rows.any() and not nan_rows.all()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert_close_bf16(got[~nan_rows], ref[~nan_rows], what=f"nan scale T={T}")
+
+
+def test_w4a16_scale_outside_f16_range_is_reported_on_the_tensor_memory_path(moe):
+    """The tensor-memory path decodes codes x scale to f16: a block with nonzero codes whose
+    scale is below 2^-23 cannot be represented exactly and sets MOE_ERR_RANGE (-6); the
+    weight-streaming path scales f32 partial sums and stays exact."""
+    w = synth.Workload("tiny_scale", T=300, K=256, I=256, E=16, k=4, quant="mxfp4", seed=22,
+                       scale_exp=(-6, -2), bias=True)
+    lay = synth.make_layer(w)
+    lay["w1_scale"] = lay["w1_scale"].copy()
+    lay["w1"] = lay["w1"].copy()
+    lay["w1_scale"][2, 7, 1] = 127 - 30
+    lay["w1"][2, 7, 16:32] = 0x77  # nonzero codes in that block
+    L = device_layer(moe, lay, w, 300, pad=False)
+    _, st = _run_status(moe, L, lay, 300)
+    assert st == -6
+    y64, st64 = _run_status(moe, L, lay, 64)
+    assert st64 == 0
+    assert_close_bf16(bf16_to_np(y64), oracle_y(lay, w, 64), what="weight-streaming exact")
