@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--experts", type=int, default=None,
                     help="experts of the mxfp8_wgrad workload (a smaller case for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager launches instead of replays of the step's CUDA graph")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-tokens", type=int, default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -285,11 +287,36 @@ def bench_ours(args, rank, world, local_rank):
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    # per-kernel split: eager steps with the library's CUDA events around its launches
+    n_ev = max(1, min(steps, 200))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
     for es in evs:  # torch creates the CUDA event on its first record
         for e in es:
             e.record(stream)
     torch.cuda.synchronize()
+    for i in range(n_ev):
+        step(evs[i])
+    torch.cuda.synchronize()
+    g1 = sum(e[0].elapsed_time(e[1]) for e in evs) / n_ev
+    g2 = sum(e[1].elapsed_time(e[2]) for e in evs) / n_ev
+    cb = sum(e[2].elapsed_time(e[3]) for e in evs) / n_ev
+    # the timed region: the whole step (every kernel, every step) replayed from one CUDA graph,
+    # which removes the host launch gaps between its kernels; --no-graph launches eagerly
+    graph = None
+    if not args.no_graph:
+        cs = torch.cuda.Stream(device=dev)
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            L.step(x, lg, T, y, stream=cs)
+        stream.wait_stream(cs)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cs):
+            L.step(x, lg, T, y, stream=cs)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
@@ -299,18 +326,21 @@ def bench_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.2)
-    t_start.record(stream)
+    cur = torch.cuda.current_stream()
+    t_start.record(cur)
     for i in range(steps):
-        step(evs[i])
-    t_end.record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+    t_end.record(cur)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     ck = clocks.stop(local_rank)
     ms = t_start.elapsed_time(t_end)
-    g1 = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
-    g2 = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
-    cb = sum(e[2].elapsed_time(e[3]) for e in evs) / steps
+    if int(L.status[0]) != 0:
+        raise RuntimeError(f"device status {int(L.status[0])}")
     if world > 1:
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -388,7 +418,10 @@ def bench_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded PCG64 inputs, random-init weights)",
         "config": dict(describe(w, rows), l2=f"inputs larger than L2: {step_weight_bytes / 1e9:.2f} GB "
                                               f"of expert weights streamed per step > 129 MB L2",
-                       parallelism=f"replicas x{world}"),
+                       parallelism=f"replicas x{world}",
+                       timed=("replays of one CUDA graph of the whole step (every kernel of the step runs each "
+                              "replay); the per-kernel split comes from eager steps" if graph is not None
+                              else "eager launches")),
         "useful_tflops": world * useful_flops(w) * steps / (ms * 1e-3) / 1e12,
         "layer_latency_us": ms_step * 1e3,
         "kernel_ms": {"gemm1_swiglu": g1, "gemm2_weighted": g2, "combine": cb,
