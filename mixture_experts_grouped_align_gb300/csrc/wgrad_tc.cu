@@ -67,9 +67,12 @@ __device__ __forceinline__ void cp_async16z(uint32_t dst, const void* src, bool 
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+// Arrives on the mbarrier once every cp.async this thread issued before has landed (the
+// barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 // Byte offset of (token t, 16-byte chunk c of a row of 64 MN elements) in an atom column.
 __device__ __forceinline__ uint32_t mn_offset(int t, int c) {
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_tc_kernel(WArgs wa) {
   }
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      tc::mbar_init(&full[s], kNumProd / 32);
+      tc::mbar_init(&full[s], kNumProd);  // one completion arrival per producer thread
       tc::mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -164,11 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_tc_kernel(WArgs wa) {
       b_off[i] = L.b + (j >> 3) * kAtomCol + mn_offset(t, j & 7);
     }
     const int nbj = BN / 32;  // B chunks per thread
-    // A stage is handed to the MMA LAG stages after its copies were issued (a cp.async
-    // wait only covers the waiting thread's own copies), so LAG stages of copies overlap.
-    constexpr int LAG = 2;  // <= slots - 2, leaving one stage of slack for the MMA
-    int pend[LAG];
-    int npend = 0;
+    // Each thread's copies of a stage complete on the stage's barrier by themselves
+    // (cp.async.mbarrier.arrive.noinc), so no producer waits for its own copies and every
+    // free slot can have a stage in flight; the MMA lane makes the landed bytes visible to
+    // the tensor core with a proxy fence after its wait.
     uint32_t it = 0;
     for (int64_t tt = blockIdx.x; tt < wa.tiles && !*abort_flag; tt += gridDim.x) {
       const TileInfo ti = tile_info(wa, tt, eb);
@@ -194,28 +196,11 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_tc_kernel(WArgs wa) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           if (i < nbj) cp_async16z(sl + b_off[i], isrc + (valid ? 32 * i : 0), valid);
-        cp_async_commit();
-        if (npend == LAG) {  // the oldest stage's copies have landed: hand it over
-          cp_async_wait<LAG>();
-          tc::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&full[pend[0]]);
-#pragma unroll
-          for (int j = 0; j + 1 < LAG; ++j) pend[j] = pend[j + 1];
-          --npend;
-        }
-#pragma unroll
-        for (int j = 0; j < LAG; ++j)
-          if (j == npend) pend[j] = slot;
-        ++npend;
+        cp_async_arrive_noinc(&full[slot]);
         ++it;
       }
     }
-    cp_async_wait<0>();
-    tc::fence_proxy_async_smem();
-    __syncwarp();
-    for (int j = 0; j < npend; ++j)
-      if (lane == 0) tc::mbar_arrive(&full[pend[j]]);
+    cp_async_wait_all();
   } else if (warp == 0) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -242,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_tc_kernel(WArgs wa) {
             ok = false;
             break;
           }
+          tc::fence_proxy_async_smem();  // the producers' landed copies, for the tensor core
           tc::tc_fence_after();
           const uint32_t a_s = smem_s + slot * L.slot + L.a;
           const uint32_t b_s = smem_s + slot * L.slot + L.b;
