@@ -7,6 +7,16 @@ The expert layer (per real token t and top-k slot j, e = id[t, j]):
     o_tj = h . W2[e]^T + b2[e]            W2[e]: [K, I]
     y_t  = sum_j w[t, j] * o_tj
 
+The non-gated variant ("tune the Nemotron MTP decode row on S5000 with a checked-in
+recipe", torchada PR 115, the table of added files: the Nemotron shape's activation is
+relu2_no_mul, with GEMM1 N = 1856) has one GEMM1 matrix and no gate-times-up product:
+
+    a    = x_t . W1[e]^T + b1[e]          W1[e]: [I, K]
+    h    = relu(a)^2                      relu(a) = max(a, 0)
+
+Reading taken: "relu2" is the square of the rectified value and "no_mul" is the absence of
+the gate product, so GEMM1's N is I itself (1856 on that page).
+
 Weights are decoded exactly (formats.py) and nothing is rounded in between.  The grouped
 GEMM itself -- one launch over all experts, rows taken from the alignment, optional
 per-expert bias [E, N] -- is the operation of "Add MoE GEMM variants and weight-gradient
@@ -28,15 +38,28 @@ def silu(g):
         return g / (1.0 + np.exp(-g))
 
 
+def relu2(a):
+    """max(a, 0)^2."""
+    r = np.maximum(a, 0.0)
+    return r * r
+
+
+ACTIVATIONS = ("swiglu", "relu2")
+
+
 class ExpertWeights:
     """Decodes one expert's weights on demand from the raw ABI layouts.
 
     w1 [E, 2I, K(/2)] (+ w1_scale [E, 2I, K/32]), b1 [E, 2I] bf16 bits or None,
     w2 [E, K, I(/2)]  (+ w2_scale [E, K, I/32]),  b2 [E, K]  bf16 bits or None.
+    With activation "relu2" GEMM1 has I rows: w1 [E, I, K(/2)], b1 [E, I].
     """
 
-    def __init__(self, fmt, w1, w1_scale, b1, w2, w2_scale, b2):
+    def __init__(self, fmt, w1, w1_scale, b1, w2, w2_scale, b2, activation="swiglu"):
+        if activation not in ACTIVATIONS:
+            raise ValueError(activation)
         self.fmt = fmt
+        self.activation = activation
         self.w1, self.w1_scale, self.b1 = w1, w1_scale, b1
         self.w2, self.w2_scale, self.b2 = w2, w2_scale, b2
 
@@ -65,6 +88,17 @@ def expert_ffn(x_rows, w1, b1, w2, b2):
     return o
 
 
+def expert_ffn_relu2(x_rows, w1, b1, w2, b2):
+    """float64 rows [n, K] through one non-gated expert: GEMM1 (+b1), relu^2, GEMM2 (+b2)."""
+    a = x_rows @ w1.T
+    if b1 is not None:
+        a = a + b1
+    o = relu2(a) @ w2.T
+    if b2 is not None:
+        o = o + b2
+    return o
+
+
 def moe_pairs(x, topk_ids, weights: ExpertWeights, tokens=None):
     """Unweighted expert outputs o[t, j] (float64 [T, k, K]) for the tokens listed
     (default all); rows of tokens not listed stay zero."""
@@ -73,13 +107,14 @@ def moe_pairs(x, topk_ids, weights: ExpertWeights, tokens=None):
     K = x.shape[1]
     tok = np.arange(T) if tokens is None else np.asarray(tokens)
     o = np.zeros((T, k, K))
+    ffn = expert_ffn if getattr(weights, "activation", "swiglu") == "swiglu" else expert_ffn_relu2
     sub = ids[tok]
     for e in np.unique(sub):
         rr, jj = np.nonzero(sub == e)
         t = tok[rr]
         w1, b1 = weights.gemm1(e)
         w2, b2 = weights.gemm2(e)
-        o[t, jj] = expert_ffn(x[t], w1, b1, w2, b2)
+        o[t, jj] = ffn(x[t], w1, b1, w2, b2)
     return o
 
 

@@ -220,21 +220,22 @@ def check_align_invariants(seed=2):
 
 # ----------------------------------------------------------------------------- layer
 
-def _rand_weights(rng, E, K, I, fmt="mxfp4", bias=True, scale=(-4, 0)):
+def _rand_weights(rng, E, K, I, fmt="mxfp4", bias=True, scale=(-4, 0), activation="swiglu"):
+    N1 = 2 * I if activation == "swiglu" else I
     if fmt == "mxfp4":
-        w1 = rng.integers(0, 256, size=(E, 2 * I, K // 2), dtype=np.uint8)
-        s1 = (127 + rng.integers(scale[0], scale[1] + 1, size=(E, 2 * I, K // 32))).astype(np.uint8)
+        w1 = rng.integers(0, 256, size=(E, N1, K // 2), dtype=np.uint8)
+        s1 = (127 + rng.integers(scale[0], scale[1] + 1, size=(E, N1, K // 32))).astype(np.uint8)
         w2 = rng.integers(0, 256, size=(E, K, I // 2), dtype=np.uint8)
         s2 = (127 + rng.integers(scale[0], scale[1] + 1, size=(E, K, I // 32))).astype(np.uint8)
     else:
         from synth import to_bf16_bits
-        w1 = to_bf16_bits(rng.standard_normal((E, 2 * I, K)) * 0.05)
+        w1 = to_bf16_bits(rng.standard_normal((E, N1, K)) * 0.05)
         w2 = to_bf16_bits(rng.standard_normal((E, K, I)) * 0.05)
         s1 = s2 = None
     from synth import to_bf16_bits
-    b1 = to_bf16_bits(rng.standard_normal((E, 2 * I)) * 0.1) if bias else None
+    b1 = to_bf16_bits(rng.standard_normal((E, N1)) * 0.1) if bias else None
     b2 = to_bf16_bits(rng.standard_normal((E, K)) * 0.1) if bias else None
-    return layer.ExpertWeights(fmt, w1, s1, b1, w2, s2, b2)
+    return layer.ExpertWeights(fmt, w1, s1, b1, w2, s2, b2, activation=activation)
 
 
 def _dense_all_experts(x, ids, w, W: layer.ExpertWeights, E):
@@ -242,14 +243,20 @@ def _dense_all_experts(x, ids, w, W: layer.ExpertWeights, E):
     T, K = x.shape
     W1 = np.stack([formats.dequant(W.fmt, W.w1[e], None if W.w1_scale is None else W.w1_scale[e]) for e in range(E)])
     W2 = np.stack([formats.dequant(W.fmt, W.w2[e], None if W.w2_scale is None else W.w2_scale[e]) for e in range(E)])
-    I = W1.shape[1] // 2
-    gate = np.einsum("tk,eik->tei", x, W1[:, :I, :])
-    up = np.einsum("tk,eik->tei", x, W1[:, I:, :])
-    if W.b1 is not None:
-        b1 = formats.bf16_decode(W.b1)
-        gate = gate + b1[None, :, :I]
-        up = up + b1[None, :, I:]
-    act = gate * (1.0 / (1.0 + np.exp(-gate))) * up
+    if W.activation == "relu2":  # relu(a)^2 written as a * a * step(a)
+        a = np.einsum("tk,eik->tei", x, W1)
+        if W.b1 is not None:
+            a = a + formats.bf16_decode(W.b1)[None]
+        act = a * a * (a > 0)
+    else:
+        I = W1.shape[1] // 2
+        gate = np.einsum("tk,eik->tei", x, W1[:, :I, :])
+        up = np.einsum("tk,eik->tei", x, W1[:, I:, :])
+        if W.b1 is not None:
+            b1 = formats.bf16_decode(W.b1)
+            gate = gate + b1[None, :, :I]
+            up = up + b1[None, :, I:]
+        act = gate * (1.0 / (1.0 + np.exp(-gate))) * up
     o = np.einsum("tei,eki->tek", act, W2)
     if W.b2 is not None:
         o = o + formats.bf16_decode(W.b2)[None]
@@ -334,6 +341,74 @@ def check_layer_bias_only():
     assert np.allclose(y, want, rtol=1e-14, atol=1e-15)
 
 
+def check_layer_relu2_dense_formulation(seed=10):
+    rng = np.random.default_rng(seed)
+    for fmt in ("mxfp4", "bf16"):
+        T, K, I, E, k = 13, 64, 64, 6, 3
+        W = _rand_weights(rng, E, K, I, fmt=fmt, activation="relu2")
+        from synth import to_bf16_bits
+        x = formats.bf16_decode(to_bf16_bits(rng.standard_normal((T, K))))
+        ids, w = route.route(rng.standard_normal((T, E)).astype(np.float32), k)
+        y = layer.moe_layer(x, ids, w, W)
+        yd = _dense_all_experts(x, ids, w, W, E)
+        assert np.allclose(y, yd, rtol=1e-11, atol=1e-11), np.abs(y - yd).max()
+
+
+def check_layer_relu2_single_expert_loops(seed=11):
+    """E=1, k=1, non-gated: a dense relu^2 MLP in per-element Python loops; the random bias
+    gives pre-activations of both signs."""
+    rng = np.random.default_rng(seed)
+    T, K, I = 3, 32, 64
+    W = _rand_weights(rng, 1, K, I, activation="relu2")
+    from synth import to_bf16_bits
+    x = formats.bf16_decode(to_bf16_bits(rng.standard_normal((T, K))))
+    ids = np.zeros((T, 1), dtype=np.int32)
+    w = np.ones((T, 1), dtype=np.float32)
+    y = layer.moe_layer(x, ids, w, W)
+    W1 = formats.dequant_mxfp4(W.w1[0], W.w1_scale[0])
+    W2 = formats.dequant_mxfp4(W.w2[0], W.w2_scale[0])
+    b1 = formats.bf16_decode(W.b1[0])
+    b2 = formats.bf16_decode(W.b2[0])
+    signs = set()
+    for t in range(T):
+        h = []
+        for i in range(I):
+            a = math.fsum(x[t, c] * W1[i, c] for c in range(K)) + b1[i]
+            signs.add(a > 0)
+            h.append(a * a if a > 0 else 0.0)
+        for n in range(K):
+            o = math.fsum(h[i] * W2[n, i] for i in range(I)) + b2[n]
+            assert abs(o - y[t, n]) <= 1e-12 * max(1.0, abs(o)), (t, n, o, y[t, n])
+    assert signs == {True, False}
+
+
+def check_layer_relu2_closed_form():
+    """Constant codes and scales, no bias: a positive constant activation gives h = g^2 per
+    feature; its negation gives h = 0 and y = 0; and the layer is homogeneous of degree 2."""
+    T, K, I, E = 4, 64, 32, 3
+    c1, c2 = 0x3, 0xA          # E2M1 1.5 and -1.0
+    s1, s2 = 127 - 3, 127 - 1
+    w1 = np.full((E, I, K // 2), c1 | (c1 << 4), dtype=np.uint8)
+    w2 = np.full((E, K, I // 2), c2 | (c2 << 4), dtype=np.uint8)
+    W = layer.ExpertWeights("mxfp4", w1, np.full((E, I, K // 32), s1, np.uint8), None,
+                            w2, np.full((E, K, I // 32), s2, np.uint8), None, activation="relu2")
+    ids = np.array([[0, 1], [2, 0], [1, 2], [0, 2]], dtype=np.int32)
+    w = np.array([[0.25, 0.75], [0.5, 0.5], [1.0, 0.0], [0.125, 0.875]], dtype=np.float32)
+    a = 0.75
+    y = layer.moe_layer(np.full((T, K), a), ids, w, W)
+    g = K * a * 1.5 * 2.0 ** -3
+    o = I * g * g * (-1.0) * 2.0 ** -1
+    for t in range(T):
+        assert np.allclose(y[t], float(w[t].astype(np.float64).sum()) * o, rtol=1e-14, atol=0)
+    assert np.array_equal(layer.moe_layer(np.full((T, K), -a), ids, w, W), np.zeros((T, K)))
+    rng = np.random.default_rng(12)
+    Wr = _rand_weights(rng, E, K, I, bias=False, activation="relu2")
+    x = rng.standard_normal((T, K))
+    y1 = layer.moe_layer(x, ids, w, Wr)
+    y3 = layer.moe_layer(3.0 * x, ids, w, Wr)
+    assert np.allclose(y3, 9.0 * y1, rtol=1e-12, atol=1e-12)
+
+
 def check_layer_empty_expert_no_effect(seed=7):
     rng = np.random.default_rng(seed)
     T, K, I, E, k = 9, 64, 32, 4, 2
@@ -397,5 +472,6 @@ ALL_CHECKS = [
     check_route_brute, check_align_golden, check_align_brute, check_align_invariants,
     check_layer_dense_formulation, check_layer_single_expert_mlp,
     check_layer_constant_closed_form, check_layer_bias_only,
-    check_layer_empty_expert_no_effect, check_grouped_gemm_brute, check_wgrad_closed_forms,
+    check_layer_relu2_dense_formulation, check_layer_relu2_single_expert_loops,
+    check_layer_relu2_closed_form, check_layer_empty_expert_no_effect, check_grouped_gemm_brute, check_wgrad_closed_forms,
 ]

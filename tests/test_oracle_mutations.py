@@ -146,6 +146,33 @@ def mut_silu_sign(monkeypatch):
     return [pins.check_layer_dense_formulation, pins.check_layer_constant_closed_form]
 
 
+def mut_relu2_unsquared(monkeypatch):
+    monkeypatch.setattr(layer, "relu2", lambda a: np.maximum(a, 0.0))
+    return [pins.check_layer_relu2_single_expert_loops, pins.check_layer_relu2_closed_form]
+
+
+def mut_relu2_sign(monkeypatch):
+    monkeypatch.setattr(layer, "relu2", lambda a: np.minimum(a, 0.0) ** 2)
+    return [pins.check_layer_relu2_single_expert_loops, pins.check_layer_relu2_closed_form]
+
+
+def mut_relu2_dropped_b1(monkeypatch):
+    orig = layer.expert_ffn_relu2
+    monkeypatch.setattr(layer, "expert_ffn_relu2", lambda x, w1, b1, w2, b2: orig(x, w1, None, w2, b2))
+    return [pins.check_layer_relu2_dense_formulation, pins.check_layer_relu2_single_expert_loops]
+
+
+def mut_relu2_runs_swiglu(monkeypatch):
+    orig = layer.moe_pairs
+
+    def pairs(x, ids, W, tokens=None):
+        if W.activation == "relu2":  # the non-gated weights read as gate|up halves
+            W = layer.ExpertWeights(W.fmt, W.w1, W.w1_scale, W.b1, W.w2, W.w2_scale, W.b2)
+        return orig(x, ids, W, tokens)
+    monkeypatch.setattr(layer, "moe_pairs", pairs)
+    return [pins.check_layer_relu2_closed_form]
+
+
 def mut_gemm_src_per_pair(monkeypatch):
     orig = layer.grouped_gemm
     monkeypatch.setattr(layer, "grouped_gemm", lambda a, ids, f, per_pair, pairs=None: orig(a, ids, f, True, pairs) if not per_pair else orig(a, ids, f, False, pairs))
@@ -181,7 +208,8 @@ MUTATIONS = [mut_e8m0_zero, mut_nibble_order, mut_e2m1_subnormal, mut_e4m3_bias,
              mut_bucket_floor2, mut_bucket_16_per_octave, mut_route_tie_high,
              mut_route_full_softmax, mut_align_unstable, mut_align_sentinel_zero,
              mut_gate_up_swapped, mut_dropped_b1, mut_w2_transposed, mut_combine_unweighted,
-             mut_silu_sign, mut_gemm_src_per_pair, mut_wgrad_transposed, mut_wgrad_src_index]
+             mut_silu_sign, mut_relu2_unsquared, mut_relu2_sign, mut_relu2_dropped_b1,
+             mut_relu2_runs_swiglu, mut_gemm_src_per_pair, mut_wgrad_transposed, mut_wgrad_src_index]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS, ids=lambda f: f.__name__)
