@@ -327,18 +327,34 @@ def bench_ours(args, rank, world, local_rank):
     clocks.start()
     time.sleep(0.2)
     cur = torch.cuda.current_stream()
-    t_start.record(cur)
-    for i in range(steps):
-        if graph is not None:
-            graph.replay()
-        else:
-            step()
-    t_end.record(cur)
-    torch.cuda.synchronize()
+    # a step whose weights fit twice in L2 would be served from L2 by the previous step: such
+    # workloads write a 512 MB buffer between steps, outside the timed intervals
+    flush = step_weight_bytes < 2 * L2_BYTES
+    if flush:
+        scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            scrub.fill_(i & 0xff)
+            pairs[i][0].record(cur)
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
+            pairs[i][1].record(cur)
+        torch.cuda.synchronize()
+    else:
+        t_start.record(cur)
+        for i in range(steps):
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
+        t_end.record(cur)
+        torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     ck = clocks.stop(local_rank)
-    ms = t_start.elapsed_time(t_end)
+    ms = sum(a.elapsed_time(b) for a, b in pairs) if flush else t_start.elapsed_time(t_end)
     if int(L.status[0]) != 0:
         raise RuntimeError(f"device status {int(L.status[0])}")
     if world > 1:
@@ -416,8 +432,11 @@ def bench_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": ("f16 tcgen05 mma -> f32" if tensor_path else "f16 mma -> f32") if w.quant != "bf16" else "bf16 mma -> f32",
         "data": "synthetic (seeded PCG64 inputs, random-init weights)",
-        "config": dict(describe(w, rows), l2=f"inputs larger than L2: {step_weight_bytes / 1e9:.2f} GB "
-                                              f"of expert weights streamed per step > 129 MB L2",
+        "config": dict(describe(w, rows),
+                       l2=(f"L2 flushed between steps (512 MB written outside the timed intervals): "
+                           f"{step_weight_bytes / 1e9:.3f} GB of expert weights per step" if flush else
+                           f"inputs larger than L2: {step_weight_bytes / 1e9:.2f} GB "
+                           f"of expert weights streamed per step > 129 MB L2"),
                        parallelism=f"replicas x{world}",
                        timed=("replays of one CUDA graph of the whole step (every kernel of the step runs each "
                               "replay); the per-kernel split comes from eager steps" if graph is not None

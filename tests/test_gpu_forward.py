@@ -29,7 +29,7 @@ def device_layer(moe, lay, w, max_rows, pad):
     from mixture_experts_grouped_align_gb300.runner import DeviceLayer
     return DeviceLayer(w.quant, w.E, w.K, w.I, w.k, dev(lay["w1"]), dev(lay["w1_scale"]),
                        dev(lay["b1"]), dev(lay["w2"]), dev(lay["w2_scale"]), dev(lay["b2"]),
-                       max_rows=max_rows, pad=pad)
+                       max_rows=max_rows, pad=pad, activation=w.activation)
 
 
 def run(moe, L, lay, T):
@@ -45,7 +45,7 @@ def run(moe, L, lay, T):
 
 def oracle_y(lay, w, T, tokens=None):
     W = olayer.ExpertWeights(w.quant, lay["w1"], lay["w1_scale"], lay["b1"], lay["w2"],
-                             lay["w2_scale"], lay["b2"])
+                             lay["w2_scale"], lay["b2"], activation=w.activation)
     x = ofmt.bf16_decode(lay["x"][:T])
     ids, wt = oroute.route(lay["logits"][:T], w.k)
     return olayer.moe_layer(x, ids, wt, W, tokens)
@@ -181,3 +181,85 @@ def test_w4a16_scale_outside_f16_range_is_reported_on_the_tensor_memory_path(moe
     y64, st64 = _run_status(moe, L, lay, 64)
     assert st64 == 0
     assert_close_bf16(bf16_to_np(y64), oracle_y(lay, w, 64), what="weight-streaming exact")
+
+
+def test_bucket_graphs_replay_equal_eager_padded_steps(moe):
+    """One CUDA graph per bucket (prewarm) replays the same bits as the eager padded step on
+    every real row, for batches that share a bucket (stale pad rows are re-zeroed) and for
+    batches in different buckets, including the largest."""
+    w = synth.Workload("graphs", T=1100, K=256, I=256, E=16, k=4, quant="mxfp4", seed=13,
+                       scale_exp=(-6, -2), bias=True)
+    lay = synth.make_layer(w)
+    Lg = device_layer(moe, lay, w, w.T, pad=True)
+    Le = device_layer(moe, lay, w, w.T, pad=True)
+    got = Lg.prewarm()
+    assert got == obucket.bucket_iter(obucket.bucket(w.T))
+    assert sorted(Lg.graphs) == got
+    for T in [300, 290, 1, 17, 256, 257, 1001, 1100, 300]:
+        x = dev(lay["x"][:T])
+        lg = dev(lay["logits"][:T])
+        Lg.status.zero_()
+        yg = Lg.step_bucketed(x, lg, T).clone()
+        torch.cuda.synchronize()
+        assert int(Lg.status[0]) == 0
+        ye, _ = run(moe, Le, lay, T)
+        assert torch.equal(yg.view(torch.int16), ye.view(torch.int16)), f"T={T}"
+    assert_close_bf16(bf16_to_np(yg), oracle_y(lay, w, 300), what="graph T=300")
+    with pytest.raises(ValueError):
+        device_layer(moe, lay, w, 64, pad=False).prewarm()
+
+
+# ---------------------------------------------------------------- non-gated relu^2 layers
+
+@pytest.mark.parametrize("M", [1, 7, 28])
+def test_relu2_decode_bf16_nemotron_shape(moe, M):
+    """The Nemotron decode shape with its non-gated relu^2 (GEMM1 N = 1856), bf16."""
+    w = synth.decode_bf16_relu2_workload(M)
+    lay = synth.make_layer(w)
+    L = device_layer(moe, lay, w, M, pad=True)
+    y, rows = run(moe, L, lay, M)
+    assert rows == M
+    assert_close_bf16(bf16_to_np(y), oracle_y(lay, w, M), what=f"relu2 bf16 M={M}")
+
+
+@pytest.mark.parametrize("T,I", [(64, 512), (300, 320), (1001, 384)])
+def test_relu2_w4a16_padded_equals_unpadded_and_oracle(moe, T, I):
+    """W4A16 relu^2 on both variants (64 rows: weight streaming; 300 and 1001: tensor
+    memory with slot-ordered h), feature counts that leave a partial and an empty 128-feature
+    box in the last tile; padded and unpadded runs give the same bits on every real row."""
+    w = synth.Workload("relu2", T=T, K=256, I=I, E=16, k=4, quant="mxfp4", seed=14,
+                       scale_exp=(-6, -2), bias=True, activation="relu2")
+    lay = synth.make_layer(w)
+    Lp = device_layer(moe, lay, w, T, pad=True)
+    Lu = device_layer(moe, lay, w, T, pad=False)
+    yp, _ = run(moe, Lp, lay, T)
+    yu, _ = run(moe, Lu, lay, T)
+    assert torch.equal(yp.view(torch.int16), yu.view(torch.int16))
+    assert_close_bf16(bf16_to_np(yp), oracle_y(lay, w, T), what=f"relu2 w4a16 T={T}")
+
+
+def test_relu2_w4a16_long_k_runs_the_shared_memory_decode_kernel(moe):
+    """K = 4160 is past the tensor-memory kernel's limit: GEMM1 runs the shared-memory-decode
+    tensor-core kernel with the relu^2 epilogue."""
+    w = synth.Workload("relu2_longk", T=300, K=4160, I=256, E=4, k=2, quant="mxfp4", seed=15,
+                       scale_exp=(-7, -4), bias=True, activation="relu2")
+    lay = synth.make_layer(w)
+    L = device_layer(moe, lay, w, w.T, pad=False)
+    y, _ = run(moe, L, lay, w.T)
+    assert_close_bf16(bf16_to_np(y), oracle_y(lay, w, w.T), what="relu2 K=4160")
+
+
+def test_relu2_graph_replay_equals_eager(moe):
+    w = synth.Workload("relu2_graph", T=300, K=256, I=320, E=16, k=4, quant="mxfp4", seed=16,
+                       scale_exp=(-6, -2), bias=True, activation="relu2")
+    lay = synth.make_layer(w)
+    Lg = device_layer(moe, lay, w, w.T, pad=True)
+    Le = device_layer(moe, lay, w, w.T, pad=True)
+    Lg.prewarm()
+    for T in (300, 40):
+        Lg.status.zero_()
+        yg = Lg.step_bucketed(dev(lay["x"][:T]), dev(lay["logits"][:T]), T).clone()
+        torch.cuda.synchronize()
+        assert int(Lg.status[0]) == 0
+        ye, _ = run(moe, Le, lay, T)
+        assert torch.equal(yg.view(torch.int16), ye.view(torch.int16)), f"T={T}"
