@@ -148,16 +148,25 @@ moe_status moe_bucket_pad(int64_t T, moe_quant quant, int64_t* T_pad,
  * Forward: grouped GEMM1 + SwiGLU -> grouped GEMM2 -> combine                           *
  * ------------------------------------------------------------------------------------ */
 
+/* Activation between the GEMMs.  MOE_ACT_RELU2 is the non-gated relu2_no_mul of [DECODE]
+ * (the Nemotron recipe in its table of added files: GEMM1 N = 1856 = I, no gate product). */
+typedef enum {
+  MOE_ACT_SWIGLU = 0,     /* h = silu(gate) * up; GEMM1 has 2I rows (gate | up)           */
+  MOE_ACT_RELU2 = 1       /* h = max(a, 0)^2;     GEMM1 has I rows                        */
+} moe_activation;
+
+/* N1 = 2I for MOE_ACT_SWIGLU, I for MOE_ACT_RELU2. */
 typedef struct {
   moe_quant quant;
   int32_t E, K, I;        /* experts, hidden size, intermediate size                      */
-  const void* w1;         /* [E, 2I, K] (MXFP4: [E, 2I, K/2] bytes); rows 0..I-1 gate,
-                             rows I..2I-1 up                                              */
-  const uint8_t* w1_scale;/* [E, 2I, K/32] E8M0 (NULL for bf16)                           */
-  const void* b1;         /* [E, 2I] bf16 or NULL                                         */
+  const void* w1;         /* [E, N1, K] (MXFP4: [E, N1, K/2] bytes); SwiGLU: rows 0..I-1
+                             gate, rows I..2I-1 up                                        */
+  const uint8_t* w1_scale;/* [E, N1, K/32] E8M0 (NULL for bf16)                           */
+  const void* b1;         /* [E, N1] bf16 or NULL                                         */
   const void* w2;         /* [E, K, I] (MXFP4: [E, K, I/2] bytes)                         */
   const uint8_t* w2_scale;/* [E, K, I/32] E8M0 (NULL for bf16)                            */
   const void* b2;         /* [E, K] bf16 or NULL                                          */
+  int32_t activation;     /* moe_activation (a zero-initialised struct is SwiGLU)         */
 } moe_weights;
 
 /* Workspace bytes moe_forward needs for T_rows rows of top-k with an alignment of
@@ -169,8 +178,9 @@ size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t 
 
 /* For every real token t < T_real (the others, e.g. bucket pad rows, are computed and
  * then sliced off):
- *   gu = x_t . W1[e]^T + b1[e];  h = silu(gu[:I]) * gu[I:]  (fp32, then stored as the
- *        MMA operand type of GEMM2: f16 RNE for MXFP4 weights -- |h| or |x| > 65504 sets
+ *   gu = x_t . W1[e]^T + b1[e];  h = silu(gu[:I]) * gu[I:]  (SwiGLU) or
+ *        h = max(gu, 0)^2  (relu^2; a NaN stays NaN)  (fp32, then stored as the MMA
+ *        operand type of GEMM2: f16 RNE for MXFP4 weights -- |h| or |x| > 65504 sets
  *        MOE_ERR_RANGE -- and bf16 RNE for bf16 weights)
  *   o_tj = w[t,j] * (h . W2[e]^T + b2[e])                    (fp32)
  *   y_t  = sum_{j=0..k-1} o_tj, in order of j, rounded to bf16 RNE.

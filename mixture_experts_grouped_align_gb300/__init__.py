@@ -17,7 +17,7 @@ import os
 from .build import LIB, build  # noqa: F401
 
 __all__ = [
-    "MoeError", "load", "Ctx", "QUANT", "moe_align_capacity", "moe_align", "moe_bucket",
+    "MoeError", "load", "Ctx", "QUANT", "ACTIVATION", "moe_align_capacity", "moe_align", "moe_bucket",
     "moe_bucket_count", "moe_bucket_pad", "moe_forward_workspace_size", "moe_forward",
     "moe_forward_no_alloc", "moe_grouped_gemm", "moe_wgrad", "EXPORTED_SYMBOLS",
 ]
@@ -28,6 +28,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_WARN_PAD_IGNORED", -1: "MOE_ERR_INVALID_ARG
                 -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CAPACITY", -4: "MOE_ERR_CUDA",
                 -5: "MOE_ERR_INVALID_EXPERT", -6: "MOE_ERR_RANGE", -7: "MOE_ERR_TIMEOUT"}
 QUANT = {"bf16": 0, "mxfp4": 1, "mxfp8": 2}
+ACTIVATION = {"swiglu": 0, "relu2": 1}
 
 EXPORTED_SYMBOLS = [
     "moe_last_error", "moe_align_capacity", "moe_align", "moe_bucket", "moe_bucket_count",
@@ -52,7 +53,7 @@ class _Weights(ctypes.Structure):
     _fields_ = [("quant", ctypes.c_int), ("E", ctypes.c_int32), ("K", ctypes.c_int32),
                 ("I", ctypes.c_int32), ("w1", ctypes.c_void_p), ("w1_scale", ctypes.c_void_p),
                 ("b1", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("w2_scale", ctypes.c_void_p),
-                ("b2", ctypes.c_void_p)]
+                ("b2", ctypes.c_void_p), ("activation", ctypes.c_int32)]
 
 
 _lib = None
@@ -176,11 +177,16 @@ def moe_forward_workspace_size(T_rows, k, K, I, cap_tokens) -> int:
     return load().moe_forward_workspace_size(T_rows, k, K, I, cap_tokens)
 
 
+def _act(activation):
+    return ACTIVATION[activation] if isinstance(activation, str) else int(activation)
+
+
 def moe_forward(quant, E, K, I, w1, w1_scale, b1, w2, w2_scale, b2, x, x_scale, T_rows, T_real, k,
                 topk_w, sorted_token_ids, expert_ids, num_tokens_post_padded, expert_offsets,
-                block_m, cap_tokens, y, ctx):
+                block_m, cap_tokens, y, ctx, activation="swiglu"):
     q = QUANT[quant] if isinstance(quant, str) else quant
-    W = _Weights(q, E, K, I, _ptr(w1), _ptr(w1_scale), _ptr(b1), _ptr(w2), _ptr(w2_scale), _ptr(b2))
+    W = _Weights(q, E, K, I, _ptr(w1), _ptr(w1_scale), _ptr(b1), _ptr(w2), _ptr(w2_scale), _ptr(b2),
+                 _act(activation))
     return _check(load().moe_forward(ctypes.byref(W), _ptr(x), _ptr(x_scale), T_rows, T_real, k,
                                      _ptr(topk_w), _ptr(sorted_token_ids), _ptr(expert_ids),
                                      _ptr(num_tokens_post_padded), _ptr(expert_offsets), block_m,
@@ -189,10 +195,11 @@ def moe_forward(quant, E, K, I, w1, w1_scale, b1, w2, w2_scale, b2, x, x_scale, 
 
 def moe_forward_no_alloc(quant, E, K, I, w1, w1_scale, b1, w2, w2_scale, b2, x, x_scale, T_rows,
                          T_real, k, topk_w, sorted_token_ids, expert_ids, num_tokens_post_padded,
-                         expert_offsets, block_m, cap_tokens, y, ctx=None):
+                         expert_offsets, block_m, cap_tokens, y, ctx=None, activation="swiglu"):
     """moe_forward with its scratch in the library's fixed device array (no workspace)."""
     q = QUANT[quant] if isinstance(quant, str) else quant
-    W = _Weights(q, E, K, I, _ptr(w1), _ptr(w1_scale), _ptr(b1), _ptr(w2), _ptr(w2_scale), _ptr(b2))
+    W = _Weights(q, E, K, I, _ptr(w1), _ptr(w1_scale), _ptr(b1), _ptr(w2), _ptr(w2_scale), _ptr(b2),
+                 _act(activation))
     return _check(load().moe_forward_no_alloc(
         ctypes.byref(W), _ptr(x), _ptr(x_scale), T_rows, T_real, k, _ptr(topk_w),
         _ptr(sorted_token_ids), _ptr(expert_ids), _ptr(num_tokens_post_padded),

@@ -560,6 +560,17 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
             } else {   // bf16 for the bf16 MMA of GEMM2
               static_cast<uint16_t*>(a.out)[(int64_t)p * a.Nout + n] = moe::f32_to_bf16_bits(hval);
             }
+          } else if (EPI == EPI_RELU2) {
+            float av = v[0][i];
+            if (bias) av += moe::bf16_bits_to_f32(bias[e * a.Nw + n]);
+            const float hval = moe::relu2(av);
+            if (MX) {
+              const __half hv = __float2half_rn(hval);
+              if (__hisinf(hv)) bad = true;
+              static_cast<__half*>(a.out)[(int64_t)p * a.Nout + n] = hv;
+            } else {
+              static_cast<uint16_t*>(a.out)[(int64_t)p * a.Nout + n] = moe::f32_to_bf16_bits(hval);
+            }
           } else if (EPI == EPI_WEIGHTED_F32) {
             float o = v[0][i];
             if (bias) o += moe::bf16_bits_to_f32(bias[e * a.Nw + n]);
@@ -621,9 +632,11 @@ cudaError_t decode_gemm(const GroupedGemm& g, cudaStream_t stream) {
   MOE_CASE(WF_MXFP4, EPI_SWIGLU)
   MOE_CASE(WF_MXFP4, EPI_WEIGHTED_F32)
   MOE_CASE(WF_MXFP4, EPI_PLAIN_BF16)
+  MOE_CASE(WF_MXFP4, EPI_RELU2)
   MOE_CASE(WF_BF16, EPI_SWIGLU)
   MOE_CASE(WF_BF16, EPI_WEIGHTED_F32)
   MOE_CASE(WF_BF16, EPI_PLAIN_BF16)
+  MOE_CASE(WF_BF16, EPI_RELU2)
   MOE_CASE(WF_MXFP8, EPI_SWIGLU)
   MOE_CASE(WF_MXFP8, EPI_WEIGHTED_F32)
   MOE_CASE(WF_MXFP8, EPI_PLAIN_BF16)

@@ -197,6 +197,9 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
               "moe_forward supports MOE_Q_BF16 and MOE_Q_MXFP4_W4A16 (MXFP8: moe_grouped_gemm)");
   const int32_t E = W->E, K = W->K, I = W->I;
   MOE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= E, MOE_ERR_INVALID_ARG, "bad E or k");
+  MOE_REQUIRE(W->activation == MOE_ACT_SWIGLU || W->activation == MOE_ACT_RELU2, MOE_ERR_INVALID_ARG,
+              "unknown activation");
+  const bool relu2 = W->activation == MOE_ACT_RELU2;
   MOE_REQUIRE(K >= 32 && I >= 32 && K % 32 == 0 && I % 32 == 0, MOE_ERR_UNSUPPORTED,
               "K and I must be positive multiples of 32");
   MOE_REQUIRE(T_rows >= 0 && T_real >= 0 && T_real <= T_rows, MOE_ERR_INVALID_ARG,
@@ -230,12 +233,12 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
 
   moe_launch::GroupedGemm g1{};
   g1.wfmt = wf;
-  g1.epi = moe_launch::EPI_SWIGLU;
+  g1.epi = relu2 ? moe_launch::EPI_RELU2 : moe_launch::EPI_SWIGLU;
   g1.w = W->w1; g1.w_scale = W->w1_scale; g1.bias = W->b1;
   g1.act = fp4 ? x16 : x;  // the f16 MMA of the MXFP4 path reads x converted once to f16
   g1.act_fmt = fp4 ? moe_launch::ACT_F16 : moe_launch::ACT_BF16;
   g1.act_scale = nullptr; g1.act_per_pair = 0;
-  g1.Nw = 2 * (int64_t)I; g1.Kin = K; g1.Nout = I; g1.k = k; g1.P = P; g1.E = E;
+  g1.Nw = relu2 ? (int64_t)I : 2 * (int64_t)I; g1.Kin = K; g1.Nout = I; g1.k = k; g1.P = P; g1.E = E;
   g1.sorted = sorted_token_ids; g1.expert_ids = expert_ids; g1.ntpp = num_tokens_post_padded;
   g1.bm = block_m; g1.grid_blocks = blocks; g1.topk_w = topk_w; g1.out = h;
   g1.status = status_of(ctx);

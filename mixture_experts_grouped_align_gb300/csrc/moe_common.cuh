@@ -127,6 +127,12 @@ MOE_DEV uint4 ldg_nc_u128(const void* p) {
 // near 1e-6, far below the f16 / bf16 rounding of the value it feeds); 0 for g -> -inf.
 MOE_DEV float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
+// relu(a)^2, exact up to the one rounding of the product; a NaN passes through.
+MOE_DEV float relu2(float a) {
+  const float r = a < 0.f ? 0.f : a;
+  return r * r;
+}
+
 }  // namespace moe
 
 // Host-side error reporting shared by the translation units.

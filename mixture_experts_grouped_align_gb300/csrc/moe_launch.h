@@ -24,7 +24,9 @@ cudaError_t gather_rows_f16(const void* x, const int32_t* sorted, const int32_t*
 
 // ---- grouped GEMMs on the weight-streaming (decode) path (decode_gemm.cu)
 enum WFmt { WF_BF16 = 0, WF_MXFP4 = 1, WF_MXFP8 = 2 };
-enum Epi { EPI_SWIGLU = 0, EPI_WEIGHTED_F32 = 1, EPI_PLAIN_BF16 = 2 };
+// SwiGLU and relu^2 write h (f16 for MX weights, bf16 for bf16 weights); relu^2 reads one
+// weight matrix (Nw = Nout), SwiGLU two (gate rows then up rows, Nw = 2 * Nout).
+enum Epi { EPI_SWIGLU = 0, EPI_WEIGHTED_F32 = 1, EPI_PLAIN_BF16 = 2, EPI_RELU2 = 3 };
 enum ActFmt { ACT_BF16 = 0, ACT_F16 = 1 };
 
 struct GroupedGemm {
@@ -51,7 +53,7 @@ struct GroupedGemm {
   int bm;
   int64_t grid_blocks;      // block slots to launch for
   const float* topk_w;      // [P] (EPI_WEIGHTED_F32)
-  void* out;                // [P, Nout]: f16 (SWIGLU), bf16 (PLAIN) or f32 (WEIGHTED)
+  void* out;                // [P, Nout]: f16 / bf16 (SWIGLU, RELU2), bf16 (PLAIN) or f32 (WEIGHTED)
   int32_t* status;
 };
 size_t decode_gemm_smem_bytes(const GroupedGemm& g);

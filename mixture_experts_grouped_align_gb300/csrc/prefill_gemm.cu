@@ -18,8 +18,9 @@
 //               Every thread copies exactly the raw bytes it later decodes: a cp.async
 //               wait only covers the waiting thread's own copies;
 //   warps 4-7   drain an accumulator with tcgen05.ld (one TMEM lane = one tile row)
-//               and run the fused epilogue: bias + SwiGLU -> h (f16), bias * routing
-//               weight -> o (fp32), or bias -> out (bf16), each row to its pair index.
+//               and run the fused epilogue: bias + SwiGLU or bias + relu^2 -> h (f16),
+//               bias * routing weight -> o (fp32), or bias -> out (bf16), each row to
+//               its pair index.
 // Every mbarrier wait is bounded; a wait that runs out sets MOE_ERR_TIMEOUT, every role
 // leaves its loop, the MMA lane drains its own work and the TMEM is freed.
 //
@@ -452,6 +453,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(PArgs pa) {
 #pragma unroll
               for (int q = 0; q < 8; ++q)
                 dst[q] = make_float4(o[4 * q] * wgt, o[4 * q + 1] * wgt, o[4 * q + 2] * wgt, o[4 * q + 3] * wgt);
+            } else if (EPI == EPI_RELU2) {
+              __half hv[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                hv[j] = __float2half_rn(moe::relu2(o[j]));
+                if (__hisinf(hv[j])) bad = true;
+              }
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(a.out) + (int64_t)p * a.Nout + n0 + c0);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) dst[q] = reinterpret_cast<const uint4*>(hv)[q];
             } else {
               uint32_t pk[16];
 #pragma unroll
@@ -540,6 +551,7 @@ cudaError_t prefill_gemm(const GroupedGemm& g, cudaStream_t stream) {
   MOE_CASE(WF_MXFP4, EPI_SWIGLU, false)
   MOE_CASE(WF_MXFP4, EPI_WEIGHTED_F32, false)
   MOE_CASE(WF_MXFP4, EPI_PLAIN_BF16, false)
+  MOE_CASE(WF_MXFP4, EPI_RELU2, false)
   MOE_CASE(WF_MXFP8, EPI_PLAIN_BF16, true)
   MOE_CASE(WF_MXFP8, EPI_SWIGLU, true)
   MOE_CASE(WF_MXFP8, EPI_WEIGHTED_F32, true)

@@ -32,9 +32,9 @@
 //               and writes them into the stage's TMEM columns with tcgen05.st;
 //   warps 4-7 and 16-19 drain the accumulators (one TMEM lane = one feature, one column =
 //               one pair; each group of four takes half of the columns), release them before
-//               computing the last chunk, and run the fused epilogue: bias + SwiGLU -> h
-//               (f16, through a shared staging tile and one TMA store when h is in slot
-//               order), bias * routing weight -> o (fp32), or bias -> out (bf16).
+//               computing the last chunk, and run the fused epilogue: bias + SwiGLU or
+//               bias + relu^2 -> h (f16, through a shared staging tile and TMA stores when h
+//               is in slot order), bias * routing weight -> o (fp32), or bias -> out (bf16).
 // Every mbarrier wait is bounded; one that runs out sets MOE_ERR_TIMEOUT, every role leaves
 // its loop, the MMA lane drains its own work and the TMEM is freed.
 //
@@ -61,7 +61,12 @@ constexpr int kBK = 64;     // K elements per stage
 // 128 features for SwiGLU, else 256 consecutive features.  The token tile is read once for
 // both, which halves its L2 traffic per flop.
 constexpr int kMats = 2;
-__host__ __device__ constexpr int smem_stages(bool swiglu) { return swiglu ? 5 : 7; }
+// (fewer stages where the h staging tile takes shared memory: 128 x 128 f16 for SwiGLU,
+// 128 x 256 for relu^2)
+__host__ __device__ constexpr int smem_stages(int epi) { return epi == EPI_SWIGLU ? 5 : (epi == EPI_RELU2 ? 4 : 7); }
+__host__ __device__ constexpr int stage_out_bytes(int epi) {
+  return epi == EPI_SWIGLU ? kTN * kTM * 2 : (epi == EPI_RELU2 ? kMats * kTN * kTM * 2 : 0);
+}
 constexpr int kTmemStages = 4;
 // epilogue warps 4-7 take token columns 0-63, warps 16-19 columns 64-127 (warp % 4 = TMEM
 // lane quarter); decoders are warps 8-15
@@ -82,18 +87,18 @@ struct TArgs {
 };
 
 // Shared memory: token-tile stages (16 KB each) | raw-code slots (2 x 128 rows x 128 B,
-// 128-byte swizzle) | SwiGLU output staging (128 slots x 128 f16) | barriers.
+// 128-byte swizzle) | h output staging (128 slots x 128 f16 per matrix) | barriers.
 struct TLayout {
   int slot, raw, raw_slot, stg, bars, total;
 };
 
-__host__ __device__ inline TLayout tlayout(bool swiglu) {
+__host__ __device__ inline TLayout tlayout(int epi) {
   TLayout L;
   L.slot = kTN * 128;
-  L.raw = smem_stages(swiglu) * L.slot;
+  L.raw = smem_stages(epi) * L.slot;
   L.raw_slot = kMats * kTM * 128;
   L.stg = L.raw + kRawSlots * L.raw_slot;
-  L.bars = L.stg + (swiglu ? kTN * kTM * 2 : 0);
+  L.bars = L.stg + stage_out_bytes(epi);
   L.total = L.bars + 512 + 1024;
   return L;
 }
@@ -199,8 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const GroupedGemm& a = ta.g;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const TLayout L = tlayout(SW);
-  constexpr int S1 = smem_stages(SW), S2 = kTmemStages;
+  constexpr bool R2 = (EPI == EPI_RELU2);
+  const TLayout L = tlayout(EPI);
+  constexpr int S1 = smem_stages(EPI), S2 = kTmemStages;
   uint64_t* ld_full = reinterpret_cast<uint64_t*>(smem + L.bars);  // [S1] token tile + raw codes landed
   uint64_t* empty = ld_full + S1;                                   // [S1] shared stage consumed by the MMA
   uint64_t* a_full = empty + S1;                                    // [S2] decoded weights in TMEM
@@ -462,9 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int cbase = warp >= kEpiWarp1 ? kEpiCols : 0;  // this warp's token columns
     const uint16_t* bias = static_cast<const uint16_t*>(a.bias);
-    // SwiGLU into slot-ordered h: the tile goes through shared memory and leaves as one TMA
-    // store, and the accumulators are released before the last chunk is computed
-    const bool staged = (EPI == EPI_SWIGLU) && a.out_by_slot;
+    // SwiGLU or relu^2 into slot-ordered h: the tile goes through shared memory and leaves
+    // as one TMA store per 128 features, and the accumulators are released before the last
+    // chunk is computed
+    const bool staged = (SW || R2) && a.out_by_slot;
     __half* stg = reinterpret_cast<__half*>(smem + L.stg);
     const uint32_t stg_s = smem_s + L.stg;
     uint32_t acc_it = 0, eb_it = 0;
@@ -541,6 +548,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               static_cast<__half*>(a.out)[row * a.Nout + fA] = hv;
             }
           }
+        } else if (R2) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int p = __shfl_sync(0xffffffffu, pl, j);
+            const __half hA = __float2half_rn(moe::relu2(__uint_as_float(v0[j]) + b0));
+            const __half hB = __float2half_rn(moe::relu2(__uint_as_float(v1[j]) + b1));
+            if (p < a.P && ((vA && __hisinf(hA)) || (vB && __hisinf(hB)))) bad = true;
+            if (staged) {
+              stg[(c0 + j) * kTM + 32 * q + lane] = hA;
+              stg[kTN * kTM + (c0 + j) * kTM + 32 * q + lane] = hB;
+            } else if (p < a.P) {
+              const int64_t row = a.out_by_slot ? slot0 + c0 + j : (int64_t)p;
+              if (vA) static_cast<__half*>(a.out)[row * a.Nout + fA] = hA;
+              if (vB) static_cast<__half*>(a.out)[row * a.Nout + fB] = hB;
+            }
+          }
         } else {
           const float wl = wls[cc / 32];
 #pragma unroll
@@ -561,11 +584,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (staged) {  // the tile's h rows [slot0, slot0 + 128) x features [mt * 128, + 128)
+      if (staged) {  // the tile's h rows [slot0, slot0 + 128) x its features, 128 per box
         tc::fence_proxy_async_smem();
         if (!epi_sync()) break;
         if (warp == kEpiWarp0 && lane == 0) {
-          tma::store_2d(&tmap_h, mt * kTM * 2, (int32_t)slot0, stg_s);
+          if (SW) {
+            tma::store_2d(&tmap_h, mt * kTM * 2, (int32_t)slot0, stg_s);
+          } else {
+#pragma unroll
+            for (int m = 0; m < kMats; ++m)  // a box past the last feature is not stored
+              if (tile_feature<false>(mt, m, 0) < a.Nout)
+                tma::store_2d(&tmap_h, (int32_t)tile_feature<false>(mt, m, 0) * 2, (int32_t)slot0,
+                              stg_s + m * kTN * kTM * 2);
+          }
           tma::bulk_commit();
         }
       }
@@ -596,7 +627,7 @@ int sm_count_ts() {
 template <int EPI>
 cudaError_t launch_ts(const TArgs& ta, const CUtensorMap& mx, const CUtensorMap& mw, const CUtensorMap& mh,
                       cudaStream_t stream) {
-  const TLayout L = tlayout(EPI == EPI_SWIGLU);
+  const TLayout L = tlayout(EPI);
   cudaError_t err = cudaFuncSetAttribute(prefill_ts_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
   int64_t grid = sm_count_ts();
@@ -612,7 +643,8 @@ namespace moe_launch {
 
 bool ts_supported(const GroupedGemm& g) {
   if (g.wfmt != WF_MXFP4 || g.act_fmt != ACT_F16) return false;
-  if (g.epi != EPI_SWIGLU && g.epi != EPI_WEIGHTED_F32 && g.epi != EPI_PLAIN_BF16) return false;
+  if (g.epi != EPI_SWIGLU && g.epi != EPI_RELU2 && g.epi != EPI_WEIGHTED_F32 && g.epi != EPI_PLAIN_BF16)
+    return false;
   if (g.bm != kTN || g.Kin <= 0 || g.Kin % kBK != 0 || g.Kin > kMaxKin) return false;
   const int64_t rows_total = g.act_by_slot ? g.grid_blocks * g.bm : (g.act_per_pair ? g.P : g.P / g.k);
   if (rows_total >= ((int64_t)1 << 31) - 1 || (int64_t)g.E * g.Nw >= ((int64_t)1 << 31)) return false;
@@ -620,7 +652,7 @@ bool ts_supported(const GroupedGemm& g) {
   uintptr_t al16 = reinterpret_cast<uintptr_t>(g.act) | reinterpret_cast<uintptr_t>(g.w);
   if (g.out_by_slot) al16 |= reinterpret_cast<uintptr_t>(g.out);
   if ((al16 & 15) != 0) return false;
-  return tlayout(g.epi == EPI_SWIGLU).total <= 227 * 1024;
+  return tlayout(g.epi).total <= 227 * 1024;
 }
 
 cudaError_t prefill_ts(const GroupedGemm& g, cudaStream_t stream) {
@@ -641,13 +673,15 @@ cudaError_t prefill_ts(const GroupedGemm& g, cudaStream_t stream) {
   if (!tma::encode_2d_u8(&mw, g.w, (uint64_t)g.Kin / 2, (uint64_t)g.E * g.Nw, (uint64_t)g.Kin / 2, 128, kTM,
                          true))
     return cudaErrorInvalidValue;
-  // SwiGLU output in slot order: h rows of Nout f16, stored 128 slots x 128 features per box
+  // SwiGLU or relu^2 output in slot order: h rows of Nout f16, stored 128 slots x 128
+  // features per box
   CUtensorMap mh = mx;
-  if (g.epi == EPI_SWIGLU && g.out_by_slot &&
+  if ((g.epi == EPI_SWIGLU || g.epi == EPI_RELU2) && g.out_by_slot &&
       !tma::encode_2d_u8(&mh, g.out, (uint64_t)g.Nout * 2, (uint64_t)(g.grid_blocks * g.bm), (uint64_t)g.Nout * 2,
                          kTM * 2, kTN, false))
     return cudaErrorInvalidValue;
   if (g.epi == EPI_SWIGLU) return launch_ts<EPI_SWIGLU>(ta, mx, mw, mh, stream);
+  if (g.epi == EPI_RELU2) return launch_ts<EPI_RELU2>(ta, mx, mw, mh, stream);
   if (g.epi == EPI_WEIGHTED_F32) return launch_ts<EPI_WEIGHTED_F32>(ta, mx, mw, mh, stream);
   return launch_ts<EPI_PLAIN_BF16>(ta, mx, mw, mh, stream);
 }

@@ -48,7 +48,7 @@ class Workload:
     name: str
     T: int              # real tokens (for decode_bf16: the M of the run)
     K: int              # hidden size
-    I: int              # intermediate size (GEMM1 N = 2I, gate|up)
+    I: int              # intermediate size (GEMM1 N = 2I gate|up; relu2: N = I)
     E: int              # experts
     k: int              # top-k
     quant: str          # "mxfp4" (W4A16), "bf16", "mxfp8"
@@ -57,6 +57,12 @@ class Workload:
     bias: bool = False
     weight_std: float = 0.02    # bf16 / mxfp8 weights
     lengths: tuple = ()         # request lengths when T is a sum of requests
+    activation: str = "swiglu"  # "swiglu" or "relu2" (non-gated)
+
+    @property
+    def n1(self) -> int:
+        """Rows of GEMM1 per expert."""
+        return 2 * self.I if self.activation == "swiglu" else self.I
 
 
 TINY = Workload("tiny", T=64, K=256, I=512, E=8, k=2, quant="mxfp4", seed=0,
@@ -86,6 +92,12 @@ def prefill_workload(seed: int = 2) -> Workload:
 def decode_bf16_workload(M: int, seed: int = 3) -> Workload:
     return Workload(f"decode_bf16_M{M}", T=M, K=2688, I=928, E=128, k=6, quant="bf16",
                     seed=seed)
+
+
+def decode_bf16_relu2_workload(M: int, seed: int = 5) -> Workload:
+    """The Nemotron decode shape with its own activation: non-gated relu^2, GEMM1 N = 1856."""
+    return Workload(f"decode_bf16_relu2_M{M}", T=M, K=2688, I=1856, E=128, k=6, quant="bf16",
+                    seed=seed, activation="relu2")
 
 
 def scaled(w: Workload, **changes) -> Workload:
@@ -180,7 +192,8 @@ def make_layer(w: Workload, T: int | None = None, with_logits: bool = True):
 
     Keys: x (uint16 bf16 [T,K]) or x_codes/x_scale (mxfp8), logits (fp32 [T,E]),
     w1 / w1_scale / b1, w2 / w2_scale / b2 in the layouts of the C ABI:
-    w1 [E, 2I, K(/2)] rows 0..I-1 gate and I..2I-1 up; w2 [E, K, I(/2)].
+    w1 [E, 2I, K(/2)] rows 0..I-1 gate and I..2I-1 up (relu2: w1 [E, I, K(/2)]);
+    w2 [E, K, I(/2)].
     """
     T = w.T if T is None else T
     out = {"workload": w, "T": T}
@@ -193,21 +206,21 @@ def make_layer(w: Workload, T: int | None = None, with_logits: bool = True):
     if with_logits:
         out["logits"] = gen_logits(r_log, T, w.E)
     if w.quant == "mxfp4":
-        out["w1"], out["w1_scale"] = gen_mxfp4_weight(r_w1, w.E, 2 * w.I, w.K, w.scale_exp)
+        out["w1"], out["w1_scale"] = gen_mxfp4_weight(r_w1, w.E, w.n1, w.K, w.scale_exp)
         out["w2"], out["w2_scale"] = gen_mxfp4_weight(r_w2, w.E, w.K, w.I, w.scale_exp)
     elif w.quant == "bf16":
-        out["w1"] = gen_bf16_weight(r_w1, w.E, 2 * w.I, w.K, w.weight_std)
+        out["w1"] = gen_bf16_weight(r_w1, w.E, w.n1, w.K, w.weight_std)
         out["w2"] = gen_bf16_weight(r_w2, w.E, w.K, w.I, w.weight_std)
         out["w1_scale"] = out["w2_scale"] = None
     elif w.quant == "mxfp8":
-        v1 = r_w1.standard_normal((w.E, 2 * w.I, w.K), dtype=np.float32) * np.float32(w.weight_std)
+        v1 = r_w1.standard_normal((w.E, w.n1, w.K), dtype=np.float32) * np.float32(w.weight_std)
         out["w1"], out["w1_scale"] = mx_quantise_e4m3(v1)
         v2 = r_w2.standard_normal((w.E, w.K, w.I), dtype=np.float32) * np.float32(w.weight_std)
         out["w2"], out["w2_scale"] = mx_quantise_e4m3(v2)
     else:
         raise ValueError(w.quant)
     if w.bias:
-        out["b1"] = to_bf16_bits(r_b.standard_normal((w.E, 2 * w.I), dtype=np.float32) * np.float32(0.02))
+        out["b1"] = to_bf16_bits(r_b.standard_normal((w.E, w.n1), dtype=np.float32) * np.float32(0.02))
         out["b2"] = to_bf16_bits(r_b.standard_normal((w.E, w.K), dtype=np.float32) * np.float32(0.02))
     else:
         out["b1"] = out["b2"] = None

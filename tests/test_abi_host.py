@@ -93,6 +93,11 @@ def test_argument_errors_are_reported_without_a_launch(lib):
                         16, 16, 16, 16, None, 16, 256, 16, moe.Ctx(stream=0))
     assert ei.value.status == -2            # MXFP8 forward needs the quantiser
     with pytest.raises(moe.MoeError) as ei:
+        moe.moe_forward("mxfp4", 8, 256, 512, 16, 16, None, 16, 16, None, 16, None, 4, 4, 2,
+                        16, 16, 16, 16, None, 16, 256, 16, moe.Ctx(stream=0), activation=5)
+    assert ei.value.status == -1            # unknown activation
+    assert "activation" in lib.moe_last_error().decode()
+    with pytest.raises(moe.MoeError) as ei:
         moe.moe_wgrad(16, 16, 0, 4, 2, 8, 100, 64, 16, 16, 16, 16, 256, 16, 0, moe.Ctx(stream=0))
     assert ei.value.status == -2            # N not a multiple of 64
     with pytest.raises(moe.MoeError) as ei:
