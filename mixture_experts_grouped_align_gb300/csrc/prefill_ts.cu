@@ -22,8 +22,9 @@
 // once for both halves its L2 traffic per flop.  Per thread block (one per SM, 640 threads),
 // persistent over (alignment block, feature tile):
 //   warp 0      allocates the 512 TMEM columns (the two 128-column accumulators in 0..255,
-//               the decoded weight stages in 256..511) and, on one lane, issues the MMAs
-//               (M = 128, N = 128, K = 16, two per K step);
+//               the decoded weight stages in 256..511);
+//   warps 2-3   issue the MMAs, one lane each, warp 2 + m for weight matrix m (M = 128,
+//               N = 128, K = 16);
 //   warp 1      loads each 64-wide K stage of the token tile with TMA (one box of 128 slot
 //               rows when the rows are in slot order, else gathered four rows per
 //               instruction) and the raw E2M1 codes 128 bytes (four stages) per weight row;
@@ -46,10 +47,15 @@
 #include "moe_launch.h"
 #include "tcgen05.cuh"
 #include "tma.cuh"
+#include "ts_common.cuh"
 
 namespace {
 
 using namespace moe_launch;
+using ts::decode_block;
+using ts::mma_ts;
+using ts::tma_gather4;
+using ts::tmem_st16;
 
 constexpr int kThreads = 640;
 constexpr int kTM = 128;    // weight rows (features) per tile: MMA M
@@ -70,7 +76,7 @@ __host__ __device__ constexpr int stage_out_bytes(int epi) {
 constexpr int kTmemStages = 4;
 // epilogue warps 4-7 take token columns 0-63, warps 16-19 columns 64-127 (warp % 4 = TMEM
 // lane quarter); decoders are warps 8-15
-constexpr int kEpiWarp0 = 4, kEpiWarp1 = 16, kDecWarp0 = 8;
+constexpr int kMmaWarp0 = 2, kEpiWarp0 = 4, kEpiWarp1 = 16, kDecWarp0 = 8;
 constexpr int kEpiCols = kTN / 2;
 constexpr int kTmemCols = 512;
 constexpr int kAcol0 = 256;  // first TMEM column of the decoded weight stages
@@ -120,32 +126,6 @@ __device__ __forceinline__ int64_t next_tile(const TArgs& ta, int64_t t, int ntp
   return t;
 }
 
-// TMA gather of four 128-byte rows (rows y0..y3 of the tensor, bytes x..x+127) to dst.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y0,
-                                            int32_t y1, int32_t y2, int32_t y3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(tc::smem_addr(bar))
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] . B[smem]^T (kind::f16), issued by one thread.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t v, __half2 s) {
-  __half2 h = __hmul2(*reinterpret_cast<__half2*>(&v), s);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
 // TMEM column of stage s, matrix m, in the decoded-weight region.
 __device__ __forceinline__ uint32_t a_col(int s, int m) { return kAcol0 + s * 32 * kMats + 32 * m; }
 
@@ -157,43 +137,6 @@ __device__ __forceinline__ int64_t tile_feature(int mt, int m, int r) {
 template <bool SWIGLU>
 __device__ __forceinline__ int64_t tile_wrow(const GroupedGemm& a, int64_t e, int mt, int m, int r) {
   return e * a.Nw + (SWIGLU ? (int64_t)m * a.Nout : 0) + tile_feature<SWIGLU>(mt, m, r);
-}
-
-// f16x2 holding 2^(s-127) in both halves: NaN for 0xFF; the exponent clamped to the f16
-// range (a block whose nonzero codes need a scale outside 2^-23..2^13 is reported, and all-zero
-// codes stay zero under any finite scale).
-__device__ __forceinline__ __half2 scale_h2(uint32_t sb) {
-  if (sb == 255u) return __half2half2(__ushort_as_half((unsigned short)0x7e00u));
-  int se = (int)sb - 127;
-  se = se < -24 ? -24 : (se > 15 ? 15 : se);
-  const unsigned short bits = se >= -14 ? (unsigned short)((se + 15) << 10) : (unsigned short)(1u << (se + 24));
-  return __half2half2(__ushort_as_half(bits));
-}
-
-// 16 E2M1 codes of one 32-element block (16 bytes, low nibble first) -> 16 f16x2 words scaled.
-__device__ __forceinline__ void decode_block(const uint4 w, uint32_t sb, uint32_t* out, bool& bad) {
-  const int se = (int)sb - 127;
-  if ((w.x | w.y | w.z | w.w) && sb != 255u && (se < -23 || se > 13)) bad = true;
-  const __half2 s2 = scale_h2(sb);
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t o0, o1, o2, o3;
-    moe::e2m1x8_to_f16x2(ws[q], o0, o1, o2, o3);
-    out[4 * q + 0] = hmul2_u32(o0, s2);
-    out[4 * q + 1] = hmul2_u32(o1, s2);
-    out[4 * q + 2] = hmul2_u32(o2, s2);
-    out[4 * q + 3] = hmul2_u32(o3, s2);
-  }
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-      "%14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
 }
 
 template <int EPI>
@@ -224,21 +167,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < S1; ++s) {
       tc::mbar_init(&ld_full[s], 1);
-      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&empty[s], kMats);
     }
     for (int s = 0; s < S2; ++s) {
       tc::mbar_init(&a_full[s], 8);
-      tc::mbar_init(&a_empty[s], 1);
+      tc::mbar_init(&a_empty[s], kMats);
     }
     for (int s = 0; s < kRawSlots; ++s) {
       tc::mbar_init(&raw_full[s], 1);
       tc::mbar_init(&raw_empty[s], 8);
     }
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&tfull[i], 1);
+      tc::mbar_init(&tfull[i], kMats);
       tc::mbar_init(&tempty[i], 8);
     }
-    tc::mbar_init(drain, 1);
+    tc::mbar_init(drain, kMats);
     tc::mbar_init(epi_bar, 8);
     *abort_flag = 0;
     tc::mbar_fence_init();
@@ -417,8 +360,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 0) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kMats) {
+    // ------------------------------------------------------------------ MMA issuers
+    // one thread per weight matrix, in two warps on different SM sub-partitions: the waits,
+    // commits and issues of a stage cost the issuing thread about as long as the tensor core
+    // needs for the stage's MMAs, so one thread alone would pace the tensor core
+    const int m = warp - kMmaWarp0;
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_f16(kTM, kTN, 0);
       uint32_t it = 0, acc_it = 0;
@@ -445,12 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tc_fence_after();
           const uint32_t bs = smem_s + s * L.slot;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t bd = tc::sdesc_sw128(bs + kk * 32);
-#pragma unroll
-            for (int m = 0; m < kMats; ++m)
-              mma_ts(taddr + m * 128, taddr + a_col(s2, m) + kk * 8, bd, idesc, (kc | kk) != 0);
-          }
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_ts(taddr + m * 128, taddr + a_col(s2, m) + kk * 8, tc::sdesc_sw128(bs + kk * 32), idesc,
+                   (kc | kk) != 0);
           tc::mma_commit(&empty[s]);
           tc::mma_commit(&a_empty[s2]);
           ++it;

@@ -95,6 +95,22 @@ def test_padded_equals_unpadded_and_oracle(moe, T):
     assert_close_bf16(bf16_to_np(yp), oracle_y(lay, w, T), what=f"ragged T={T}")
 
 
+@pytest.mark.parametrize("T,E,k", [(256, 4, 2), (250, 2, 1), (200, 8, 8)])
+def test_few_experts_fill_whole_blocks_on_the_decode_path(moe, T, E, k):
+    """Up to 256 rows with few experts: alignment blocks of up to 128 pairs (eight token
+    groups, both accumulator halves) on the few-tokens kernels; padded = unpadded bit for
+    bit, and the oracle."""
+    w = synth.Workload("dense_blocks", T=T, K=320, I=256, E=E, k=k, quant="mxfp4", seed=17,
+                       scale_exp=(-6, -2), bias=True)
+    lay = synth.make_layer(w)
+    Lp = device_layer(moe, lay, w, T, pad=True)
+    Lu = device_layer(moe, lay, w, T, pad=False)
+    yp, _ = run(moe, Lp, lay, T)
+    yu, _ = run(moe, Lu, lay, T)
+    assert torch.equal(yp.view(torch.int16), yu.view(torch.int16))
+    assert_close_bf16(bf16_to_np(yp), oracle_y(lay, w, T), what=f"dense blocks T={T} E={E}")
+
+
 def test_prefill_full_size_padded_vs_unpadded_and_sampled_oracle(moe):
     w = synth.prefill_workload()
     lay = synth.make_layer(w)
@@ -222,7 +238,7 @@ def test_relu2_decode_bf16_nemotron_shape(moe, M):
     assert_close_bf16(bf16_to_np(y), oracle_y(lay, w, M), what=f"relu2 bf16 M={M}")
 
 
-@pytest.mark.parametrize("T,I", [(64, 512), (300, 320), (1001, 384)])
+@pytest.mark.parametrize("T,I", [(64, 512), (200, 320), (300, 320), (1001, 384)])
 def test_relu2_w4a16_padded_equals_unpadded_and_oracle(moe, T, I):
     """W4A16 relu^2 on both variants (64 rows: weight streaming; 300 and 1001: tensor
     memory with slot-ordered h), feature counts that leave a partial and an empty 128-feature

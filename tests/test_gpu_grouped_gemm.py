@@ -91,6 +91,23 @@ def test_w4a16_and_bf16_small(moe, T, quant):
     assert_close_bf16(bf16_to_np(out), ref, what=quant)
 
 
+def test_w4a16_weight_streaming_is_exact_for_any_scale(moe):
+    """bf16 activations up to 256 rows run the weight-streaming kernel, which multiplies each
+    32-block's f32 partial sum by its scale: a scale of 2^-30 on nonzero codes (outside what
+    an f16 weight can hold) still gives the oracle's result."""
+    rng = np.random.default_rng(23)
+    T, E, k, N, Kin = 64, 9, 2, 64, 256
+    ids = random_ids(rng, T, E, k)
+    a = synth.to_bf16_bits(rng.standard_normal((T, Kin)))
+    w, ws = synth.gen_mxfp4_weight(rng, E, N, Kin, (-5, 0))
+    ws[:, :, 1] = 127 - 30
+    w[:, :, 16:32] = 0x77
+    out = gemm_dev(moe, "mxfp4", E, N, Kin, dev(a), None, False, dev(w), dev(ws), None, ids)
+    Wd = lambda e: (ofmt.dequant("mxfp4", w[e], ws[e]), None)
+    ref = olayer.grouped_gemm(ofmt.bf16_decode(a), ids, Wd, False)
+    assert_close_bf16(bf16_to_np(out), ref, what="mxfp4 scale 2^-30")
+
+
 def test_mxfp8_constant_roundtrip(moe):
     """Constant codes and scales: every output is Kin * a * w * 2^(sa + sw) exactly."""
     T, E, k, N, Kin = 16, 4, 2, 32, 128
