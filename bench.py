@@ -399,8 +399,9 @@ def bench_ours(args, rank, world, local_rank):
     dominant = "gemm1" if g1 >= g2 else "gemm2"
     dom_bytes, dom_ms = (gemm1_bytes, g1) if dominant == "gemm1" else (gemm2_bytes, g2)
     tensor_path = rows > 256  # row counts above the bucket value 256 run the tcgen05 kernels
-    kernel_file = "prefill_gemm.cu" if tensor_path else "decode_gemm.cu"
-    kernel_name = ("prefill_gemm" if tensor_path else "decode_gemm") + f" ({dominant})"
+    # the W4A16 layer above 256 rows runs the kernel with the decoded weights in tensor memory
+    kernel_file = ("prefill_ts.cu" if w.quant == "mxfp4" else "prefill_gemm.cu") if tensor_path else "decode_gemm.cu"
+    kernel_name = kernel_file[:-3] + f" ({dominant})"
     key = f"{kernel_file}:{dominant}@{w.name}"
     tr = TRAFFIC.get(key)
     traffic = tr["bytes"] if tr and tr.get("src") == src_hash(kernel_file) else None

@@ -223,9 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(PArgs pa) {
       b_raw[i] = L.raw_b + r * kBrawRow + h * kBrawHalf;
     }
     // stages whose copies are in flight, oldest first
-    uint32_t pend_st[kLag];
-    uint32_t pend_sb[kLag][2], pend_sa[kLag];
-    bool pend_va[kLag];
+    uint32_t pend_st[kLag] = {};
+    uint32_t pend_sb[kLag][2] = {}, pend_sa[kLag] = {};
+    bool pend_va[kLag] = {};
     int npend = 0;
     uint32_t it = 0;
     auto finish_oldest = [&]() {  // decode + hand over pend[0], shift the queue
