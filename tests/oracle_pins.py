@@ -11,7 +11,7 @@ import numpy as np
 import torch
 
 import oracle
-from oracle import align, bucket, formats, layer, route, wgrad
+from oracle import align, bucket, formats, layer, per_token, route, wgrad
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -466,6 +466,87 @@ def check_wgrad_closed_forms(seed=9):
     assert np.allclose(wgrad.moe_wgrad(g1, xp, ids, E, True), want, rtol=1e-12, atol=1e-12)
 
 
+# ----------------------------------------------------------------------------- per-token FP8
+
+def _e4m3_codes(rng, shape):
+    """Random finite E4M3 codes (0x7F / 0xFF are NaN)."""
+    c = rng.integers(0, 256, size=shape, dtype=np.uint8)
+    return np.where((c & 0x7F) == 0x7F, c - 1, c).astype(np.uint8)
+
+
+def check_per_token_constant_closed_form():
+    """Constant codes (the page's constant-input round trip): every row is
+    K * a * w * a_scale[m] * w_scale[e] (+ bias[e, n]), with an empty expert in between."""
+    K, N = 64, 16
+    g = np.array([3, 0, 5, 2])
+    M = int(g.sum())
+    a = np.full((M, K), 0x38, np.uint8)            # E4M3 1.0
+    w = np.full((4, N, K), 0xB4, np.uint8)         # E4M3 -0.75
+    sa = np.linspace(0.5, 2.0, M)
+    sw = np.array([2.0, 3.0, 0.25, -1.0])
+    from synth import to_bf16_bits
+    b = to_bf16_bits(np.arange(4 * N, dtype=np.float64).reshape(4, N) * 0.125)
+    y = per_token.gemm_per_token(a, sa, w, sw, b, g)
+    exp_of = np.repeat(np.arange(4), g)
+    want = K * 1.0 * -0.75 * sa[:, None] * sw[exp_of][:, None] + formats.bf16_decode(b)[exp_of]
+    assert np.array_equal(y, want)
+    y0 = per_token.gemm_per_token(a, sa, w, sw, None, g)
+    assert np.array_equal(y0, np.broadcast_to(K * -0.75 * sa[:, None] * sw[exp_of][:, None], (M, N)))
+
+
+def check_per_token_brute(seed=13):
+    """Per-element Python loops on a ragged grouping: the row's expert comes from the
+    running sum of the group sizes."""
+    rng = np.random.default_rng(seed)
+    E, N, K = 4, 6, 32
+    g = np.array([2, 0, 3, 1])
+    M = int(g.sum())
+    a = _e4m3_codes(rng, (M, K))
+    w = _e4m3_codes(rng, (E, N, K))
+    sa = rng.uniform(0.1, 2.0, M)
+    sw = rng.uniform(0.1, 2.0, E)
+    from synth import to_bf16_bits
+    b = to_bf16_bits(rng.standard_normal((E, N)))
+    y = per_token.gemm_per_token(a, sa, w, sw, b, g)
+    A = formats.e4m3_decode(a)
+    W = formats.e4m3_decode(w)
+    B = formats.bf16_decode(b)
+    m = 0
+    for e in range(E):
+        for _ in range(int(g[e])):
+            for n in range(N):
+                dot = math.fsum(A[m, k] * W[e, n, k] for k in range(K))
+                want = dot * sa[m] * sw[e] + B[e, n]
+                assert abs(y[m, n] - want) <= 1e-12 * max(1.0, abs(want)), (m, n, y[m, n], want)
+            m += 1
+
+
+def check_per_token_scale_linearity(seed=14):
+    """Scaling one row's activation scale scales that row only; scaling an expert's weight
+    scale scales exactly that expert's rows (bias-free)."""
+    rng = np.random.default_rng(seed)
+    E, N, K = 3, 8, 32
+    g = np.array([4, 3, 5])
+    M = int(g.sum())
+    a = _e4m3_codes(rng, (M, K))
+    w = _e4m3_codes(rng, (E, N, K))
+    sa = rng.uniform(0.5, 1.5, M)
+    sw = rng.uniform(0.5, 1.5, E)
+    y = per_token.gemm_per_token(a, sa, w, sw, None, g)
+    sa2 = sa.copy()
+    sa2[5] *= 4.0
+    y2 = per_token.gemm_per_token(a, sa2, w, sw, None, g)
+    assert np.allclose(y2[5], 4.0 * y[5], rtol=1e-14)
+    assert np.array_equal(np.delete(y2, 5, 0), np.delete(y, 5, 0))
+    sw2 = sw.copy()
+    sw2[1] *= -2.0
+    y3 = per_token.gemm_per_token(a, sa, w, sw2, None, g)
+    rows1 = np.arange(4, 7)
+    assert np.allclose(y3[rows1], -2.0 * y[rows1], rtol=1e-14)
+    others = np.setdiff1d(np.arange(M), rows1)
+    assert np.array_equal(y3[others], y[others])
+
+
 ALL_CHECKS = [
     check_e2m1_table, check_e8m0_vs_torch, check_e4m3_vs_torch, check_bf16_vs_torch,
     check_mxfp4_dequant_layout, check_bucket_count_20000, check_pad_restriction,
@@ -473,5 +554,7 @@ ALL_CHECKS = [
     check_layer_dense_formulation, check_layer_single_expert_mlp,
     check_layer_constant_closed_form, check_layer_bias_only,
     check_layer_relu2_dense_formulation, check_layer_relu2_single_expert_loops,
-    check_layer_relu2_closed_form, check_layer_empty_expert_no_effect, check_grouped_gemm_brute, check_wgrad_closed_forms,
+    check_layer_relu2_closed_form, check_layer_empty_expert_no_effect, check_grouped_gemm_brute,
+    check_wgrad_closed_forms, check_per_token_constant_closed_form, check_per_token_brute,
+    check_per_token_scale_linearity,
 ]

@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 import oracle_pins as pins
-from oracle import align, bucket, formats, layer, route, wgrad
+from oracle import align, bucket, formats, layer, per_token, route, wgrad
 
 
 def _fails(checks):
@@ -204,12 +204,39 @@ def mut_wgrad_src_index(monkeypatch):
     return [pins.check_wgrad_closed_forms]
 
 
+def mut_per_token_offsets_inclusive(monkeypatch):
+    # expert e's first row taken as g_0 + ... + g_e (an inclusive running sum)
+    monkeypatch.setattr(per_token, "group_offsets",
+                        lambda g: np.concatenate([np.cumsum(np.asarray(g, dtype=np.int64)), [int(np.sum(g))]]))
+    return [pins.check_per_token_constant_closed_form, pins.check_per_token_brute]
+
+
+def mut_per_token_scale_of_next_row(monkeypatch):
+    orig = per_token.gemm_per_token
+
+    def f(a, sa, w, sw, b, g, rows=None):
+        return orig(a, np.roll(np.asarray(sa), 1), w, sw, b, g, rows)
+    monkeypatch.setattr(per_token, "gemm_per_token", f)
+    return [pins.check_per_token_constant_closed_form, pins.check_per_token_brute]
+
+
+def mut_per_token_weight_scale_dropped(monkeypatch):
+    orig = per_token.gemm_per_token
+
+    def f(a, sa, w, sw, b, g, rows=None):
+        return orig(a, sa, w, np.ones_like(np.asarray(sw, dtype=np.float64)), b, g, rows)
+    monkeypatch.setattr(per_token, "gemm_per_token", f)
+    return [pins.check_per_token_constant_closed_form, pins.check_per_token_brute]
+
+
 MUTATIONS = [mut_e8m0_zero, mut_nibble_order, mut_e2m1_subnormal, mut_e4m3_bias,
              mut_bucket_floor2, mut_bucket_16_per_octave, mut_route_tie_high,
              mut_route_full_softmax, mut_align_unstable, mut_align_sentinel_zero,
              mut_gate_up_swapped, mut_dropped_b1, mut_w2_transposed, mut_combine_unweighted,
              mut_silu_sign, mut_relu2_unsquared, mut_relu2_sign, mut_relu2_dropped_b1,
-             mut_relu2_runs_swiglu, mut_gemm_src_per_pair, mut_wgrad_transposed, mut_wgrad_src_index]
+             mut_relu2_runs_swiglu, mut_per_token_offsets_inclusive,
+             mut_per_token_scale_of_next_row, mut_per_token_weight_scale_dropped,
+             mut_gemm_src_per_pair, mut_wgrad_transposed, mut_wgrad_src_index]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS, ids=lambda f: f.__name__)
