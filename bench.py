@@ -45,7 +45,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_mxfp4",
-                    choices=["decode_mxfp4", "decode_bf16", "prefill_mxfp4", "tiny", "mxfp8_wgrad"])
+                    choices=["decode_mxfp4", "decode_bf16", "prefill_mxfp4", "tiny", "mxfp8_wgrad",
+                             "pertoken_fp8"])
     ap.add_argument("--m", type=int, default=28, help="tokens for decode_bf16")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the token count (smaller cases for profiling)")
@@ -60,9 +61,13 @@ def parse():
 
 
 DEFAULT_STEPS = {"decode_mxfp4": (2000, 50), "decode_bf16": (4000, 100),
-                 "prefill_mxfp4": (10, 3), "tiny": (4000, 100), "mxfp8_wgrad": (3, 3)}
+                 "prefill_mxfp4": (10, 3), "tiny": (4000, 100), "mxfp8_wgrad": (3, 3),
+                 "pertoken_fp8": (20, 3)}
 ORACLE_SAMPLE = {"decode_mxfp4": 8, "decode_bf16": 28, "prefill_mxfp4": 4, "tiny": 64,
-                 "mxfp8_wgrad": 512}
+                 "mxfp8_wgrad": 512, "pertoken_fp8": 8192}
+# The per-token FP8 grouped GEMM workload: the GEMM1 shape of the MXFP8 workload (256 experts,
+# K = 7168 -> N = 4096, T = 8192 tokens at top-8, Zipf(1.1) routing), rows grouped by expert.
+PERTOKEN = {"T": 8192, "E": 256, "N": 4096, "K": 7168, "k": 8, "seed": 9}
 
 
 def workload(name, m):
@@ -140,11 +145,30 @@ def oracle_sample_mxfp8(n_tok):
     return time.perf_counter() - t0, T / 8.0
 
 
+def oracle_sample_pertoken(n_rows):
+    """The oracle on a bounded sample of the per-token FP8 workload: n_rows rows of one
+    expert (freshly drawn E4M3 codes and scales of the same shapes).  Returns seconds and
+    the tokens the rows stand for (top-8: 8 rows per token)."""
+    import numpy as np
+    from oracle import per_token
+    c = PERTOKEN
+    rng = np.random.default_rng(c["seed"])
+    a = rng.integers(0, 126, size=(n_rows, c["K"]), dtype=np.uint8) | (rng.integers(0, 2, size=(n_rows, c["K"]), dtype=np.uint8) << 7)
+    w = rng.integers(0, 126, size=(1, c["N"], c["K"]), dtype=np.uint8) | (rng.integers(0, 2, size=(1, c["N"], c["K"]), dtype=np.uint8) << 7)
+    sa = rng.uniform(2.0 ** -10, 2.0 ** -8, n_rows)
+    sw = rng.uniform(2.0 ** -10, 2.0 ** -8, 1)
+    t0 = time.perf_counter()
+    per_token.gemm_per_token(a, sa, w, sw, None, np.array([n_rows]))
+    return time.perf_counter() - t0, n_rows / float(c["k"])
+
+
 def oracle_sample(name, m, n_tok):
     """Times the float64 oracle on the first n_tok tokens of the workload (this process
     was started with one BLAS / OpenMP thread).  Returns seconds."""
     if name == "mxfp8_wgrad":
         return oracle_sample_mxfp8(n_tok)
+    if name == "pertoken_fp8":
+        return oracle_sample_pertoken(n_tok)
     import synth
     from oracle import formats, layer, route
     w = workload(name, m)
@@ -604,6 +628,136 @@ def bench_mxfp8_wgrad(args, rank, world, local_rank):
     return line
 
 
+def bench_pertoken(args, rank, world, local_rank):
+    """One per-token FP8 grouped GEMM over group sizes: 256 experts, K = 7168 -> N = 4096,
+    65,536 rows (8192 tokens at top-8, Zipf(1.1) routing with cold experts), E4M3 operands
+    with one scale per row and one per expert."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_grouped_align_gb300 as moe
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    moe.build()
+    moe.load()
+    c = PERTOKEN
+    steps, warmup = DEFAULT_STEPS["pertoken_fp8"]
+    steps = args.steps if args.steps is not None else steps
+    warmup = max(3, args.warmup if args.warmup is not None else warmup)
+    T = args.tokens or c["T"]
+    E, N, K, k = (args.experts or c["E"]), c["N"], c["K"], c["k"]
+    rng = np.random.default_rng(c["seed"])
+    ids, _ = synth.zipf_topk_ids(rng, T, E, k, n_cold=min(16, E // 4))
+    gs = np.bincount(ids.reshape(-1), minlength=E).astype(np.int32)
+    M = int(gs.sum())
+    # per-token quantisation of N(0,1) activations and per-expert quantisation of N(0,0.02)
+    # weights to E4M3 (input preparation, outside the timed region)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(c["seed"])
+    x = torch.randn((M, K), device=dev, generator=gen)
+    a_scale = (x.abs().amax(dim=1) / 448.0).clamp_min(2.0 ** -30)
+    a = (x / a_scale[:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    del x
+    w = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
+    w_scale = torch.empty(E, dtype=torch.float32, device=dev)
+    for e0 in range(0, E, 16):
+        v = torch.randn((min(16, E - e0), N, K), device=dev, generator=gen) * 0.02
+        s = (v.abs().amax(dim=(1, 2)) / 448.0).clamp_min(2.0 ** -30)
+        w[e0:e0 + v.shape[0]] = (v / s[:, None, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+        w_scale[e0:e0 + v.shape[0]] = s
+        del v
+    a_scale = a_scale.float().contiguous()
+    gsd = torch.from_numpy(gs).to(dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        moe.moe_gemm_per_token(E, N, K, a, a_scale, w, w_scale, None, gsd, M, out,
+                               moe.Ctx(dev_status=status, events=evs))
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status[0]) != 0:
+        raise RuntimeError(f"device status {int(status[0])}")
+    evs = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(steps)]
+    for pair in evs:  # a torch event has a CUDA event only once it has been recorded
+        for e_ in pair:
+            e_.record(stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ck = clocks.stop(local_rank)
+    ms = t0.elapsed_time(t1)
+    kms = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    # end to end: activations, their scales and the group sizes from pinned host memory, the
+    # output back to the host; weights stay resident
+    ins = [a, a_scale, gsd]
+    host = [t.cpu().pin_memory() for t in ins]
+    oh = torch.empty_like(out, device="cpu").pin_memory()
+    e2e_steps = max(1, min(steps, 3))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for d_, h_ in zip(ins, host):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        oh.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if rank != 0:
+        return None
+    hbm, bf16, src = peaks()
+    fl = 2.0 * M * N * K
+    achieved = fl / (kms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "pertoken_gemm", "achieved": achieved, "peak": 2 * bf16,
+                "unit": "TFLOP/s", "frac": achieved / (2 * bf16), "traffic": None, "algorithmic_flops": fl,
+                "peak_source": f"{src} (bf16_tflops x 2, the nominal fp8/bf16 dense ratio)"}
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    return {
+        "metric": METRIC, "value": world * T * steps / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 tcgen05 mma -> f32, scales after the dot",
+        "data": "synthetic (per-token E4M3 quantisation of N(0,1) activations drawn on the device, "
+                "random-init weights)",
+        "config": {"workload": f"pertoken_fp8: T={T} tokens, top-{k}, {M} rows grouped by expert, "
+                               f"{E} experts, K={K} -> N={N}, Zipf(1.1) routing",
+                   "T": T, "rows": M, "experts": E, "N": N, "K": K, "top_k": k,
+                   "l2": f"inputs larger than L2: {E * N * K / 1e9:.1f} GB of E4M3 weights and "
+                         f"{M * K / 1e9:.2f} GB of activations per step",
+                   "parallelism": f"replicas x{world}"},
+        "useful_tflops": world * fl * steps / (ms * 1e-3) / 1e12,
+        "kernel_ms": {"gemm_per_token": kms},
+        "roofline": roofline,
+        "e2e": {"value": world * T * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out.numel() * 2, "steps": e2e_steps},
+        "gpu_launches": steps,
+        "clocks": ck,
+    }
+
+
 def launches_per_step(w, rows):
     n = 3  # GEMM1, GEMM2, combine
     n += 1  # align (routing fused for rows <= 512)
@@ -620,7 +774,10 @@ def cpu_baseline(args):
     name = args.workload
     n = args.sample_tokens or ORACLE_SAMPLE[name]
     r = run_oracle_subprocess(name, args.m, n)
-    if name == "mxfp8_wgrad":
+    if name == "pertoken_fp8":
+        what = (f"float64 oracle: {n} rows of one expert of the per-token FP8 GEMM "
+                f"({r['tokens']:g} tokens at top-8; {r['seconds']:.1f} s, one thread)")
+    elif name == "mxfp8_wgrad":
         what = (f"float64 oracle: both MXFP8 grouped GEMMs and both weight gradients for {n} "
                 f"token-expert pairs of 2 experts ({r['tokens']:g} tokens at top-8; "
                 f"{r['seconds']:.1f} s, one thread)")
@@ -650,6 +807,8 @@ def main():
         dist.init_process_group("nccl")
     if args.workload == "mxfp8_wgrad":
         line = bench_mxfp8_wgrad(args, rank, world, local_rank)
+    elif args.workload == "pertoken_fp8":
+        line = bench_pertoken(args, rank, world, local_rank)
     else:
         line = bench_ours(args, rank, world, local_rank)
     if rank == 0:
@@ -682,7 +841,8 @@ def bench_reference(args):
     line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1, "steps": steps,
             "warmup": warmup, "ms_per_step": secs / steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": describe(w, w.T), "impl": "reference",
+            "config": (describe(w, w.T) if args.workload not in ("mxfp8_wgrad", "pertoken_fp8")
+                       else {"workload": args.workload}), "impl": "reference",
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": f"{n} token(s) of the workload per step (float64 oracle, one "
                                        f"thread; input generation untimed; wall {wall:.1f} s)"},

@@ -249,6 +249,25 @@ moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin,
                             int64_t cap_tokens, void* out, const moe_ctx* ctx);
 
 /* ------------------------------------------------------------------------------------ *
+ * Per-token FP8 grouped GEMM over group sizes ([AITER] Summary: moe_gemm_per_token)      *
+ * ------------------------------------------------------------------------------------ */
+
+/* The rows of a are grouped by expert in expert order: expert e owns rows
+ * O_e .. O_e + group_sizes[e] - 1, O_e = group_sizes[0] + ... + group_sizes[e-1]. For each
+ * such row m:
+ *   out[m, n] = bf16 RNE( (sum_k a[m, k] * w[e, n, k]) * a_scale[m] * w_scale[e] + bias[e, n] )
+ * with the dot product of the E4M3 codes accumulated in fp32 before either scale.
+ * a: [M, K] E4M3 codes; a_scale: [M] fp32; w: [E, N, K] E4M3; w_scale: [E] fp32;
+ * bias: [E, N] bf16 or NULL; group_sizes: [E] int32 in device memory; out: [M, N] bf16.
+ * Rows past the sum of the group sizes are not written.  Negative sizes, or sizes adding up
+ * to more than M, set MOE_ERR_CAPACITY in ctx->dev_status (the sizes are read as clamped to
+ * the M rows).  Limits: 1 <= E <= 1024, N and K multiples of 128, M < 2^31,
+ * E * N < 2^31.  Needs no workspace. */
+moe_status moe_gemm_per_token(int32_t E, int32_t N, int32_t K, const uint8_t* a, const float* a_scale,
+                              const uint8_t* w, const float* w_scale, const void* bias,
+                              const int32_t* group_sizes, int64_t M, void* out, const moe_ctx* ctx);
+
+/* ------------------------------------------------------------------------------------ *
  * Weight gradient ([AITER] Summary: moe_wgrad; Tests & Benchmarks)                      *
  * ------------------------------------------------------------------------------------ */
 

@@ -323,6 +323,29 @@ moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin, 
   return st;
 }
 
+moe_status moe_gemm_per_token(int32_t E, int32_t N, int32_t K, const uint8_t* a, const float* a_scale,
+                              const uint8_t* w, const float* w_scale, const void* bias,
+                              const int32_t* group_sizes, int64_t M, void* out, const moe_ctx* ctx) {
+  MOE_REQUIRE(E >= 1 && E <= 1024 && M >= 0, MOE_ERR_INVALID_ARG, "need 1 <= E <= 1024 and M >= 0");
+  MOE_REQUIRE(N >= 128 && N % 128 == 0 && K >= 128 && K % 128 == 0, MOE_ERR_UNSUPPORTED,
+              "N and K must be positive multiples of 128");
+  MOE_REQUIRE(M < ((int64_t)1 << 31) && (int64_t)E * N < ((int64_t)1 << 31), MOE_ERR_UNSUPPORTED,
+              "M and E*N must be < 2^31");
+  MOE_REQUIRE(a && a_scale && w && w_scale && group_sizes && out, MOE_ERR_INVALID_ARG, "null tensor pointer");
+  MOE_REQUIRE(aligned16(a) && aligned16(a_scale) && aligned16(w) && aligned16(w_scale) && aligned16(bias) &&
+                  aligned16(group_sizes) && aligned16(out),
+              MOE_ERR_INVALID_ARG, "all pointers must be 16-byte aligned");
+  if (M == 0) return MOE_OK;
+  moe_launch::PerTokenGemm g{};
+  g.E = E; g.N = N; g.K = K; g.M = M;
+  g.a = a; g.a_scale = a_scale; g.w = w; g.w_scale = w_scale; g.bias = bias;
+  g.group_sizes = group_sizes; g.out = out; g.status = status_of(ctx);
+  rec(ctx, 0, 2);
+  moe_status st = cuda_status(moe_launch::pertoken_gemm(g, stream_of(ctx)), "moe_gemm_per_token");
+  rec(ctx, 1, 2);
+  return st;
+}
+
 moe_status moe_wgrad(const void* grad, const void* input, int32_t input_per_pair, int64_t T,
                      int32_t k, int32_t E, int32_t N, int32_t Kin, const int32_t* sorted_token_ids,
                      const int32_t* expert_ids, const int32_t* num_tokens_post_padded,

@@ -73,6 +73,22 @@ cudaError_t prefill_ts(const GroupedGemm& g, cudaStream_t stream);
 bool mx8_supported(const GroupedGemm& g);
 cudaError_t mx8_gemm(const GroupedGemm& g, cudaStream_t stream);
 
+// ---- per-token FP8 grouped GEMM over group sizes (pertoken_gemm.cu)
+struct PerTokenGemm {
+  int E, N, K;
+  int64_t M;                   // rows of a and out
+  const void* a;               // [M, K] E4M3, rows grouped by expert in expert order
+  const float* a_scale;        // [M]
+  const void* w;               // [E, N, K] E4M3
+  const float* w_scale;        // [E]
+  const void* bias;            // [E, N] bf16 or null
+  const int32_t* group_sizes;  // [E] rows per expert (device)
+  void* out;                   // [M, N] bf16
+  int32_t* status;
+};
+// N and K multiples of 128, 1 <= E <= 1024.
+cudaError_t pertoken_gemm(const PerTokenGemm& g, cudaStream_t stream);
+
 // Row counts above this bucket value use the tensor-memory path.  A bucket value (a
 // fixed point of the bucket map) keeps a batch and its bucket-padded copy on the same
 // side of the threshold, so both run the same kernel.

@@ -105,3 +105,9 @@ def test_argument_errors_are_reported_without_a_launch(lib):
                              256, 16, moe.Ctx(stream=0))
     assert ei.value.status == -1            # misaligned pointer
     assert "aligned" in lib.moe_last_error().decode()
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_gemm_per_token(8, 192, 256, 16, 16, 16, 16, None, 16, 100, 16, moe.Ctx(stream=0))
+    assert ei.value.status == -2            # N not a multiple of 128
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_gemm_per_token(8, 256, 256, 16, 16, 16, 16, None, None, 100, 16, moe.Ctx(stream=0))
+    assert ei.value.status == -1            # no group sizes
