@@ -7,6 +7,9 @@ The expert layer (per real token t and top-k slot j, e = id[t, j]):
     o_tj = h . W2[e]^T + b2[e]            W2[e]: [K, I]
     y_t  = sum_j w[t, j] * o_tj
 
+With MXFP8 weights the activations are MXFP8 too, and h is quantised to MXFP8 (mx_quant.py)
+before GEMM2.
+
 The non-gated variant ("tune the Nemotron MTP decode row on S5000 with a checked-in
 recipe", torchada PR 115, the table of added files: the Nemotron shape's activation is
 relu2_no_mul, with GEMM1 N = 1856) has one GEMM1 matrix and no gate-times-up product:
@@ -118,6 +121,35 @@ def moe_pairs(x, topk_ids, weights: ExpertWeights, tokens=None):
     return o
 
 
+def moe_pairs_mxfp8(x, topk_ids, weights: ExpertWeights, tokens=None):
+    """MXFP8 layer, unweighted pair outputs: as moe_pairs, with h brought to MXFP8 (E4M3
+    codes, one E8M0 scale per 32 features; mx_quant.mx_quantize) before GEMM2 -- GEMM2's
+    operands are MXFP8 on both sides.  ``x`` is the decoded activation (float64)."""
+    from . import mx_quant
+    ids = np.asarray(topk_ids)
+    T, k = ids.shape
+    K = x.shape[1]
+    tok = np.arange(T) if tokens is None else np.asarray(tokens)
+    o = np.zeros((T, k, K))
+    sub = ids[tok]
+    for e in np.unique(sub):
+        rr, jj = np.nonzero(sub == e)
+        t = tok[rr]
+        w1, b1 = weights.gemm1(e)
+        w2, b2 = weights.gemm2(e)
+        gu = x[t] @ w1.T
+        if b1 is not None:
+            gu = gu + b1
+        inter = w1.shape[0] // 2
+        h = silu(gu[:, :inter]) * gu[:, inter:]
+        hq, hs = mx_quant.mx_quantize(h)
+        r = formats.dequant_mxfp8(hq, hs) @ w2.T
+        if b2 is not None:
+            r = r + b2
+        o[t, jj] = r
+    return o
+
+
 def combine(o_pairs, topk_w, tokens=None):
     """y_t = sum_j w[t, j] * o[t, j] (float64)."""
     w = np.asarray(topk_w, dtype=np.float64)
@@ -126,8 +158,10 @@ def combine(o_pairs, topk_w, tokens=None):
 
 
 def moe_layer(x, topk_ids, topk_w, weights: ExpertWeights, tokens=None):
-    """The layer output y [T or len(tokens), K] in float64."""
-    return combine(moe_pairs(x, topk_ids, weights, tokens), topk_w, tokens)
+    """The layer output y [T or len(tokens), K] in float64 (MXFP8 weights: h quantised to
+    MXFP8 between the GEMMs)."""
+    pairs = moe_pairs_mxfp8 if weights.fmt == "mxfp8" else moe_pairs
+    return combine(pairs(x, topk_ids, weights, tokens), topk_w, tokens)
 
 
 def grouped_gemm(a, topk_ids, w_of_expert, per_pair: bool, pairs=None):

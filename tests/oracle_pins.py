@@ -11,7 +11,7 @@ import numpy as np
 import torch
 
 import oracle
-from oracle import align, bucket, formats, layer, per_token, route, wgrad
+from oracle import align, bucket, formats, layer, mx_quant, per_token, route, wgrad
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -547,6 +547,100 @@ def check_per_token_scale_linearity(seed=14):
     assert np.array_equal(y3[others], y[others])
 
 
+# ----------------------------------------------------------------------------- MX quantiser
+
+def check_e4m3_encode_vs_torch(seed=15):
+    """Round-to-nearest-even E4M3 codes of in-range float32 values, including every exact
+    midpoint between neighbouring codes, against torch's float8_e4m3fn conversion."""
+    rng = np.random.default_rng(seed)
+    mags = formats.e4m3_decode(np.arange(0x7F))
+    mids = (mags[:-1] + mags[1:]) / 2
+    v = np.concatenate([rng.uniform(-448, 448, 4000), rng.standard_normal(4000) * 2.0 ** rng.integers(-12, 6, 4000),
+                        mids, -mids, mags, -mags]).astype(np.float32)
+    want = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(mx_quant.e4m3_encode(v), want)
+
+
+def check_e4m3_encode_saturates_and_round_trips():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F])
+    assert np.array_equal(mx_quant.e4m3_encode(formats.e4m3_decode(codes)), codes.astype(np.uint8))
+    big = np.array([448.0, 460.0, 464.0, 1e6, np.inf, -500.0, -np.inf])
+    assert list(mx_quant.e4m3_encode(big)) == [0x7E] * 5 + [0xFE] * 2
+    assert mx_quant.e4m3_encode(np.array([np.nan]))[0] == 0x7F
+
+
+def check_mx_quantize_scale_rule(seed=16):
+    """The block exponent is the smallest e with amax < 2^(e + 9) (an integer search, not a
+    logarithm); fixed cases: amax 1 -> byte 119, 448 * 2^k -> 127 + k with the codes of 448,
+    an all-zero block -> byte 0 and zero codes, a NaN block -> 0xFF and 0x7F codes."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((64, 96)) * 2.0 ** rng.integers(-30, 30, (64, 1))
+    x[3, 32:64] = 0.0
+    codes, scales = mx_quant.mx_quantize(x)
+    amax = np.abs(x.reshape(64, 3, 32)).max(-1)
+    for r in range(64):
+        for b in range(3):
+            if amax[r, b] == 0:
+                assert scales[r, b] == 0 and not codes[r, 32 * b:32 * b + 32].any()
+                continue
+            e = -200
+            while not amax[r, b] < 2.0 ** (e + 9):
+                e += 1
+            assert scales[r, b] == e + 127, (r, b)
+    c1, s1 = mx_quant.mx_quantize(np.full((1, 32), 1.0))
+    assert s1[0, 0] == 119 and (c1 == 0x78).all()          # 1.0 / 2^-8 = 256 = E4M3 0x78
+    for k in (-5, 0, 7):
+        ck, sk = mx_quant.mx_quantize(np.full((1, 32), 448.0 * 2.0 ** k))
+        assert sk[0, 0] == 127 + k and (ck == 0x7E).all()
+    xn = np.ones((1, 64))
+    xn[0, 40] = np.nan
+    cn, sn = mx_quant.mx_quantize(xn)
+    assert sn[0, 1] == 0xFF and (cn[0, 32:] == 0x7F).all() and sn[0, 0] == 119
+
+
+def check_mx_quantize_error_bound(seed=17):
+    """Dequantised values are within half an E4M3 step (2^-4 relative) of the input for
+    every element at least 2^-6 of its block's maximum (E4M3 normals under the scale) and
+    at most 448 after scaling; above 448 (the block maximum can scale to 448..512) the
+    element saturates to the code of 448."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((32, 128)) * np.exp(rng.uniform(-3, 3, (32, 128)))
+    c, s = mx_quant.mx_quantize(x)
+    d = formats.dequant_mxfp8(c, s)
+    blk_max = np.repeat(np.abs(x.reshape(32, 4, 32)).max(-1), 32, axis=-1)
+    scaled = np.abs(x) / np.repeat(formats.e8m0_decode(s), 32, axis=-1)
+    sat = scaled > 448
+    m = (np.abs(x) >= blk_max * 2.0 ** -6) & ~sat
+    assert sat.any() and m.sum() > 0.5 * x.size
+    assert np.all(np.abs(d - x)[m] <= np.abs(x)[m] * 2.0 ** -4 * (1 + 1e-12))
+    assert np.all((c[sat] & 0x7F) == 0x7E)
+
+
+def check_layer_mxfp8_constant_closed_form():
+    """Constant E4M3 codes and scales: h = silu(g) * g is the same for every feature, so its
+    block maximum is itself and it quantises to the code nearest h / 2^e; the output follows
+    in closed form from that code."""
+    T, K, I, E = 3, 64, 64, 2
+    x = np.full((T, K), 0x38, np.uint8)                 # 1.0
+    xs = np.full((T, K // 32), 127 - 4, np.uint8)        # x = 2^-4
+    w1 = np.full((E, 2 * I, K), 0x30, np.uint8)         # 0.5
+    w1s = np.full((E, 2 * I, K // 32), 127 - 2, np.uint8)
+    w2 = np.full((E, K, I), 0xB8, np.uint8)             # -1.0
+    w2s = np.full((E, K, I // 32), 127 - 3, np.uint8)
+    W = layer.ExpertWeights("mxfp8", w1, w1s, None, w2, w2s, None)
+    ids = np.array([[0, 1], [1, 0], [0, 1]], dtype=np.int32)
+    wt = np.array([[0.75, 0.25], [0.5, 0.5], [1.0, 0.0]], dtype=np.float32)
+    y = layer.moe_layer(formats.dequant_mxfp8(x, xs), ids, wt, W)
+    g = K * 2.0 ** -4 * 0.5 * 2.0 ** -2                   # 0.5
+    h = g / (1.0 + math.exp(-g)) * g
+    e = math.frexp(h)[1] - 1 - 8
+    hq = formats.e4m3_decode(mx_quant.e4m3_encode(np.array([h * 2.0 ** -e])))[0] * 2.0 ** e
+    assert hq != h                                     # the quantisation step is visible
+    o = I * hq * -1.0 * 2.0 ** -3
+    for t in range(T):
+        assert np.allclose(y[t], float(wt[t].astype(np.float64).sum()) * o, rtol=1e-14, atol=0)
+
+
 ALL_CHECKS = [
     check_e2m1_table, check_e8m0_vs_torch, check_e4m3_vs_torch, check_bf16_vs_torch,
     check_mxfp4_dequant_layout, check_bucket_count_20000, check_pad_restriction,
@@ -556,5 +650,7 @@ ALL_CHECKS = [
     check_layer_relu2_dense_formulation, check_layer_relu2_single_expert_loops,
     check_layer_relu2_closed_form, check_layer_empty_expert_no_effect, check_grouped_gemm_brute,
     check_wgrad_closed_forms, check_per_token_constant_closed_form, check_per_token_brute,
-    check_per_token_scale_linearity,
+    check_per_token_scale_linearity, check_e4m3_encode_vs_torch,
+    check_e4m3_encode_saturates_and_round_trips, check_mx_quantize_scale_rule,
+    check_mx_quantize_error_bound, check_layer_mxfp8_constant_closed_form,
 ]

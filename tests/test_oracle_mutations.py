@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 import oracle_pins as pins
-from oracle import align, bucket, formats, layer, per_token, route, wgrad
+from oracle import align, bucket, formats, layer, mx_quant, per_token, route, wgrad
 
 
 def _fails(checks):
@@ -229,6 +229,43 @@ def mut_per_token_weight_scale_dropped(monkeypatch):
     return [pins.check_per_token_constant_closed_form, pins.check_per_token_brute]
 
 
+def mut_mx_scale_ceil(monkeypatch):
+    orig = mx_quant.block_exponent
+    monkeypatch.setattr(mx_quant, "block_exponent", lambda amax: orig(amax) + 1)
+    return [pins.check_mx_quantize_scale_rule]
+
+
+def mut_mx_emax_7(monkeypatch):
+    monkeypatch.setattr(mx_quant, "E4M3_EMAX", 7)
+    return [pins.check_mx_quantize_scale_rule]
+
+
+def mut_e4m3_ties_away(monkeypatch):
+    mags = formats.e4m3_decode(np.arange(0x7F))
+
+    def enc(v):
+        v = np.asarray(v, dtype=np.float64)
+        a = np.abs(v)
+        code = np.abs(a[..., None] - mags).argmin(-1)       # first minimum: ties go down
+        code = np.where(a >= 448, 0x7E, code) | np.where(np.signbit(v), 0x80, 0)
+        return np.where(np.isnan(v), 0x7F, code).astype(np.uint8)
+    monkeypatch.setattr(mx_quant, "e4m3_encode", enc)
+    return [pins.check_e4m3_encode_vs_torch]
+
+
+def mut_e4m3_no_saturation(monkeypatch):
+    orig = mx_quant.e4m3_encode
+    monkeypatch.setattr(mx_quant, "e4m3_encode",
+                        lambda v: np.where(np.abs(np.asarray(v, dtype=np.float64)) > 464, 0x7F, orig(v)).astype(np.uint8))
+    return [pins.check_e4m3_encode_saturates_and_round_trips]
+
+
+def mut_mxfp8_layer_skips_quantiser(monkeypatch):
+    monkeypatch.setattr(mx_quant, "mx_quantize",
+                        lambda x: (np.zeros(np.shape(x), np.uint8), np.zeros(np.shape(x)[:-1] + (np.shape(x)[-1] // 32,), np.uint8)))
+    return [pins.check_layer_mxfp8_constant_closed_form]
+
+
 MUTATIONS = [mut_e8m0_zero, mut_nibble_order, mut_e2m1_subnormal, mut_e4m3_bias,
              mut_bucket_floor2, mut_bucket_16_per_octave, mut_route_tie_high,
              mut_route_full_softmax, mut_align_unstable, mut_align_sentinel_zero,
@@ -236,6 +273,8 @@ MUTATIONS = [mut_e8m0_zero, mut_nibble_order, mut_e2m1_subnormal, mut_e4m3_bias,
              mut_silu_sign, mut_relu2_unsquared, mut_relu2_sign, mut_relu2_dropped_b1,
              mut_relu2_runs_swiglu, mut_per_token_offsets_inclusive,
              mut_per_token_scale_of_next_row, mut_per_token_weight_scale_dropped,
+             mut_mx_scale_ceil, mut_mx_emax_7, mut_e4m3_ties_away, mut_e4m3_no_saturation,
+             mut_mxfp8_layer_skips_quantiser,
              mut_gemm_src_per_pair, mut_wgrad_transposed, mut_wgrad_src_index]
 
 
