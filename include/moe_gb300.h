@@ -187,8 +187,11 @@ size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t 
  * x: [T_rows, K] bf16 (BF16 and MXFP4_W4A16 modes).  topk_w [T_rows, k]; the alignment
  * arrays come from moe_align over T_rows rows with the same block_m and cap_tokens.
  * y: [T_real, K] bf16.  K and I must be multiples of 32 (and of 16 output rows).
- * MXFP8 needs a quantiser between the GEMMs and returns MOE_ERR_UNSUPPORTED here; its
- * GEMMs are available through moe_grouped_gemm.  No pair-count-dependent split of K is
+ * MXFP8 (SwiGLU only): x is E4M3 codes [T_rows, K] with x_scale [T_rows, K/32] E8M0, the
+ * weights E4M3 with E8M0 scales; h is computed in fp32 and quantised to MXFP8 by the rule of
+ * moe_mx_quantize before GEMM2, whose operands are then MXFP8 on both sides.  Below the
+ * tensor-memory threshold (or for shapes the block-scaled kernel does not take: I or K not
+ * a multiple of 128) this mode needs I <= K.  No pair-count-dependent split of K is
  * made and every output row depends only on its own input row, so padded and unpadded
  * calls give bit-identical real rows. */
 moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_scale,
@@ -247,6 +250,21 @@ moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin,
                             const int32_t* sorted_token_ids, const int32_t* expert_ids,
                             const int32_t* num_tokens_post_padded, int32_t block_m,
                             int64_t cap_tokens, void* out, const moe_ctx* ctx);
+
+/* ------------------------------------------------------------------------------------ *
+ * MXFP8 quantisation (the step between the GEMMs of an MXFP8 layer)                      *
+ * ------------------------------------------------------------------------------------ */
+
+/* x [rows, cols] fp32 (cols a multiple of 32) -> codes [rows, cols] E4M3 and scales
+ * [rows, cols / 32] E8M0, per 32 consecutive values of a row, by the OCP microscaling rule
+ * for E4M3 elements: e = floor(log2(max |v|)) - 8 clamped to [-127, 127] (-127 for an
+ * all-zero block), scale byte e + 127, code = E4M3(v / 2^e) rounded to nearest even and
+ * saturated at 448, signs (zero included) kept.  A block holding a NaN gets scale 0xFF and
+ * codes 0x7F.  [AITER] Summary gives the GEMM operands this format (moe_gemm_mxfp8); the
+ * rule itself is the reading this library takes where the pages stop.  moe_forward applies
+ * it to h in MXFP8 mode. */
+moe_status moe_mx_quantize(const float* x, int64_t rows, int32_t cols, uint8_t* codes, uint8_t* scales,
+                           const moe_ctx* ctx);
 
 /* ------------------------------------------------------------------------------------ *
  * Per-token FP8 grouped GEMM over group sizes ([AITER] Summary: moe_gemm_per_token)      *

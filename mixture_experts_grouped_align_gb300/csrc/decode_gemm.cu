@@ -553,7 +553,9 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
               up += moe::bf16_bits_to_f32(bias[e * a.Nw + a.Nout + n]);
             }
             const float hval = moe::silu(gt) * up;
-            if (MX) {  // f16 for the f16 MMA of GEMM2; an overflow is reported
+            if (ACT_E4M3) {  // MXFP8 layer: fp32, quantised to MXFP8 before GEMM2
+              static_cast<float*>(a.out)[(int64_t)p * a.Nout + n] = hval;
+            } else if (MX) {  // f16 for the f16 MMA of GEMM2; an overflow is reported
               const __half hv = __float2half_rn(hval);
               if (__hisinf(hv)) bad = true;  // an overflow (NaN only comes from NaN inputs)
               static_cast<__half*>(a.out)[(int64_t)p * a.Nout + n] = hv;
@@ -564,7 +566,9 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
             float av = v[0][i];
             if (bias) av += moe::bf16_bits_to_f32(bias[e * a.Nw + n]);
             const float hval = moe::relu2(av);
-            if (MX) {
+            if (ACT_E4M3) {
+              static_cast<float*>(a.out)[(int64_t)p * a.Nout + n] = hval;
+            } else if (MX) {
               const __half hv = __float2half_rn(hval);
               if (__hisinf(hv)) bad = true;
               static_cast<__half*>(a.out)[(int64_t)p * a.Nout + n] = hv;
@@ -638,6 +642,7 @@ cudaError_t decode_gemm(const GroupedGemm& g, cudaStream_t stream) {
   MOE_CASE(WF_BF16, EPI_PLAIN_BF16)
   MOE_CASE(WF_BF16, EPI_RELU2)
   MOE_CASE(WF_MXFP8, EPI_SWIGLU)
+  MOE_CASE(WF_MXFP8, EPI_RELU2)
   MOE_CASE(WF_MXFP8, EPI_WEIGHTED_F32)
   MOE_CASE(WF_MXFP8, EPI_PLAIN_BF16)
 #undef MOE_CASE

@@ -8,6 +8,7 @@
 // below only produces the real rows.
 #include "moe_common.cuh"
 #include "moe_launch.h"
+#include "mx_quant.cuh"
 
 namespace {
 
@@ -106,6 +107,27 @@ __global__ void gather_rows_f16_kernel(const uint4* __restrict__ x, const int32_
   if (bad) moe::set_status(status, MOE_ERR_RANGE);
 }
 
+// One thread per 32-element block of a row: 128 bytes in, 32 codes and a scale byte out.
+__global__ void mx_quantize_kernel(const float4* __restrict__ x, int64_t nblocks, uint4* __restrict__ codes,
+                                   uint8_t* __restrict__ scales) {
+  for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < nblocks; b += (int64_t)gridDim.x * blockDim.x) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 f = x[b * 8 + i];
+      v[4 * i] = f.x;
+      v[4 * i + 1] = f.y;
+      v[4 * i + 2] = f.z;
+      v[4 * i + 3] = f.w;
+    }
+    uint32_t c[8], s;
+    mxq::quant32(v, c, s);
+    codes[b * 2] = make_uint4(c[0], c[1], c[2], c[3]);
+    codes[b * 2 + 1] = make_uint4(c[4], c[5], c[6], c[7]);
+    scales[b] = (uint8_t)s;
+  }
+}
+
 }  // namespace
 
 namespace moe_launch {
@@ -116,6 +138,14 @@ cudaError_t gather_rows_f16(const void* x, const int32_t* sorted, const int32_t*
   if (n8 == 0) return cudaSuccess;
   gather_rows_f16_kernel<<<grid_for(n8, 256), 256, 0, stream>>>((const uint4*)x, sorted, ntpp, P, k, per, n8,
                                                                  (uint4*)y, status);
+  return cudaGetLastError();
+}
+
+cudaError_t mx_quantize(const float* x, int64_t rows, int cols, uint8_t* codes, uint8_t* scales,
+                        cudaStream_t stream) {
+  const int64_t nblocks = rows * (cols / 32);
+  if (nblocks == 0) return cudaSuccess;
+  mx_quantize_kernel<<<grid_for(nblocks, 256), 256, 0, stream>>>((const float4*)x, nblocks, (uint4*)codes, scales);
   return cudaGetLastError();
 }
 

@@ -185,16 +185,81 @@ size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t 
   return round256((size_t)rows_h * I * 2) + round256((size_t)P * K * 4) + round256((size_t)rows_x * K * 2);
 }
 
+// The MXFP8 layer: GEMM1 + SwiGLU, h quantised to MXFP8 (E4M3 codes and one E8M0 scale per
+// 32 features), GEMM2 on MXFP8 operands, combine.  Above the threshold the block-scaled kernel
+// quantises h in its epilogue; otherwise the weight-streaming kernels run and h goes through
+// fp32 in the o scratch (which needs I <= K) and the standalone quantiser.  The workspace
+// regions are those of the other modes: h codes and scales in the h region, o as before.
+static moe_status forward_mxfp8(const moe_weights* W, const void* x, const uint8_t* x_scale, int64_t T_rows,
+                                int64_t T_real, int32_t k, const float* topk_w, const int32_t* sorted_token_ids,
+                                const int32_t* expert_ids, const int32_t* num_tokens_post_padded,
+                                int32_t block_m, int64_t cap_tokens, void* y, const moe_ctx* ctx) {
+  const int32_t E = W->E, K = W->K, I = W->I;
+  MOE_REQUIRE(W->activation == MOE_ACT_SWIGLU, MOE_ERR_UNSUPPORTED, "the MXFP8 layer takes SwiGLU");
+  MOE_REQUIRE(x_scale && W->w1_scale && W->w2_scale, MOE_ERR_INVALID_ARG, "MXFP8 needs x_scale and weight scales");
+  MOE_REQUIRE(aligned16(x_scale), MOE_ERR_INVALID_ARG, "all pointers must be 16-byte aligned");
+  const int64_t P = T_rows * k;
+  int64_t rows_h, rows_x;
+  forward_scratch_rows(T_rows, k, cap_tokens, &rows_h, &rows_x);
+  uint8_t* ws = static_cast<uint8_t*>(ctx->workspace);
+  uint8_t* hq = ws;                                   // [P, I] E4M3 codes of h
+  uint8_t* hs = ws + (size_t)P * I;                   // [P, I / 32] E8M0 scales of h
+  float* o = reinterpret_cast<float*>(ws + round256((size_t)rows_h * I * 2));
+  cudaStream_t s = stream_of(ctx);
+  const int64_t blocks = used_blocks_bound(P, E, block_m, cap_tokens);
+
+  moe_launch::GroupedGemm g1{};
+  g1.wfmt = moe_launch::WF_MXFP8;
+  g1.epi = moe_launch::EPI_SWIGLU;
+  g1.w = W->w1; g1.w_scale = W->w1_scale; g1.bias = W->b1;
+  g1.act = x; g1.act_fmt = moe_launch::ACT_BF16; g1.act_scale = x_scale; g1.act_per_pair = 0;
+  g1.Nw = 2 * (int64_t)I; g1.Kin = K; g1.Nout = I; g1.k = k; g1.P = P; g1.E = E;
+  g1.sorted = sorted_token_ids; g1.expert_ids = expert_ids; g1.ntpp = num_tokens_post_padded;
+  g1.bm = block_m; g1.grid_blocks = blocks; g1.topk_w = topk_w; g1.out = hq; g1.out_scale = hs;
+  g1.status = status_of(ctx);
+  moe_launch::GroupedGemm g2 = g1;
+  g2.epi = moe_launch::EPI_WEIGHTED_F32;
+  g2.w = W->w2; g2.w_scale = W->w2_scale; g2.bias = W->b2;
+  g2.act = hq; g2.act_scale = hs; g2.act_per_pair = 1;
+  g2.Nw = K; g2.Kin = I; g2.Nout = K; g2.out = o; g2.out_scale = nullptr;
+  const bool tc1 = T_rows > moe_launch::kPrefillRowsAbove && moe_launch::mx8_supported(g1);
+  const bool tc2 = T_rows > moe_launch::kPrefillRowsAbove && moe_launch::mx8_supported(g2);
+  if (!tc1) {
+    MOE_REQUIRE(I <= K, MOE_ERR_UNSUPPORTED, "the MXFP8 weight-streaming path keeps fp32 h in the o scratch: needs I <= K");
+    MOE_REQUIRE(moe_launch::decode_gemm_smem_bytes(g1) <= 227 * 1024, MOE_ERR_UNSUPPORTED, "K too large for the decode path");
+  }
+  if (!tc2)
+    MOE_REQUIRE(moe_launch::decode_gemm_smem_bytes(g2) <= 227 * 1024, MOE_ERR_UNSUPPORTED, "I too large for the decode path");
+  rec(ctx, 0, 4);
+  moe_status st;
+  if (tc1) {
+    st = cuda_status(moe_launch::mx8_gemm(g1, s), "moe_forward GEMM1");
+  } else {
+    moe_launch::GroupedGemm gf = g1;
+    gf.out = o;  // fp32 h, quantised next
+    gf.out_scale = nullptr;
+    st = cuda_status(moe_launch::decode_gemm(gf, s), "moe_forward GEMM1");
+    if (st == MOE_OK) st = cuda_status(moe_launch::mx_quantize(o, P, I, hq, hs, s), "moe_forward quantise h");
+  }
+  if (st != MOE_OK) return st;
+  rec(ctx, 1, 4);
+  st = cuda_status(tc2 ? moe_launch::mx8_gemm(g2, s) : moe_launch::decode_gemm(g2, s), "moe_forward GEMM2");
+  if (st != MOE_OK) return st;
+  rec(ctx, 2, 4);
+  st = cuda_status(moe_launch::combine(o, T_real, k, K, y, s), "moe_forward combine");
+  rec(ctx, 3, 4);
+  return st;
+}
+
 moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_scale, int64_t T_rows,
                        int64_t T_real, int32_t k, const float* topk_w,
                        const int32_t* sorted_token_ids, const int32_t* expert_ids,
                        const int32_t* num_tokens_post_padded, const int32_t* expert_offsets,
                        int32_t block_m, int64_t cap_tokens, void* y, const moe_ctx* ctx) {
   (void)expert_offsets;
-  (void)x_scale;
   MOE_REQUIRE(W && ctx, MOE_ERR_INVALID_ARG, "null weights or context");
-  MOE_REQUIRE(W->quant == MOE_Q_BF16 || W->quant == MOE_Q_MXFP4_W4A16, MOE_ERR_UNSUPPORTED,
-              "moe_forward supports MOE_Q_BF16 and MOE_Q_MXFP4_W4A16 (MXFP8: moe_grouped_gemm)");
+  MOE_REQUIRE(W->quant == MOE_Q_BF16 || W->quant == MOE_Q_MXFP4_W4A16 || W->quant == MOE_Q_MXFP8,
+              MOE_ERR_INVALID_ARG, "unknown quant mode");
   const int32_t E = W->E, K = W->K, I = W->I;
   MOE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= E, MOE_ERR_INVALID_ARG, "bad E or k");
   MOE_REQUIRE(W->activation == MOE_ACT_SWIGLU || W->activation == MOE_ACT_RELU2, MOE_ERR_INVALID_ARG,
@@ -220,6 +285,9 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
   MOE_REQUIRE(ctx->workspace && ctx->workspace_bytes >= need && aligned16(ctx->workspace),
               MOE_ERR_CAPACITY, "workspace of %zu bytes needed", need);
   if (T_rows == 0) return MOE_OK;
+  if (W->quant == MOE_Q_MXFP8)
+    return forward_mxfp8(W, x, x_scale, T_rows, T_real, k, topk_w, sorted_token_ids, expert_ids,
+                         num_tokens_post_padded, block_m, cap_tokens, y, ctx);
 
   int64_t rows_h, rows_x;
   forward_scratch_rows(T_rows, k, cap_tokens, &rows_h, &rows_x);
@@ -321,6 +389,16 @@ moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin, 
   st = cuda_status(moe_launch::grouped_gemm(g, T, stream_of(ctx)), "moe_grouped_gemm");
   rec(ctx, 1, 2);
   return st;
+}
+
+moe_status moe_mx_quantize(const float* x, int64_t rows, int32_t cols, uint8_t* codes, uint8_t* scales,
+                           const moe_ctx* ctx) {
+  MOE_REQUIRE(rows >= 0 && cols >= 32 && cols % 32 == 0, MOE_ERR_INVALID_ARG,
+              "need rows >= 0 and cols a positive multiple of 32");
+  MOE_REQUIRE(x && codes && scales, MOE_ERR_INVALID_ARG, "null tensor pointer");
+  MOE_REQUIRE(aligned16(x) && aligned16(codes) && aligned16(scales), MOE_ERR_INVALID_ARG,
+              "all pointers must be 16-byte aligned");
+  return cuda_status(moe_launch::mx_quantize(x, rows, cols, codes, scales, stream_of(ctx)), "moe_mx_quantize");
 }
 
 moe_status moe_gemm_per_token(int32_t E, int32_t N, int32_t K, const uint8_t* a, const float* a_scale,

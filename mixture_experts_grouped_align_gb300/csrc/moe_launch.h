@@ -18,6 +18,10 @@ cudaError_t pad_rows(const void* src, void* dst, int64_t rows, int64_t rows_pad,
 cudaError_t zero_f32(float* p, int64_t n, cudaStream_t stream);
 cudaError_t combine(const float* o, int64_t T_real, int k, int K, void* y, cudaStream_t stream);
 cudaError_t bf16_to_f16(const void* x, void* y, int64_t n, int32_t* status, cudaStream_t stream);
+// MXFP8 quantisation of fp32 rows ([rows, cols], cols % 32 == 0) -> E4M3 codes [rows, cols]
+// and E8M0 scales [rows, cols / 32] (mx_quant.cuh).
+cudaError_t mx_quantize(const float* x, int64_t rows, int cols, uint8_t* codes, uint8_t* scales,
+                        cudaStream_t stream);
 // Token rows of bf16 x gathered into alignment-slot order as f16 ([slots, K]).
 cudaError_t gather_rows_f16(const void* x, const int32_t* sorted, const int32_t* ntpp, int64_t P, int k,
                             int64_t K, int64_t slots, void* y, int32_t* status, cudaStream_t stream);
@@ -53,7 +57,10 @@ struct GroupedGemm {
   int bm;
   int64_t grid_blocks;      // block slots to launch for
   const float* topk_w;      // [P] (EPI_WEIGHTED_F32)
-  void* out;                // [P, Nout]: f16 / bf16 (SWIGLU, RELU2), bf16 (PLAIN) or f32 (WEIGHTED)
+  void* out;                // [P, Nout]: f16 / bf16 (SWIGLU, RELU2), bf16 (PLAIN) or f32 (WEIGHTED);
+                            // MXFP8 weights: f32 h (SWIGLU, RELU2), or E4M3 codes of h when
+                            // out_scale is set (SWIGLU on the block-scaled kernel)
+  uint8_t* out_scale;       // [P, Nout / 32] E8M0 scales of an MXFP8 h, or null
   int32_t* status;
 };
 size_t decode_gemm_smem_bytes(const GroupedGemm& g);

@@ -18,8 +18,12 @@
 //               and the stage's scale words with cp.async; two stages later they write the
 //               scale words into TMEM (warps 8-11 the activation scales, 12-15 the weight
 //               scales) and hand the stage to the MMA;
-//   warps 4-7   drain the accumulator (one TMEM lane = one tile row), add the bias and
-//               store bf16 rows at their pair index.
+//   warps 4-7   drain the accumulator (one TMEM lane = one tile row) and run the epilogue
+//               at the row's pair index: bias -> bf16; bias * routing weight -> f32; or, for
+//               GEMM1 of an MXFP8 layer, bias + SwiGLU and the MXFP8 quantisation of h
+//               (mx_quant.cuh: 32 features per E8M0 scale, all in the thread's registers).
+// SwiGLU tiles hold 128 features: weight rows 0..127 of the B tile are their gate rows and
+// 128..255 their up rows (two TMA boxes), so gate and up of a feature share a TMEM lane.
 // Tiles past num_tokens_post_padded or of the -1 sentinel are skipped by every role before
 // anything is read (second review of the same page).  Expert offsets are 64-bit (Notes).
 // Every mbarrier wait is bounded; one that runs out sets MOE_ERR_TIMEOUT, every role leaves
@@ -32,6 +36,7 @@
 // lane of every 32-lane quarter).
 #include "moe_common.cuh"
 #include "moe_launch.h"
+#include "mx_quant.cuh"
 #include "tcgen05.cuh"
 #include "tma.cuh"
 
@@ -100,6 +105,15 @@ __device__ __forceinline__ int64_t act_row(const GroupedGemm& a, int p) {
   return a.act_per_pair ? (int64_t)p : (int64_t)(p / a.k);
 }
 
+// Weight row of B-tile row n in N tile nt (SwiGLU: gate rows, then up rows of 128 features).
+template <int EPI>
+__device__ __forceinline__ int64_t b_row(const GroupedGemm& a, int64_t e, int nt, int BN, int n) {
+  if (EPI == EPI_SWIGLU)
+    return e * a.Nw + (n < 128 ? (int64_t)nt * 128 + n : (int64_t)a.Nout + (int64_t)nt * 128 + (n - 128));
+  return e * a.Nw + (int64_t)nt * BN + n;
+}
+
+template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, MArgs ma) {
   const GroupedGemm& a = ma.g;
   extern __shared__ uint8_t smem_raw[];
@@ -176,13 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
         const int p = a.sorted[blk * a.bm + r0 + 32 * i];
         aptr[i] = p < a.P ? abase + act_row(a, p) * Kin + c16 * 16 : nullptr;
       }
-      const int64_t brow0 = e * a.Nw + (int64_t)nt * BN;
-      const uint8_t* sfsrc = nullptr;  // A: this lane's row; B: row lane (+ 32 j)
+      const uint8_t* sfsrc = nullptr;  // A: this lane's row (B rows: b_row below)
       if (wp < 4) {
         const int p = a.sorted[blk * a.bm + q * 32 + lane];
         if (p < a.P) sfsrc = a.act_scale + act_row(a, p) * nkb;
-      } else {
-        sfsrc = a.w_scale + (brow0 + lane) * nkb;
       }
       for (int kc = 0; kc < nk; ++kc) {
         // hand the oldest stage over before waiting for a free slot, so that the MMA has two
@@ -201,7 +212,12 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
         const uint32_t sl = smem_s + s * L.slot;
         if (pt == 0) {
           tma::mbar_arrive_expect_tx(&full[s], (uint32_t)(BN * kBK));
-          tma::load_2d(sl + L.b, &tmap_w, kc * kBK, (int32_t)brow0, &full[s]);
+          if (EPI == EPI_SWIGLU) {  // gate rows, then up rows: two boxes of 128
+            tma::load_2d(sl + L.b, &tmap_w, kc * kBK, (int32_t)b_row<EPI>(a, e, nt, BN, 0), &full[s]);
+            tma::load_2d(sl + L.b + 128 * kBK, &tmap_w, kc * kBK, (int32_t)b_row<EPI>(a, e, nt, BN, 128), &full[s]);
+          } else {
+            tma::load_2d(sl + L.b, &tmap_w, kc * kBK, (int32_t)b_row<EPI>(a, e, nt, BN, 0), &full[s]);
+          }
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -212,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             if (j < NBW)
-              cp_async4(sl + L.sfb + ((q * NBW + j) * 32 + lane) * 4, sfsrc + (int64_t)(32 * j) * nkb + kc * 4);
+              cp_async4(sl + L.sfb + ((q * NBW + j) * 32 + lane) * 4,
+                        a.w_scale + b_row<EPI>(a, e, nt, BN, 32 * j + lane) * nkb + kc * 4);
         }
         cp_async_commit();
         ++it;
@@ -285,26 +302,62 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
       tc::tc_fence_after();
       const int p = a.sorted[blk * a.bm + r];
       const bool valid = p < a.P;
-      const int n0 = nt * BN;
       const uint32_t tb = taddr + ((uint32_t)(quarter * 32) << 16);
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t v[32];
-        tc::tmem_ld32(tb + c0, v);
-        tc::tmem_ld_wait();
-        if (valid) {
-          uint32_t pk[16];
+      if (EPI == EPI_SWIGLU) {  // 128 features: h = silu(gate) * up, quantised 32 at a time
+        const int f0 = nt * 128;
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t gv[32], uv[32];
+          tc::tmem_ld32(tb + c0, gv);
+          tc::tmem_ld32(tb + 128 + c0, uv);
+          tc::tmem_ld_wait();
+          if (valid) {
+            float h[32];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float o0 = __uint_as_float(v[2 * j]), o1 = __uint_as_float(v[2 * j + 1]);
-            if (bias) {
-              o0 += moe::bf16_bits_to_f32(bias[e * a.Nw + n0 + c0 + 2 * j]);
-              o1 += moe::bf16_bits_to_f32(bias[e * a.Nw + n0 + c0 + 2 * j + 1]);
+            for (int j = 0; j < 32; ++j) {
+              float gt = __uint_as_float(gv[j]), up = __uint_as_float(uv[j]);
+              if (bias) {
+                gt += moe::bf16_bits_to_f32(bias[e * a.Nw + f0 + c0 + j]);
+                up += moe::bf16_bits_to_f32(bias[e * a.Nw + a.Nout + f0 + c0 + j]);
+              }
+              h[j] = moe::silu(gt) * up;
             }
-            pk[j] = (uint32_t)moe::f32_to_bf16_bits(o0) | ((uint32_t)moe::f32_to_bf16_bits(o1) << 16);
+            uint32_t code[8], sc;
+            mxq::quant32(h, code, sc);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + (int64_t)p * a.Nout + f0 + c0);
+            dst[0] = make_uint4(code[0], code[1], code[2], code[3]);
+            dst[1] = make_uint4(code[4], code[5], code[6], code[7]);
+            a.out_scale[(int64_t)p * (a.Nout / 32) + (f0 + c0) / 32] = (uint8_t)sc;
           }
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + (int64_t)p * a.Nout + n0 + c0);
+        }
+      } else {
+        const int n0 = nt * BN;
+        const float wgt = (EPI == EPI_WEIGHTED_F32 && valid) ? a.topk_w[p] : 1.f;
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t v[32];
+          tc::tmem_ld32(tb + c0, v);
+          tc::tmem_ld_wait();
+          if (valid) {
+            float o[32];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            for (int j = 0; j < 32; ++j) {
+              o[j] = __uint_as_float(v[j]);
+              if (bias) o[j] += moe::bf16_bits_to_f32(bias[e * a.Nw + n0 + c0 + j]);
+            }
+            if (EPI == EPI_WEIGHTED_F32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + (int64_t)p * a.Nout + n0 + c0);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(o[4 * j] * wgt, o[4 * j + 1] * wgt, o[4 * j + 2] * wgt, o[4 * j + 3] * wgt);
+            } else {
+              uint32_t pk[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                pk[j] = (uint32_t)moe::f32_to_bf16_bits(o[2 * j]) | ((uint32_t)moe::f32_to_bf16_bits(o[2 * j + 1]) << 16);
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + (int64_t)p * a.Nout + n0 + c0);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
+          }
         }
       }
       tc::tc_fence_before();
@@ -332,12 +385,26 @@ int sm_count_mx8() {
   return n;
 }
 
+template <int EPI>
+cudaError_t launch_mx8(const MArgs& ma, const CUtensorMap& tmap, cudaStream_t stream) {
+  const MLayout L = mlayout(ma.BN);
+  cudaError_t err = cudaFuncSetAttribute(mx8_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  if (err != cudaSuccess) return err;
+  int64_t grid = sm_count_mx8();
+  if (ma.tiles < grid) grid = ma.tiles;
+  if (grid <= 0) return cudaSuccess;
+  mx8_gemm_kernel<EPI><<<(unsigned)grid, kThreads, L.total, stream>>>(tmap, ma);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 namespace moe_launch {
 
 bool mx8_supported(const GroupedGemm& g) {
-  if (g.wfmt != WF_MXFP8 || g.epi != EPI_PLAIN_BF16 || g.act_scale == nullptr) return false;
+  if (g.wfmt != WF_MXFP8 || g.act_scale == nullptr) return false;
+  if (g.epi != EPI_PLAIN_BF16 && g.epi != EPI_WEIGHTED_F32 && !(g.epi == EPI_SWIGLU && g.out_scale)) return false;
+  if (g.act_by_slot || g.out_by_slot) return false;
   if (g.bm != kBM || g.Kin <= 0 || g.Kin % kBK != 0) return false;
   if (g.Nout % 128 != 0) return false;
   if ((int64_t)g.E * g.Nw >= ((int64_t)1 << 31)) return false;  // TMA row coordinates are 32-bit
@@ -351,21 +418,18 @@ cudaError_t mx8_gemm(const GroupedGemm& g, cudaStream_t stream) {
   if (!mx8_supported(g)) return cudaErrorInvalidValue;
   MArgs ma;
   ma.g = g;
-  ma.BN = (g.Nout % 256 == 0) ? 256 : 128;
-  ma.n_tiles = g.Nout / ma.BN;
+  const bool sw = g.epi == EPI_SWIGLU;
+  ma.BN = (sw || g.Nout % 256 == 0) ? 256 : 128;
+  ma.n_tiles = sw ? g.Nout / 128 : g.Nout / ma.BN;
   ma.tiles = g.grid_blocks * ma.n_tiles;
   // weights as E * Nw rows of Kin bytes; boxes of 128 bytes x BN rows in the 128-byte swizzle
   CUtensorMap tmap;
-  if (!tma::encode_2d_u8(&tmap, g.w, (uint64_t)g.Kin, (uint64_t)g.E * g.Nw, (uint64_t)g.Kin, kBK, ma.BN, true))
+  if (!tma::encode_2d_u8(&tmap, g.w, (uint64_t)g.Kin, (uint64_t)g.E * g.Nw, (uint64_t)g.Kin, kBK,
+                         sw ? 128 : ma.BN, true))
     return cudaErrorInvalidValue;
-  const MLayout L = mlayout(ma.BN);
-  cudaError_t err = cudaFuncSetAttribute(mx8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-  if (err != cudaSuccess) return err;
-  int64_t grid = sm_count_mx8();
-  if (ma.tiles < grid) grid = ma.tiles;
-  if (grid <= 0) return cudaSuccess;
-  mx8_gemm_kernel<<<(unsigned)grid, kThreads, L.total, stream>>>(tmap, ma);
-  return cudaGetLastError();
+  if (g.epi == EPI_SWIGLU) return launch_mx8<EPI_SWIGLU>(ma, tmap, stream);
+  if (g.epi == EPI_WEIGHTED_F32) return launch_mx8<EPI_WEIGHTED_F32>(ma, tmap, stream);
+  return launch_mx8<EPI_PLAIN_BF16>(ma, tmap, stream);
 }
 
 }  // namespace moe_launch

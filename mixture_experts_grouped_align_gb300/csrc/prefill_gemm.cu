@@ -534,7 +534,7 @@ int prefill_tile_n(const GroupedGemm& g) {
 bool prefill_supported(const GroupedGemm& g) {
   if (g.wfmt == WF_BF16) return false;
   if (g.wfmt == WF_MXFP4 && g.act_fmt != ACT_F16) return false;
-  if (g.wfmt == WF_MXFP8 && g.act_scale == nullptr) return false;
+  if (g.wfmt == WF_MXFP8 && (g.act_scale == nullptr || g.epi == EPI_SWIGLU || g.epi == EPI_RELU2)) return false;
   return prefill_tile_n(g) > 0;
 }
 
@@ -553,7 +553,6 @@ cudaError_t prefill_gemm(const GroupedGemm& g, cudaStream_t stream) {
   MOE_CASE(WF_MXFP4, EPI_PLAIN_BF16, false)
   MOE_CASE(WF_MXFP4, EPI_RELU2, false)
   MOE_CASE(WF_MXFP8, EPI_PLAIN_BF16, true)
-  MOE_CASE(WF_MXFP8, EPI_SWIGLU, true)
   MOE_CASE(WF_MXFP8, EPI_WEIGHTED_F32, true)
 #undef MOE_CASE
   return cudaErrorInvalidValue;

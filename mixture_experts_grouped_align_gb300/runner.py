@@ -68,9 +68,10 @@ class DeviceLayer:
     def rows_for(self, T):
         return moe_bucket(T) if (self.pad and T > 0) else T
 
-    def step(self, x, logits, T, y, stream=None, events=None):
-        """x [T, K] bf16, logits [T, E] fp32 on the device -> y [T, K] bf16.  ``events``
-        (4 torch.cuda.Event) are recorded around the forward's kernels."""
+    def step(self, x, logits, T, y, stream=None, events=None, x_scale=None):
+        """x [T, K] bf16 (MXFP8: E4M3 codes with x_scale [T, K/32] E8M0), logits [T, E] fp32
+        on the device -> y [T, K] bf16.  ``events`` (4 torch.cuda.Event) are recorded around
+        the forward's kernels."""
         ctx = self.ctx(stream)
         if self.pad:
             _, T_rows = moe_bucket_pad(T, self.quant, x, self.x_pad, self.K * 2, logits,
@@ -82,7 +83,7 @@ class DeviceLayer:
         moe_align(ls, self.topk_ids, self.topk_w, T_rows, self.k, self.E, self.block_m,
                   self.sorted, cap, self.expert_ids, self.ntpp, self.expert_offsets, ctx)
         moe_forward(self.quant, self.E, self.K, self.I, self.w1, self.w1_scale, self.b1, self.w2,
-                    self.w2_scale, self.b2, xs, None, T_rows, T, self.k, self.topk_w, self.sorted,
+                    self.w2_scale, self.b2, xs, x_scale, T_rows, T, self.k, self.topk_w, self.sorted,
                     self.expert_ids, self.ntpp, self.expert_offsets, self.block_m, cap, y,
                     self.ctx(stream, events) if events else ctx, activation=self.activation)
         return T_rows

@@ -88,10 +88,18 @@ def test_argument_errors_are_reported_without_a_launch(lib):
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_align(None, 16, None, 4, 2, 8, 16, 16, 16, 16, 16)
     assert ei.value.status == -3            # capacity too small
+    big = moe.Ctx(stream=0, workspace=16, workspace_bytes=1 << 40)  # checked, never touched
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_forward("mxfp8", 8, 256, 512, 16, 16, None, 16, 16, None, 16, 16, 4, 4, 2,
+                        16, 16, 16, 16, None, 16, 256, 16, big, activation="relu2")
+    assert ei.value.status == -2            # the MXFP8 layer takes SwiGLU only
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_forward("mxfp8", 8, 256, 512, 16, 16, None, 16, 16, None, 16, None, 4, 4, 2,
-                        16, 16, 16, 16, None, 16, 256, 16, moe.Ctx(stream=0))
-    assert ei.value.status == -2            # MXFP8 forward needs the quantiser
+                        16, 16, 16, 16, None, 16, 256, 16, big)
+    assert ei.value.status == -1            # MXFP8 activations need their scales
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_mx_quantize(16, 4, 48, 16, 16, moe.Ctx(stream=0))
+    assert ei.value.status == -1            # 48 columns: not whole 32-blocks
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_forward("mxfp4", 8, 256, 512, 16, 16, None, 16, 16, None, 16, None, 4, 4, 2,
                         16, 16, 16, 16, None, 16, 256, 16, moe.Ctx(stream=0), activation=5)
