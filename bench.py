@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_mxfp4",
                     choices=["decode_mxfp4", "decode_bf16", "prefill_mxfp4", "tiny", "mxfp8_wgrad",
-                             "pertoken_fp8"])
+                             "pertoken_fp8", "mxfp8_layer"])
     ap.add_argument("--m", type=int, default=28, help="tokens for decode_bf16")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the token count (smaller cases for profiling)")
@@ -62,9 +62,9 @@ def parse():
 
 DEFAULT_STEPS = {"decode_mxfp4": (2000, 50), "decode_bf16": (4000, 100),
                  "prefill_mxfp4": (10, 3), "tiny": (4000, 100), "mxfp8_wgrad": (3, 3),
-                 "pertoken_fp8": (20, 3)}
+                 "pertoken_fp8": (20, 3), "mxfp8_layer": (5, 3)}
 ORACLE_SAMPLE = {"decode_mxfp4": 8, "decode_bf16": 28, "prefill_mxfp4": 4, "tiny": 64,
-                 "mxfp8_wgrad": 512, "pertoken_fp8": 8192}
+                 "mxfp8_wgrad": 512, "pertoken_fp8": 8192, "mxfp8_layer": 4096}
 # The per-token FP8 grouped GEMM workload: the GEMM1 shape of the MXFP8 workload (256 experts,
 # K = 7168 -> N = 4096, T = 8192 tokens at top-8, Zipf(1.1) routing), rows grouped by expert.
 PERTOKEN = {"T": 8192, "E": 256, "N": 4096, "K": 7168, "k": 8, "seed": 9}
@@ -162,9 +162,32 @@ def oracle_sample_pertoken(n_rows):
     return time.perf_counter() - t0, n_rows / float(c["k"])
 
 
+def oracle_sample_mxfp8_layer(n_pairs):
+    """The oracle MXFP8 layer on a bounded sample: n_pairs token-expert pairs over 2 experts'
+    worth of freshly drawn weights of the workload's shapes (top-1 here; the workload has 8
+    pairs per token)."""
+    import numpy as np
+    import synth
+    from oracle import formats, layer
+    w = synth.MXFP8_WGRAD
+    rng = np.random.default_rng(5)
+    E, K, I = 2, w.K, w.I
+    xc, xs = synth.mx_quantise_e4m3(rng.standard_normal((n_pairs, K)).astype(np.float32))
+    w1c, w1s = synth.mx_quantise_e4m3((rng.standard_normal((E, 2 * I, K)) * 0.02).astype(np.float32))
+    w2c, w2s = synth.mx_quantise_e4m3((rng.standard_normal((E, K, I)) * 0.02).astype(np.float32))
+    ids = (np.arange(n_pairs) % E).astype(np.int32)[:, None]
+    wt = np.ones((n_pairs, 1), dtype=np.float32)
+    t0 = time.perf_counter()
+    W = layer.ExpertWeights("mxfp8", w1c, w1s, None, w2c, w2s, None)
+    layer.moe_layer(formats.dequant_mxfp8(xc, xs), ids, wt, W)
+    return time.perf_counter() - t0, n_pairs / 8.0
+
+
 def oracle_sample(name, m, n_tok):
     """Times the float64 oracle on the first n_tok tokens of the workload (this process
     was started with one BLAS / OpenMP thread).  Returns seconds."""
+    if name == "mxfp8_layer":
+        return oracle_sample_mxfp8_layer(n_tok)
     if name == "mxfp8_wgrad":
         return oracle_sample_mxfp8(n_tok)
     if name == "pertoken_fp8":
@@ -758,6 +781,131 @@ def bench_pertoken(args, rank, world, local_rank):
     }
 
 
+def bench_mxfp8_layer(args, rank, world, local_rank):
+    """The whole MXFP8 layer through moe_forward on the MXFP8 workload's shapes (256 experts,
+    hidden 7168, intermediate 2048, top-8, T = 8192, Zipf(1.1) routing with the routing
+    weights uniform 1/8): GEMM1 + SwiGLU with h quantised to MXFP8 in the epilogue, GEMM2,
+    combine."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_grouped_align_gb300 as moe
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    moe.build()
+    moe.load()
+    steps, warmup = DEFAULT_STEPS["mxfp8_layer"]
+    steps = args.steps if args.steps is not None else steps
+    warmup = max(3, args.warmup if args.warmup is not None else warmup)
+    kw = {} if not args.tokens else {"T": args.tokens}
+    if args.experts:
+        kw["E"] = args.experts
+    g = synth.make_mxfp8_gemm_wgrad(device=dev, **kw)
+    T, E, K, I, k, P = g["T"], g["E"], g["K"], g["I"], g["k"], g["P"]
+    for n in ("grad1", "grad2", "x_bf16", "h_bf16", "a2_codes", "a2_scale"):
+        g.pop(n, None)
+    torch.cuda.empty_cache()
+    bm = 128
+    cap, capb = moe.moe_align_capacity(P, E, bm)
+    ids = torch.from_numpy(g["topk_ids"]).to(dev)
+    topk_w = torch.full((T, k), 1.0 / k, dtype=torch.float32, device=dev)
+    srt = torch.empty(cap, dtype=torch.int32, device=dev)
+    eid = torch.empty(capb, dtype=torch.int32, device=dev)
+    ntpp = torch.empty(4, dtype=torch.int32, device=dev)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+    moe.moe_align(None, ids, None, T, k, E, bm, srt, cap, eid, ntpp, None, moe.Ctx(dev_status=status))
+    ws = torch.empty(moe.moe_forward_workspace_size(T, k, K, I, cap), dtype=torch.uint8, device=dev)
+    y = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        moe.moe_forward("mxfp8", E, K, I, g["w1"], g["w1_scale"], None, g["w2"], g["w2_scale"], None,
+                        g["x_codes"], g["x_scale"], T, T, k, topk_w, srt, eid, ntpp, None, bm, cap, y,
+                        moe.Ctx(workspace=ws, dev_status=status, events=evs))
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status[0]) != 0:
+        raise RuntimeError(f"device status {int(status[0])}")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for quad in evs:  # a torch event has a CUDA event only once it has been recorded
+        for e_ in quad:
+            e_.record(stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ck = clocks.stop(local_rank)
+    ms = t0.elapsed_time(t1)
+    g1 = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
+    g2 = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
+    cb = sum(e[2].elapsed_time(e[3]) for e in evs) / steps
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    # end to end: the step's activation codes and scales from pinned host memory, y back
+    ins = [g["x_codes"], g["x_scale"]]
+    host = [t.cpu().pin_memory() for t in ins]
+    yh = torch.empty_like(y, device="cpu").pin_memory()
+    e2e_steps = max(1, min(steps, 3))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for d_, h_ in zip(ins, host):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        yh.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if rank != 0:
+        return None
+    hbm, bf16, src = peaks()
+    f1, f2 = 2.0 * P * K * 2 * I, 2.0 * P * I * K
+    dom, fl, dms = ("gemm1", f1, g1) if g1 >= g2 else ("gemm2", f2, g2)
+    achieved = fl / (dms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": f"mx8_gemm ({dom})", "achieved": achieved, "peak": 2 * bf16,
+                "unit": "TFLOP/s", "frac": achieved / (2 * bf16), "traffic": None, "algorithmic_flops": fl,
+                "peak_source": f"{src} (bf16_tflops x 2, the nominal fp8/bf16 dense ratio)"}
+    return {
+        "metric": METRIC, "value": world * T * steps / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 block-scaled tcgen05 mma -> f32, h quantised to MXFP8 between the GEMMs",
+        "data": "synthetic (seeded inputs drawn on the device, random-init weights)",
+        "config": {"workload": f"mxfp8_layer: T={T} tokens, hidden {K}, intermediate {I}, {E} experts, top-{k}, "
+                               f"Zipf(1.1) routing, uniform routing weights, MXFP8 layer forward",
+                   "T": T, "experts": E, "hidden": K, "intermediate": I, "top_k": k, "block_m": bm,
+                   "l2": "inputs larger than L2: 11.3 GB of MXFP8 weights per step",
+                   "parallelism": f"replicas x{world}"},
+        "useful_tflops": world * (f1 + f2) * steps / (ms * 1e-3) / 1e12,
+        "kernel_ms": {"gemm1_swiglu_quant": g1, "gemm2_weighted": g2, "combine": cb},
+        "roofline": roofline,
+        "e2e": {"value": world * T * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host),
+                "d2h_bytes_per_step": y.numel() * 2, "steps": e2e_steps},
+        "gpu_launches": steps * 3,
+        "clocks": ck,
+    }
+
+
 def launches_per_step(w, rows):
     n = 3  # GEMM1, GEMM2, combine
     n += 1  # align (routing fused for rows <= 512)
@@ -774,7 +922,10 @@ def cpu_baseline(args):
     name = args.workload
     n = args.sample_tokens or ORACLE_SAMPLE[name]
     r = run_oracle_subprocess(name, args.m, n)
-    if name == "pertoken_fp8":
+    if name == "mxfp8_layer":
+        what = (f"float64 oracle MXFP8 layer: {n} token-expert pairs over 2 experts "
+                f"({r['tokens']:g} tokens at top-8; {r['seconds']:.1f} s, one thread)")
+    elif name == "pertoken_fp8":
         what = (f"float64 oracle: {n} rows of one expert of the per-token FP8 GEMM "
                 f"({r['tokens']:g} tokens at top-8; {r['seconds']:.1f} s, one thread)")
     elif name == "mxfp8_wgrad":
@@ -809,6 +960,8 @@ def main():
         line = bench_mxfp8_wgrad(args, rank, world, local_rank)
     elif args.workload == "pertoken_fp8":
         line = bench_pertoken(args, rank, world, local_rank)
+    elif args.workload == "mxfp8_layer":
+        line = bench_mxfp8_layer(args, rank, world, local_rank)
     else:
         line = bench_ours(args, rank, world, local_rank)
     if rank == 0:
@@ -841,7 +994,7 @@ def bench_reference(args):
     line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1, "steps": steps,
             "warmup": warmup, "ms_per_step": secs / steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": (describe(w, w.T) if args.workload not in ("mxfp8_wgrad", "pertoken_fp8")
+            "config": (describe(w, w.T) if args.workload not in ("mxfp8_wgrad", "pertoken_fp8", "mxfp8_layer")
                        else {"workload": args.workload}), "impl": "reference",
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": f"{n} token(s) of the workload per step (float64 oracle, one "

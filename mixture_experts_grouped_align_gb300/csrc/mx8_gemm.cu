@@ -54,9 +54,11 @@ constexpr int kStages = 4;
 constexpr int kLag = 2;                    // stages between a stage's copies and its hand-over
 
 // One stage slot: A tile | B tile | A scale words (one per row) | B scale words (one copy
-// per 32-lane quarter: [4][BN/32][32 lanes], lanes contiguous).
+// per 32-lane quarter: [4][BN/32][32 lanes], lanes contiguous).  When Kin is a multiple of
+// 512 the scale words instead arrive four stages at a time, 16 bytes per row, into two group
+// buffers (A [128 rows][16 B], B [BN rows][16 B]): far fewer, larger copies.
 struct MLayout {
-  int a, b, sfa, sfb, slot, bars, total;
+  int a, b, sfa, sfb, slot, ga, gb, bars, total;
 };
 
 __host__ __device__ inline MLayout mlayout(int BN) {
@@ -66,9 +68,15 @@ __host__ __device__ inline MLayout mlayout(int BN) {
   L.sfa = L.b + BN * kBK;
   L.sfb = L.sfa + kBM * 4;
   L.slot = (L.sfb + 4 * 32 * (BN / 32) * 4 + 1023) / 1024 * 1024;
-  L.bars = kStages * L.slot;
+  L.ga = kStages * L.slot;
+  L.gb = L.ga + 2 * kBM * 16;
+  L.bars = L.gb + 2 * BN * 16;
   L.total = L.bars + 256 + 1024;
   return L;
+}
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_addr(bar)) : "memory");
 }
 
 // TMEM columns of a stage's scale words: A (4 columns at +0), B (BN / 32 <= 8 columns at +8).
@@ -125,7 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
-  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* gb_full = drain + 1;  // [2] B scale group landed (every B-scale thread's copies)
+  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(gb_full + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(taddr_s + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -137,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
     tc::mbar_init(tfull, 1);
     tc::mbar_init(tempty, 4);
     tc::mbar_init(drain, 1);
+    for (int i = 0; i < 2; ++i) tc::mbar_init(&gb_full[i], kNumProd / 2);
     *abort_flag = 0;
     tc::mbar_fence_init();
   }
@@ -160,25 +170,44 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
     if (pt == 0) tma::prefetch_map(&tmap_w);
     uint32_t it = 0;
     int npend = 0;
+    // scale words by groups of four stages (16-byte rows) when Kin % 512 == 0: a tile's stage
+    // count is then a multiple of four, so stage it belongs to group it / 4
+    const bool grouped = (nkb % 16) == 0;
+    const int tb = pt - 128;  // B-scale copier index (warps 12-15)
     // hand stage h over to the MMA: its copies (this thread's own) have landed
-    auto hand_over = [&](uint32_t h) {
+    auto hand_over = [&](uint32_t h) -> bool {
       const int hs = (int)(h % kStages);
       const uint8_t* sl = smem + hs * L.slot;
       tc::fence_proxy_async_smem();
       if (wp < 4) {
-        const uint32_t wv = *reinterpret_cast<const uint32_t*>(sl + L.sfa + (q * 32 + lane) * 4);
+        const uint32_t wv = grouped
+            ? *reinterpret_cast<const uint32_t*>(smem + L.ga + ((h >> 2) & 1) * kBM * 16 + (q * 32 + lane) * 16 + (h & 3) * 4)
+            : *reinterpret_cast<const uint32_t*>(sl + L.sfa + (q * 32 + lane) * 4);
         tc::tmem_st4(taddr + ((uint32_t)(q * 32) << 16) + sfa_col(hs), wv, wv, wv, wv);
       } else {
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(sl + L.sfb) + q * NBW * 32 + lane;
         uint32_t v[8];
+        if (grouped) {  // rows 32 j + lane of the group, copied by all four B-scale warps
+          const uint32_t g = h >> 2;
+          if ((h & 3) == 0 && !tc::mbar_wait(&gb_full[g & 1], (g >> 1) & 1)) {
+            moe::set_status(a.status, MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+          }
+          const uint8_t* gsrc = smem + L.gb + (g & 1) * BN * 16 + (h & 3) * 4;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = j < NBW ? src[j * 32] : 0u;
+          for (int j = 0; j < 8; ++j) v[j] = j < NBW ? *reinterpret_cast<const uint32_t*>(gsrc + (32 * j + lane) * 16) : 0u;
+        } else {
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(sl + L.sfb) + q * NBW * 32 + lane;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = j < NBW ? src[j * 32] : 0u;
+        }
         tc::tmem_st8(taddr + ((uint32_t)(q * 32) << 16) + sfb_col(hs), v);
       }
       tc::tmem_st_wait();
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&full[hs]);
+      return true;
     };
     for (int64_t t = blockIdx.x; t < ma.tiles && !*abort_flag; t += gridDim.x) {
       int64_t blk, e;
@@ -200,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
         // stages queued while this one's copies fly
         if (npend == kLag) {
           cp_async_wait<kLag - 1>();
-          hand_over(it - kLag);
+          if (!hand_over(it - kLag)) break;
           --npend;
         }
         const int s = (int)(it % kStages);
@@ -222,7 +251,19 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           if (aptr[i]) cp_async16(sl + L.a + tc::sw128_offset(r0 + 32 * i, c16), aptr[i] + kc * kBK);
-        if (wp < 4) {
+        if (grouped) {
+          if ((kc & 3) == 0) {  // this group's four stages of scale words, 16 bytes per row
+            const uint32_t gsel = (it >> 2) & 1;
+            if (wp < 4) {
+              if (sfsrc) cp_async16(smem_s + L.ga + gsel * kBM * 16 + (q * 32 + lane) * 16, sfsrc + kc * 4);
+            } else {
+              for (int n = tb; n < BN; n += 128)
+                cp_async16(smem_s + L.gb + gsel * BN * 16 + n * 16,
+                           a.w_scale + b_row<EPI>(a, e, nt, BN, n) * nkb + kc * 4);
+              cp_async_arrive_noinc(&gb_full[gsel]);
+            }
+          }
+        } else if (wp < 4) {
           if (sfsrc) cp_async4(sl + L.sfa + (q * 32 + lane) * 4, sfsrc + kc * 4);
         } else {
 #pragma unroll
@@ -237,8 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
       }
     }
     cp_async_wait<0>();
-    while (npend > 0) {
-      hand_over(it - npend);
+    while (npend > 0 && !*abort_flag) {
+      if (!hand_over(it - npend)) break;
       --npend;
     }
   } else if (warp == 0) {

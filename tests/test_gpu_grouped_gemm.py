@@ -151,11 +151,13 @@ def test_mxfp8_full_size_sampled(moe):
 @pytest.mark.parametrize("N", [256, 384])          # N tile 256 / N tile 128
 @pytest.mark.parametrize("per_pair", [False, True])
 @pytest.mark.parametrize("bias", [False, True])
-def test_mxfp8_block_scaled(moe, N, per_pair, bias):
+@pytest.mark.parametrize("Kin", [384, 1024])        # scale words per stage / per four stages
+def test_mxfp8_block_scaled(moe, N, per_pair, bias, Kin):
     """Rows above the threshold, K a multiple of 128 and N of 128: the block-scaled MMA path.
-    Ragged experts (two empty) over several 128-row tiles, three K stages."""
+    Ragged experts (two empty) over several 128-row tiles, three or eight K stages (K a
+    multiple of 512 takes the scale words four stages at a time)."""
     rng = np.random.default_rng(13)
-    T, E, k, Kin = 700, 12, 3, 384
+    T, E, k = 700, 12, 3
     ids = random_ids(rng, T, E, k, empty=(5, 9))
     rows = T * k if per_pair else T
     a_c, a_s = synth.mx_quantise_e4m3(rng.standard_normal((rows, Kin)).astype(np.float32))

@@ -76,11 +76,13 @@ def oracle_layer(w, lay, T):
     return olayer.moe_layer(x, ids, wt, W)
 
 
-@pytest.mark.parametrize("T,bias", [(64, True), (200, False), (300, True), (700, False)])
-def test_mxfp8_layer(moe, T, bias):
+@pytest.mark.parametrize("T,bias,K,I", [(64, True, 384, 256), (200, False, 384, 256), (300, True, 384, 256),
+                                        (700, False, 384, 256), (600, True, 1024, 512)])
+def test_mxfp8_layer(moe, T, bias, K, I):
     """Up to 256 rows the weight-streaming kernels with fp32 h and the standalone quantiser;
-    above, the block-scaled kernel with the quantiser in its epilogue."""
-    w = synth.Workload("mxfp8_layer", T=T, K=384, I=256, E=8, k=4, quant="mxfp8", seed=31,
+    above, the block-scaled kernel with the quantiser in its epilogue (K and I multiples of
+    512: scale words four stages at a time)."""
+    w = synth.Workload("mxfp8_layer", T=T, K=K, I=I, E=8, k=4, quant="mxfp8", seed=31,
                        weight_std=0.05, bias=bias)
     lay = synth.make_layer(w)
     assert_close_bf16(layer(moe, w, lay, T), oracle_layer(w, lay, T), what=f"mxfp8 layer T={T}")
