@@ -25,11 +25,13 @@
 // partial sum that is multiplied by the block's scale (per weight row, and per token for
 // MXFP8 activations) and added to the float32 accumulator.
 #include "moe_common.cuh"
+#include "cp_async.cuh"
 #include "moe_launch.h"
 
 namespace {
 
 using namespace moe_launch;
+using namespace cpa;
 
 constexpr int kWarps = 4;   // warps per block, each a quarter of K
 constexpr int kTok = 8;     // tokens per tile (MMA N)
@@ -132,16 +134,6 @@ template <int WF>
 __host__ __device__ inline int64_t wrow_bytes(int Kin) {
   return WF == WF_MXFP4 ? Kin / 2 : (WF == WF_MXFP8 ? Kin : (int64_t)Kin * 2);
 }
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 // Work units are (alignment block, 16-row tile) pairs, block-major; a thread block owns
 // a contiguous run of the units that num_tokens_post_padded makes live, so that each

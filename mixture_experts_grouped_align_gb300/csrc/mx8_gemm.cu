@@ -35,6 +35,7 @@
 // the word of B row n in column n / 32 of the B region at lane n % 32 (written to that
 // lane of every 32-lane quarter).
 #include "moe_common.cuh"
+#include "cp_async.cuh"
 #include "moe_launch.h"
 #include "mx_quant.cuh"
 #include "tcgen05.cuh"
@@ -43,6 +44,7 @@
 namespace {
 
 using namespace moe_launch;
+using namespace cpa;
 
 constexpr int kThreads = 512;
 constexpr int kBM = 128, kBK = 128;        // tile rows, K elements (bytes) per stage
@@ -75,10 +77,6 @@ __host__ __device__ inline MLayout mlayout(int BN) {
   return L;
 }
 
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_addr(bar)) : "memory");
-}
-
 // TMEM columns of a stage's scale words: A (4 columns at +0), B (BN / 32 <= 8 columns at +8).
 __device__ __forceinline__ uint32_t sfa_col(int s) { return kSfCol0 + 16 * s; }
 __device__ __forceinline__ uint32_t sfb_col(int s) { return kSfCol0 + 16 * s + 8; }
@@ -89,16 +87,6 @@ struct MArgs {
   int n_tiles;
   int64_t tiles;
 };
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ bool tile_info(const MArgs& ma, int64_t t, int ntpp, int64_t& blk, int& nt,
                                           int64_t& e) {

@@ -24,6 +24,7 @@
 // Every mbarrier wait is bounded; one that runs out sets MOE_ERR_TIMEOUT, every role leaves
 // its loop, the MMA lane drains its own work and the TMEM is freed.
 #include "moe_common.cuh"
+#include "cp_async.cuh"
 #include "moe_launch.h"
 #include "tcgen05.cuh"
 #include "tma.cuh"
@@ -31,6 +32,7 @@
 namespace {
 
 using namespace moe_launch;
+using namespace cpa;
 
 constexpr int kThreads = 512;
 constexpr int kBM = 128, kBK = 128;        // tile rows, K elements (bytes) per stage
@@ -72,13 +74,6 @@ struct PTArgs {
   int E, N, K, BN, n_tiles;
   int64_t tiles;           // upper bound of row blocks (ceil(M / 128) + E) * n_tiles
 };
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 // D[tmem] (+)= A[smem] . B[smem]^T, E4M3 x E4M3 -> f32 (kind::f8f6f4), issued by one thread.
 __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,

@@ -29,12 +29,14 @@
 // Each output row depends on its own A row only and K is always reduced in the same
 // order, so padded and unpadded batches give identical real rows.
 #include "moe_common.cuh"
+#include "cp_async.cuh"
 #include "moe_launch.h"
 #include "tcgen05.cuh"
 
 namespace {
 
 using namespace moe_launch;
+using namespace cpa;
 
 constexpr int kThreads = 512;
 constexpr int kBM = 128, kBK = 64;
@@ -84,13 +86,6 @@ struct PArgs {
   int n_tiles;   // N tiles per block
   int64_t tiles; // block slots * n_tiles
 };
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t v, __half2 s) {
   __half2 h = __hmul2(*reinterpret_cast<__half2*>(&v), s);

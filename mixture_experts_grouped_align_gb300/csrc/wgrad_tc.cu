@@ -17,12 +17,14 @@
 // Every mbarrier wait is bounded; a wait that runs out sets MOE_ERR_TIMEOUT and every
 // role leaves its loop.  Each tile sums its tokens in one fixed order: repeatable bits.
 #include "moe_common.cuh"
+#include "cp_async.cuh"
 #include "moe_launch.h"
 #include "tcgen05.cuh"
 
 namespace {
 
 using namespace moe_launch;
+using namespace cpa;
 
 constexpr int kThreads = 512;
 constexpr int kTM = 128;          // dW rows (N) per tile
@@ -61,18 +63,6 @@ struct WArgs {
   int c_tiles;     // Kin / BN
   int64_t tiles;   // E * n_tiles * c_tiles
 };
-
-__device__ __forceinline__ void cp_async16z(uint32_t dst, const void* src, bool valid) {
-  const int sz = valid ? 16 : 0;  // 0 bytes read -> 16 zero bytes written
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz)
-               : "memory");
-}
-// Arrives on the mbarrier once every cp.async this thread issued before has landed (the
-// barrier's expected count includes this arrival).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 // Byte offset of (token t, 16-byte chunk c of a row of 64 MN elements) in an atom column.
 __device__ __forceinline__ uint32_t mn_offset(int t, int c) {
