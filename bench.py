@@ -34,7 +34,7 @@ L2_BYTES = 129 * 1024 * 1024
 # hashes the same; otherwise reported as null.
 TRAFFIC = {
     "decode_gemm.cu:gemm1@decode_mxfp4": {  # profiles/decode_gemm_decode_mxfp4_T64.md
-        "src": "978915d2a01efc1e", "bytes": 998010112 + 4668416},
+        "src": "11884d6b9aeb3576", "bytes": 997830656 + 4369408},
 }
 
 
