@@ -98,6 +98,11 @@ def test_argument_errors_are_reported_without_a_launch(lib):
                         16, 16, 16, 16, None, 16, 256, 16, big)
     assert ei.value.status == -1            # MXFP8 activations need their scales
     with pytest.raises(moe.MoeError) as ei:
+        moe.moe_forward("mxfp8", 8, 256, 512, 16, 16, None, 16, 16, None, 16, 16, 4, 4, 2,
+                        16, 16, 16, 16, None, 16, 256, 16, big)
+    assert ei.value.status == -2            # few rows keep fp32 h in the o scratch: I <= K
+    assert "I <= K" in lib.moe_last_error().decode()
+    with pytest.raises(moe.MoeError) as ei:
         moe.moe_mx_quantize(16, 4, 48, 16, 16, moe.Ctx(stream=0))
     assert ei.value.status == -1            # 48 columns: not whole 32-blocks
     with pytest.raises(moe.MoeError) as ei:
