@@ -112,6 +112,31 @@ def src_hash(*names):
     return h.hexdigest()[:16]
 
 
+# ------------------------------------------------------------------------------ ranks
+
+def barrier(world):
+    """Every rank reaches this point (one process per GPU; nothing to do alone)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    """The largest of every rank's x (the slowest rank's time); x itself when alone."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(world, units_per_rank, ms):
+    """Whole-job rate: the units every rank processed over the slowest rank's time (per s)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 # ------------------------------------------------------------------------------ oracle
 
 def oracle_sample_mxfp8(n_tok):
@@ -276,7 +301,6 @@ class ClockSampler:
 def bench_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
-    import torch.distributed as dist
 
     import mixture_experts_grouped_align_gb300 as moe
     from mixture_experts_grouped_align_gb300.runner import DeviceLayer
@@ -368,8 +392,7 @@ def bench_ours(args, rank, world, local_rank):
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.2)
@@ -398,16 +421,12 @@ def bench_ours(args, rank, world, local_rank):
                 step()
         t_end.record(cur)
         torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     ck = clocks.stop(local_rank)
     ms = sum(a.elapsed_time(b) for a, b in pairs) if flush else t_start.elapsed_time(t_end)
     if int(L.status[0]) != 0:
         raise RuntimeError(f"device status {int(L.status[0])}")
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
 
     # end to end: pinned host inputs in, output back out, inside the timed region
     xh = torch.empty_like(x, device="cpu").pin_memory()
@@ -422,8 +441,7 @@ def bench_ours(args, rank, world, local_rank):
         xd.copy_(xh, non_blocking=True); ld.copy_(lh, non_blocking=True)
         L.step(xd, ld, T, y); yh.copy_(y, non_blocking=True)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -435,10 +453,7 @@ def bench_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     if rank != 0:
         return None
@@ -469,7 +484,7 @@ def bench_ours(args, rank, world, local_rank):
     ms_step = ms / steps
     line = {
         "metric": METRIC,
-        "value": world * T * steps / (ms * 1e-3),
+        "value": aggregate_rate(world, T * steps, ms),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": steps,
@@ -497,7 +512,7 @@ def bench_ours(args, rank, world, local_rank):
         "roofline": roofline,
         "step_roofline": {"bytes": step_weight_bytes, "achieved_gbs": step_weight_bytes / (ms_step * 1e-3) / 1e9,
                           "frac": step_weight_bytes / (ms_step * 1e-3) / 1e9 / hbm},
-        "e2e": {"value": world * T * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": aggregate_rate(world, T * e2e_steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * 2 + lg.numel() * 4,
                 "d2h_bytes_per_step": y.numel() * 2, "steps": e2e_steps},
         "gpu_launches": steps * launches_per_step(w, rows),
@@ -512,7 +527,6 @@ def bench_mxfp8_wgrad(args, rank, world, local_rank):
     the deterministic weight gradients dW1 [256, 4096, 7168] and dW2 [256, 7168, 2048]."""
     import numpy as np
     import torch
-    import torch.distributed as dist
 
     import mixture_experts_grouped_align_gb300 as moe
     import synth
@@ -566,8 +580,7 @@ def bench_mxfp8_wgrad(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.2)
@@ -577,15 +590,11 @@ def bench_mxfp8_wgrad(args, rank, world, local_rank):
         step(evs[i])
     t1.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     ck = clocks.stop(local_rank)
     ms = t0.elapsed_time(t1)
     kms = [sum(e[j][0].elapsed_time(e[j][1]) for e in evs) / steps for j in range(4)]
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, dev)
     # end to end: the step's activations and output gradients from pinned host memory,
     # the GEMM outputs back to the host; weights and dW stay resident
     ins = ["x_codes", "x_scale", "a2_codes", "a2_scale", "grad1", "grad2", "x_bf16", "h_bf16"]
@@ -605,7 +614,7 @@ def bench_mxfp8_wgrad(args, rank, world, local_rank):
         o2h.copy_(out2, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     if rank != 0:
         return None
     hbm, bf16, src = peaks()
@@ -629,7 +638,7 @@ def bench_mxfp8_wgrad(args, rank, world, local_rank):
                     "peak_source": f"{src} (bf16_tflops x 2, the nominal fp8/bf16 dense ratio)"}
     h2d = sum(host[n].numel() * host[n].element_size() for n in ins)
     line = {
-        "metric": METRIC, "value": world * T * steps / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": aggregate_rate(world, T * steps, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": warmup, "ms_per_step": ms / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 block-scaled tcgen05 mma (GEMMs), bf16 tcgen05 mma (wgrad) -> f32",
@@ -642,7 +651,7 @@ def bench_mxfp8_wgrad(args, rank, world, local_rank):
         "useful_tflops": world * 2 * (f_gemm1 + f_gemm2) * steps / (ms * 1e-3) / 1e12,
         "kernel_ms": dict(zip(names, kms)),
         "roofline": roofline,
-        "e2e": {"value": world * T * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": aggregate_rate(world, T * e2e_steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out1.numel() * 2 + out2.numel() * 2,
                 "steps": e2e_steps},
         "gpu_launches": steps * 4,
@@ -657,7 +666,6 @@ def bench_pertoken(args, rank, world, local_rank):
     with one scale per row and one per expert."""
     import numpy as np
     import torch
-    import torch.distributed as dist
 
     import mixture_experts_grouped_align_gb300 as moe
     import synth
@@ -714,8 +722,7 @@ def bench_pertoken(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.2)
@@ -725,15 +732,11 @@ def bench_pertoken(args, rank, world, local_rank):
         step(evs[i])
     t1.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     ck = clocks.stop(local_rank)
     ms = t0.elapsed_time(t1)
     kms = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, dev)
     # end to end: activations, their scales and the group sizes from pinned host memory, the
     # output back to the host; weights stay resident
     ins = [a, a_scale, gsd]
@@ -749,7 +752,7 @@ def bench_pertoken(args, rank, world, local_rank):
         oh.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     if rank != 0:
         return None
     hbm, bf16, src = peaks()
@@ -760,7 +763,7 @@ def bench_pertoken(args, rank, world, local_rank):
                 "peak_source": f"{src} (bf16_tflops x 2, the nominal fp8/bf16 dense ratio)"}
     h2d = sum(t.numel() * t.element_size() for t in host)
     return {
-        "metric": METRIC, "value": world * T * steps / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": aggregate_rate(world, T * steps, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": warmup, "ms_per_step": ms / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 tcgen05 mma -> f32, scales after the dot",
         "data": "synthetic (per-token E4M3 quantisation of N(0,1) activations drawn on the device, "
@@ -774,7 +777,7 @@ def bench_pertoken(args, rank, world, local_rank):
         "useful_tflops": world * fl * steps / (ms * 1e-3) / 1e12,
         "kernel_ms": {"gemm_per_token": kms},
         "roofline": roofline,
-        "e2e": {"value": world * T * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": aggregate_rate(world, T * e2e_steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out.numel() * 2, "steps": e2e_steps},
         "gpu_launches": steps,
         "clocks": ck,
@@ -788,7 +791,6 @@ def bench_mxfp8_layer(args, rank, world, local_rank):
     combine."""
     import numpy as np
     import torch
-    import torch.distributed as dist
 
     import mixture_experts_grouped_align_gb300 as moe
     import synth
@@ -838,8 +840,7 @@ def bench_mxfp8_layer(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.2)
@@ -849,17 +850,13 @@ def bench_mxfp8_layer(args, rank, world, local_rank):
         step(evs[i])
     t1.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     ck = clocks.stop(local_rank)
     ms = t0.elapsed_time(t1)
     g1 = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
     g2 = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
     cb = sum(e[2].elapsed_time(e[3]) for e in evs) / steps
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, dev)
     # end to end: the step's activation codes and scales from pinned host memory, y back
     ins = [g["x_codes"], g["x_scale"]]
     host = [t.cpu().pin_memory() for t in ins]
@@ -874,7 +871,7 @@ def bench_mxfp8_layer(args, rank, world, local_rank):
         yh.copy_(y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     if rank != 0:
         return None
     hbm, bf16, src = peaks()
@@ -885,7 +882,7 @@ def bench_mxfp8_layer(args, rank, world, local_rank):
                 "unit": "TFLOP/s", "frac": achieved / (2 * bf16), "traffic": None, "algorithmic_flops": fl,
                 "peak_source": f"{src} (bf16_tflops x 2, the nominal fp8/bf16 dense ratio)"}
     return {
-        "metric": METRIC, "value": world * T * steps / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": aggregate_rate(world, T * steps, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": warmup, "ms_per_step": ms / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 block-scaled tcgen05 mma -> f32, h quantised to MXFP8 between the GEMMs",
@@ -898,7 +895,7 @@ def bench_mxfp8_layer(args, rank, world, local_rank):
         "useful_tflops": world * (f1 + f2) * steps / (ms * 1e-3) / 1e12,
         "kernel_ms": {"gemm1_swiglu_quant": g1, "gemm2_weighted": g2, "combine": cb},
         "roofline": roofline,
-        "e2e": {"value": world * T * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": aggregate_rate(world, T * e2e_steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host),
                 "d2h_bytes_per_step": y.numel() * 2, "steps": e2e_steps},
         "gpu_launches": steps * 3,
