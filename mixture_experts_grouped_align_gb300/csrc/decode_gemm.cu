@@ -83,11 +83,10 @@ __host__ __device__ constexpr int ring_slot_total(int nmat) {
   return act_offset<WF>(nmat) + kTok * act_row_stride<WF>();
 }
 
-template <int WF>
+template <int WF, int R>
 __host__ __device__ inline Smem smem_layout(int nmat, int Kin) {
-  using PP = Pipe<WF>;
   Smem s;
-  s.ring_warp = PP::R * ring_slot_total<WF>(nmat);
+  s.ring_warp = R * ring_slot_total<WF>(nmat);
   s.sw = 0;
   (void)Kin;
   int off = 0;
@@ -268,7 +267,7 @@ struct Issuer {
   }
 };
 
-template <int WF, int NMAT>
+template <int WF, int NMAT, int R>
 __device__ __forceinline__ void issue_next(const GroupedGemm& a, Issuer<WF, NMAT>& c, uint32_t ring_s,
                                            int64_t rb, int kb0, int kb1, int nst, int row_tiles,
                                            int lane) {
@@ -281,7 +280,7 @@ __device__ __forceinline__ void issue_next(const GroupedGemm& a, Issuer<WF, NMAT
   constexpr int AOFF = act_offset<WF>(NMAT);
   if (c.iu < c.u_end) {
     const int kbs = kb0 + c.ist * PP::D;
-    const uint32_t slot = ring_s + (c.issued % PP::R) * SLOT;
+    const uint32_t slot = ring_s + (c.issued % R) * SLOT;
     const int j = LN::blk(lane), sub = LN::sub(lane);
     if (kbs + j < kb1) {
 #pragma unroll
@@ -326,7 +325,10 @@ __device__ __forceinline__ void issue_next(const GroupedGemm& a, Issuer<WF, NMAT
   ++c.issued;
 }
 
-template <int WF, int EPI>
+// R: stages in each warp's ring.  Fewer stages leave room for more resident warps, which
+// hide the conversion and MMA latencies better when there are many units; more stages keep
+// more bytes in flight per warp when there are few.
+template <int WF, int EPI, int R>
 __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm a) {
   constexpr int NMAT = (EPI == EPI_SWIGLU) ? 2 : 1;
   constexpr int NROWS = NMAT * kRows;
@@ -339,7 +341,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
   constexpr int AOFF = act_offset<WF>(NMAT);
 
   extern __shared__ __align__(16) uint8_t smem[];
-  const Smem L = smem_layout<WF>(NMAT, a.Kin);
+  const Smem L = smem_layout<WF, R>(NMAT, a.Kin);
   float* red = reinterpret_cast<float*>(smem + L.red);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -379,7 +381,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
     cur.bind_act(a, lane);
   }
 #pragma unroll 1
-  for (int s = 0; s < PP::R - 1; ++s) issue_next<WF, NMAT>(a, cur, ring_s, rb, kb0, kb1, nst, row_tiles, lane);
+  for (int s = 0; s < R - 1; ++s) issue_next<WF, NMAT, R>(a, cur, ring_s, rb, kb0, kb1, nst, row_tiles, lane);
 
   bool bad = false;
   uint32_t consumed = 0, red_buf = 0;
@@ -418,11 +420,11 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
         for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
 
       for (int st = 0; st < nst; ++st) {
-        issue_next<WF, NMAT>(a, cur, ring_s, rb, kb0, kb1, nst, row_tiles, lane);
-        cp_async_wait<PP::R - 1>();
+        issue_next<WF, NMAT, R>(a, cur, ring_s, rb, kb0, kb1, nst, row_tiles, lane);
+        cp_async_wait<R - 1>();
         __syncwarp();
-        const uint8_t* slot = ring + (consumed % PP::R) * SLOT;
-        float* sf = reinterpret_cast<float*>(ring + (consumed % PP::R) * SLOT + NROWS * PP::RS + NROWS * 8);
+        const uint8_t* slot = ring + (consumed % R) * SLOT;
+        float* sf = reinterpret_cast<float*>(ring + (consumed % R) * SLOT + NROWS * PP::RS + NROWS * 8);
         const int kbs = kb0 + st * PP::D;
         const uint8_t* xs = slot + AOFF + g * act_row_stride<WF>() + q * (act_block_bytes<WF>() / 4);
         if (MX) {  // decode this stage's scale bytes (row r, block j) to floats
@@ -585,13 +587,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
   if (bad) moe::set_status(a.status, MOE_ERR_RANGE);
 }
 
-template <int WF, int EPI>
-cudaError_t launch_t(const GroupedGemm& g, cudaStream_t stream) {
-  const Smem L = smem_layout<WF>(EPI == EPI_SWIGLU ? 2 : 1, g.Kin);
-  cudaError_t err = cudaFuncSetAttribute(decode_gemm_kernel<WF, EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-  if (err != cudaSuccess) return err;
-  // enough resident blocks to keep every SM streaming; each owns a run of live units
+int sm_count_dec() {
   static int sms = 0;
   if (!sms) {
     int dev = 0;
@@ -599,16 +595,49 @@ cudaError_t launch_t(const GroupedGemm& g, cudaStream_t stream) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 1;
   }
+  return sms;
+}
+
+// Resident blocks of the R-stage variant on the whole GPU (0 on error).
+template <int WF, int EPI, int R>
+int64_t resident_blocks(const GroupedGemm& g) {
+  const Smem L = smem_layout<WF, R>(EPI == EPI_SWIGLU ? 2 : 1, g.Kin);
+  if (cudaFuncSetAttribute(decode_gemm_kernel<WF, EPI, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) !=
+      cudaSuccess)
+    return 0;
   int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_gemm_kernel<WF, EPI>, kWarps * 32, L.total);
-  if (err != cudaSuccess) return err;
-  if (per_sm < 1) per_sm = 1;
-  int64_t grid = (int64_t)sms * per_sm;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_gemm_kernel<WF, EPI, R>, kWarps * 32, L.total) !=
+      cudaSuccess)
+    return 0;
+  return (int64_t)sm_count_dec() * (per_sm < 1 ? 1 : per_sm);
+}
+
+template <int WF, int EPI, int R>
+cudaError_t launch_t(const GroupedGemm& g, cudaStream_t stream) {
+  const Smem L = smem_layout<WF, R>(EPI == EPI_SWIGLU ? 2 : 1, g.Kin);
+  // enough resident blocks to keep every SM streaming; each owns a run of live units
+  int64_t grid = resident_blocks<WF, EPI, R>(g);
+  if (grid <= 0) return cudaErrorInvalidValue;
   const int64_t units = g.grid_blocks * (g.Nout / kRows);
   if (units < grid) grid = units;
   if (grid <= 0) return cudaSuccess;
-  decode_gemm_kernel<WF, EPI><<<(unsigned)grid, kWarps * 32, L.total, stream>>>(g);
+  decode_gemm_kernel<WF, EPI, R><<<(unsigned)grid, kWarps * 32, L.total, stream>>>(g);
   return cudaGetLastError();
+}
+
+// Ring depth: two stages for MXFP4 codes (measured faster on the 64-token decode layer).
+// For bf16 weights, two stages when every unit fits in two rounds of the two-stage
+// variant's resident blocks (a one-token step: the smaller ring lets one more block per SM
+// in and shortens the longest run), else three; MXFP8 keeps its four.
+template <int WF, int EPI>
+cudaError_t launch_r(const GroupedGemm& g, cudaStream_t stream) {
+  if (WF == WF_MXFP4) return launch_t<WF, EPI, 2>(g, stream);
+  if (WF == WF_BF16) {
+    const int64_t units = g.grid_blocks * (g.Nout / kRows);
+    if (units <= 2 * resident_blocks<WF, EPI, 2>(g)) return launch_t<WF, EPI, 2>(g, stream);
+    return launch_t<WF, EPI, 3>(g, stream);
+  }
+  return launch_t<WF, EPI, Pipe<WF>::R>(g, stream);
 }
 
 }  // namespace
@@ -617,14 +646,14 @@ namespace moe_launch {
 
 size_t decode_gemm_smem_bytes(const GroupedGemm& g) {
   const int nmat = g.epi == EPI_SWIGLU ? 2 : 1;
-  if (g.wfmt == WF_MXFP4) return smem_layout<WF_MXFP4>(nmat, g.Kin).total;
-  if (g.wfmt == WF_MXFP8) return smem_layout<WF_MXFP8>(nmat, g.Kin).total;
-  return smem_layout<WF_BF16>(nmat, g.Kin).total;
+  if (g.wfmt == WF_MXFP4) return smem_layout<WF_MXFP4, 2>(nmat, g.Kin).total;
+  if (g.wfmt == WF_MXFP8) return smem_layout<WF_MXFP8, Pipe<WF_MXFP8>::R>(nmat, g.Kin).total;
+  return smem_layout<WF_BF16, 3>(nmat, g.Kin).total;
 }
 
 cudaError_t decode_gemm(const GroupedGemm& g, cudaStream_t stream) {
 #define MOE_CASE(WF, EP) \
-  if (g.wfmt == WF && g.epi == EP) return launch_t<WF, EP>(g, stream);
+  if (g.wfmt == WF && g.epi == EP) return launch_r<WF, EP>(g, stream);
   MOE_CASE(WF_MXFP4, EPI_SWIGLU)
   MOE_CASE(WF_MXFP4, EPI_WEIGHTED_F32)
   MOE_CASE(WF_MXFP4, EPI_PLAIN_BF16)
