@@ -167,9 +167,17 @@ __device__ __forceinline__ Unit load_unit(const GroupedGemm& a, int64_t u, int r
   return x;
 }
 
+// Weight row of unit row r (0..31): SwiGLU pairs gate row f with up row Nout + f; the
+// routing-weighted GEMM takes 32 consecutive rows per unit (two 16-row MMA tiles against one
+// copy of the token rows); the others 16.
 __device__ __forceinline__ int64_t unit_row(const GroupedGemm& a, const Unit& x, int r) {
+  if (a.epi == EPI_WEIGHTED_F32) return x.e * a.Nw + (int64_t)x.rt * (2 * kRows) + r;
   return x.e * a.Nw + ((r >= kRows) ? a.Nout : 0) + (int64_t)x.rt * kRows + (r & (kRows - 1));
 }
+
+// Weight-row matrices per unit and output rows per unit.
+__host__ __device__ constexpr int unit_mats(int epi) { return (epi == EPI_SWIGLU || epi == EPI_WEIGHTED_F32) ? 2 : 1; }
+__host__ __device__ constexpr int unit_out_rows(int epi) { return epi == EPI_WEIGHTED_F32 ? 2 * kRows : kRows; }
 
 // E8M0 byte -> float bits: 2^(s-127); 0x00 -> 2^-127 (subnormal), 0xFF -> NaN.
 __device__ __forceinline__ float e8m0_fast(uint32_t s) {
@@ -330,7 +338,7 @@ __device__ __forceinline__ void issue_next(const GroupedGemm& a, Issuer<WF, NMAT
 // more bytes in flight per warp when there are few.
 template <int WF, int EPI, int R>
 __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm a) {
-  constexpr int NMAT = (EPI == EPI_SWIGLU) ? 2 : 1;
+  constexpr int NMAT = unit_mats(EPI);
   constexpr int NROWS = NMAT * kRows;
   constexpr bool MX = (WF != WF_BF16);
   constexpr bool ACT_E4M3 = (WF == WF_MXFP8);
@@ -354,7 +362,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
   const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
 
   // this block's run of live units
-  const int row_tiles = a.Nout / kRows;
+  const int row_tiles = a.Nout / unit_out_rows(EPI);
   const int64_t n_units = ((int64_t)*a.ntpp / a.bm) * row_tiles;
   const int64_t per = (n_units + gridDim.x - 1) / gridDim.x;
   const int64_t u_begin = blockIdx.x * per;
@@ -569,10 +577,14 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
             } else {
               static_cast<uint16_t*>(a.out)[(int64_t)p * a.Nout + n] = moe::f32_to_bf16_bits(hval);
             }
-          } else if (EPI == EPI_WEIGHTED_F32) {
-            float o = v[0][i];
-            if (bias) o += moe::bf16_bits_to_f32(bias[e * a.Nw + n]);
-            static_cast<float*>(a.out)[(int64_t)p * a.Nout + n] = o * a.topk_w[p];
+          } else if (EPI == EPI_WEIGHTED_F32) {  // rows rt * 32 + 16 m + (g, g + 8)
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) {
+              const int nm = cx.rt * (2 * kRows) + m * kRows + g + ((i >> 1) << 3);
+              float o = v[m][i];
+              if (bias) o += moe::bf16_bits_to_f32(bias[e * a.Nw + nm]);
+              static_cast<float*>(a.out)[(int64_t)p * a.Nout + nm] = o * a.topk_w[p];
+            }
           } else {
             float o = v[0][i];
             if (bias) o += moe::bf16_bits_to_f32(bias[e * a.Nw + n]);
@@ -601,7 +613,7 @@ int sm_count_dec() {
 // Resident blocks of the R-stage variant on the whole GPU (0 on error).
 template <int WF, int EPI, int R>
 int64_t resident_blocks(const GroupedGemm& g) {
-  const Smem L = smem_layout<WF, R>(EPI == EPI_SWIGLU ? 2 : 1, g.Kin);
+  const Smem L = smem_layout<WF, R>(unit_mats(EPI), g.Kin);
   if (cudaFuncSetAttribute(decode_gemm_kernel<WF, EPI, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) !=
       cudaSuccess)
     return 0;
@@ -614,11 +626,11 @@ int64_t resident_blocks(const GroupedGemm& g) {
 
 template <int WF, int EPI, int R>
 cudaError_t launch_t(const GroupedGemm& g, cudaStream_t stream) {
-  const Smem L = smem_layout<WF, R>(EPI == EPI_SWIGLU ? 2 : 1, g.Kin);
+  const Smem L = smem_layout<WF, R>(unit_mats(EPI), g.Kin);
   // enough resident blocks to keep every SM streaming; each owns a run of live units
   int64_t grid = resident_blocks<WF, EPI, R>(g);
   if (grid <= 0) return cudaErrorInvalidValue;
-  const int64_t units = g.grid_blocks * (g.Nout / kRows);
+  const int64_t units = g.grid_blocks * (g.Nout / unit_out_rows(EPI));
   if (units < grid) grid = units;
   if (grid <= 0) return cudaSuccess;
   decode_gemm_kernel<WF, EPI, R><<<(unsigned)grid, kWarps * 32, L.total, stream>>>(g);
@@ -633,7 +645,7 @@ template <int WF, int EPI>
 cudaError_t launch_r(const GroupedGemm& g, cudaStream_t stream) {
   if (WF == WF_MXFP4) return launch_t<WF, EPI, 2>(g, stream);
   if (WF == WF_BF16) {
-    const int64_t units = g.grid_blocks * (g.Nout / kRows);
+    const int64_t units = g.grid_blocks * (g.Nout / unit_out_rows(EPI));
     if (units <= 2 * resident_blocks<WF, EPI, 2>(g)) return launch_t<WF, EPI, 2>(g, stream);
     return launch_t<WF, EPI, 3>(g, stream);
   }
@@ -645,7 +657,7 @@ cudaError_t launch_r(const GroupedGemm& g, cudaStream_t stream) {
 namespace moe_launch {
 
 size_t decode_gemm_smem_bytes(const GroupedGemm& g) {
-  const int nmat = g.epi == EPI_SWIGLU ? 2 : 1;
+  const int nmat = unit_mats(g.epi);
   if (g.wfmt == WF_MXFP4) return smem_layout<WF_MXFP4, 2>(nmat, g.Kin).total;
   if (g.wfmt == WF_MXFP8) return smem_layout<WF_MXFP8, Pipe<WF_MXFP8>::R>(nmat, g.Kin).total;
   return smem_layout<WF_BF16, 3>(nmat, g.Kin).total;
