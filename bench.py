@@ -34,7 +34,7 @@ L2_BYTES = 129 * 1024 * 1024
 # hashes the same; otherwise reported as null.
 TRAFFIC = {
     "decode_gemm.cu:gemm1@decode_mxfp4": {  # profiles/decode_gemm_decode_mxfp4_T64.md
-        "src": "4952109009f6978b", "bytes": 997869056 + 4302848},
+        "src": "f6b2ff3ac8958c8e", "bytes": 997873152 + 4293888},
 }
 
 
