@@ -2,10 +2,11 @@
  * moe_gb300.h -- C ABI of the Mixture-of-Experts expert-layer hot path on GB300 (sm_103a).
  *
  * The path: top-k routing -> token-to-expert alignment (moe_align) -> geometric
- * token-dimension bucketing and padding (moe_bucket_pad) -> grouped GEMM1 + bias + SwiGLU ->
- * grouped GEMM2 + bias * routing weight -> top-k combine (moe_forward); a single grouped
- * GEMM over given operands (moe_grouped_gemm); and the per-expert weight gradient
- * (moe_wgrad).
+ * token-dimension bucketing and padding (moe_bucket_pad) -> grouped GEMM1 + bias + SwiGLU
+ * (or relu^2) -> grouped GEMM2 + bias * routing weight -> top-k combine (moe_forward; in
+ * MXFP8 with h quantised between the GEMMs, moe_mx_quantize); a single grouped GEMM over
+ * given operands (moe_grouped_gemm); a per-token-scaled FP8 grouped GEMM over per-expert
+ * group sizes (moe_gemm_per_token); and the per-expert weight gradient (moe_wgrad).
  *
  * Sources of the definitions (pull-request pages):
  *  [BUCKET] "Bound Triton MoE JIT specializations via token-dim bucketing and warmup",
