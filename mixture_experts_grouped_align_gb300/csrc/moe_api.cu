@@ -50,6 +50,15 @@ void rec(const moe_ctx* ctx, int i, int need) {
     cudaEventRecord(static_cast<cudaEvent_t>(ctx->events[i]), stream_of(ctx));
 }
 
+// T*k pairs index int32 slots: true when 0 <= T and T*k <= INT32_MAX, without forming an
+// overflowing product for huge T.
+bool pairs_fit(int64_t T, int32_t k) { return T >= 0 && k >= 1 && T <= INT32_MAX / k; }
+
+// An [E, N, Kin] weight array (elements) is indexed with int64 inside the kernels.
+bool weights_fit(int32_t E, int64_t N, int64_t Kin) {
+  return E >= 1 && N >= 1 && Kin >= 1 && N <= (INT64_MAX / 4) / Kin / E;
+}
+
 size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
 
 int64_t bucket_of(int64_t m) {
@@ -106,7 +115,7 @@ moe_status moe_align(const float* logits, int32_t* topk_ids, float* topk_w, int6
   MOE_REQUIRE(T >= 0, MOE_ERR_INVALID_ARG, "T must be >= 0");
   MOE_REQUIRE(k >= 1 && k <= 32 && E >= k && E <= 1024, MOE_ERR_UNSUPPORTED,
               "need 1 <= k <= 32 and k <= E <= 1024 (k=%d, E=%d)", k, E);
-  MOE_REQUIRE(T * k < ((int64_t)1 << 31), MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
+  MOE_REQUIRE(pairs_fit(T, k), MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
   MOE_REQUIRE(topk_ids && aligned16(topk_ids), MOE_ERR_INVALID_ARG,
               "topk_ids must be a 16-byte aligned device pointer");
   if (logits) {
@@ -269,7 +278,9 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
               "K and I must be positive multiples of 32");
   MOE_REQUIRE(T_rows >= 0 && T_real >= 0 && T_real <= T_rows, MOE_ERR_INVALID_ARG,
               "need 0 <= T_real <= T_rows");
-  MOE_REQUIRE(T_rows * k < ((int64_t)1 << 31), MOE_ERR_UNSUPPORTED, "T_rows*k must be < 2^31");
+  MOE_REQUIRE(pairs_fit(T_rows, k), MOE_ERR_UNSUPPORTED, "T_rows*k must be < 2^31");
+  MOE_REQUIRE(weights_fit(E, 2 * (int64_t)I, K) && weights_fit(E, K, I), MOE_ERR_UNSUPPORTED,
+              "weight arrays too large for 64-bit indexing");
   const bool fp4 = (W->quant == MOE_Q_MXFP4_W4A16);
   MOE_REQUIRE(W->w1 && W->w2 && x && topk_w && y, MOE_ERR_INVALID_ARG, "null tensor pointer");
   MOE_REQUIRE(!fp4 || (W->w1_scale && W->w2_scale), MOE_ERR_INVALID_ARG, "MXFP4 needs scales");
@@ -361,7 +372,8 @@ moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin, 
               "bad E, k or T");
   MOE_REQUIRE(N >= 16 && N % 16 == 0 && Kin >= 32 && Kin % 32 == 0, MOE_ERR_UNSUPPORTED,
               "N must be a multiple of 16 and Kin of 32");
-  MOE_REQUIRE(T * k < ((int64_t)1 << 31), MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
+  MOE_REQUIRE(weights_fit(E, N, Kin), MOE_ERR_UNSUPPORTED, "weight array too large for 64-bit indexing");
+  MOE_REQUIRE(pairs_fit(T, k), MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
   const bool mx8 = quant == MOE_Q_MXFP8, fp4 = quant == MOE_Q_MXFP4_W4A16;
   MOE_REQUIRE(a && w && out, MOE_ERR_INVALID_ARG, "null tensor pointer");
   MOE_REQUIRE(!(mx8 || fp4) || w_scale, MOE_ERR_INVALID_ARG, "MX weights need w_scale");
@@ -435,7 +447,7 @@ moe_status moe_wgrad(const void* grad, const void* input, int32_t input_per_pair
   MOE_REQUIRE(N >= 64 && N % 64 == 0 && Kin >= 64 && Kin % 64 == 0, MOE_ERR_UNSUPPORTED,
               "N and Kin must be multiples of 64");
   MOE_REQUIRE(N / 64 <= 65535 && Kin / 64 <= 65535, MOE_ERR_UNSUPPORTED, "N or Kin too large");
-  MOE_REQUIRE(T * k < ((int64_t)1 << 31), MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
+  MOE_REQUIRE(pairs_fit(T, k), MOE_ERR_UNSUPPORTED, "T*k must be < 2^31");
   MOE_REQUIRE(grad && input && dW, MOE_ERR_INVALID_ARG, "null tensor pointer");
   MOE_REQUIRE(aligned16(grad) && aligned16(input) && aligned16(dW), MOE_ERR_INVALID_ARG,
               "all pointers must be 16-byte aligned");

@@ -124,3 +124,27 @@ def test_argument_errors_are_reported_without_a_launch(lib):
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_gemm_per_token(8, 256, 256, 16, 16, 16, 16, None, None, 100, 16, moe.Ctx(stream=0))
     assert ei.value.status == -1            # no group sizes
+
+
+def test_size_overflow_is_rejected_before_any_launch(lib):
+    # T*k beyond int32 slot indices, including a T whose product with k overflows int64.
+    for T, k in ((1 << 30, 2), (1 << 62, 8), ((1 << 31) - 1, 1)):
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_align(None, 16, None, T, k, 8, 16, 16, 16, 16, 16)
+        if T * k >= 1 << 31:
+            assert ei.value.status == -2 and "2^31" in lib.moe_last_error().decode()
+        else:                                 # fits: then the capacity of 16 slots is short
+            assert ei.value.status == -3
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_wgrad(16, 16, 0, 1 << 62, 4, 8, 64, 64, 16, 16, 16, 16, 256, 16, 0, moe.Ctx(stream=0))
+    assert ei.value.status == -2
+    # An [E, N, Kin] weight array past 64-bit element indexing.
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_grouped_gemm("bf16", 1024, (1 << 31) - 16, (1 << 31) - 32, 16, None, 0, 16, None,
+                             None, 4, 2, 16, 16, 16, 16, 1 << 20, 16, moe.Ctx(stream=0))
+    assert ei.value.status == -2 and "64-bit" in lib.moe_last_error().decode()
+    big = moe.Ctx(stream=0, workspace=16, workspace_bytes=1 << 40)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_forward("bf16", 1024, (1 << 31) - 32, (1 << 31) - 32, 16, None, None, 16, None, None,
+                        16, None, 4, 4, 2, 16, 16, 16, 16, None, 16, 256, 16, big)
+    assert ei.value.status == -2 and "64-bit" in lib.moe_last_error().decode()
