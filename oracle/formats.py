@@ -43,7 +43,8 @@ def e4m3_decode(codes) -> np.ndarray:
 
 def bf16_decode(bits) -> np.ndarray:
     b = np.asarray(bits).astype(np.uint32) << 16
-    return b.view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):  # signalling-NaN patterns widen to NaN
+        return b.view(np.float32).astype(np.float64)
 
 
 def unpack_e2m1(packed) -> np.ndarray:
