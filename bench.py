@@ -20,6 +20,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -53,6 +54,8 @@ def parse():
     ap.add_argument("--experts", type=int, default=None,
                     help="experts of the mxfp8_wgrad workload (a smaller case for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-dir", default=None,
+                    help="directory for the raw clock samples of the timed region")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of replays of the step's CUDA graph")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
@@ -246,6 +249,14 @@ def run_oracle_subprocess(name, m, n_tok):
 
 # ------------------------------------------------------------------------------ clocks
 
+def clocks_csv(args, rank):
+    """Where the raw nvidia-smi samples of the timed region go (--clocks-dir, else the
+    system temporary directory); the JSON line carries their summary."""
+    d = args.clocks_dir or tempfile.gettempdir()
+    os.makedirs(d, exist_ok=True)
+    return os.path.join(d, f"clocks_rank{rank}.csv")
+
+
 class ClockSampler:
     def __init__(self, path):
         self.path = path
@@ -390,8 +401,7 @@ def bench_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
+    clocks = ClockSampler(clocks_csv(args, rank))
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
@@ -578,8 +588,7 @@ def bench_mxfp8_wgrad(args, rank, world, local_rank):
         raise RuntimeError(f"device status {int(status[0])}")
     evs = [[[ev(), ev()] for _ in range(4)] for _ in range(steps)]
     torch.cuda.synchronize()
-    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
+    clocks = ClockSampler(clocks_csv(args, rank))
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
@@ -720,8 +729,7 @@ def bench_pertoken(args, rank, world, local_rank):
         for e_ in pair:
             e_.record(stream)
     torch.cuda.synchronize()
-    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
+    clocks = ClockSampler(clocks_csv(args, rank))
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
@@ -838,8 +846,7 @@ def bench_mxfp8_layer(args, rank, world, local_rank):
         for e_ in quad:
             e_.record(stream)
     torch.cuda.synchronize()
-    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
+    clocks = ClockSampler(clocks_csv(args, rank))
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
