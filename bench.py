@@ -1,18 +1,25 @@
 #!/usr/bin/env python
 """Benchmark of the MoE expert-layer hot path on one or more GPUs (one process per GPU).
 
-Default workload: the decode-shaped W4A16 MXFP4 layer (T=64 tokens, hidden 2880,
-intermediate 2880, 128 experts, top-4, bf16 biases).  One step = bucket padding of the
-token dimension, routing + alignment, grouped GEMM1 + bias + SwiGLU, grouped GEMM2 + bias
-* routing weight, and the top-k combine, through the C ABI.
+Default run: the headline workload -- prefill with token-dimension bucketing: the W4A16
+MXFP4 layer (hidden 2880, intermediate 2880, 128 experts, top-4, bf16 biases) over 16
+requests of 3277..4096 tokens (58,879 tokens, padded to the bucket of 61,440 rows) -- timed
+for exactly --steps steps, and after it every other workload, each with its own line in the
+``workloads`` map: the tiny layer, the 64-token decode layer, the tiny-M bf16 decode layer
+at M = 1, 7, 14, 21, 28, the MXFP8 grouped GEMMs + weight gradients, the MXFP8 layer and the
+per-token FP8 grouped GEMM.  One step of a layer workload = bucket padding of the token
+dimension (W4A16 only), routing + alignment, grouped GEMM1 + bias + SwiGLU, grouped GEMM2 +
+bias * routing weight, and the top-k combine, through the C ABI.
 
 Prints one JSON line.  value = tokens/s over all ranks with inputs resident in HBM;
 e2e = the same metric with the step's inputs copied from pinned host memory and the
 output copied back inside the timed region; roofline = the dominant kernel's algorithmic
-bytes / its CUDA-event time against the measured HBM copy bandwidth; cpu_baseline = the
-float64 oracle timed on a bounded sample on this host (one thread).
+bytes (or flops) / its CUDA-event time against the measured HBM copy bandwidth (or bf16
+tensor peak); cpu_baseline = the float64 oracle timed on a bounded sample on this host, with
+every core available to its BLAS and with one thread.
 
-``--impl reference`` times that oracle alone (the reference arm), on rank 0.
+``--workload NAME`` runs one workload alone (smaller cases for profiling: --tokens,
+--experts).  ``--impl reference`` times the oracle alone (the reference arm), on rank 0.
 """
 import argparse
 import hashlib
@@ -31,10 +38,10 @@ METRIC = "MoE layer useful TFLOP/s & tokens/s; % of GB300 block-scaled TC / HBM 
 L2_BYTES = 129 * 1024 * 1024
 
 # DRAM traffic (read + write bytes) of one launch of the dominant kernel, from an ncu
-# capture of the same command (summary under profiles/), valid while the kernel source
-# hashes the same; otherwise reported as null.
+# capture of the same command, valid while the kernel source hashes the same; otherwise
+# reported as null.
 TRAFFIC = {
-    "decode_gemm.cu:gemm1@decode_mxfp4": {  # profiles/decode_gemm_decode_mxfp4_T64.md
+    "decode_gemm.cu:gemm1@decode_mxfp4": {
         "src": "f6b2ff3ac8958c8e", "bytes": 997873152 + 4293888},
 }
 
@@ -45,9 +52,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode_mxfp4",
-                    choices=["decode_mxfp4", "decode_bf16", "prefill_mxfp4", "tiny", "mxfp8_wgrad",
-                             "pertoken_fp8", "mxfp8_layer"])
+    ap.add_argument("--workload", default="all",
+                    choices=["all", "decode_mxfp4", "decode_bf16", "prefill_mxfp4", "tiny", "mxfp8_wgrad",
+                             "pertoken_fp8", "mxfp8_layer"],
+                    help="all (default): the prefill headline plus every other workload")
     ap.add_argument("--m", type=int, default=28, help="tokens for decode_bf16")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the token count (smaller cases for profiling)")
@@ -63,6 +71,13 @@ def parse():
     return ap.parse_args()
 
 
+HEADLINE = "prefill_mxfp4"
+# the other workloads of the default run, each with its own entry of the ``workloads`` map
+MAP_WORKLOADS = ["tiny", "decode_mxfp4"] + [f"decode_bf16_M{m}" for m in (1, 7, 14, 21, 28)] + \
+    ["mxfp8_wgrad", "mxfp8_layer", "pertoken_fp8"]
+# workloads whose expert weights would fit twice in the 129 MB L2: a 512 MB buffer is written
+# between their steps, outside the timed intervals
+L2_FLUSHED = {"tiny", "decode_bf16_M1"}
 DEFAULT_STEPS = {"decode_mxfp4": (2000, 50), "decode_bf16": (4000, 100),
                  "prefill_mxfp4": (10, 3), "tiny": (4000, 100), "mxfp8_wgrad": (3, 3),
                  "pertoken_fp8": (20, 3), "mxfp8_layer": (5, 3)}
@@ -154,10 +169,11 @@ def oracle_sample_mxfp8(n_tok):
     E, K, I, k = 2, w.K, w.I, 1
     T = n_tok
     ids = (np.arange(T) % E).astype(np.int32)[:, None]
-    xc, xs = synth.mx_quantise_e4m3(rng.standard_normal((T, K)).astype(np.float32))
-    ac, as_ = synth.mx_quantise_e4m3(rng.standard_normal((T, I)).astype(np.float32))
-    w1c, w1s = synth.mx_quantise_e4m3((rng.standard_normal((E, 2 * I, K)) * 0.02).astype(np.float32))
-    w2c, w2s = synth.mx_quantise_e4m3((rng.standard_normal((E, K, I)) * 0.02).astype(np.float32))
+    se = synth.scale_exp_for_std(w.weight_std)
+    xc, xs = synth.gen_mx_e4m3(rng, (T, K))
+    ac, as_ = synth.gen_mx_e4m3(rng, (T, I))
+    w1c, w1s = synth.gen_mx_e4m3(rng, (E, 2 * I, K), se)
+    w2c, w2s = synth.gen_mx_e4m3(rng, (E, K, I), se)
     g1 = synth.to_bf16_bits(rng.standard_normal((T, 2 * I)).astype(np.float32))
     g2 = synth.to_bf16_bits(rng.standard_normal((T, K)).astype(np.float32))
     xb = synth.to_bf16_bits(rng.standard_normal((T, K)).astype(np.float32))
@@ -200,9 +216,10 @@ def oracle_sample_mxfp8_layer(n_pairs):
     w = synth.MXFP8_WGRAD
     rng = np.random.default_rng(5)
     E, K, I = 2, w.K, w.I
-    xc, xs = synth.mx_quantise_e4m3(rng.standard_normal((n_pairs, K)).astype(np.float32))
-    w1c, w1s = synth.mx_quantise_e4m3((rng.standard_normal((E, 2 * I, K)) * 0.02).astype(np.float32))
-    w2c, w2s = synth.mx_quantise_e4m3((rng.standard_normal((E, K, I)) * 0.02).astype(np.float32))
+    se = synth.scale_exp_for_std(w.weight_std)
+    xc, xs = synth.gen_mx_e4m3(rng, (n_pairs, K))
+    w1c, w1s = synth.gen_mx_e4m3(rng, (E, 2 * I, K), se)
+    w2c, w2s = synth.gen_mx_e4m3(rng, (E, K, I), se)
     ids = (np.arange(n_pairs) % E).astype(np.int32)[:, None]
     wt = np.ones((n_pairs, 1), dtype=np.float32)
     t0 = time.perf_counter()
@@ -234,17 +251,40 @@ def oracle_sample(name, m, n_tok):
     return time.perf_counter() - t0, n
 
 
-def run_oracle_subprocess(name, m, n_tok):
+def run_oracle_subprocess(name, m, n_tok, threads=1, timeout=900):
+    """Runs oracle_sample in a fresh process whose BLAS / OpenMP pools have ``threads``
+    threads (and no GPU); returns {"seconds", "tokens"}."""
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
-        env[v] = "1"
+        env[v] = str(threads)
     env["CUDA_VISIBLE_DEVICES"] = ""
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", "--workload", name,
            "--m", str(m), "--sample-tokens", str(n_tok)]
-    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=timeout)
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
     return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def workload_name(base, m):
+    return f"decode_bf16_M{m}" if base == "decode_bf16" else base
+
+
+def layer_config(w, rows, world, flush):
+    """The ``config`` of a layer workload: its shapes and how the L2 is kept cold (the same
+    dict for both arms of the benchmark)."""
+    return dict(describe(w, rows),
+                l2=("L2 flushed between steps (a 512 MB buffer written outside the timed intervals): the "
+                    "step's expert weights would fit in the 129 MB L2" if flush else
+                    "inputs larger than L2: the expert weights streamed per step exceed the 129 MB L2"),
+                parallelism=f"replicas x{world}")
 
 
 # ------------------------------------------------------------------------------ clocks
@@ -409,7 +449,7 @@ def bench_ours(args, rank, world, local_rank):
     cur = torch.cuda.current_stream()
     # a step whose weights fit twice in L2 would be served from L2 by the previous step: such
     # workloads write a 512 MB buffer between steps, outside the timed intervals
-    flush = step_weight_bytes < 2 * L2_BYTES
+    flush = workload_name(args.workload, args.m) in L2_FLUSHED and not args.tokens
     if flush:
         scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
         pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
@@ -505,15 +545,10 @@ def bench_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": ("f16 tcgen05 mma -> f32" if tensor_path else "f16 mma -> f32") if w.quant != "bf16" else "bf16 mma -> f32",
         "data": "synthetic (seeded PCG64 inputs, random-init weights)",
-        "config": dict(describe(w, rows),
-                       l2=(f"L2 flushed between steps (512 MB written outside the timed intervals): "
-                           f"{step_weight_bytes / 1e9:.3f} GB of expert weights per step" if flush else
-                           f"inputs larger than L2: {step_weight_bytes / 1e9:.2f} GB "
-                           f"of expert weights streamed per step > 129 MB L2"),
-                       parallelism=f"replicas x{world}",
-                       timed=("replays of one CUDA graph of the whole step (every kernel of the step runs each "
-                              "replay); the per-kernel split comes from eager steps" if graph is not None
-                              else "eager launches")),
+        "config": layer_config(w, rows, world, flush),
+        "timing": ("replays of one CUDA graph of the whole step (every kernel of the step runs each replay); "
+                   "the per-kernel split comes from eager steps with the library's CUDA events"
+                   if graph is not None else "eager launches"),
         "useful_tflops": world * useful_flops(w) * steps / (ms * 1e-3) / 1e12,
         "layer_latency_us": ms_step * 1e3,
         "kernel_ms": {"gemm1_swiglu": g1, "gemm2_weighted": g2, "combine": cb,
@@ -693,22 +728,22 @@ def bench_pertoken(args, rank, world, local_rank):
     ids, _ = synth.zipf_topk_ids(rng, T, E, k, n_cold=min(16, E // 4))
     gs = np.bincount(ids.reshape(-1), minlength=E).astype(np.int32)
     M = int(gs.sum())
-    # per-token quantisation of N(0,1) activations and per-expert quantisation of N(0,0.02)
-    # weights to E4M3 (input preparation, outside the timed region)
+    # E4M3 codes of N(0, 64^2) values (truncated at 448) for activations and weights, with one
+    # scale per row drawn uniformly in [2^-7, 2^-5] and one per expert in [2^-13, 2^-11]
+    # (input preparation, outside the timed region)
     gen = torch.Generator(device=dev)
     gen.manual_seed(c["seed"])
-    x = torch.randn((M, K), device=dev, generator=gen)
-    a_scale = (x.abs().amax(dim=1) / 448.0).clamp_min(2.0 ** -30)
-    a = (x / a_scale[:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
-    del x
+
+    def codes(shape):
+        v = torch.randn(shape, device=dev, generator=gen) * 64.0
+        return v.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+
+    a = codes((M, K))
+    a_scale = torch.rand(M, device=dev, generator=gen) * (2.0 ** -5 - 2.0 ** -7) + 2.0 ** -7
     w = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
-    w_scale = torch.empty(E, dtype=torch.float32, device=dev)
     for e0 in range(0, E, 16):
-        v = torch.randn((min(16, E - e0), N, K), device=dev, generator=gen) * 0.02
-        s = (v.abs().amax(dim=(1, 2)) / 448.0).clamp_min(2.0 ** -30)
-        w[e0:e0 + v.shape[0]] = (v / s[:, None, None]).to(torch.float8_e4m3fn).view(torch.uint8)
-        w_scale[e0:e0 + v.shape[0]] = s
-        del v
+        w[e0:e0 + 16] = codes((min(16, E - e0), N, K))
+    w_scale = (torch.rand(E, device=dev, generator=gen) * (2.0 ** -11 - 2.0 ** -13) + 2.0 ** -13).float()
     a_scale = a_scale.float().contiguous()
     gsd = torch.from_numpy(gs).to(dev)
     out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -914,33 +949,68 @@ def launches_per_step(w, rows):
     n = 3  # GEMM1, GEMM2, combine
     n += 1  # align (routing fused for rows <= 512)
     if w.quant == "mxfp4":
-        n += 1  # x -> f16
+        n += 1  # x -> f16 (or gathered into slot order)
     if rows > 512:
-        n += 1
+        n += 1  # separate routing kernel
     if w.quant == "mxfp4":
         n += 2  # pad x, pad logits
     return n
 
 
-def cpu_baseline(args):
-    name = args.workload
-    n = args.sample_tokens or ORACLE_SAMPLE[name]
-    r = run_oracle_subprocess(name, args.m, n)
+def sample_text(name, n, r):
     if name == "mxfp8_layer":
-        what = (f"float64 oracle MXFP8 layer: {n} token-expert pairs over 2 experts "
-                f"({r['tokens']:g} tokens at top-8; {r['seconds']:.1f} s, one thread)")
-    elif name == "pertoken_fp8":
-        what = (f"float64 oracle: {n} rows of one expert of the per-token FP8 GEMM "
-                f"({r['tokens']:g} tokens at top-8; {r['seconds']:.1f} s, one thread)")
-    elif name == "mxfp8_wgrad":
-        what = (f"float64 oracle: both MXFP8 grouped GEMMs and both weight gradients for {n} "
-                f"token-expert pairs of 2 experts ({r['tokens']:g} tokens at top-8; "
-                f"{r['seconds']:.1f} s, one thread)")
+        return f"the MXFP8 layer for {n} token-expert pairs over 2 experts ({r['tokens']:g} tokens at top-8)"
+    if name == "pertoken_fp8":
+        return f"{n} rows of one expert of the per-token FP8 GEMM ({r['tokens']:g} tokens at top-8)"
+    if name == "mxfp8_wgrad":
+        return (f"both MXFP8 grouped GEMMs and both weight gradients for {n} token-expert pairs of 2 "
+                f"experts ({r['tokens']:g} tokens at top-8)")
+    return f"the first {r['tokens']} tokens of the workload"
+
+
+def cpu_baseline(name, m, n=None):
+    """The float64 oracle on a bounded sample of the workload, timed twice on this host:
+    with every core available to its BLAS / OpenMP pools, and with one thread."""
+    base = "decode_bf16" if name.startswith("decode_bf16_M") else name
+    n = n or ORACLE_SAMPLE[base]
+    cores = host_cores()
+    r_all = run_oracle_subprocess(base, m, n, threads=cores)
+    r_one = run_oracle_subprocess(base, m, n, threads=1)
+    return {"value": r_all["tokens"] / r_all["seconds"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"float64 oracle: {sample_text(base, n, r_all)}; {r_all['seconds']:.2f} s with "
+                      f"{cores} BLAS threads, {r_one['seconds']:.2f} s with one; input generation untimed",
+            "one_thread": {"value": r_one["tokens"] / r_one["seconds"], "cores": 1}}
+
+
+def run_workload(args, name, rank, world, local_rank, steps=None, warmup=None):
+    """One workload of the benchmark, by name (decode_bf16_M<m> for the tiny-M bf16 layer)."""
+    a = argparse.Namespace(**vars(args))
+    a.steps, a.warmup = steps, warmup
+    if name.startswith("decode_bf16_M"):
+        a.workload, a.m = "decode_bf16", int(name[len("decode_bf16_M"):])
     else:
-        what = (f"float64 oracle on the first {r['tokens']} tokens of the workload "
-                f"({r['seconds']:.1f} s, one thread)")
-    return {"value": r["tokens"] / r["seconds"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": what}
+        a.workload = name
+    if a.workload == "mxfp8_wgrad":
+        return bench_mxfp8_wgrad(a, rank, world, local_rank)
+    if a.workload == "pertoken_fp8":
+        return bench_pertoken(a, rank, world, local_rank)
+    if a.workload == "mxfp8_layer":
+        return bench_mxfp8_layer(a, rank, world, local_rank)
+    return bench_ours(a, rank, world, local_rank)
+
+
+# keys of a workload's own line that its entry in the ``workloads`` map keeps
+MAP_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config", "layer_latency_us",
+            "useful_tflops", "kernel_ms", "experts_touched", "roofline", "step_roofline", "e2e",
+            "gpu_launches", "clocks", "timing")
+
+
+def free_device_memory():
+    import gc
+    import torch
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
 
 def main():
@@ -953,56 +1023,72 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     if args.impl == "reference":
-        if rank != 0:
-            return
-        bench_reference(args)
+        if rank == 0:
+            bench_reference(args, world)
         return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    if args.workload == "mxfp8_wgrad":
-        line = bench_mxfp8_wgrad(args, rank, world, local_rank)
-    elif args.workload == "pertoken_fp8":
-        line = bench_pertoken(args, rank, world, local_rank)
-    elif args.workload == "mxfp8_layer":
-        line = bench_mxfp8_layer(args, rank, world, local_rank)
-    else:
-        line = bench_ours(args, rank, world, local_rank)
+    single = args.workload != "all"
+    head = args.workload if single else HEADLINE
+    line = run_workload(args, workload_name(head, args.m), rank, world, local_rank, args.steps, args.warmup)
+    workloads = {}
+    if not single:
+        for name in MAP_WORKLOADS:
+            free_device_memory()
+            sub = run_workload(args, name, rank, world, local_rank)
+            if rank == 0:
+                workloads[name] = {k: sub[k] for k in MAP_KEYS if k in sub}
     if rank == 0:
         if not args.no_cpu_baseline:
-            try:
-                line["cpu_baseline"] = cpu_baseline(args)
-            except Exception as e:  # reported, not fatal
-                line["cpu_baseline"] = {"error": str(e)[:300]}
+            for name, entry in [(workload_name(head, args.m), line)] + list(workloads.items()):
+                try:
+                    entry["cpu_baseline"] = cpu_baseline(name, args.m, args.sample_tokens if single else None)
+                except Exception as e:  # reported, not fatal
+                    entry["cpu_baseline"] = {"error": str(e)[:300]}
+        if workloads:
+            line["workloads"] = workloads
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
 
 
-def bench_reference(args):
-    """The reference arm: the float64 CPU oracle as it stands, one bounded sample per step."""
-    w = workload(args.workload, args.m)
-    steps, warmup = args.steps or 3, max(3, args.warmup or 3)
-    n = 1 if args.workload != "tiny" else 8
+def bench_reference(args, world):
+    """The reference arm: the float64 CPU oracle as it stands, on the headline workload (or
+    --workload), one bounded sample of that workload per step, every core available to its
+    BLAS."""
+    base = HEADLINE if args.workload == "all" else args.workload
+    w = workload(base, args.m)
+    steps, warmup = (args.steps if args.steps is not None else 3), max(3, args.warmup or 3)
+    n = 8 if base == "tiny" else 1
+    cores = host_cores()
     for _ in range(min(warmup, 1)):
-        run_oracle_subprocess(args.workload, args.m, n)
+        run_oracle_subprocess(base, args.m, n, threads=cores)
     secs, toks = 0.0, 0
     t_wall = time.perf_counter()
     for _ in range(steps):
-        r = run_oracle_subprocess(args.workload, args.m, n)
+        r = run_oracle_subprocess(base, args.m, n, threads=cores)
         secs += r["seconds"]
         toks += r["tokens"]
     wall = time.perf_counter() - t_wall
     v = toks / secs
+    if w is not None and base not in ("mxfp8_wgrad", "pertoken_fp8", "mxfp8_layer"):
+        rows = w.T
+        if w.quant == "mxfp4":
+            from oracle import bucket as obucket   # the padded row count the GPU arm reports
+            rows = obucket.bucket(w.T)
+        config = layer_config(w, rows, world, workload_name(base, args.m) in L2_FLUSHED)
+    else:
+        config = {"workload": base, "parallelism": f"replicas x{world}"}
+    # one host process ran it (n_gpus 1); the config is the GPU arm's at this world size
     line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1, "steps": steps,
             "warmup": warmup, "ms_per_step": secs / steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": (describe(w, w.T) if args.workload not in ("mxfp8_wgrad", "pertoken_fp8", "mxfp8_layer")
-                       else {"workload": args.workload}), "impl": "reference",
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{n} token(s) of the workload per step (float64 oracle, one "
-                                       f"thread; input generation untimed; wall {wall:.1f} s)"},
+            "config": config, "impl": "reference",
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{n} token(s) of the workload per step (float64 oracle, {cores} BLAS "
+                                       f"threads; input generation untimed; wall {wall:.1f} s)"},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 

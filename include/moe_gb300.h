@@ -177,7 +177,15 @@ typedef struct {
  * alignment-slot order and rows_h = rows_x = cap_tokens.  Returns 0 for a negative argument. */
 size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t I, int64_t cap_tokens);
 
-/* For every real token t < T_real (the others, e.g. bucket pad rows, are computed and
+/* One MoE expert layer over the alignment of moe_align: both grouped GEMMs run as single
+ * launches over every expert, each with an optional contiguous per-expert bias ([AITER]
+ * Summary: the grouped GEMM over all experts in one launch with per-expert bias), and
+ * token-dimension pad rows are computed like any other row but sliced off before the
+ * top-k reduction, so only rows t < T_real reach y ([BUCKET] Description: padded rows are
+ * removed ahead of the combine).  Blocks whose expert id is the -1 sentinel are skipped
+ * before any weight is read ([AITER] second review: return at once on the sentinel).
+ *
+ * For every real token t < T_real (the others, e.g. bucket pad rows, are computed and
  * then sliced off):
  *   gu = x_t . W1[e]^T + b1[e];  h = silu(gu[:I]) * gu[I:]  (SwiGLU) or
  *        h = max(gu, 0)^2  (relu^2; a NaN stays NaN)  (fp32, then stored as the MMA
@@ -216,9 +224,11 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
  * the library; every GPU that loads the library holds it until the process exits.
  *  - A call whose moe_forward_workspace_size exceeds the array returns MOE_ERR_CAPACITY
  *    (e.g. the 64-token, 2880/2880, top-4 layer needs about 4.8 MB and fits).
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call before any
- *    stream capture.
+ *  - Every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress).  The first call on a device also loads the library's device
+ *    code there; make that first call before any stream capture.
+ *  - An empty batch (T_rows == 0) returns MOE_OK, as moe_forward does; invalid arguments
+ *    are reported by moe_forward's own checks.
  *  - Every call shares the one array, which keeps the last call's contents.  Nothing in
  *    it has to start at zero: each call writes every scratch element it reads.  Calls
  *    that can overlap on the GPU (other streams, other host threads) race on the array:

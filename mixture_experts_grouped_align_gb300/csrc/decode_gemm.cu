@@ -599,16 +599,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_gemm_kernel(GroupedGemm
   if (bad) moe::set_status(a.status, MOE_ERR_RANGE);
 }
 
-int sm_count_dec() {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
-  }
-  return sms;
-}
+int sm_count_dec() { return moe_launch::sm_count_current(); }
 
 // Resident blocks of the R-stage variant on the whole GPU (0 on error).
 template <int WF, int EPI, int R>

@@ -13,13 +13,7 @@
 namespace {
 
 int grid_for(int64_t work, int threads) {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
-  }
+  const int sms = moe_launch::sm_count_current();
   int64_t need = (work + threads - 1) / threads;
   int64_t cap = (int64_t)sms * 8;
   return (int)(need < cap ? (need > 0 ? need : 1) : cap);

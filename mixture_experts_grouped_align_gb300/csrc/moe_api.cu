@@ -3,6 +3,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "moe_common.cuh"
 #include "moe_launch.h"
 
@@ -18,6 +20,25 @@ void set_error(const char* fmt, ...) {
 }
 
 }  // namespace moe_host
+
+namespace moe_launch {
+
+int sm_count_current() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  if (dev >= 0 && dev < kMaxDev) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  if (dev >= 0 && dev < kMaxDev && n > 1) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+}  // namespace moe_launch
 
 namespace {
 

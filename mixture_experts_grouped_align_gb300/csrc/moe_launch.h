@@ -6,6 +6,10 @@
 
 namespace moe_launch {
 
+// Streaming multiprocessors of the current device (cached per device index; 1 if the
+// query fails).
+int sm_count_current();
+
 // ---- route + align (route_align.cu)
 size_t align_smem_bytes(int E);
 cudaError_t align(const float* logits, int32_t* ids, float* w, int64_t T, int k, int E, int bm,

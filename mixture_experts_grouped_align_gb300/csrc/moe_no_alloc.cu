@@ -8,48 +8,28 @@
 // For them the layer's scratch (h, o and the f16 copy of x) lives in a file-scope
 // device array of kNoAllocScratchBytes.  Every GPU that loads this library holds that
 // array until the process exits.
-#include <mutex>
-
 #include "moe_common.cuh"
 
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = MOE_NO_ALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 // The scratch.  Host code must not pass this symbol to a kernel: on the host it names a
 // host-side stand-in, not device memory.  Its device address comes from
-// cudaGetSymbolAddress, once per device.
+// cudaGetSymbolAddress on the current device.
 static __device__ __align__(256) uint8_t g_no_alloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the scratch on the current device (looked up on the first call
-// made on that device).
+// Device address of the scratch on the current device.  Looked up on every call (the
+// lookup allocates nothing and is cheap once the library's module is loaded on the
+// device), so a context torn down and created again never leaves a stale address.
 moe_status scratch_address(void** out) {
-  int dev = -1;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) {
-    moe_host::set_error("moe_forward_no_alloc: cudaGetDevice: %s", cudaGetErrorString(err));
+  void* p = nullptr;
+  const cudaError_t err = cudaGetSymbolAddress(&p, g_no_alloc_scratch);
+  if (err != cudaSuccess || !p) {
+    moe_host::set_error("moe_forward_no_alloc: cudaGetSymbolAddress: %s", cudaGetErrorString(err));
     return MOE_ERR_CUDA;
   }
-  if (dev < 0 || dev >= kMaxDevices) {
-    moe_host::set_error("moe_forward_no_alloc: device %d out of range", dev);
-    return MOE_ERR_UNSUPPORTED;
-  }
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_no_alloc_scratch);
-    if (err != cudaSuccess || !p) {
-      moe_host::set_error("moe_forward_no_alloc: cudaGetSymbolAddress: %s",
-                          cudaGetErrorString(err));
-      return MOE_ERR_CUDA;
-    }
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return MOE_OK;
 }
 
@@ -64,8 +44,10 @@ extern "C" moe_status moe_forward_no_alloc(
     moe_host::set_error("moe_forward_no_alloc: null weights");
     return MOE_ERR_INVALID_ARG;
   }
+  // Only the size is checked here; moe_forward validates every argument itself (invalid
+  // sizes give a workspace size of 0, which always fits, and are then rejected there).
   const size_t need = moe_forward_workspace_size(T_rows, k, W->K, W->I, cap_tokens);
-  if (need == 0 || need > kNoAllocScratchBytes) {
+  if (need > kNoAllocScratchBytes) {
     moe_host::set_error(
         "moe_forward_no_alloc: the call needs %zu bytes of scratch; the fixed array holds %zu "
         "(use moe_forward with a workspace for larger calls)",

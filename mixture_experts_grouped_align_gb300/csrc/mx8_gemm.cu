@@ -403,16 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
   }
 }
 
-int sm_count_mx8() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
-}
+int sm_count_mx8() { return moe_launch::sm_count_current(); }
 
 template <int EPI>
 cudaError_t launch_mx8(const MArgs& ma, const CUtensorMap& tmap, cudaStream_t stream) {

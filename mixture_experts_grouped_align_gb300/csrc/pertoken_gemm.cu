@@ -340,16 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) pertoken_gemm_kernel(const __grid
   }
 }
 
-int sm_count_pt() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
-}
+int sm_count_pt() { return moe_launch::sm_count_current(); }
 
 }  // namespace
 

@@ -485,16 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(PArgs pa) {
   }
 }
 
-int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
-}
+int sm_count() { return moe_launch::sm_count_current(); }
 
 template <int WF, int EPI, bool AE>
 cudaError_t launch_t(const PArgs& pa, cudaStream_t stream) {

@@ -557,16 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-int sm_count_ts() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
-}
+int sm_count_ts() { return moe_launch::sm_count_current(); }
 
 template <int EPI>
 cudaError_t launch_ts(const TArgs& ta, const CUtensorMap& mx, const CUtensorMap& mw, const CUtensorMap& mh,

@@ -293,16 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_tc_kernel(WArgs wa) {
   }
 }
 
-int sm_count_w() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
-}
+int sm_count_w() { return moe_launch::sm_count_current(); }
 
 }  // namespace
 

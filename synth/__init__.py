@@ -17,7 +17,8 @@ Workloads (each named by what it is, with its sizes):
 * ``decode_bf16``     128 experts, hidden 2688, GEMM1 N=1856 (intermediate 928), top-6,
                       bf16 weights ~N(0, 0.02), M in {1, 7, 14, 21, 28}, seed 3.
 * ``mxfp8_wgrad``     256 experts, hidden 7168, intermediate 2048, top-8, T=8192; E4M3
-                      operands with one E8M0 scale per 32 along K, routing drawn from a
+                      operands with one E8M0 scale per 32 along K (codes and scale bytes
+                      drawn directly, see gen_mx_e4m3), routing drawn from a
                       Zipf(1.1) law over a seeded expert permutation with 16 cold experts,
                       bf16 output gradients ~N(0, 1), seed 4.
 
@@ -150,23 +151,31 @@ def gen_bf16_weight(rng, E, N, K, std):
     return to_bf16_bits(rng.standard_normal((E, N, K), dtype=np.float32) * np.float32(std))
 
 
-def mx_quantise_e4m3(values: np.ndarray):
-    """Quantise float values [..., K] to E4M3 codes with one E8M0 scale per 32 along K.
+# MXFP8 operands are drawn directly as codes and scales: E4M3 codes are the torch cast of
+# normal values of standard deviation E4M3_CODE_STD (truncated at the largest E4M3 value,
+# 448, which a 7-sigma draw reaches), and each 32-element block gets its own E8M0 scale
+# byte 127 + U{lo..hi}.  The decoded operand code * 2^(byte - 127) then has roughly the
+# standard deviation E4M3_CODE_STD * 2^e of the workload's values.
+E4M3_CODE_STD = 64.0
+ACT_SCALE_EXP = (-7, -5)        # activations ~ N(0, 1): 64 * 2^-6 = 1
 
-    The scale of a block is 2^(floor(log2(amax)) - 8) (8 = the largest E4M3 exponent),
-    the rule of the OCP microscaling specification; elements are divided by it, clamped
-    to +-448 and cast with round-to-nearest-even.  Used only to make inputs.
-    """
-    v = np.asarray(values, dtype=np.float32)
-    K = v.shape[-1]
-    blk = v.reshape(*v.shape[:-1], K // 32, 32)
-    amax = np.abs(blk).max(axis=-1)
-    e = np.where(amax > 0, np.floor(np.log2(np.maximum(amax, 1e-38))) - 8, -127)
-    e = np.clip(e, -127, 127).astype(np.int32)
-    scaled_v = blk / np.ldexp(np.float32(1.0), e)[..., None]
-    scaled_v = np.clip(scaled_v, -448.0, 448.0).reshape(v.shape)
-    codes = to_e4m3_codes(scaled_v)
-    return codes, (e + 127).astype(np.uint8)
+
+def scale_exp_for_std(std: float) -> tuple:
+    """E8M0 exponent offsets whose middle value scales E4M3_CODE_STD codes to ``std``."""
+    c = int(np.round(np.log2(std / E4M3_CODE_STD)))
+    return (c - 1, c + 1)
+
+
+def gen_mx_e4m3(rng, shape, scale_exp=ACT_SCALE_EXP):
+    """E4M3 codes of ``shape`` (last axis a multiple of 32) and E8M0 scale bytes
+    [..., shape[-1] / 32], drawn as described above (numpy PCG64 generator)."""
+    shape = tuple(shape)
+    v = rng.standard_normal(shape, dtype=np.float32) * np.float32(E4M3_CODE_STD)
+    np.clip(v, -448.0, 448.0, out=v)
+    codes = to_e4m3_codes(v)
+    lo, hi = scale_exp
+    scales = (127 + rng.integers(lo, hi + 1, size=shape[:-1] + (shape[-1] // 32,))).astype(np.uint8)
+    return codes, scales
 
 
 def zipf_topk_ids(rng, T, E, k, s=ZIPF_S, n_cold=ZIPF_COLD_EXPERTS):
@@ -199,8 +208,7 @@ def make_layer(w: Workload, T: int | None = None, with_logits: bool = True):
     out = {"workload": w, "T": T}
     r_act, r_log, r_w1, r_w2, r_b = (rng_for(w.seed, s) for s in range(5))
     if w.quant == "mxfp8":
-        xv = r_act.standard_normal((T, w.K), dtype=np.float32)
-        out["x_codes"], out["x_scale"] = mx_quantise_e4m3(xv)
+        out["x_codes"], out["x_scale"] = gen_mx_e4m3(r_act, (T, w.K))
     else:
         out["x"] = gen_activations_bf16(r_act, T, w.K)
     if with_logits:
@@ -213,10 +221,9 @@ def make_layer(w: Workload, T: int | None = None, with_logits: bool = True):
         out["w2"] = gen_bf16_weight(r_w2, w.E, w.K, w.I, w.weight_std)
         out["w1_scale"] = out["w2_scale"] = None
     elif w.quant == "mxfp8":
-        v1 = r_w1.standard_normal((w.E, w.n1, w.K), dtype=np.float32) * np.float32(w.weight_std)
-        out["w1"], out["w1_scale"] = mx_quantise_e4m3(v1)
-        v2 = r_w2.standard_normal((w.E, w.K, w.I), dtype=np.float32) * np.float32(w.weight_std)
-        out["w2"], out["w2_scale"] = mx_quantise_e4m3(v2)
+        se = scale_exp_for_std(w.weight_std)
+        out["w1"], out["w1_scale"] = gen_mx_e4m3(r_w1, (w.E, w.n1, w.K), se)
+        out["w2"], out["w2_scale"] = gen_mx_e4m3(r_w2, (w.E, w.K, w.I), se)
     else:
         raise ValueError(w.quant)
     if w.bias:
@@ -263,10 +270,11 @@ def make_mxfp8_gemm_wgrad(w: Workload = MXFP8_WGRAD, T: int | None = None, E: in
     out = {"T": T, "E": E, "K": K, "I": I, "k": k, "P": P, "topk_ids": ids, "cold": cold}
     if device is None:
         rs = [rng_for(w.seed, 11 + i) for i in range(8)]
-        out["x_codes"], out["x_scale"] = mx_quantise_e4m3(rs[0].standard_normal((T, K), dtype=np.float32))
-        out["a2_codes"], out["a2_scale"] = mx_quantise_e4m3(rs[1].standard_normal((P, I), dtype=np.float32))
-        out["w1"], out["w1_scale"] = mx_quantise_e4m3(rs[2].standard_normal((E, 2 * I, K), dtype=np.float32) * np.float32(w.weight_std))
-        out["w2"], out["w2_scale"] = mx_quantise_e4m3(rs[3].standard_normal((E, K, I), dtype=np.float32) * np.float32(w.weight_std))
+        se = scale_exp_for_std(w.weight_std)
+        out["x_codes"], out["x_scale"] = gen_mx_e4m3(rs[0], (T, K))
+        out["a2_codes"], out["a2_scale"] = gen_mx_e4m3(rs[1], (P, I))
+        out["w1"], out["w1_scale"] = gen_mx_e4m3(rs[2], (E, 2 * I, K), se)
+        out["w2"], out["w2_scale"] = gen_mx_e4m3(rs[3], (E, K, I), se)
         out["x_bf16"] = gen_activations_bf16(rs[4], T, K)
         out["h_bf16"] = gen_activations_bf16(rs[5], P, I)
         out["grad1"] = gen_activations_bf16(rs[6], P, 2 * I)
@@ -274,24 +282,23 @@ def make_mxfp8_gemm_wgrad(w: Workload = MXFP8_WGRAD, T: int | None = None, E: in
         return out
     g = torch.Generator(device=device)
 
-    def dev_quant(shape, std, sub):
+    def dev_mx(shape, scale_exp, sub):
         g.manual_seed(w.seed * 1000 + sub)
-        v = torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std
-        blk = v.view(*shape[:-1], shape[-1] // 32, 32)
-        amax = blk.abs().amax(dim=-1)
-        e = torch.where(amax > 0, torch.floor(torch.log2(amax.clamp_min(1e-38))) - 8,
-                        torch.full_like(amax, -127)).clamp(-127, 127)
-        sv = (blk / torch.exp2(e)[..., None]).clamp(-448.0, 448.0).view(shape)
-        codes = sv.to(torch.float8_e4m3fn).view(torch.uint8)
-        del v, blk, sv
-        return codes.contiguous(), (e + 127).to(torch.uint8).contiguous()
+        v = torch.randn(shape, generator=g, device=device, dtype=torch.float32) * E4M3_CODE_STD
+        codes = v.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        del v
+        lo, hi = scale_exp
+        sc = torch.randint(127 + lo, 127 + hi + 1, shape[:-1] + (shape[-1] // 32,), generator=g,
+                           device=device, dtype=torch.int32).to(torch.uint8)
+        return codes.contiguous(), sc.contiguous()
 
     def dev_bf16(shape, sub):
         g.manual_seed(w.seed * 1000 + sub)
         return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
-    out["x_codes"], out["x_scale"] = dev_quant((T, K), 1.0, 1)
-    out["a2_codes"], out["a2_scale"] = dev_quant((P, I), 1.0, 2)
+    se = scale_exp_for_std(w.weight_std)
+    out["x_codes"], out["x_scale"] = dev_mx((T, K), ACT_SCALE_EXP, 1)
+    out["a2_codes"], out["a2_scale"] = dev_mx((P, I), ACT_SCALE_EXP, 2)
     # weights are drawn one expert slab at a time to bound the float32 temporaries
     w1c = torch.empty((E, 2 * I, K), dtype=torch.uint8, device=device)
     w1s = torch.empty((E, 2 * I, K // 32), dtype=torch.uint8, device=device)
@@ -300,9 +307,9 @@ def make_mxfp8_gemm_wgrad(w: Workload = MXFP8_WGRAD, T: int | None = None, E: in
     step = 16
     for e0 in range(0, E, step):
         e1 = min(E, e0 + step)
-        c, s = dev_quant((e1 - e0, 2 * I, K), w.weight_std, 100 + e0)
+        c, s = dev_mx((e1 - e0, 2 * I, K), se, 100 + e0)
         w1c[e0:e1].copy_(c), w1s[e0:e1].copy_(s)
-        c, s = dev_quant((e1 - e0, K, I), w.weight_std, 5000 + e0)
+        c, s = dev_mx((e1 - e0, K, I), se, 5000 + e0)
         w2c[e0:e1].copy_(c), w2s[e0:e1].copy_(s)
     out["w1"], out["w1_scale"], out["w2"], out["w2_scale"] = w1c, w1s, w2c, w2s
     out["x_bf16"] = dev_bf16((T, K), 3)

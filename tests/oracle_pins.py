@@ -641,6 +641,61 @@ def check_layer_mxfp8_constant_closed_form():
         assert np.allclose(y[t], float(wt[t].astype(np.float64).sum()) * o, rtol=1e-14, atol=0)
 
 
+
+def check_layer_mxfp8_brute_rows(seed=23):
+    """Distinct features within and across 32-blocks: the MXFP8 layer against a brute force
+    written pair by pair -- E4M3 codes decoded through torch's float8_e4m3fn cast, E8M0 as
+    2^(byte - 127), every dot product a math.fsum, silu with math.exp, and each pair's h
+    row quantised on its own, block by block (scale 2^(floor(log2 amax) - 8), codes by
+    torch's E4M3 cast of the saturated quotient) -- so that quantising h along the wrong
+    axis, with the wrong block grouping or with scales in the wrong block order changes
+    the result."""
+    rng = np.random.default_rng(seed)
+    T, K, I, E, k = 5, 64, 96, 3, 2
+
+    def draw(shape, lo, hi):
+        v = np.clip(rng.standard_normal(shape) * 64.0, -448, 448).astype(np.float32)
+        codes = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+        return codes, (127 + rng.integers(lo, hi + 1, shape[:-1] + (shape[-1] // 32,))).astype(np.uint8)
+
+    x, xs = draw((T, K), -7, -5)
+    w1, w1s = draw((E, 2 * I, K), -11, -8)
+    w2, w2s = draw((E, K, I), -12, -9)
+    b1 = rng.standard_normal((E, 2 * I)) * 0.1
+    b2 = rng.standard_normal((E, K)) * 0.1
+    b1 = torch.from_numpy(b1).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    b2 = torch.from_numpy(b2).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ids = np.array([[0, 1], [2, 0], [1, 2], [0, 2], [2, 1]], dtype=np.int32)
+    wt = np.array([[0.7, 0.3], [0.5, 0.5], [0.9, 0.1], [0.25, 0.75], [0.6, 0.4]], dtype=np.float32)
+
+    def dec(codes, scales):
+        c = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        return c * np.repeat(2.0 ** (scales.astype(np.float64) - 127), 32, axis=-1)
+
+    def bf(b):
+        return torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+
+    xd = dec(x, xs)
+    want = np.zeros((T, K))
+    for t in range(T):
+        for j in range(k):
+            e = ids[t, j]
+            W1, W2 = dec(w1[e], w1s[e]), dec(w2[e], w2s[e])
+            gu = [math.fsum(xd[t, kk] * W1[n, kk] for kk in range(K)) + bf(b1[e])[n] for n in range(2 * I)]
+            h = np.array([gu[f] / (1.0 + math.exp(-gu[f])) * gu[I + f] for f in range(I)])
+            hd = np.empty(I)
+            for b0 in range(0, I, 32):      # OCP rule, one block at a time, E4M3 by torch's cast
+                blk = h[b0:b0 + 32]
+                ex = math.frexp(float(np.abs(blk).max()))[1] - 1 - 8
+                q = np.clip(blk * 2.0 ** -ex, -448.0, 448.0)
+                hd[b0:b0 + 32] = torch.from_numpy(q).to(torch.float8_e4m3fn).to(torch.float64).numpy() * 2.0 ** ex
+            o = [math.fsum(hd[f] * W2[c, f] for f in range(I)) + bf(b2[e])[c] for c in range(K)]
+            want[t] += float(wt[t, j]) * np.array(o)
+    W = layer.ExpertWeights("mxfp8", w1, w1s, b1, w2, w2s, b2)
+    got = layer.moe_layer(formats.dequant_mxfp8(x, xs), ids, wt, W)
+    # h itself must vary within and across blocks, or the check proves nothing
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+
 ALL_CHECKS = [
     check_e2m1_table, check_e8m0_vs_torch, check_e4m3_vs_torch, check_bf16_vs_torch,
     check_mxfp4_dequant_layout, check_bucket_count_20000, check_pad_restriction,
@@ -653,4 +708,5 @@ ALL_CHECKS = [
     check_per_token_scale_linearity, check_e4m3_encode_vs_torch,
     check_e4m3_encode_saturates_and_round_trips, check_mx_quantize_scale_rule,
     check_mx_quantize_error_bound, check_layer_mxfp8_constant_closed_form,
+    check_layer_mxfp8_brute_rows,
 ]

@@ -62,8 +62,8 @@ def test_mxfp8_small(moe, T, per_pair, bias):
     E, k, N, Kin = 12, 3, 96, 320
     ids = random_ids(rng, T, E, k, empty=(5,))
     rows = T * k if per_pair else T
-    a_c, a_s = synth.mx_quantise_e4m3(rng.standard_normal((rows, Kin)).astype(np.float32))
-    w_c, w_s = synth.mx_quantise_e4m3((rng.standard_normal((E, N, Kin)) * 0.05).astype(np.float32))
+    a_c, a_s = synth.gen_mx_e4m3(rng, (rows, Kin))
+    w_c, w_s = synth.gen_mx_e4m3(rng, (E, N, Kin), synth.scale_exp_for_std(0.05))
     b = synth.to_bf16_bits(rng.standard_normal((E, N)) * 0.1) if bias else None
     out = gemm_dev(moe, "mxfp8", E, N, Kin, dev(a_c), dev(a_s), per_pair, dev(w_c), dev(w_s),
                    dev(b), ids)
@@ -160,8 +160,8 @@ def test_mxfp8_block_scaled(moe, N, per_pair, bias, Kin):
     T, E, k = 700, 12, 3
     ids = random_ids(rng, T, E, k, empty=(5, 9))
     rows = T * k if per_pair else T
-    a_c, a_s = synth.mx_quantise_e4m3(rng.standard_normal((rows, Kin)).astype(np.float32))
-    w_c, w_s = synth.mx_quantise_e4m3((rng.standard_normal((E, N, Kin)) * 0.05).astype(np.float32))
+    a_c, a_s = synth.gen_mx_e4m3(rng, (rows, Kin))
+    w_c, w_s = synth.gen_mx_e4m3(rng, (E, N, Kin), synth.scale_exp_for_std(0.05))
     b = synth.to_bf16_bits(rng.standard_normal((E, N)) * 0.1) if bias else None
     out = gemm_dev(moe, "mxfp8", E, N, Kin, dev(a_c), dev(a_s), per_pair, dev(w_c), dev(w_s),
                    dev(b), ids)
@@ -193,8 +193,8 @@ def test_mxfp8_block_scaled_scale_edges(moe):
     rng = np.random.default_rng(17)
     T, E, k, N, Kin = 300, 4, 2, 128, 256
     ids = random_ids(rng, T, E, k)
-    a_c, a_s = synth.mx_quantise_e4m3(rng.standard_normal((T, Kin)).astype(np.float32))
-    w_c, w_s = synth.mx_quantise_e4m3((rng.standard_normal((E, N, Kin)) * 0.05).astype(np.float32))
+    a_c, a_s = synth.gen_mx_e4m3(rng, (T, Kin))
+    w_c, w_s = synth.gen_mx_e4m3(rng, (E, N, Kin), synth.scale_exp_for_std(0.05))
     a_s[:, 2] = 127 + 125
     w_s[:, :, 2] = 0x00
     w_s[2, 3:5, 1] = 0xFF

@@ -97,3 +97,57 @@ def test_mxfp8_layer_paths_agree(moe):
     ref = oracle_layer(w, lay, 256)
     assert_close_bf16(y257, ref, what="block-scaled path")
     assert_close_bf16(y256, ref, what="weight-streaming path")
+
+
+class _DeviceRows:
+    """Rows of a device tensor brought to the host on indexing (codes, or codes decoded
+    with their scales), so that the oracle reads only the rows it needs."""
+
+    def __init__(self, codes, scales=None):
+        self.codes, self.scales = codes, scales
+        self.shape = tuple(codes.shape)
+
+    def __getitem__(self, idx):
+        i = torch.as_tensor(np.asarray(idx), device=self.codes.device)
+        c = self.codes[i].cpu().numpy()
+        return c if self.scales is None else ofmt.dequant_mxfp8(c, self.scales[i].cpu().numpy())
+
+
+def test_mxfp8_layer_full_size_sampled(moe):
+    """The whole MXFP8 layer at the size of the MXFP8 workload -- 256 experts, hidden 7168,
+    intermediate 2048, top-8, T = 8192, Zipf(1.1) routing with cold experts, operands drawn
+    on the device -- through moe_forward (block-scaled kernels, SwiGLU and the MXFP8
+    quantiser fused in GEMM1's epilogue, the routing-weighted GEMM2, the combine).  Eight
+    tokens routed to the hottest experts are checked against the oracle layer."""
+    g = synth.make_mxfp8_gemm_wgrad(device="cuda")
+    T, E, K, I, k, P = g["T"], g["E"], g["K"], g["I"], g["k"], g["P"]
+    for n in ("grad1", "grad2", "x_bf16", "h_bf16", "a2_codes", "a2_scale"):
+        g.pop(n)
+    torch.cuda.empty_cache()
+    ids = g["topk_ids"]
+    rng = np.random.default_rng(5)
+    wt = rng.uniform(0.1, 1.0, (T, k)).astype(np.float32)
+    wt /= wt.sum(axis=1, keepdims=True)
+    bm = 128
+    cap, capb = moe.moe_align_capacity(P, E, bm)
+    srt = torch.empty(cap, dtype=torch.int32, device="cuda")
+    eid = torch.empty(capb, dtype=torch.int32, device="cuda")
+    ntpp = torch.empty(4, dtype=torch.int32, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    moe.moe_align(None, dev(ids), None, T, k, E, bm, srt, cap, eid, ntpp, None, moe.Ctx(dev_status=status))
+    ws = torch.empty(moe.moe_forward_workspace_size(T, k, K, I, cap), dtype=torch.uint8, device="cuda")
+    y = torch.full((T, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward("mxfp8", E, K, I, g["w1"], g["w1_scale"], None, g["w2"], g["w2_scale"], None,
+                    g["x_codes"], g["x_scale"], T, T, k, dev(wt), srt, eid, ntpp, None, bm, cap, y,
+                    moe.Ctx(workspace=ws, dev_status=status))
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    assert bool(torch.isfinite(y.float()).all())
+    cnt = np.bincount(ids.reshape(-1), minlength=E)
+    hot = cnt[ids].sum(axis=1)                       # tokens whose experts are the busiest
+    tokens = np.sort(np.argsort(-hot, kind="stable")[:8])
+    W = olayer.ExpertWeights("mxfp8", _DeviceRows(g["w1"]), _DeviceRows(g["w1_scale"]), None,
+                             _DeviceRows(g["w2"]), _DeviceRows(g["w2_scale"]), None)
+    ref = olayer.moe_layer(_DeviceRows(g["x_codes"], g["x_scale"]), ids, wt, W, tokens=tokens)
+    got = bf16_to_np(y[torch.from_numpy(tokens).cuda()])
+    assert_close_bf16(got, ref, what="MXFP8 layer, full size")

@@ -266,6 +266,47 @@ def mut_mxfp8_layer_skips_quantiser(monkeypatch):
     return [pins.check_layer_mxfp8_constant_closed_form]
 
 
+
+def mut_mxfp8_h_blocks_strided(monkeypatch):
+    # h quantised with the wrong block grouping: block b holds features b, b + C/32, ...
+    orig = mx_quant.mx_quantize
+
+    def q(x):
+        x = np.asarray(x, dtype=np.float64)
+        C = x.shape[-1]
+        xt = x.reshape(*x.shape[:-1], 32, C // 32).swapaxes(-1, -2).reshape(x.shape)
+        c, s_ = orig(xt)
+        c = c.reshape(*x.shape[:-1], C // 32, 32).swapaxes(-1, -2).reshape(x.shape)
+        return c, s_
+    monkeypatch.setattr(mx_quant, "mx_quantize", q)
+    return [pins.check_layer_mxfp8_constant_closed_form, pins.check_layer_mxfp8_brute_rows]
+
+
+def mut_mxfp8_h_scales_reversed(monkeypatch):
+    # the scales of h applied to the blocks in reverse order
+    orig = mx_quant.mx_quantize
+    monkeypatch.setattr(mx_quant, "mx_quantize", lambda x: (orig(x)[0], orig(x)[1][..., ::-1].copy()))
+    return [pins.check_layer_mxfp8_constant_closed_form, pins.check_layer_mxfp8_brute_rows]
+
+
+def mut_mxfp8_h_quantised_over_tokens(monkeypatch):
+    # h quantised along the token axis of each expert's rows (blocks run down the columns)
+    orig = mx_quant.mx_quantize
+
+    def q(x):
+        x = np.asarray(x, dtype=np.float64)
+        if x.ndim != 2:
+            return orig(x)
+        n, C = x.shape
+        pad = (-n) % 32
+        xp = np.concatenate([x, np.zeros((pad, C))], axis=0)
+        c, s_ = orig(xp.T)
+        codes = c.T[:n]
+        scale_rows = np.repeat(s_.T, 32, axis=0)[:n]          # [n, C] one scale per element
+        return codes, scale_rows[:, ::32].copy()
+    monkeypatch.setattr(mx_quant, "mx_quantize", q)
+    return [pins.check_layer_mxfp8_constant_closed_form, pins.check_layer_mxfp8_brute_rows]
+
 MUTATIONS = [mut_e8m0_zero, mut_nibble_order, mut_e2m1_subnormal, mut_e4m3_bias,
              mut_bucket_floor2, mut_bucket_16_per_octave, mut_route_tie_high,
              mut_route_full_softmax, mut_align_unstable, mut_align_sentinel_zero,
@@ -274,7 +315,8 @@ MUTATIONS = [mut_e8m0_zero, mut_nibble_order, mut_e2m1_subnormal, mut_e4m3_bias,
              mut_relu2_runs_swiglu, mut_per_token_offsets_inclusive,
              mut_per_token_scale_of_next_row, mut_per_token_weight_scale_dropped,
              mut_mx_scale_ceil, mut_mx_emax_7, mut_e4m3_ties_away, mut_e4m3_no_saturation,
-             mut_mxfp8_layer_skips_quantiser,
+             mut_mxfp8_layer_skips_quantiser, mut_mxfp8_h_blocks_strided,
+             mut_mxfp8_h_scales_reversed, mut_mxfp8_h_quantised_over_tokens,
              mut_gemm_src_per_pair, mut_wgrad_transposed, mut_wgrad_src_index]
 
 
