@@ -315,6 +315,22 @@ moe_status moe_wgrad(const void* grad, const void* input, int32_t input_per_pair
                      const int32_t* num_tokens_post_padded, int32_t block_m,
                      int64_t cap_tokens, float* dW, int32_t mode, const moe_ctx* ctx);
 
+/* ------------------------------------------------------------------------------------ *
+ * Diagnostics: failure detection of the bounded waits                                    *
+ * ------------------------------------------------------------------------------------ */
+
+/* Self-test switch of the tensor-memory kernels' failure detection (their waits on
+ * mbarriers are bounded and report MOE_ERR_TIMEOUT instead of hanging).  With stall_ns > 0,
+ * every later launch of the W4A16 and MXFP8 tensor-memory grouped GEMMs in this process
+ * (moe_forward above 256 rows, moe_grouped_gemm in MXFP8) runs with its copy and MMA roles
+ * switched off: the other roles wait on barriers that nothing arrives on, give up after
+ * stall_ns nanoseconds, write MOE_ERR_TIMEOUT to ctx->dev_status, free their tensor memory
+ * and return; no copy or MMA is in flight when they give up, and the context stays usable.
+ * Outputs of calls made meanwhile are undefined.  stall_ns <= 0 restores normal operation
+ * (2 s limits).  Process-wide; not for use while other threads run the library.  The pages
+ * have no counterpart to this call. */
+void moe_debug_stall_tensor_kernels(int64_t stall_ns);
+
 #ifdef __cplusplus
 }
 #endif

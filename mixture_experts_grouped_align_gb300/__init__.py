@@ -20,7 +20,7 @@ __all__ = [
     "MoeError", "load", "Ctx", "QUANT", "ACTIVATION", "moe_align_capacity", "moe_align", "moe_bucket",
     "moe_bucket_count", "moe_bucket_pad", "moe_forward_workspace_size", "moe_forward",
     "moe_forward_no_alloc", "moe_grouped_gemm", "moe_mx_quantize", "moe_gemm_per_token", "moe_wgrad",
-    "EXPORTED_SYMBOLS",
+    "moe_debug_stall_tensor_kernels", "EXPORTED_SYMBOLS",
 ]
 
 MOE_OK = 0
@@ -35,6 +35,7 @@ EXPORTED_SYMBOLS = [
     "moe_last_error", "moe_align_capacity", "moe_align", "moe_bucket", "moe_bucket_count",
     "moe_bucket_pad", "moe_forward_workspace_size", "moe_forward", "moe_forward_no_alloc",
     "moe_grouped_gemm", "moe_mx_quantize", "moe_gemm_per_token", "moe_wgrad",
+    "moe_debug_stall_tensor_kernels",
 ]
 
 
@@ -86,6 +87,7 @@ def load(path: str | None = None):
         "moe_mx_quantize": (I32, [P, I64, I32, P, P, P]),
         "moe_gemm_per_token": (I32, [I32, I32, I32, P, P, P, P, P, P, I64, P, P]),
         "moe_wgrad": (I32, [P, P, I32, I64, I32, I32, I32, I32, P, P, P, I32, I64, P, I32, P]),
+        "moe_debug_stall_tensor_kernels": (None, [I64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -237,3 +239,10 @@ def moe_wgrad(grad, input, input_per_pair, T, k, E, N, Kin, sorted_token_ids, ex
                                    _ptr(sorted_token_ids), _ptr(expert_ids),
                                    _ptr(num_tokens_post_padded), block_m, cap_tokens, _ptr(dW),
                                    int(mode), _ctx(ctx)))
+
+
+def moe_debug_stall_tensor_kernels(stall_ns: int) -> None:
+    """Failure-detection self-test switch: with stall_ns > 0 the tensor-memory kernels launch
+    with their copy and MMA roles off, so their waits give up after stall_ns ns and report
+    MOE_ERR_TIMEOUT; 0 restores normal operation."""
+    load().moe_debug_stall_tensor_kernels(int(stall_ns))

@@ -23,6 +23,19 @@ void set_error(const char* fmt, ...) {
 
 namespace moe_launch {
 
+namespace {
+std::atomic<int64_t> g_debug_stall_ns{0};
+}  // namespace
+
+int64_t debug_stall_ns() { return g_debug_stall_ns.load(std::memory_order_relaxed); }
+
+// The wait limit and stall flag every GroupedGemm of a call carries.
+void apply_debug_stall(GroupedGemm& g) {
+  const int64_t ns = debug_stall_ns();
+  g.wait_ns = ns > 0 ? ns : 0;
+  g.stall = ns > 0 ? 1 : 0;
+}
+
 int sm_count_current() {
   constexpr int kMaxDev = 64;
   static std::atomic<int> cache[kMaxDev];
@@ -247,6 +260,7 @@ static moe_status forward_mxfp8(const moe_weights* W, const void* x, const uint8
   g1.sorted = sorted_token_ids; g1.expert_ids = expert_ids; g1.ntpp = num_tokens_post_padded;
   g1.bm = block_m; g1.grid_blocks = blocks; g1.topk_w = topk_w; g1.out = hq; g1.out_scale = hs;
   g1.status = status_of(ctx);
+  moe_launch::apply_debug_stall(g1);
   moe_launch::GroupedGemm g2 = g1;
   g2.epi = moe_launch::EPI_WEIGHTED_F32;
   g2.w = W->w2; g2.w_scale = W->w2_scale; g2.bias = W->b2;
@@ -342,6 +356,7 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
   g1.sorted = sorted_token_ids; g1.expert_ids = expert_ids; g1.ntpp = num_tokens_post_padded;
   g1.bm = block_m; g1.grid_blocks = blocks; g1.topk_w = topk_w; g1.out = h;
   g1.status = status_of(ctx);
+  moe_launch::apply_debug_stall(g1);
   MOE_REQUIRE(moe_launch::decode_gemm_smem_bytes(g1) <= 227 * 1024, MOE_ERR_UNSUPPORTED,
               "K too large for the decode path");
   moe_launch::GroupedGemm g2 = g1;
@@ -416,6 +431,7 @@ moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin, 
   g.sorted = sorted_token_ids; g.expert_ids = expert_ids; g.ntpp = num_tokens_post_padded;
   g.bm = block_m; g.grid_blocks = used_blocks_bound(P, E, block_m, cap_tokens);
   g.topk_w = nullptr; g.out = out; g.status = status_of(ctx);
+  moe_launch::apply_debug_stall(g);
   MOE_REQUIRE(moe_launch::decode_gemm_smem_bytes(g) <= 227 * 1024, MOE_ERR_UNSUPPORTED,
               "Kin too large for the decode path");
   rec(ctx, 0, 2);
@@ -488,6 +504,10 @@ moe_status moe_wgrad(const void* grad, const void* input, int32_t input_per_pair
   st = cuda_status(moe_launch::wgrad(g, stream_of(ctx)), "moe_wgrad");
   rec(ctx, 1, 2);
   return st;
+}
+
+void moe_debug_stall_tensor_kernels(int64_t stall_ns) {
+  moe_launch::g_debug_stall_ns.store(stall_ns > 0 ? stall_ns : 0, std::memory_order_relaxed);
 }
 
 }  // extern "C"

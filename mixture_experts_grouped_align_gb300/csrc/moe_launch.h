@@ -66,7 +66,14 @@ struct GroupedGemm {
                             // out_scale is set (SWIGLU on the block-scaled kernel)
   uint8_t* out_scale;       // [P, Nout / 32] E8M0 scales of an MXFP8 h, or null
   int32_t* status;
+  int64_t wait_ns;          // limit of the tensor-memory kernels' waits (0: the 2 s default)
+  int stall;                // stalled self-test: the copy and MMA roles do nothing
 };
+
+// Stall limit set by moe_debug_stall_tensor_kernels (0: normal operation), and its
+// application to one GEMM's arguments.
+int64_t debug_stall_ns();
+void apply_debug_stall(GroupedGemm& g);
 size_t decode_gemm_smem_bytes(const GroupedGemm& g);
 cudaError_t decode_gemm(const GroupedGemm& g, cudaStream_t stream);
 

@@ -27,7 +27,11 @@
 // Tiles past num_tokens_post_padded or of the -1 sentinel are skipped by every role before
 // anything is read (second review of the same page).  Expert offsets are 64-bit (Notes).
 // Every mbarrier wait is bounded; one that runs out sets MOE_ERR_TIMEOUT, every role leaves
-// its loop, the MMA lane drains its own work and the TMEM is freed.
+// its loop, the copy threads wait for the copies they issued (cp.async groups and the
+// weight boxes), the MMA lane drains its own work and the TMEM is freed.  In the stalled
+// self-test (GroupedGemm::stall) the copy warps and the MMA lane do nothing, so the epilogue
+// waits on a barrier no one arrives on and gives up after GroupedGemm::wait_ns with no copy
+// or MMA in flight.
 //
 // Scale factors in TMEM (32-bit words, one byte per 32-element K block; the MMA of the
 // stage's K block j selects byte j): the MMA reads the word of A row m at lane m, column
@@ -122,13 +126,15 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
   uint64_t* gb_full = drain + 1;  // [2] B scale group landed (every B-scale thread's copies)
-  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(gb_full + 2);
+  uint64_t* tma_full = gb_full + 2;  // [kStages] the stage's weight box landed
+  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(tma_full + kStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(taddr_s + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&full[s], kNumProd / 32 + 1);  // producer warps + the weight box
+      tc::mbar_init(&full[s], kNumProd / 32);  // producer warps
+      tc::mbar_init(&tma_full[s], 1);          // the weight box
       tc::mbar_init(&empty[s], 1);
     }
     tc::mbar_init(tfull, 1);
@@ -149,8 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
   const int ntpp = *a.ntpp;
   const int Kin = a.Kin, nk = Kin / kBK, nkb = Kin / 32;
   const uint32_t smem_s = tc::smem_addr(smem);
+  // the limit of every wait (a caller's short limit only in the stalled self-test)
+  const uint64_t wb = a.wait_ns > 0 ? (uint64_t)a.wait_ns : tc::kWaitNs;
 
-  if (warp >= 8) {
+  if (warp >= 8 && !a.stall) {
     // ------------------------------------------------------------------ producers
     const int pt = tid - kProd0, wp = pt >> 5, q = wp & 3;
     const int c16 = pt & 7, r0 = pt >> 3;  // 16-byte chunk and first row of this thread's copies
@@ -176,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
         uint32_t v[8];
         if (grouped) {  // rows 32 j + lane of the group, copied by all four B-scale warps
           const uint32_t g = h >> 2;
-          if ((h & 3) == 0 && !tc::mbar_wait(&gb_full[g & 1], (g >> 1) & 1)) {
+          if ((h & 3) == 0 && !tc::mbar_wait(&gb_full[g & 1], (g >> 1) & 1, wb)) {
             moe::set_status(a.status, MOE_ERR_TIMEOUT);
             *abort_flag = 1;
             return false;
@@ -221,19 +229,20 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
           --npend;
         }
         const int s = (int)(it % kStages);
-        if (!tc::mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1)) {
+        if (!tc::mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, wb)) {
           moe::set_status(a.status, MOE_ERR_TIMEOUT);
           *abort_flag = 1;
           break;
         }
         const uint32_t sl = smem_s + s * L.slot;
         if (pt == 0) {
-          tma::mbar_arrive_expect_tx(&full[s], (uint32_t)(BN * kBK));
+          tma::mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(BN * kBK));
           if (EPI == EPI_SWIGLU) {  // gate rows, then up rows: two boxes of 128
-            tma::load_2d(sl + L.b, &tmap_w, kc * kBK, (int32_t)b_row<EPI>(a, e, nt, BN, 0), &full[s]);
-            tma::load_2d(sl + L.b + 128 * kBK, &tmap_w, kc * kBK, (int32_t)b_row<EPI>(a, e, nt, BN, 128), &full[s]);
+            tma::load_2d(sl + L.b, &tmap_w, kc * kBK, (int32_t)b_row<EPI>(a, e, nt, BN, 0), &tma_full[s]);
+            tma::load_2d(sl + L.b + 128 * kBK, &tmap_w, kc * kBK, (int32_t)b_row<EPI>(a, e, nt, BN, 128),
+                         &tma_full[s]);
           } else {
-            tma::load_2d(sl + L.b, &tmap_w, kc * kBK, (int32_t)b_row<EPI>(a, e, nt, BN, 0), &full[s]);
+            tma::load_2d(sl + L.b, &tmap_w, kc * kBK, (int32_t)b_row<EPI>(a, e, nt, BN, 0), &tma_full[s]);
           }
         }
 #pragma unroll
@@ -270,7 +279,13 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
       if (!hand_over(it - npend)) break;
       --npend;
     }
-  } else if (warp == 0) {
+    // Leaving early (a role gave up): the weight boxes already issued still land in this
+    // block's shared memory, so wait for each of them (the last kStages issued hold every
+    // slot's last armed phase) before exiting.
+    if (pt == 0 && *abort_flag)
+      for (uint32_t j = it > (uint32_t)kStages ? it - kStages : 0; j < it; ++j)
+        if (!tc::mbar_wait(&tma_full[j % kStages], (j / kStages) & 1, wb)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
+  } else if (warp == 0 && !a.stall) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t idesc[4];
@@ -281,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
         int64_t blk, e;
         int nt;
         if (!tile_info(ma, t, ntpp, blk, nt, e)) continue;
-        if (!tc::mbar_wait(tempty, (acc_it & 1) ^ 1)) {
+        if (!tc::mbar_wait(tempty, (acc_it & 1) ^ 1, wb)) {
           moe::set_status(a.status, MOE_ERR_TIMEOUT);
           *abort_flag = 1;
           break;
@@ -290,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
         bool ok = true;
         for (int kc = 0; kc < nk; ++kc) {
           const int s = (int)(it % kStages);
-          if (!tc::mbar_wait(&full[s], (it / kStages) & 1)) {
+          if (!tc::mbar_wait(&full[s], (it / kStages) & 1, wb) || !tc::mbar_wait(&tma_full[s], (it / kStages) & 1, wb)) {
             moe::set_status(a.status, MOE_ERR_TIMEOUT);
             *abort_flag = 1;
             ok = false;
@@ -310,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
         ++acc_it;
       }
       tc::mma_commit(drain);
-      if (!tc::mbar_wait(drain, 0)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
+      if (!tc::mbar_wait(drain, 0, wb)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
     }
     __syncwarp();
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
@@ -323,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
       int64_t blk, e;
       int nt;
       if (!tile_info(ma, t, ntpp, blk, nt, e)) continue;
-      if (!tc::mbar_wait(tfull, acc_it & 1)) {
+      if (!tc::mbar_wait(tfull, acc_it & 1, wb)) {
         moe::set_status(a.status, MOE_ERR_TIMEOUT);
         *abort_flag = 1;
         break;

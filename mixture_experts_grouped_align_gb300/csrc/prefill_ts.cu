@@ -37,12 +37,19 @@
 //               bias + relu^2 -> h (f16, through a shared staging tile and TMA stores when h
 //               is in slot order), bias * routing weight -> o (fp32), or bias -> out (bf16).
 // Every mbarrier wait is bounded; one that runs out sets MOE_ERR_TIMEOUT, every role leaves
-// its loop, the MMA lane drains its own work and the TMEM is freed.
+// its loop, the copy warp waits for the loads it has issued, the MMA lane drains its own work
+// and the TMEM is freed.  In the stalled self-test (GroupedGemm::stall) the copy warp and the
+// MMA lanes do nothing, so the decoders and the epilogue wait on barriers no one arrives on
+// and give up after GroupedGemm::wait_ns with no copy or MMA in flight.
 //
-// f16 operands: a decoded weight is exact when its scale is within 2^-23..2^13; a block with
-// nonzero codes outside that range sets MOE_ERR_RANGE.  Each output depends on its own token
-// row only and K is always reduced in the same order, so padded and unpadded batches give
-// identical real rows.
+// f16 operands: a decoded weight code * 2^se is exact when se is within -23..13.  A weight
+// row whose block scales fall outside that window is decoded as code * 2^(se - c) with one
+// shift c per row and tile (the largest block scale of the row mapped to 2^13), and the
+// epilogue multiplies that row's accumulator by 2^c: a power of two, so the result is the
+// same as with exact f16 weights.  Only a row whose nonzero blocks span more than 36
+// octaves of scale still has a block outside the window; it sets MOE_ERR_RANGE.  Each output
+// depends on its own token row only and K is always reduced in the same order, so padded
+// and unpadded batches give identical real rows.
 #include "moe_common.cuh"
 #include "moe_launch.h"
 #include "tcgen05.cuh"
@@ -95,7 +102,7 @@ struct TArgs {
 // Shared memory: token-tile stages (16 KB each) | raw-code slots (2 x 128 rows x 128 B,
 // 128-byte swizzle) | h output staging (128 slots x 128 f16 per matrix) | barriers.
 struct TLayout {
-  int slot, raw, raw_slot, stg, bars, total;
+  int slot, raw, raw_slot, stg, bars, shift, total;
 };
 
 __host__ __device__ inline TLayout tlayout(int epi) {
@@ -105,7 +112,8 @@ __host__ __device__ inline TLayout tlayout(int epi) {
   L.raw_slot = kMats * kTM * 128;
   L.stg = L.raw + kRawSlots * L.raw_slot;
   L.bars = L.stg + stage_out_bytes(epi);
-  L.total = L.bars + 512 + 1024;
+  L.shift = L.bars + 512;  // [2 tiles][kMats][kTM] int8 row shifts
+  L.total = L.shift + 2 * kMats * kTM + 1024;
   return L;
 }
 
@@ -124,6 +132,21 @@ __device__ __forceinline__ int64_t next_tile(const TArgs& ta, int64_t t, int ntp
   int mt;
   while (t < ta.tiles && !tile_info(ta, t, ntpp, blk, mt, e)) t += gridDim.x;
   return t;
+}
+
+// E8M0 byte of a block scale divided by 2^c (the row's shift): NaN (0xFF) stays NaN, and a
+// byte pushed below 0x00 is clamped there (a block with nonzero codes is then reported by
+// decode_block).
+__device__ __forceinline__ uint32_t shifted_scale(uint32_t sb, int c) {
+  if (sb == 255u || c == 0) return sb;
+  const int v = (int)sb - c;
+  return (uint32_t)(v < 0 ? 0 : (v > 254 ? 254 : v));
+}
+
+// 2^c as a float for -149 <= c <= 127 (1 for c = 0).
+__device__ __forceinline__ float pow2f(int c) {
+  if (c >= -126) return __uint_as_float((uint32_t)(c + 127) << 23);
+  return __uint_as_float(1u << (c + 149));
 }
 
 // TMEM column of stage s, matrix m, in the decoded-weight region.
@@ -198,8 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Kin = a.Kin, nk = Kin / kBK, nkb = Kin / 32;
   const uint32_t smem_s = tc::smem_addr(smem);
   bool bad = false;
+  // the limit of every wait (a caller's short limit only in the stalled self-test)
+  const uint64_t wb = a.wait_ns > 0 ? (uint64_t)a.wait_ns : tc::kWaitNs;
 
-  if (warp == 1) {
+  if (warp == 1 && !a.stall) {
     // ------------------------------------------------------------------ TMA loads
     if (lane == 0) {
       tma::prefetch_map(&tmap_x);
@@ -227,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kc = 0; kc < nk; ++kc) {
         if (kc % kGroup == 0) {  // raw codes of stages kc .. kc + 3: 128 bytes of every row
           const int rs = (int)(gi % kRawSlots);
-          if (lane == 0) ok = tc::mbar_wait(&raw_empty[rs], ((gi / kRawSlots) & 1) ^ 1);
+          if (lane == 0) ok = tc::mbar_wait(&raw_empty[rs], ((gi / kRawSlots) & 1) ^ 1, wb);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           if (lane == 0) {
@@ -241,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++gi;
         }
         const int s = (int)(it % S1);
-        if (lane == 0) ok = tc::mbar_wait(&empty[s], ((it / S1) & 1) ^ 1);
+        if (lane == 0) ok = tc::mbar_wait(&empty[s], ((it / S1) & 1) ^ 1, wb);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         const uint32_t sl = smem_s + s * L.slot;
@@ -259,6 +284,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
         break;
       }
+    }
+    // Leaving early (another role gave up): the loads already issued still land in this
+    // block's shared memory, so wait for each armed stage and code group before exiting.
+    // Every slot's last armed phase is one of the last S1 stages (kRawSlots groups) issued.
+    if (*abort_flag && lane == 0) {
+      for (uint32_t j = it > (uint32_t)S1 ? it - S1 : 0; j < it; ++j)
+        if (!tc::mbar_wait(&ld_full[j % S1], (j / S1) & 1, wb)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
+      for (uint32_t j = gi > (uint32_t)kRawSlots ? gi - kRawSlots : 0; j < gi; ++j)
+        if (!tc::mbar_wait(&raw_full[j % kRawSlots], (j / kRawSlots) & 1, wb)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
     }
   } else if (warp >= kDecWarp0 && warp < kDecWarp0 + 8) {
     // ------------------------------------------------------------------ decoders
@@ -279,6 +313,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       w[0] = v[0];
       w[1] = v[1];
     };
+    // The shift c of this row for the tile (0 when every block scale is in the f16 window;
+    // else the largest block scale is mapped to 2^13), written for the epilogue at
+    // shift[tile parity][m][r].
+    auto row_shift = [&](int64_t e, int mt) -> int {
+      if (tile_feature<SW>(mt, m, r) >= a.Nout) return 0;
+      const uint8_t* src = a.w_scale + tile_wrow<SW>(a, e, mt, m, r) * nkb;
+      int mx = 0, mn = 254;
+      for (int b = 0; b < nkb; ++b) {
+        const int sb = __ldg(src + b);
+        if (sb != 255) {
+          mx = sb > mx ? sb : mx;
+          mn = sb < mn ? sb : mn;
+        }
+      }
+      return (mx <= 127 + 13 && mn >= 127 - 23) ? 0 : mx - (127 + 13);
+    };
+    int8_t* shift_s = reinterpret_cast<int8_t*>(smem + L.shift);
+    uint32_t tseq = 0;
     uint32_t it = 0, gi = 0;
     int64_t t = next_tile(ta, blockIdx.x, ntpp);
     int64_t blk = 0, e = 0;
@@ -296,6 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool live_n = tn < ta.tiles && blk_n * a.bm < ntpp;
       const int64_t e_n = live_n ? (int64_t)a.expert_ids[blk_n] : -1;
       const bool next_ok = e_n >= 0 && e_n < a.E;
+      int csh = row_shift(e, mt);
+      csh = csh < -128 ? -128 : (csh > 127 ? 127 : csh);
+      shift_s[((tseq & 1) * kMats + m) * kTM + r] = (int8_t)csh;
+      ++tseq;
       bool ok = true;
       uint32_t sc0 = 0u, sc1 = 0u;
       int rs = 0;
@@ -307,13 +363,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           sc1 = sc_next[1];
           if (g + 1 < ngroups) load_scales(e, mt, g + 1, sc_next);
           else if (next_ok) load_scales(e_n, mt_n, 0, sc_next);
-          if (!tc::mbar_wait(&raw_full[rs], (gi / kRawSlots) & 1)) {
+          if (!tc::mbar_wait(&raw_full[rs], (gi / kRawSlots) & 1, wb)) {
             ok = false;
             break;
           }
         }
         const int s2 = (int)(it % S2);
-        if (!tc::mbar_wait(&a_empty[s2], ((it / S2) & 1) ^ 1)) {
+        if (!tc::mbar_wait(&a_empty[s2], ((it / S2) & 1) ^ 1, wb)) {
           ok = false;
           break;
         }
@@ -327,8 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v[32];
           const uint4 w0 = *reinterpret_cast<const uint4*>(rowp + (((2 * kg) ^ (r & 7)) << 4));
           const uint4 w1 = *reinterpret_cast<const uint4*>(rowp + (((2 * kg + 1) ^ (r & 7)) << 4));
-          decode_block(w0, (scw >> sh) & 0xffu, v, bad);
-          decode_block(w1, (scw >> (sh + 8)) & 0xffu, v + 16, bad);
+          decode_block(w0, shifted_scale((scw >> sh) & 0xffu, csh), v, bad);
+          decode_block(w1, shifted_scale((scw >> (sh + 8)) & 0xffu, csh), v + 16, bad);
           tmem_st16(dst, v);
           tmem_st16(dst + 16, v + 16);
         }
@@ -360,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kMats) {
+  } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kMats && !a.stall) {
     // ------------------------------------------------------------------ MMA issuers
     // one thread per weight matrix, in two warps on different SM sub-partitions: the waits,
     // commits and issues of a stage cost the issuing thread about as long as the tensor core
@@ -374,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mt;
         if (!tile_info(ta, t, ntpp, blk, mt, e)) continue;
         const int acc = 0;  // one accumulator set (two 128-column accumulators)
-        if (!tc::mbar_wait(&tempty[acc], (acc_it & 1) ^ 1)) {
+        if (!tc::mbar_wait(&tempty[acc], (acc_it & 1) ^ 1, wb)) {
           moe::set_status(a.status, MOE_ERR_TIMEOUT);
           *abort_flag = 1;
           break;
@@ -383,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int kc = 0; kc < nk; ++kc) {
           const int s = (int)(it % S1), s2 = (int)(it % S2);
-          if (!tc::mbar_wait(&ld_full[s], (it / S1) & 1) || !tc::mbar_wait(&a_full[s2], (it / S2) & 1)) {
+          if (!tc::mbar_wait(&ld_full[s], (it / S1) & 1, wb) || !tc::mbar_wait(&a_full[s2], (it / S2) & 1, wb)) {
             moe::set_status(a.status, MOE_ERR_TIMEOUT);
             *abort_flag = 1;
             ok = false;
@@ -404,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++acc_it;
       }
       tc::mma_commit(drain);
-      if (!tc::mbar_wait(drain, 0)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
+      if (!tc::mbar_wait(drain, 0, wb)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
     }
     __syncwarp();
   } else if ((warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) || warp >= kEpiWarp1) {
@@ -423,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto epi_sync = [&]() -> bool {
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(epi_bar);
-      const bool ok = tc::mbar_wait(epi_bar, eb_it & 1);
+      const bool ok = tc::mbar_wait(epi_bar, eb_it & 1, wb);
       ++eb_it;
       if (!ok) {
         moe::set_status(a.status, MOE_ERR_TIMEOUT);
@@ -444,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < kEpiCols / 32; ++i)
         wls[i] = (EPI == EPI_WEIGHTED_F32 && pls[i] < a.P) ? a.topk_w[pls[i]] : 1.f;
-      if (!tc::mbar_wait(&tfull[acc], acc_it & 1)) {
+      if (!tc::mbar_wait(&tfull[acc], acc_it & 1, wb)) {
         moe::set_status(a.status, MOE_ERR_TIMEOUT);
         *abort_flag = 1;
         break;
@@ -454,6 +510,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // feature fA in accumulator 0 and fB in accumulator 1
       const int64_t fA = tile_feature<SW>(mt, 0, 32 * q + lane), fB = tile_feature<SW>(mt, 1, 32 * q + lane);
       const bool vA = fA < a.Nout, vB = fB < a.Nout;
+      // 2^c of the two rows of this lane (their weights were decoded with 2^-c)
+      const int8_t* shift_s = reinterpret_cast<const int8_t*>(smem + L.shift) + (acc_it & 1) * kMats * kTM;
+      const float fsA = pow2f(shift_s[32 * q + lane]), fsB = pow2f(shift_s[kTM + 32 * q + lane]);
       float b0 = 0.f, b1 = 0.f;
       if (bias) {
         if (vA) b0 = moe::bf16_bits_to_f32(bias[e * a.Nw + fA]);
@@ -482,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int p = __shfl_sync(0xffffffffu, pl, j);
-            const float gt = __uint_as_float(v0[j]) + b0, up = __uint_as_float(v1[j]) + b1;
+            const float gt = __uint_as_float(v0[j]) * fsA + b0, up = __uint_as_float(v1[j]) * fsB + b1;
             const __half hv = __float2half_rn(moe::silu(gt) * up);
             if (p < a.P && vA && __hisinf(hv)) bad = true;
             if (staged) {
@@ -496,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int p = __shfl_sync(0xffffffffu, pl, j);
-            const __half hA = __float2half_rn(moe::relu2(__uint_as_float(v0[j]) + b0));
-            const __half hB = __float2half_rn(moe::relu2(__uint_as_float(v1[j]) + b1));
+            const __half hA = __float2half_rn(moe::relu2(__uint_as_float(v0[j]) * fsA + b0));
+            const __half hB = __float2half_rn(moe::relu2(__uint_as_float(v1[j]) * fsB + b1));
             if (p < a.P && ((vA && __hisinf(hA)) || (vB && __hisinf(hB)))) bad = true;
             if (staged) {
               stg[(c0 + j) * kTM + 32 * q + lane] = hA;
@@ -516,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float wp = __shfl_sync(0xffffffffu, wl, j);
             if (p < a.P) {
               const int64_t row = a.out_by_slot ? slot0 + c0 + j : (int64_t)p;
-              const float o0 = __uint_as_float(v0[j]) + b0, o1 = __uint_as_float(v1[j]) + b1;
+              const float o0 = __uint_as_float(v0[j]) * fsA + b0, o1 = __uint_as_float(v1[j]) * fsB + b1;
               if (EPI == EPI_WEIGHTED_F32) {
                 if (vA) static_cast<float*>(a.out)[row * a.Nout + fA] = o0 * wp;
                 if (vB) static_cast<float*>(a.out)[row * a.Nout + fB] = o1 * wp;

@@ -38,9 +38,12 @@ MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Default limit of a bounded wait: 2 s, far beyond any stage of a healthy kernel.
+constexpr uint64_t kWaitNs = 2000000000ull;
+
 // Waits for the phase with the given parity to complete.  Gives up after about
 // `budget_ns` nanoseconds (globaltimer) and returns false; never spins forever.
-MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns = 2000000000ull) {
+MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));

@@ -1,0 +1,81 @@
+"""Failure detection of the tensor-memory kernels, without a GPU fault: with the stall
+self-test switch on, the W4A16 and MXFP8 forward GEMMs above 256 rows launch with their copy
+and MMA roles off, so their other roles wait on barriers nothing arrives on.  Every wait is
+bounded: the kernels must give up after the short limit, report MOE_ERR_TIMEOUT in the
+device status word and return, and the next normal call on the same context must succeed
+and match the float64 oracle."""
+import time
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import formats, layer, route
+
+from helpers import assert_close_bf16, bf16_to_np, dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+MOE_ERR_TIMEOUT = -7
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import mixture_experts_grouped_align_gb300 as m
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    m.build()
+    m.load()
+    yield m
+    m.moe_debug_stall_tensor_kernels(0)
+
+
+def _layer(w):
+    from mixture_experts_grouped_align_gb300.runner import DeviceLayer
+    lay = synth.make_layer(w)
+    L = DeviceLayer(w.quant, w.E, w.K, w.I, w.k, dev(lay["w1"]), dev(lay["w1_scale"]), dev(lay["b1"]),
+                    dev(lay["w2"]), dev(lay["w2_scale"]), dev(lay["b2"]), max_rows=w.T)
+    return lay, L
+
+
+def _step(L, lay, w):
+    y = torch.full((w.T, w.K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    if w.quant == "mxfp8":
+        L.step(dev(lay["x_codes"]), dev(lay["logits"]), w.T, y, x_scale=dev(lay["x_scale"]))
+    else:
+        L.step(dev(lay["x"]), dev(lay["logits"]), w.T, y)
+    torch.cuda.synchronize()
+    return y
+
+
+def _oracle(lay, w):
+    W = layer.ExpertWeights(w.quant, lay["w1"], lay["w1_scale"], lay["b1"], lay["w2"], lay["w2_scale"], lay["b2"])
+    ids, wt = route.route(lay["logits"], w.k)
+    x = formats.dequant_mxfp8(lay["x_codes"], lay["x_scale"]) if w.quant == "mxfp8" else formats.bf16_decode(lay["x"])
+    return layer.moe_layer(x, ids, wt, W)
+
+
+@pytest.mark.parametrize("quant", ["mxfp4", "mxfp8"])
+def test_stalled_waits_time_out_and_the_context_recovers(moe, quant):
+    if quant == "mxfp4":   # prefill_ts kernels (W4A16, decoded weights in tensor memory)
+        w = synth.scaled(synth.TINY, T=300, bias=True)
+    else:                  # mx8_gemm kernels (block-scaled MXFP8)
+        w = synth.Workload("stall_mxfp8", T=300, K=512, I=512, E=8, k=2, quant="mxfp8", seed=7,
+                           weight_std=0.05, bias=True)
+    lay, L = _layer(w)
+    _step(L, lay, w)                              # module loaded, kernels set up
+    L.status.zero_()
+    try:
+        moe.moe_debug_stall_tensor_kernels(5_000)   # 5 us limit on every wait
+        t0 = time.perf_counter()
+        _step(L, lay, w)
+        elapsed = time.perf_counter() - t0
+    finally:
+        moe.moe_debug_stall_tensor_kernels(0)
+    assert int(L.status[0]) == MOE_ERR_TIMEOUT
+    assert elapsed < 1.0, elapsed                 # gave up after the short limit, not 2 s
+    # the context is still usable: a normal call succeeds and is correct
+    L.status.zero_()
+    y = _step(L, lay, w)
+    assert int(L.status[0]) == 0
+    assert_close_bf16(bf16_to_np(y), _oracle(lay, w), what=f"{quant} after the stalled call")

@@ -180,17 +180,51 @@ def test_w4a16_nan_scale_reaches_exactly_its_tokens(moe, T):
     assert_close_bf16(got[~nan_rows], ref[~nan_rows], what=f"nan scale T={T}")
 
 
-def test_w4a16_scale_outside_f16_range_is_reported_on_the_tensor_memory_path(moe):
-    """The tensor-memory path decodes codes x scale to f16: a block with nonzero codes whose
-    scale is below 2^-23 cannot be represented exactly and sets MOE_ERR_RANGE (-6); the
-    weight-streaming path scales f32 partial sums and stays exact."""
-    w = synth.Workload("tiny_scale", T=300, K=256, I=256, E=16, k=4, quant="mxfp4", seed=22,
+@pytest.mark.parametrize("T", [64, 300])  # weight-streaming / tensor-memory path
+def test_w4a16_scales_outside_the_f16_window_are_exact(moe, T):
+    """Blocks with nonzero codes whose E8M0 scale is far below (2^-30) or above (2^+20) the
+    window in which code * scale is an exact f16 (2^-23..2^13): the weight-streaming path
+    scales f32 partial sums, the tensor-memory path shifts the row's decoded weights by a
+    power of two and undoes it on the accumulator.  Both must succeed and match the oracle,
+    whichever side of the 256-row threshold the batch falls on."""
+    # no bias: with the up rows' weights scaled down, a bias would dominate up and push
+    # h = silu(gate) * up beyond the float16 range of h (a legitimate MOE_ERR_RANGE)
+    w = synth.Workload("tiny_scale", T=T, K=256, I=256, E=16, k=4, quant="mxfp4", seed=22,
+                       scale_exp=(-6, -2), bias=False)
+    lay = synth.make_layer(w)
+    lay["w1_scale"] = lay["w1_scale"].copy()
+    lay["w1"] = lay["w1"].copy()
+    lay["w2_scale"] = lay["w2_scale"].copy()
+    I = w.I
+    lay["w1_scale"][2, 7, 1] = 127 - 30       # one block of a row far below the window
+    lay["w1"][2, 7, 16:32] = 0x77             # nonzero codes in that block
+    lay["w1_scale"][5, :I, :] += 20           # expert 5: gate rows above the window and up
+    lay["w1_scale"][5, I:, :] -= 20           # rows below it (h = silu(gate) * up stays normal)
+    lay["w2_scale"][3, 11, :] += 20           # a GEMM2 row above the window (output column 11)
+    lay["w2_scale"][3, 12, 0] = 127 + 20      # one GEMM2 block above the window (column 12)
+    L = device_layer(moe, lay, w, T, pad=False)
+    y, st = _run_status(moe, L, lay, T)
+    assert st == 0
+    got, ref = bf16_to_np(y), oracle_y(lay, w, T)
+    big = [11, 12]                            # the columns the large GEMM2 scales reach
+    rest = np.setdiff1d(np.arange(w.K), big)
+    assert_close_bf16(got[:, rest], ref[:, rest], what=f"scales outside the f16 window, T={T}")
+    assert_close_bf16(got[:, big], ref[:, big], what=f"large GEMM2 scales, T={T}")
+
+
+def test_w4a16_scale_spread_beyond_36_octaves_is_reported_on_the_tensor_memory_path(moe):
+    """A weight row whose nonzero blocks span more than 36 octaves of scale cannot be put into
+    one f16 window by a single shift: the tensor-memory path reports MOE_ERR_RANGE (-6) for
+    it; the weight-streaming path stays exact."""
+    w = synth.Workload("tiny_spread", T=300, K=256, I=256, E=16, k=4, quant="mxfp4", seed=23,
                        scale_exp=(-6, -2), bias=True)
     lay = synth.make_layer(w)
     lay["w1_scale"] = lay["w1_scale"].copy()
     lay["w1"] = lay["w1"].copy()
-    lay["w1_scale"][2, 7, 1] = 127 - 30
-    lay["w1"][2, 7, 16:32] = 0x77  # nonzero codes in that block
+    lay["w1_scale"][2, 7, 0] = 127 + 6        # block 0: codes 0.5 * 2^6 (h stays in range)
+    lay["w1"][2, 7, :16] = 0x11
+    lay["w1_scale"][2, 7, 1] = 127 - 31       # 37 octaves below block 0 of the same row
+    lay["w1"][2, 7, 16:32] = 0x77
     L = device_layer(moe, lay, w, 300, pad=False)
     _, st = _run_status(moe, L, lay, 300)
     assert st == -6
