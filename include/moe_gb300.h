@@ -247,13 +247,26 @@ moe_status moe_forward_no_alloc(const moe_weights* W, const void* x, const uint8
  * One grouped GEMM over all experts in a single launch ([AITER] Summary: moe_gemm_mxfp8) *
  * ------------------------------------------------------------------------------------ */
 
+/* Workspace bytes that let moe_grouped_gemm run W4A16 (MOE_Q_MXFP4_W4A16) weights on the
+ * tensor cores: above 256 token rows the tcgen05 kernel reads A as float16, and the call
+ * converts A into the workspace first (rows x Kin x 2 bytes, rows = T*k if a_per_pair else
+ * T).  0 for the other modes, for T <= 256, or for invalid sizes. */
+size_t moe_grouped_gemm_workspace_size(moe_quant quant, int64_t T, int32_t k, int32_t Kin, int32_t a_per_pair);
+
 /* out[p, :] = A[src(p), :] . W[e_p]^T + bias[e_p]   for every pair p < T*k, in bf16 RNE.
  * A: [T, Kin] (a_per_pair == 0, src = p / k) or [T*k, Kin] (a_per_pair != 0, src = p);
  *    bf16 for MOE_Q_BF16 / MOE_Q_MXFP4_W4A16, E4M3 bytes + a_scale [rows, Kin/32] E8M0
  *    for MOE_Q_MXFP8.
  * W: [E, N, Kin] (MXFP4: [E, N, Kin/2] bytes) + w_scale [E, N, Kin/32]; bias [E, N] bf16
  *    or NULL.  out: [T*k, N] bf16, indexed by pair.
- * N must be a multiple of 16 and Kin of 32.  Needs no workspace. */
+ * N must be a multiple of 16 and Kin of 32.
+ * Kernels: MXFP8 above 256 token rows runs the block-scaled tensor-core kernel (K and N
+ * multiples of 128); W4A16 above 256 rows runs the tcgen05 kernel with decoded weights in
+ * tensor memory when ctx->workspace holds moe_grouped_gemm_workspace_size() bytes (block_m
+ * 128, Kin a multiple of 64 up to 4096; |A| <= 65504, else MOE_ERR_RANGE in dev_status);
+ * every other call runs the weight-streaming kernel, which needs no workspace.  The kernel
+ * choice depends on T only through the bucket value 256, and each kernel reduces K in one
+ * fixed order. */
 moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin,
                             const void* a, const uint8_t* a_scale, int32_t a_per_pair,
                             const void* w, const uint8_t* w_scale, const void* bias,

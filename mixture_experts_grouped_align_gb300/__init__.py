@@ -19,8 +19,8 @@ from .build import LIB, build  # noqa: F401
 __all__ = [
     "MoeError", "load", "Ctx", "QUANT", "ACTIVATION", "moe_align_capacity", "moe_align", "moe_bucket",
     "moe_bucket_count", "moe_bucket_pad", "moe_forward_workspace_size", "moe_forward",
-    "moe_forward_no_alloc", "moe_grouped_gemm", "moe_mx_quantize", "moe_gemm_per_token", "moe_wgrad",
-    "moe_debug_stall_tensor_kernels", "EXPORTED_SYMBOLS",
+    "moe_forward_no_alloc", "moe_grouped_gemm", "moe_grouped_gemm_workspace_size", "moe_mx_quantize",
+    "moe_gemm_per_token", "moe_wgrad", "moe_debug_stall_tensor_kernels", "EXPORTED_SYMBOLS",
 ]
 
 MOE_OK = 0
@@ -34,7 +34,7 @@ ACTIVATION = {"swiglu": 0, "relu2": 1}
 EXPORTED_SYMBOLS = [
     "moe_last_error", "moe_align_capacity", "moe_align", "moe_bucket", "moe_bucket_count",
     "moe_bucket_pad", "moe_forward_workspace_size", "moe_forward", "moe_forward_no_alloc",
-    "moe_grouped_gemm", "moe_mx_quantize", "moe_gemm_per_token", "moe_wgrad",
+    "moe_grouped_gemm", "moe_grouped_gemm_workspace_size", "moe_mx_quantize", "moe_gemm_per_token", "moe_wgrad",
     "moe_debug_stall_tensor_kernels",
 ]
 
@@ -84,6 +84,7 @@ def load(path: str | None = None):
         "moe_forward_no_alloc": (I32, [P, P, P, I64, I64, I32, P, P, P, P, P, I32, I64, P, P]),
         "moe_grouped_gemm": (I32, [ctypes.c_int, I32, I32, I32, P, P, I32, P, P, P, I64, I32,
                                    P, P, P, I32, I64, P, P]),
+        "moe_grouped_gemm_workspace_size": (SZ, [ctypes.c_int, I64, I32, I32, I32]),
         "moe_mx_quantize": (I32, [P, I64, I32, P, P, P]),
         "moe_gemm_per_token": (I32, [I32, I32, I32, P, P, P, P, P, P, I64, P, P]),
         "moe_wgrad": (I32, [P, P, I32, I64, I32, I32, I32, I32, P, P, P, I32, I64, P, I32, P]),
@@ -220,6 +221,11 @@ def moe_grouped_gemm(quant, E, N, Kin, a, a_scale, a_per_pair, w, w_scale, bias,
                                           _ptr(sorted_token_ids), _ptr(expert_ids),
                                           _ptr(num_tokens_post_padded), block_m, cap_tokens,
                                           _ptr(out), _ctx(ctx)))
+
+
+def moe_grouped_gemm_workspace_size(quant, T, k, Kin, a_per_pair) -> int:
+    q = QUANT[quant] if isinstance(quant, str) else quant
+    return load().moe_grouped_gemm_workspace_size(q, T, k, Kin, int(a_per_pair))
 
 
 def moe_mx_quantize(x, rows, cols, codes, scales, ctx=None):

@@ -396,6 +396,14 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
   return st;
 }
 
+size_t moe_grouped_gemm_workspace_size(moe_quant quant, int64_t T, int32_t k, int32_t Kin, int32_t a_per_pair) {
+  // the W4A16 tensor-memory kernel reads the activations as f16: one converted copy of A
+  if (quant != MOE_Q_MXFP4_W4A16 || T <= moe_launch::kPrefillRowsAbove || k < 1 || Kin < 1) return 0;
+  if (!pairs_fit(T, k)) return 0;
+  const int64_t rows = a_per_pair ? T * k : T;
+  return round256((size_t)rows * Kin * 2);
+}
+
 moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin, const void* a,
                             const uint8_t* a_scale, int32_t a_per_pair, const void* w,
                             const uint8_t* w_scale, const void* bias, int64_t T, int32_t k,
@@ -432,6 +440,23 @@ moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin, 
   g.bm = block_m; g.grid_blocks = used_blocks_bound(P, E, block_m, cap_tokens);
   g.topk_w = nullptr; g.out = out; g.status = status_of(ctx);
   moe_launch::apply_debug_stall(g);
+  // W4A16 above the tensor-memory threshold, with a workspace for the f16 copy of A: the
+  // tcgen05 kernel (decoded weights in tensor memory) where it takes the shape
+  const size_t ws_need = moe_grouped_gemm_workspace_size(quant, T, k, Kin, a_per_pair);
+  if (ws_need > 0 && ctx && ctx->workspace && ctx->workspace_bytes >= ws_need && aligned16(ctx->workspace)) {
+    moe_launch::GroupedGemm gt = g;
+    gt.act = ctx->workspace;
+    gt.act_fmt = moe_launch::ACT_F16;
+    if (moe_launch::ts_supported(gt)) {
+      const int64_t rows = a_per_pair ? P : T;
+      rec(ctx, 0, 2);
+      st = cuda_status(moe_launch::bf16_to_f16(a, ctx->workspace, rows * Kin, status_of(ctx), stream_of(ctx)),
+                       "moe_grouped_gemm activations");
+      if (st == MOE_OK) st = cuda_status(moe_launch::prefill_ts(gt, stream_of(ctx)), "moe_grouped_gemm");
+      rec(ctx, 1, 2);
+      return st;
+    }
+  }
   MOE_REQUIRE(moe_launch::decode_gemm_smem_bytes(g) <= 227 * 1024, MOE_ERR_UNSUPPORTED,
               "Kin too large for the decode path");
   rec(ctx, 0, 2);

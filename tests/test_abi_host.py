@@ -148,3 +148,12 @@ def test_size_overflow_is_rejected_before_any_launch(lib):
         moe.moe_forward("bf16", 1024, (1 << 31) - 32, (1 << 31) - 32, 16, None, None, 16, None, None,
                         16, None, 4, 4, 2, 16, 16, 16, 16, None, 16, 256, 16, big)
     assert ei.value.status == -2 and "64-bit" in lib.moe_last_error().decode()
+
+
+def test_grouped_gemm_workspace_size(lib):
+    r = lambda v: (v + 255) // 256 * 256
+    assert moe.moe_grouped_gemm_workspace_size("mxfp4", 256, 4, 2880, 0) == 0     # weight streaming
+    assert moe.moe_grouped_gemm_workspace_size("mxfp4", 257, 4, 2880, 0) == r(257 * 2880 * 2)
+    assert moe.moe_grouped_gemm_workspace_size("mxfp4", 300, 4, 2880, 1) == r(1200 * 2880 * 2)
+    assert moe.moe_grouped_gemm_workspace_size("mxfp8", 4096, 8, 7168, 0) == 0     # reads E4M3 as is
+    assert moe.moe_grouped_gemm_workspace_size("bf16", 4096, 8, 7168, 0) == 0

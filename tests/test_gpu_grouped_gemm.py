@@ -37,13 +37,13 @@ def align_dev(moe, ids, E, bm=BM):
     return srt, eid, ntpp, cap
 
 
-def gemm_dev(moe, quant, E, N, Kin, a, a_scale, per_pair, w, w_scale, bias, ids, bm=BM):
+def gemm_dev(moe, quant, E, N, Kin, a, a_scale, per_pair, w, w_scale, bias, ids, bm=BM, workspace=None):
     T, k = ids.shape
     srt, eid, ntpp, cap = align_dev(moe, ids, E, bm)
     out = torch.full((T * k, N), float("nan"), dtype=torch.bfloat16, device="cuda")
     st = torch.zeros(4, dtype=torch.int32, device="cuda")
     moe.moe_grouped_gemm(quant, E, N, Kin, a, a_scale, per_pair, w, w_scale, bias, T, k, srt, eid,
-                         ntpp, bm, cap, out, moe.Ctx(dev_status=st))
+                         ntpp, bm, cap, out, moe.Ctx(dev_status=st, workspace=workspace))
     torch.cuda.synchronize()
     assert int(st[0]) == 0
     return out
@@ -208,3 +208,28 @@ def test_mxfp8_block_scaled_scale_edges(moe):
     assert np.array_equal(np.isnan(out), nan_ref)
     keep = ~nan_ref.any(axis=1)
     assert_close_bf16(out[keep], ref[keep], what="mxfp8 scale edges")
+
+
+@pytest.mark.parametrize("per_pair", [False, True])
+def test_mxfp4_above_threshold_tensor_path_with_workspace(moe, per_pair):
+    """W4A16 above 256 rows: with moe_grouped_gemm_workspace_size() bytes of workspace the call
+    converts A to f16 and runs the tcgen05 kernel (decoded weights in tensor memory); without it
+    the weight-streaming kernel runs.  Both against the oracle: ragged experts over several
+    128-row blocks, one empty expert, per-expert bias, Kin with a partial last scale group."""
+    rng = np.random.default_rng(41)
+    T, E, k, N, Kin = 760, 12, 3, 256, 576
+    ids = random_ids(rng, T, E, k, empty=(4,))
+    rows = T * k if per_pair else T
+    a = synth.to_bf16_bits(rng.standard_normal((rows, Kin)))
+    w, ws = synth.gen_mxfp4_weight(rng, E, N, Kin, (-6, -2))
+    b = synth.to_bf16_bits(rng.standard_normal((E, N)) * 0.1)
+    need = moe.moe_grouped_gemm_workspace_size("mxfp4", T, k, Kin, per_pair)
+    assert need >= rows * Kin * 2
+    wsp = torch.empty(need, dtype=torch.uint8, device="cuda")
+    Wd = lambda e: (ofmt.dequant("mxfp4", w[e], ws[e]), ofmt.bf16_decode(b[e]))
+    ref = olayer.grouped_gemm(ofmt.bf16_decode(a), ids, Wd, per_pair)
+    got_tc = gemm_dev(moe, "mxfp4", E, N, Kin, dev(a), None, per_pair, dev(w), dev(ws), dev(b), ids,
+                      workspace=wsp)
+    got_ws = gemm_dev(moe, "mxfp4", E, N, Kin, dev(a), None, per_pair, dev(w), dev(ws), dev(b), ids)
+    assert_close_bf16(bf16_to_np(got_tc), ref, what="mxfp4 grouped GEMM, tensor-memory kernel")
+    assert_close_bf16(bf16_to_np(got_ws), ref, what="mxfp4 grouped GEMM, weight-streaming kernel")
