@@ -174,7 +174,9 @@ typedef struct {
  * cap_tokens slots (moe_align_capacity): h [rows_h, I] (f16 for MXFP4 weights, bf16 for bf16
  * weights), o [T_rows*k, K] fp32 and x as f16 [rows_x, K], each 256-byte aligned.  rows_h =
  * T_rows*k and rows_x = T_rows up to 256 rows; above that h and x may be kept in
- * alignment-slot order and rows_h = rows_x = cap_tokens.  Returns 0 for a negative argument. */
+ * alignment-slot order and rows_h = rows_x = cap_tokens, and two small regions (one bit per
+ * output tile of each GEMM) follow, which mark tiles whose weight scales need the exact
+ * second pass.  Returns 0 for a negative argument. */
 size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t I, int64_t cap_tokens);
 
 /* One MoE expert layer over the alignment of moe_align: both grouped GEMMs run as single
@@ -187,6 +189,13 @@ size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t 
  *
  * For every real token t < T_real (the others, e.g. bucket pad rows, are computed and
  * then sliced off):
+ * Exactness of the W4A16 tensor-core path (above 256 rows): weights are decoded to float16
+ * as code * 2^(E8M0 - 127), exact while that exponent lies in -23..13; a tile with a
+ * nonzero block outside that window is computed again by a second pass with each weight row
+ * shifted by a power of two (undone on its fp32 accumulator), so any E8M0 scale gives the
+ * exact products the weight-streaming path gives below 256 rows.  Only a weight row whose
+ * nonzero blocks span more than 36 octaves of scale is reported (MOE_ERR_RANGE).
+ *
  *   gu = x_t . W1[e]^T + b1[e];  h = silu(gu[:I]) * gu[I:]  (SwiGLU) or
  *        h = max(gu, 0)^2  (relu^2; a NaN stays NaN)  (fp32, then stored as the MMA
  *        operand type of GEMM2: f16 RNE for MXFP4 weights -- |h| or |x| > 65504 sets
@@ -250,8 +259,11 @@ moe_status moe_forward_no_alloc(const moe_weights* W, const void* x, const uint8
 /* Workspace bytes that let moe_grouped_gemm run W4A16 (MOE_Q_MXFP4_W4A16) weights on the
  * tensor cores: above 256 token rows the tcgen05 kernel reads A as float16, and the call
  * converts A into the workspace first (rows x Kin x 2 bytes, rows = T*k if a_per_pair else
- * T).  0 for the other modes, for T <= 256, or for invalid sizes. */
-size_t moe_grouped_gemm_workspace_size(moe_quant quant, int64_t T, int32_t k, int32_t Kin, int32_t a_per_pair);
+ * T), followed by one bit per output tile that marks tiles whose weight scales need the
+ * exact second pass (see moe_forward).  0 for the other modes, for T <= 256, or for invalid
+ * sizes. */
+size_t moe_grouped_gemm_workspace_size(moe_quant quant, int64_t T, int32_t k, int32_t N, int32_t Kin,
+                                       int32_t a_per_pair);
 
 /* out[p, :] = A[src(p), :] . W[e_p]^T + bias[e_p]   for every pair p < T*k, in bf16 RNE.
  * A: [T, Kin] (a_per_pair == 0, src = p / k) or [T*k, Kin] (a_per_pair != 0, src = p);

@@ -84,7 +84,7 @@ def load(path: str | None = None):
         "moe_forward_no_alloc": (I32, [P, P, P, I64, I64, I32, P, P, P, P, P, I32, I64, P, P]),
         "moe_grouped_gemm": (I32, [ctypes.c_int, I32, I32, I32, P, P, I32, P, P, P, I64, I32,
                                    P, P, P, I32, I64, P, P]),
-        "moe_grouped_gemm_workspace_size": (SZ, [ctypes.c_int, I64, I32, I32, I32]),
+        "moe_grouped_gemm_workspace_size": (SZ, [ctypes.c_int, I64, I32, I32, I32, I32]),
         "moe_mx_quantize": (I32, [P, I64, I32, P, P, P]),
         "moe_gemm_per_token": (I32, [I32, I32, I32, P, P, P, P, P, P, I64, P, P]),
         "moe_wgrad": (I32, [P, P, I32, I64, I32, I32, I32, I32, P, P, P, I32, I64, P, I32, P]),
@@ -223,9 +223,9 @@ def moe_grouped_gemm(quant, E, N, Kin, a, a_scale, a_per_pair, w, w_scale, bias,
                                           _ptr(out), _ctx(ctx)))
 
 
-def moe_grouped_gemm_workspace_size(quant, T, k, Kin, a_per_pair) -> int:
+def moe_grouped_gemm_workspace_size(quant, T, k, N, Kin, a_per_pair) -> int:
     q = QUANT[quant] if isinstance(quant, str) else quant
-    return load().moe_grouped_gemm_workspace_size(q, T, k, Kin, int(a_per_pair))
+    return load().moe_grouped_gemm_workspace_size(q, T, k, N, Kin, int(a_per_pair))
 
 
 def moe_mx_quantize(x, rows, cols, codes, scales, ctx=None):

@@ -220,12 +220,23 @@ static void forward_scratch_rows(int64_t T_rows, int32_t k, int64_t cap_tokens, 
   *rows_x = slots ? cap_tokens : T_rows;
 }
 
+// Bytes of the two GEMMs' marks of out-of-window weight tiles (the slot-ordered tensor-memory
+// path only; see moe_launch::GroupedGemm::fix_bits).
+static size_t forward_fix_bytes(int64_t T_rows, int32_t k, int32_t K, int32_t I, int64_t cap_tokens) {
+  int64_t rows_h, rows_x;
+  forward_scratch_rows(T_rows, k, cap_tokens, &rows_h, &rows_x);
+  if (rows_h <= T_rows * k) return 0;  // pair order: the weight-streaming kernels
+  const int64_t blocks = cap_tokens / 128;
+  return moe_launch::ts_fix_bytes(blocks, I) + moe_launch::ts_fix_bytes(blocks, K);
+}
+
 size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t I, int64_t cap_tokens) {
   if (T_rows < 0 || k < 1 || K < 1 || I < 1 || cap_tokens < 0) return 0;
   const int64_t P = T_rows * k;
   int64_t rows_h, rows_x;
   forward_scratch_rows(T_rows, k, cap_tokens, &rows_h, &rows_x);
-  return round256((size_t)rows_h * I * 2) + round256((size_t)P * K * 4) + round256((size_t)rows_x * K * 2);
+  return round256((size_t)rows_h * I * 2) + round256((size_t)P * K * 4) + round256((size_t)rows_x * K * 2) +
+         forward_fix_bytes(T_rows, k, K, I, cap_tokens);
 }
 
 // The MXFP8 layer: GEMM1 + SwiGLU, h quantised to MXFP8 (E4M3 codes and one E8M0 scale per
@@ -366,6 +377,8 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
   g2.Nw = K; g2.Kin = I; g2.Nout = K; g2.out = o;
   // Above the threshold the MXFP4 path keeps x and h in alignment-slot order: a block of 128
   // slots is then 128 consecutive rows, which the tensor-memory kernel loads as one box.
+  uint8_t* fix = nullptr;  // marks of out-of-window weight tiles (tensor-memory kernels)
+  size_t fix_bytes = 0;
   if (fp4 && rows_x == rows_h && rows_h > P) {
     moe_launch::GroupedGemm s1 = g1, s2 = g2;
     s1.act_by_slot = 1; s1.out_by_slot = 1;
@@ -373,9 +386,21 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
     if (blocks * block_m <= rows_h && moe_launch::ts_supported(s1) && moe_launch::ts_supported(s2)) {
       g1 = s1;
       g2 = s2;
+      const int64_t cap_blocks = cap_tokens / 128;
+      fix = static_cast<uint8_t*>(x16) + round256((size_t)rows_x * K * 2);
+      const size_t f1 = moe_launch::ts_fix_bytes(cap_blocks, I);
+      fix_bytes = f1 + moe_launch::ts_fix_bytes(cap_blocks, K);
+      g1.fix_count = reinterpret_cast<int32_t*>(fix);
+      g1.fix_bits = reinterpret_cast<uint32_t*>(fix + 256);
+      g2.fix_count = reinterpret_cast<int32_t*>(fix + f1);
+      g2.fix_bits = reinterpret_cast<uint32_t*>(fix + f1 + 256);
     }
   }
   rec(ctx, 0, 4);
+  if (fix) {
+    st = cuda_status(cudaMemsetAsync(fix, 0, fix_bytes, s), "moe_forward marks");
+    if (st != MOE_OK) return st;
+  }
   if (fp4 && g1.act_by_slot) {
     st = cuda_status(moe_launch::gather_rows_f16(x, sorted_token_ids, num_tokens_post_padded, P, k, K,
                                                  blocks * block_m, x16, status_of(ctx), s),
@@ -396,12 +421,18 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
   return st;
 }
 
-size_t moe_grouped_gemm_workspace_size(moe_quant quant, int64_t T, int32_t k, int32_t Kin, int32_t a_per_pair) {
-  // the W4A16 tensor-memory kernel reads the activations as f16: one converted copy of A
-  if (quant != MOE_Q_MXFP4_W4A16 || T <= moe_launch::kPrefillRowsAbove || k < 1 || Kin < 1) return 0;
+// Block slots a grouped GEMM over P pairs can launch for, whatever E: every used block holds
+// a pair, and the launch covers at most P / bm + min(E, P) of them.
+static int64_t grouped_blocks_bound(int64_t P) { return P + P / 128 + 1; }
+
+size_t moe_grouped_gemm_workspace_size(moe_quant quant, int64_t T, int32_t k, int32_t N, int32_t Kin,
+                                       int32_t a_per_pair) {
+  // the W4A16 tensor-memory kernel reads the activations as f16: one converted copy of A, and
+  // the marks of out-of-window weight tiles
+  if (quant != MOE_Q_MXFP4_W4A16 || T <= moe_launch::kPrefillRowsAbove || k < 1 || N < 1 || Kin < 1) return 0;
   if (!pairs_fit(T, k)) return 0;
   const int64_t rows = a_per_pair ? T * k : T;
-  return round256((size_t)rows * Kin * 2);
+  return round256((size_t)rows * Kin * 2) + moe_launch::ts_fix_bytes(grouped_blocks_bound(T * k), N);
 }
 
 moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin, const void* a,
@@ -442,16 +473,22 @@ moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin, 
   moe_launch::apply_debug_stall(g);
   // W4A16 above the tensor-memory threshold, with a workspace for the f16 copy of A: the
   // tcgen05 kernel (decoded weights in tensor memory) where it takes the shape
-  const size_t ws_need = moe_grouped_gemm_workspace_size(quant, T, k, Kin, a_per_pair);
+  const size_t ws_need = moe_grouped_gemm_workspace_size(quant, T, k, N, Kin, a_per_pair);
   if (ws_need > 0 && ctx && ctx->workspace && ctx->workspace_bytes >= ws_need && aligned16(ctx->workspace)) {
     moe_launch::GroupedGemm gt = g;
     gt.act = ctx->workspace;
     gt.act_fmt = moe_launch::ACT_F16;
+    const int64_t rows = a_per_pair ? P : T;
+    uint8_t* fix = static_cast<uint8_t*>(ctx->workspace) + round256((size_t)rows * Kin * 2);
+    gt.fix_count = reinterpret_cast<int32_t*>(fix);
+    gt.fix_bits = reinterpret_cast<uint32_t*>(fix + 256);
     if (moe_launch::ts_supported(gt)) {
-      const int64_t rows = a_per_pair ? P : T;
       rec(ctx, 0, 2);
-      st = cuda_status(moe_launch::bf16_to_f16(a, ctx->workspace, rows * Kin, status_of(ctx), stream_of(ctx)),
-                       "moe_grouped_gemm activations");
+      st = cuda_status(cudaMemsetAsync(fix, 0, moe_launch::ts_fix_bytes(grouped_blocks_bound(P), N), stream_of(ctx)),
+                       "moe_grouped_gemm marks");
+      if (st == MOE_OK)
+        st = cuda_status(moe_launch::bf16_to_f16(a, ctx->workspace, rows * Kin, status_of(ctx), stream_of(ctx)),
+                         "moe_grouped_gemm activations");
       if (st == MOE_OK) st = cuda_status(moe_launch::prefill_ts(gt, stream_of(ctx)), "moe_grouped_gemm");
       rec(ctx, 1, 2);
       return st;

@@ -68,7 +68,18 @@ struct GroupedGemm {
   int32_t* status;
   int64_t wait_ns;          // limit of the tensor-memory kernels' waits (0: the 2 s default)
   int stall;                // stalled self-test: the copy and MMA roles do nothing
+  // W4A16 tensor-memory kernel: tiles with a weight block scale outside the f16 window are
+  // marked here (one bit per tile, zeroed by the caller) and done again with shifted
+  // weights by a second launch; null: such blocks are reported (MOE_ERR_RANGE)
+  uint32_t* fix_bits;
+  int32_t* fix_count;
 };
+
+// Bytes of the marks of one W4A16 tensor-memory GEMM over at most `blocks` alignment blocks
+// and `nout` output features (256-byte aligned: the count, then one bit per tile).
+size_t ts_fix_bytes(int64_t blocks, int64_t nout);
+// Tiles of that GEMM: feature tiles per block (128 features, two matrices per tile).
+int64_t ts_fix_tiles(int64_t blocks, int64_t nout);
 
 // Stall limit set by moe_debug_stall_tensor_kernels (0: normal operation), and its
 // application to one GEMM's arguments.

@@ -42,12 +42,17 @@
 // MMA lanes do nothing, so the decoders and the epilogue wait on barriers no one arrives on
 // and give up after GroupedGemm::wait_ns with no copy or MMA in flight.
 //
-// f16 operands: a decoded weight code * 2^se is exact when se is within -23..13.  A weight
-// row whose block scales fall outside that window is decoded as code * 2^(se - c) with one
-// shift c per row and tile (the largest block scale of the row mapped to 2^13), and the
-// epilogue multiplies that row's accumulator by 2^c: a power of two, so the result is the
-// same as with exact f16 weights.  Only a row whose nonzero blocks span more than 36
-// octaves of scale still has a block outside the window; it sets MOE_ERR_RANGE.  Each output
+// f16 operands: a decoded weight code * 2^se is exact when se is within -23..13.  The main
+// launch decodes every block that way and only marks a tile (a bit in GroupedGemm::fix_bits,
+// counted in fix_count) when one of its blocks with nonzero codes has a scale outside that
+// window; a second launch of the same kernel (FIX) then does exactly the marked tiles again,
+// with every weight row decoded as code * 2^(se - c) for one shift c per row (its largest
+// block scale mapped to 2^13) and the row's accumulator multiplied by 2^c in the epilogue:
+// a power of two, so the result is the same as with exact f16 weights.  It exits at once
+// when no tile is marked, so weights with ordinary scales cost one empty launch.  Only a
+// row whose nonzero blocks span more than 36 octaves of scale still has a block outside
+// the window; it sets MOE_ERR_RANGE (as does any out-of-window block when the caller gives
+// no room for the marks).  Each output
 // depends on its own token row only and K is always reduced in the same order, so padded
 // and unpadded batches give identical real rows.
 #include "moe_common.cuh"
@@ -117,20 +122,29 @@ __host__ __device__ inline TLayout tlayout(int epi) {
   return L;
 }
 
+template <bool FIX = false>
 __device__ __forceinline__ bool tile_info(const TArgs& ta, int64_t t, int ntpp, int64_t& blk, int& mt,
                                           int64_t& e) {
   blk = t / ta.m_tiles;
   mt = (int)(t - blk * ta.m_tiles);
   if (blk * ta.g.bm >= ntpp) return false;
+  if (FIX && ((ta.g.fix_bits[t >> 5] >> (t & 31)) & 1u) == 0) return false;  // only the marked tiles
   e = ta.g.expert_ids[blk];
   return e >= 0 && e < ta.g.E;
 }
 
+// Marks tile t for the FIX launch (counted once).
+__device__ __forceinline__ void mark_tile(const GroupedGemm& a, int64_t t) {
+  const uint32_t bit = 1u << (t & 31);
+  if ((atomicOr(&a.fix_bits[t >> 5], bit) & bit) == 0) atomicAdd(a.fix_count, 1);
+}
+
 // First tile of this block's sequence at or after t that some role works on (or >= tiles).
+template <bool FIX>
 __device__ __forceinline__ int64_t next_tile(const TArgs& ta, int64_t t, int ntpp) {
   int64_t blk, e;
   int mt;
-  while (t < ta.tiles && !tile_info(ta, t, ntpp, blk, mt, e)) t += gridDim.x;
+  while (t < ta.tiles && !tile_info<FIX>(ta, t, ntpp, blk, mt, e)) t += gridDim.x;
   return t;
 }
 
@@ -162,12 +176,13 @@ __device__ __forceinline__ int64_t tile_wrow(const GroupedGemm& a, int64_t e, in
   return e * a.Nw + (SWIGLU ? (int64_t)m * a.Nout : 0) + tile_feature<SWIGLU>(mt, m, r);
 }
 
-template <int EPI>
+template <int EPI, bool FIX>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_ts_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                       const __grid_constant__ CUtensorMap tmap_h, TArgs ta) {
   constexpr bool SW = (EPI == EPI_SWIGLU);
   const GroupedGemm& a = ta.g;
+  if (FIX && *a.fix_count == 0) return;  // no marked tile: nothing to do again
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr bool R2 = (EPI == EPI_RELU2);
@@ -182,8 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = raw_empty + kRawSlots;                          // [2]
   uint64_t* tempty = tfull + 2;                                     // [2]
   uint64_t* drain = tempty + 2;
-  uint64_t* epi_bar = drain + 1;  // the four epilogue warps meet here (bounded, unlike bar.sync)
-  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(epi_bar + 1);
+  uint64_t* epi_bar = drain + 1;  // the eight epilogue warps meet here (bounded, unlike bar.sync)
+  uint64_t* shift_full = epi_bar + 1;  // [2] FIX: a tile's row shifts written (by tile parity)
+  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(shift_full + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(taddr_s + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -206,6 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(drain, kMats);
     tc::mbar_init(epi_bar, 8);
+    tc::mbar_init(&shift_full[0], 8);
+    tc::mbar_init(&shift_full[1], 8);
     *abort_flag = 0;
     tc::mbar_fence_init();
   }
@@ -237,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t t = blockIdx.x; t < ta.tiles && !*abort_flag; t += gridDim.x) {
       int64_t blk, e;
       int mt;
-      if (!tile_info(ta, t, ntpp, blk, mt, e)) continue;
+      if (!tile_info<FIX>(ta, t, ntpp, blk, mt, e)) continue;
       // token rows of slots 4 lane .. 4 lane + 3 (this lane's gather); an empty slot reads
       // past the end of the activations (zeros).  Rows already in slot order need no gather.
       int32_t y[4] = {0, 0, 0, 0};
@@ -332,12 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int8_t* shift_s = reinterpret_cast<int8_t*>(smem + L.shift);
     uint32_t tseq = 0;
     uint32_t it = 0, gi = 0;
-    int64_t t = next_tile(ta, blockIdx.x, ntpp);
+    int64_t t = next_tile<FIX>(ta, blockIdx.x, ntpp);
     int64_t blk = 0, e = 0;
     int mt = 0;
     uint32_t sc_next[2] = {0x7f7f7f7fu, 0x7f7f7f7fu};
     if (t < ta.tiles) {
-      tile_info(ta, t, ntpp, blk, mt, e);
+      tile_info<FIX>(ta, t, ntpp, blk, mt, e);
       load_scales(e, mt, 0, sc_next);
     }
     while (t < ta.tiles && !*abort_flag) {
@@ -345,13 +363,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t tn = t + gridDim.x;
       const int64_t blk_n = tn / ta.m_tiles;
       const int mt_n = (int)(tn - blk_n * ta.m_tiles);
-      const bool live_n = tn < ta.tiles && blk_n * a.bm < ntpp;
+      const bool live_n = tn < ta.tiles && blk_n * a.bm < ntpp &&
+                          (!FIX || ((a.fix_bits[tn >> 5] >> (tn & 31)) & 1u) != 0);
       const int64_t e_n = live_n ? (int64_t)a.expert_ids[blk_n] : -1;
       const bool next_ok = e_n >= 0 && e_n < a.E;
-      int csh = row_shift(e, mt);
-      csh = csh < -128 ? -128 : (csh > 127 ? 127 : csh);
-      shift_s[((tseq & 1) * kMats + m) * kTM + r] = (int8_t)csh;
+      int csh = 0;
+      if (FIX) {  // this row's shift, for the decoding below and (through shift_full) the epilogue
+        csh = row_shift(e, mt);
+        csh = csh < -128 ? -128 : (csh > 127 ? 127 : csh);
+        shift_s[((tseq & 1) * kMats + m) * kTM + r] = (int8_t)csh;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&shift_full[tseq & 1]);
+      }
       ++tseq;
+      bool oow = false;  // a block with nonzero codes outside the f16 window
       bool ok = true;
       uint32_t sc0 = 0u, sc1 = 0u;
       int rs = 0;
@@ -383,8 +408,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v[32];
           const uint4 w0 = *reinterpret_cast<const uint4*>(rowp + (((2 * kg) ^ (r & 7)) << 4));
           const uint4 w1 = *reinterpret_cast<const uint4*>(rowp + (((2 * kg + 1) ^ (r & 7)) << 4));
-          decode_block(w0, shifted_scale((scw >> sh) & 0xffu, csh), v, bad);
-          decode_block(w1, shifted_scale((scw >> (sh + 8)) & 0xffu, csh), v + 16, bad);
+          if (FIX) {
+            decode_block(w0, shifted_scale((scw >> sh) & 0xffu, csh), v, oow);
+            decode_block(w1, shifted_scale((scw >> (sh + 8)) & 0xffu, csh), v + 16, oow);
+          } else {
+            decode_block(w0, (scw >> sh) & 0xffu, v, oow);
+            decode_block(w1, (scw >> (sh + 8)) & 0xffu, v + 16, oow);
+          }
           tmem_st16(dst, v);
           tmem_st16(dst + 16, v + 16);
         }
@@ -403,15 +433,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
         break;
       }
+      // an out-of-window block: the FIX launch does the tile again (or, out of room for the
+      // marks or in that launch itself, the block cannot be exact: reported)
+      if (oow) {
+        if (!FIX && a.fix_bits) mark_tile(a, t);
+        else bad = true;
+      }
       if (next_ok) {
         t = tn;
         blk = blk_n;
         mt = mt_n;
         e = e_n;
       } else {  // no live next tile, or an expert id the roles skip: search on
-        t = next_tile(ta, tn, ntpp);
+        t = next_tile<FIX>(ta, tn, ntpp);
         if (t < ta.tiles) {
-          tile_info(ta, t, ntpp, blk, mt, e);
+          tile_info<FIX>(ta, t, ntpp, blk, mt, e);
           load_scales(e, mt, 0, sc_next);
         }
       }
@@ -428,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t t = blockIdx.x; t < ta.tiles && !*abort_flag; t += gridDim.x) {
         int64_t blk, e;
         int mt;
-        if (!tile_info(ta, t, ntpp, blk, mt, e)) continue;
+        if (!tile_info<FIX>(ta, t, ntpp, blk, mt, e)) continue;
         const int acc = 0;  // one accumulator set (two 128-column accumulators)
         if (!tc::mbar_wait(&tempty[acc], (acc_it & 1) ^ 1, wb)) {
           moe::set_status(a.status, MOE_ERR_TIMEOUT);
@@ -490,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t t = blockIdx.x; t < ta.tiles && !*abort_flag; t += gridDim.x) {
       int64_t blk, e;
       int mt;
-      if (!tile_info(ta, t, ntpp, blk, mt, e)) continue;
+      if (!tile_info<FIX>(ta, t, ntpp, blk, mt, e)) continue;
       const int acc = 0;  // one accumulator set
       int pls[kEpiCols / 32];  // pair of token column cbase + 32 i + lane, read while the MMAs run
       float wls[kEpiCols / 32];
@@ -510,9 +546,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // feature fA in accumulator 0 and fB in accumulator 1
       const int64_t fA = tile_feature<SW>(mt, 0, 32 * q + lane), fB = tile_feature<SW>(mt, 1, 32 * q + lane);
       const bool vA = fA < a.Nout, vB = fB < a.Nout;
-      // 2^c of the two rows of this lane (their weights were decoded with 2^-c)
-      const int8_t* shift_s = reinterpret_cast<const int8_t*>(smem + L.shift) + (acc_it & 1) * kMats * kTM;
-      const float fsA = pow2f(shift_s[32 * q + lane]), fsB = pow2f(shift_s[kTM + 32 * q + lane]);
+      // FIX: 2^c of the two rows of this lane (their weights were decoded with 2^-c)
+      float fsA = 1.f, fsB = 1.f;
+      if (FIX) {
+        if (!tc::mbar_wait(&shift_full[acc_it & 1], (acc_it >> 1) & 1, wb)) {
+          moe::set_status(a.status, MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        const int8_t* shift_s = reinterpret_cast<const int8_t*>(smem + L.shift) + (acc_it & 1) * kMats * kTM;
+        fsA = pow2f(shift_s[32 * q + lane]);
+        fsB = pow2f(shift_s[kTM + 32 * q + lane]);
+      }
       float b0 = 0.f, b1 = 0.f;
       if (bias) {
         if (vA) b0 = moe::bf16_bits_to_f32(bias[e * a.Nw + fA]);
@@ -618,22 +663,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int sm_count_ts() { return moe_launch::sm_count_current(); }
 
-template <int EPI>
-cudaError_t launch_ts(const TArgs& ta, const CUtensorMap& mx, const CUtensorMap& mw, const CUtensorMap& mh,
-                      cudaStream_t stream) {
+template <int EPI, bool FIX>
+cudaError_t launch_ts1(const TArgs& ta, const CUtensorMap& mx, const CUtensorMap& mw, const CUtensorMap& mh,
+                       cudaStream_t stream) {
   const TLayout L = tlayout(EPI);
-  cudaError_t err = cudaFuncSetAttribute(prefill_ts_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  cudaError_t err =
+      cudaFuncSetAttribute(prefill_ts_kernel<EPI, FIX>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
   int64_t grid = sm_count_ts();
   if (ta.tiles < grid) grid = ta.tiles;
   if (grid <= 0) return cudaSuccess;
-  prefill_ts_kernel<EPI><<<(unsigned)grid, kThreads, L.total, stream>>>(mx, mw, mh, ta);
+  prefill_ts_kernel<EPI, FIX><<<(unsigned)grid, kThreads, L.total, stream>>>(mx, mw, mh, ta);
   return cudaGetLastError();
+}
+
+// The main launch, then (with room for the marks) the launch that does the marked tiles
+// again; the caller zeroed the marks and their count.
+template <int EPI>
+cudaError_t launch_ts(const TArgs& ta, const CUtensorMap& mx, const CUtensorMap& mw, const CUtensorMap& mh,
+                      cudaStream_t stream) {
+  cudaError_t err = launch_ts1<EPI, false>(ta, mx, mw, mh, stream);
+  if (err != cudaSuccess || ta.g.fix_bits == nullptr) return err;
+  return launch_ts1<EPI, true>(ta, mx, mw, mh, stream);
 }
 
 }  // namespace
 
 namespace moe_launch {
+
+// An upper bound of the tiles of any epilogue: 128 features per tile (SwiGLU; the others
+// take 256 per tile).
+int64_t ts_fix_tiles(int64_t blocks, int64_t nout) { return blocks * ((nout + kTM - 1) / kTM); }
+
+size_t ts_fix_bytes(int64_t blocks, int64_t nout) {
+  const int64_t words = (ts_fix_tiles(blocks, nout) + 31) / 32;
+  return (size_t)(256 + (words * 4 + 255) / 256 * 256);
+}
 
 bool ts_supported(const GroupedGemm& g) {
   if (g.wfmt != WF_MXFP4 || g.act_fmt != ACT_F16) return false;

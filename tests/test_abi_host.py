@@ -74,7 +74,8 @@ def test_workspace_size(lib):
     assert n == r(P * 2880 * 2) + r(P * 2880 * 4) + r(64 * 2880 * 2)
     cap, _ = moe.moe_align_capacity(4 * 1000, 128, 128)
     n = moe.moe_forward_workspace_size(1000, 4, 2880, 2880, cap)
-    assert n == r(cap * 2880 * 2) + r(4000 * 2880 * 4) + r(cap * 2880 * 2)  # slot order
+    assert n == r(cap * 2880 * 2) + r(4000 * 2880 * 4) + r(cap * 2880 * 2) + \
+        2 * fix_bytes(cap // 128, 2880)  # slot order, and the marks of both GEMMs
     assert moe.moe_forward_workspace_size(-1, 4, 1, 1, 0) == 0
 
 
@@ -150,10 +151,21 @@ def test_size_overflow_is_rejected_before_any_launch(lib):
     assert ei.value.status == -2 and "64-bit" in lib.moe_last_error().decode()
 
 
+def fix_bytes(blocks, nout):
+    """The marks of one tensor-memory GEMM: a 256-byte count, then one bit per tile (128
+    output features per tile), rounded up to 256 bytes."""
+    r = lambda v: (v + 255) // 256 * 256
+    tiles = blocks * -(-nout // 128)
+    return 256 + r(-(-tiles // 32) * 4)
+
+
 def test_grouped_gemm_workspace_size(lib):
     r = lambda v: (v + 255) // 256 * 256
-    assert moe.moe_grouped_gemm_workspace_size("mxfp4", 256, 4, 2880, 0) == 0     # weight streaming
-    assert moe.moe_grouped_gemm_workspace_size("mxfp4", 257, 4, 2880, 0) == r(257 * 2880 * 2)
-    assert moe.moe_grouped_gemm_workspace_size("mxfp4", 300, 4, 2880, 1) == r(1200 * 2880 * 2)
-    assert moe.moe_grouped_gemm_workspace_size("mxfp8", 4096, 8, 7168, 0) == 0     # reads E4M3 as is
-    assert moe.moe_grouped_gemm_workspace_size("bf16", 4096, 8, 7168, 0) == 0
+    blocks = lambda P: P + P // 128 + 1
+    assert moe.moe_grouped_gemm_workspace_size("mxfp4", 256, 4, 5760, 2880, 0) == 0     # weight streaming
+    assert moe.moe_grouped_gemm_workspace_size("mxfp4", 257, 4, 5760, 2880, 0) == \
+        r(257 * 2880 * 2) + fix_bytes(blocks(257 * 4), 5760)
+    assert moe.moe_grouped_gemm_workspace_size("mxfp4", 300, 4, 2880, 2880, 1) == \
+        r(1200 * 2880 * 2) + fix_bytes(blocks(1200), 2880)
+    assert moe.moe_grouped_gemm_workspace_size("mxfp8", 4096, 8, 4096, 7168, 0) == 0     # reads E4M3 as is
+    assert moe.moe_grouped_gemm_workspace_size("bf16", 4096, 8, 4096, 7168, 0) == 0
