@@ -42,7 +42,10 @@ L2_BYTES = 129 * 1024 * 1024
 # reported as null.
 TRAFFIC = {
     "decode_gemm.cu:gemm1@decode_mxfp4": {
-        "src": "f6b2ff3ac8958c8e", "bytes": 997873152 + 4293888},
+        "src": "1d10e33c80844cd4", "bytes": 997873920 + 4255232},
+    # both launches of the call: the main pass and the (empty) exact-scale pass
+    "prefill_ts.cu:gemm1@prefill_mxfp4": {
+        "src": "22f52e91b9b3601a", "bytes": 2601815296 + 1444242688 + 68352},
 }
 
 
