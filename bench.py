@@ -603,6 +603,9 @@ def bench_mxfp8_wgrad(args, rank, world, local_rank):
     out2 = torch.empty((P, K), dtype=torch.bfloat16, device=dev)
     dW1 = torch.empty((E, 2 * I, K), dtype=torch.float32, device=dev)
     dW2 = torch.empty((E, K, I), dtype=torch.float32, device=dev)
+    # the weight gradients' slot-ordered copies of grad and input (one workspace, used in turn)
+    wg_ws = torch.empty(max(moe.moe_wgrad_workspace_size(E, 2 * I, K, bm, cap, 0),
+                            moe.moe_wgrad_workspace_size(E, K, I, bm, cap, 0), 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def ev():
@@ -611,7 +614,8 @@ def bench_mxfp8_wgrad(args, rank, world, local_rank):
         return e
 
     def step(evs=None):
-        c = [moe.Ctx(dev_status=status, events=None if evs is None else evs[i]) for i in range(4)]
+        c = [moe.Ctx(dev_status=status, events=None if evs is None else evs[i], workspace=wg_ws if i >= 2 else None)
+             for i in range(4)]
         moe.moe_grouped_gemm("mxfp8", E, 2 * I, K, g["x_codes"], g["x_scale"], 0, g["w1"], g["w1_scale"],
                              None, T, k, srt, eid, ntpp, bm, cap, out1, c[0])
         moe.moe_grouped_gemm("mxfp8", E, K, I, g["a2_codes"], g["a2_scale"], 1, g["w2"], g["w2_scale"],

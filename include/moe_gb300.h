@@ -275,7 +275,7 @@ size_t moe_grouped_gemm_workspace_size(moe_quant quant, int64_t T, int32_t k, in
  * Kernels: MXFP8 above 256 token rows runs the block-scaled tensor-core kernel (K and N
  * multiples of 128); W4A16 above 256 rows runs the tcgen05 kernel with decoded weights in
  * tensor memory when ctx->workspace holds moe_grouped_gemm_workspace_size() bytes (block_m
- * 128, Kin a multiple of 64 up to 4096; |A| <= 65504, else MOE_ERR_RANGE in dev_status);
+ * 128, Kin a multiple of 64; |A| <= 65504, else MOE_ERR_RANGE in dev_status);
  * every other call runs the weight-streaming kernel, which needs no workspace.  The kernel
  * choice depends on T only through the bucket value 256, and each kernel reduces K in one
  * fixed order. */
@@ -325,6 +325,12 @@ moe_status moe_gemm_per_token(int32_t E, int32_t N, int32_t K, const uint8_t* a,
  * Weight gradient ([AITER] Summary: moe_wgrad; Tests & Benchmarks)                      *
  * ------------------------------------------------------------------------------------ */
 
+/* Workspace bytes for moe_wgrad's slot-ordered copies (cap_tokens x N and cap_tokens x Kin
+ * bf16, each 256-byte aligned): mode 0 with N a multiple of 128, Kin of 64, block_m of 64
+ * and E <= 1024; 0 otherwise (moe_wgrad then needs none). */
+size_t moe_wgrad_workspace_size(int32_t E, int32_t N, int32_t Kin, int32_t block_m, int64_t cap_tokens,
+                                int32_t mode);
+
 /* dW[e] = sum over pairs p routed to e of grad[p, :]^T (outer) input[src(p), :], fp32
  * accumulation, read straight from the alignment outputs (sentinel slots add nothing).
  * grad: [T*k, N] bf16 indexed by pair; input: [T, Kin] bf16 (input_per_pair == 0,
@@ -333,7 +339,10 @@ moe_status moe_gemm_per_token(int32_t E, int32_t N, int32_t K, const uint8_t* a,
  *         repeated calls give identical bits.
  * mode 1: accumulate -- the library zeroes dW, then adds token-chunk partial sums with
  *         atomics (summation order varies between runs).
- * N and Kin must be multiples of 64.  Needs no workspace. */
+ * N and Kin must be multiples of 64.  Needs no workspace; with ctx->workspace holding
+ * moe_wgrad_workspace_size() bytes, mode 0 first copies grad and input rows into slot order
+ * there and the tensor-core kernel loads whole stages of them by TMA -- the same sums in the
+ * same order, so the same bits as without a workspace. */
 moe_status moe_wgrad(const void* grad, const void* input, int32_t input_per_pair,
                      int64_t T, int32_t k, int32_t E, int32_t N, int32_t Kin,
                      const int32_t* sorted_token_ids, const int32_t* expert_ids,

@@ -20,7 +20,8 @@ __all__ = [
     "MoeError", "load", "Ctx", "QUANT", "ACTIVATION", "moe_align_capacity", "moe_align", "moe_bucket",
     "moe_bucket_count", "moe_bucket_pad", "moe_forward_workspace_size", "moe_forward",
     "moe_forward_no_alloc", "moe_grouped_gemm", "moe_grouped_gemm_workspace_size", "moe_mx_quantize",
-    "moe_gemm_per_token", "moe_wgrad", "moe_debug_stall_tensor_kernels", "EXPORTED_SYMBOLS",
+    "moe_gemm_per_token", "moe_wgrad", "moe_wgrad_workspace_size", "moe_debug_stall_tensor_kernels",
+    "EXPORTED_SYMBOLS",
 ]
 
 MOE_OK = 0
@@ -35,7 +36,7 @@ EXPORTED_SYMBOLS = [
     "moe_last_error", "moe_align_capacity", "moe_align", "moe_bucket", "moe_bucket_count",
     "moe_bucket_pad", "moe_forward_workspace_size", "moe_forward", "moe_forward_no_alloc",
     "moe_grouped_gemm", "moe_grouped_gemm_workspace_size", "moe_mx_quantize", "moe_gemm_per_token", "moe_wgrad",
-    "moe_debug_stall_tensor_kernels",
+    "moe_wgrad_workspace_size", "moe_debug_stall_tensor_kernels",
 ]
 
 
@@ -88,6 +89,7 @@ def load(path: str | None = None):
         "moe_mx_quantize": (I32, [P, I64, I32, P, P, P]),
         "moe_gemm_per_token": (I32, [I32, I32, I32, P, P, P, P, P, P, I64, P, P]),
         "moe_wgrad": (I32, [P, P, I32, I64, I32, I32, I32, I32, P, P, P, I32, I64, P, I32, P]),
+        "moe_wgrad_workspace_size": (SZ, [I32, I32, I32, I32, I64, I32]),
         "moe_debug_stall_tensor_kernels": (None, [I64]),
     }
     for name, (res, args) in sig.items():
@@ -245,6 +247,10 @@ def moe_wgrad(grad, input, input_per_pair, T, k, E, N, Kin, sorted_token_ids, ex
                                    _ptr(sorted_token_ids), _ptr(expert_ids),
                                    _ptr(num_tokens_post_padded), block_m, cap_tokens, _ptr(dW),
                                    int(mode), _ctx(ctx)))
+
+
+def moe_wgrad_workspace_size(E, N, Kin, block_m, cap_tokens, mode=0) -> int:
+    return load().moe_wgrad_workspace_size(E, N, Kin, block_m, cap_tokens, int(mode))
 
 
 def moe_debug_stall_tensor_kernels(stall_ns: int) -> None:

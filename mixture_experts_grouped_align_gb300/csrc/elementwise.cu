@@ -101,6 +101,20 @@ __global__ void gather_rows_f16_kernel(const uint4* __restrict__ x, const int32_
   if (bad) moe::set_status(status, MOE_ERR_RANGE);
 }
 
+// Rows of `per` 16-byte chunks into alignment-slot order: row s <- src row p / div of the
+// pair p in slot s (zeros for the sentinel), one chunk per thread.
+__global__ void gather_slot_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ sorted,
+                                        const int32_t* __restrict__ ntpp, int64_t P, int div, int64_t per,
+                                        int64_t n16, uint4* __restrict__ y) {
+  const int64_t lim = (int64_t)*ntpp * per;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16 && i < lim;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t s = i / per, c = i - s * per;
+    const int p = __ldg(sorted + s);
+    y[i] = p < P ? __ldg(src + (int64_t)(p / div) * per + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // One thread per 32-element block of a row: 128 bytes in, 32 codes and a scale byte out.
 __global__ void mx_quantize_kernel(const float4* __restrict__ x, int64_t nblocks, uint4* __restrict__ codes,
                                    uint8_t* __restrict__ scales) {
@@ -132,6 +146,15 @@ cudaError_t gather_rows_f16(const void* x, const int32_t* sorted, const int32_t*
   if (n8 == 0) return cudaSuccess;
   gather_rows_f16_kernel<<<grid_for(n8, 256), 256, 0, stream>>>((const uint4*)x, sorted, ntpp, P, k, per, n8,
                                                                  (uint4*)y, status);
+  return cudaGetLastError();
+}
+
+cudaError_t gather_slot_rows(const void* src, int64_t row_bytes, const int32_t* sorted, const int32_t* ntpp,
+                             int64_t P, int div, int64_t slots, void* y, cudaStream_t stream) {
+  const int64_t per = row_bytes / 16, n16 = slots * per;
+  if (n16 == 0) return cudaSuccess;
+  gather_slot_rows_kernel<<<grid_for(n16, 256), 256, 0, stream>>>((const uint4*)src, sorted, ntpp, P, div, per,
+                                                                  n16, (uint4*)y);
   return cudaGetLastError();
 }
 

@@ -535,6 +535,22 @@ moe_status moe_gemm_per_token(int32_t E, int32_t N, int32_t K, const uint8_t* a,
   return st;
 }
 
+// The slot-ordered copies of grad and input that let the tensor-memory wgrad load whole
+// stages by TMA: [cap_tokens, N] and [cap_tokens, Kin] bf16, each 256-byte aligned.
+static moe_launch::Wgrad wgrad_shape(int32_t E, int32_t N, int32_t Kin, int32_t block_m, int64_t cap_tokens,
+                                     int32_t mode) {
+  moe_launch::Wgrad g{};
+  g.E = E; g.N = N; g.Kin = Kin; g.bm = block_m; g.cap = cap_tokens; g.mode = mode;
+  return g;
+}
+
+size_t moe_wgrad_workspace_size(int32_t E, int32_t N, int32_t Kin, int32_t block_m, int64_t cap_tokens,
+                                int32_t mode) {
+  if (E < 1 || N < 64 || Kin < 64 || block_m < 1 || cap_tokens < 1) return 0;
+  if (!moe_launch::wgrad_tc_slot_feed(wgrad_shape(E, N, Kin, block_m, cap_tokens, mode))) return 0;
+  return round256((size_t)cap_tokens * N * 2) + round256((size_t)cap_tokens * Kin * 2);
+}
+
 moe_status moe_wgrad(const void* grad, const void* input, int32_t input_per_pair, int64_t T,
                      int32_t k, int32_t E, int32_t N, int32_t Kin, const int32_t* sorted_token_ids,
                      const int32_t* expert_ids, const int32_t* num_tokens_post_padded,
@@ -562,7 +578,27 @@ moe_status moe_wgrad(const void* grad, const void* input, int32_t input_per_pair
   g.P = P; g.k = k; g.E = E; g.N = N; g.Kin = Kin;
   g.sorted = sorted_token_ids; g.expert_ids = expert_ids; g.ntpp = num_tokens_post_padded;
   g.bm = block_m; g.cap_blocks = cap_blocks; g.dW = dW; g.mode = mode; g.status = status_of(ctx);
+  g.cap = cap_tokens;
   rec(ctx, 0, 2);
+  // With a workspace: grad and input copied into slot order first, then the tensor-memory
+  // kernel loads whole 64-slot stages by TMA (the same MMAs in the same order: same bits).
+  const size_t ws_need = moe_wgrad_workspace_size(E, N, Kin, block_m, cap_tokens, mode);
+  if (ws_need > 0 && ctx && ctx->workspace && ctx->workspace_bytes >= ws_need && aligned16(ctx->workspace)) {
+    uint8_t* ws = static_cast<uint8_t*>(ctx->workspace);
+    void* grad_s = ws;
+    void* input_s = ws + round256((size_t)cap_tokens * N * 2);
+    st = cuda_status(moe_launch::gather_slot_rows(grad, (int64_t)N * 2, sorted_token_ids, num_tokens_post_padded,
+                                                  P, 1, cap_tokens, grad_s, stream_of(ctx)),
+                     "moe_wgrad grad rows");
+    if (st == MOE_OK)
+      st = cuda_status(moe_launch::gather_slot_rows(input, (int64_t)Kin * 2, sorted_token_ids,
+                                                    num_tokens_post_padded, P, input_per_pair ? 1 : k, cap_tokens,
+                                                    input_s, stream_of(ctx)),
+                       "moe_wgrad input rows");
+    if (st != MOE_OK) return st;
+    g.grad_s = grad_s;
+    g.input_s = input_s;
+  }
   st = cuda_status(moe_launch::wgrad(g, stream_of(ctx)), "moe_wgrad");
   rec(ctx, 1, 2);
   return st;

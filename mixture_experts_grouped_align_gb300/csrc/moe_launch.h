@@ -29,6 +29,10 @@ cudaError_t mx_quantize(const float* x, int64_t rows, int cols, uint8_t* codes, 
 // Token rows of bf16 x gathered into alignment-slot order as f16 ([slots, K]).
 cudaError_t gather_rows_f16(const void* x, const int32_t* sorted, const int32_t* ntpp, int64_t P, int k,
                             int64_t K, int64_t slots, void* y, int32_t* status, cudaStream_t stream);
+// Rows of row_bytes (a multiple of 16) copied into alignment-slot order: y[s] = src[p / div]
+// for slot s < num_tokens_post_padded holding pair p < P, zeros for a sentinel slot.
+cudaError_t gather_slot_rows(const void* src, int64_t row_bytes, const int32_t* sorted, const int32_t* ntpp,
+                             int64_t P, int div, int64_t slots, void* y, cudaStream_t stream);
 
 // ---- grouped GEMMs on the weight-streaming (decode) path (decode_gemm.cu)
 enum WFmt { WF_BF16 = 0, WF_MXFP4 = 1, WF_MXFP8 = 2 };
@@ -141,11 +145,19 @@ struct Wgrad {
   float* dW;
   int mode;
   int32_t* status;
+  // slot-ordered copies of grad [cap, N] and input [cap, Kin] (gather_slot_rows), or null:
+  // with them the tensor-memory kernel loads whole 64-slot tiles by TMA
+  const void* grad_s;
+  const void* input_s;
+  int64_t cap;
 };
 cudaError_t wgrad(const Wgrad& g, cudaStream_t stream);
 
 // ---- weight gradient on the tensor-memory path (wgrad_tc.cu)
 int wgrad_tc_tile(const Wgrad& g);
+// Whether the tensor-memory kernel can read the slot-ordered copies (block_m a multiple of
+// the 64-slot stage, dW rows addressable by TMA).
+bool wgrad_tc_slot_feed(const Wgrad& g);
 cudaError_t wgrad_tc(const Wgrad& g, cudaStream_t stream);
 
 }  // namespace moe_launch

@@ -92,7 +92,7 @@ constexpr int kMmaWarp0 = 2, kEpiWarp0 = 4, kEpiWarp1 = 16, kDecWarp0 = 8;
 constexpr int kEpiCols = kTN / 2;
 constexpr int kTmemCols = 512;
 constexpr int kAcol0 = 256;  // first TMEM column of the decoded weight stages
-constexpr int kMaxKin = 4096;
+constexpr int kMaxKin = 1 << 16;  // a sanity bound: every loop and coordinate takes far more
 // The raw codes of a weight row are loaded 128 bytes (four K stages) per TMA box, into a
 // ring of their own.
 constexpr int kGroup = 4;

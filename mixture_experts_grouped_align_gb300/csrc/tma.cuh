@@ -66,6 +66,9 @@ MOE_DEV void store_2d(const CUtensorMap* map, int32_t x, int32_t y, uint32_t src
 MOE_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until the shared memory of every committed bulk store of this thread has been read.
 MOE_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Waits until the shared memory of all but the most recent committed bulk store of this
+// thread has been read.
+MOE_DEV void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // Waits until every committed bulk store of this thread has completed.
 MOE_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 

@@ -288,9 +288,9 @@ def test_relu2_w4a16_padded_equals_unpadded_and_oracle(moe, T, I):
     assert_close_bf16(bf16_to_np(yp), oracle_y(lay, w, T), what=f"relu2 w4a16 T={T}")
 
 
-def test_relu2_w4a16_long_k_runs_the_shared_memory_decode_kernel(moe):
-    """K = 4160 is past the tensor-memory kernel's limit: GEMM1 runs the shared-memory-decode
-    tensor-core kernel with the relu^2 epilogue."""
+def test_relu2_w4a16_long_k(moe):
+    """K = 4160 (65 stages of 64, an odd count of four-stage code groups: the last group is
+    one stage) through the tensor-memory kernel with the relu^2 epilogue."""
     w = synth.Workload("relu2_longk", T=300, K=4160, I=256, E=4, k=2, quant="mxfp4", seed=15,
                        scale_exp=(-7, -4), bias=True, activation="relu2")
     lay = synth.make_layer(w)

@@ -43,11 +43,19 @@ def align_dev(moe, ids, E, bm=BM):
     return srt, eid, ntpp, cap
 
 
-def wgrad_dev(moe, grad, inp, per_pair, ids, E, N, Kin, mode, bm=BM, fill=np.nan):
+def wgrad_dev(moe, grad, inp, per_pair, ids, E, N, Kin, mode, bm=BM, fill=np.nan, slot=False):
+    """slot=True gives the call moe_wgrad_workspace_size() bytes of workspace (NaN-filled), so
+    that the tensor-core kernel reads slot-ordered copies by TMA (the test asserts it applies)."""
     T, k = ids.shape
     srt, eid, ntpp, cap = align_dev(moe, ids, E, bm)
     dW = torch.full((E, N, Kin), fill, dtype=torch.float32, device="cuda")
-    moe.moe_wgrad(grad, inp, per_pair, T, k, E, N, Kin, srt, eid, ntpp, bm, cap, dW, mode)
+    ctx = None
+    if slot:
+        need = moe.moe_wgrad_workspace_size(E, N, Kin, bm, cap, mode)
+        assert need > 0
+        ws = torch.full((need // 2,), float("nan"), dtype=torch.bfloat16, device="cuda")
+        ctx = moe.Ctx(workspace=ws)
+    moe.moe_wgrad(grad, inp, per_pair, T, k, E, N, Kin, srt, eid, ntpp, bm, cap, dW, mode, ctx)
     torch.cuda.synchronize()
     return dW
 
@@ -80,6 +88,27 @@ def test_wgrad_small(moe, mode, per_pair, bm):
     dW = wgrad_dev(moe, dev(g), dev(x), per_pair, ids, E, N, Kin, mode, bm=bm).cpu().numpy()
     check_wgrad(dW, ofmt.bf16_decode(g), ofmt.bf16_decode(x), ids, E, per_pair, what=f"mode {mode}")
     assert np.all(dW[E - 1] == 0)                   # empty expert written as zeros
+
+
+@pytest.mark.parametrize("per_pair", [False, True])
+@pytest.mark.parametrize("bm", [128, 64])
+@pytest.mark.parametrize("N,Kin", [(128, 192), (256, 448), (384, 256)])
+def test_wgrad_slot_feed(moe, per_pair, bm, N, Kin):
+    """The slot-ordered feed (workspace given): against the oracle, and bit-identical to the
+    gather feed on the same inputs (the same MMAs over the same stages in the same order).
+    Kin = 192 and 448 take 192- and 64-column tiles; N = 256 <= Kin and N = 384 > Kin walk
+    the tiles of an expert in the two orders."""
+    rng = np.random.default_rng(17)
+    T, E, k = 333, 7, 3
+    ids = np.stack([rng.choice(E - 1, k, replace=False) for _ in range(T)]).astype(np.int32)  # E-1 empty
+    g = synth.to_bf16_bits(rng.standard_normal((T * k, N)))
+    x = synth.to_bf16_bits(rng.standard_normal((T * k if per_pair else T, Kin)))
+    a = wgrad_dev(moe, dev(g), dev(x), per_pair, ids, E, N, Kin, 0, bm=bm, slot=True)
+    b = wgrad_dev(moe, dev(g), dev(x), per_pair, ids, E, N, Kin, 0, bm=bm)
+    assert torch.equal(a, b)
+    dW = a.cpu().numpy()
+    check_wgrad(dW, ofmt.bf16_decode(g), ofmt.bf16_decode(x), ids, E, per_pair, what="slot feed")
+    assert np.all(dW[E - 1] == 0)
 
 
 @pytest.mark.parametrize("N,Kin", [(64, 64), (128, 320)])   # mma.sync path / tcgen05 path
@@ -141,11 +170,11 @@ def test_wgrad_full_size_sampled(moe):
         cols = np.sort(rng.choice(Kin, 64, replace=False))
         gs = host_bf16(grad[:, torch.from_numpy(rows).cuda()])      # [P, 8]
         xs = host_bf16(inp[:, torch.from_numpy(cols).cuda()])       # [T or P, 64]
-        for mode in (0, 1):
-            dW = wgrad_dev(moe, grad, inp, per_pair, ids, E, N, Kin, mode)
+        for mode, slot in ((0, False), (0, True), (1, False)):
+            dW = wgrad_dev(moe, grad, inp, per_pair, ids, E, N, Kin, mode, slot=slot)
             got = np.stack([dW[e][torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].cpu().numpy()
                             for e in experts])
             assert np.all(got[1] == 0) and cnt[experts[1]] == 0
-            check_wgrad(got, gs, xs, ids, E, per_pair, experts, what=f"N={N} mode {mode}")
+            check_wgrad(got, gs, xs, ids, E, per_pair, experts, what=f"N={N} mode {mode} slot {slot}")
             del dW
             torch.cuda.empty_cache()
