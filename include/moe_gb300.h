@@ -326,8 +326,9 @@ moe_status moe_gemm_per_token(int32_t E, int32_t N, int32_t K, const uint8_t* a,
  * ------------------------------------------------------------------------------------ */
 
 /* Workspace bytes for moe_wgrad's slot-ordered copies (cap_tokens x N and cap_tokens x Kin
- * bf16, each 256-byte aligned): mode 0 with N a multiple of 128, Kin of 64, block_m of 64
- * and E <= 1024; 0 otherwise (moe_wgrad then needs none). */
+ * bf16) and the experts' block ranges (E x 2 int32), each 256-byte aligned: mode 0 with N a
+ * multiple of 128, Kin of 64, block_m of 64 and E <= 1024; 0 otherwise (moe_wgrad then
+ * needs none). */
 size_t moe_wgrad_workspace_size(int32_t E, int32_t N, int32_t Kin, int32_t block_m, int64_t cap_tokens,
                                 int32_t mode);
 

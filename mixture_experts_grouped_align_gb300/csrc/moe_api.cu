@@ -536,7 +536,8 @@ moe_status moe_gemm_per_token(int32_t E, int32_t N, int32_t K, const uint8_t* a,
 }
 
 // The slot-ordered copies of grad and input that let the tensor-memory wgrad load whole
-// stages by TMA: [cap_tokens, N] and [cap_tokens, Kin] bf16, each 256-byte aligned.
+// stages by TMA: [cap_tokens, N] and [cap_tokens, Kin] bf16, then the experts' block ranges
+// [E][2] int32, each 256-byte aligned.
 static moe_launch::Wgrad wgrad_shape(int32_t E, int32_t N, int32_t Kin, int32_t block_m, int64_t cap_tokens,
                                      int32_t mode) {
   moe_launch::Wgrad g{};
@@ -548,7 +549,7 @@ size_t moe_wgrad_workspace_size(int32_t E, int32_t N, int32_t Kin, int32_t block
                                 int32_t mode) {
   if (E < 1 || N < 64 || Kin < 64 || block_m < 1 || cap_tokens < 1) return 0;
   if (!moe_launch::wgrad_tc_slot_feed(wgrad_shape(E, N, Kin, block_m, cap_tokens, mode))) return 0;
-  return round256((size_t)cap_tokens * N * 2) + round256((size_t)cap_tokens * Kin * 2);
+  return round256((size_t)cap_tokens * N * 2) + round256((size_t)cap_tokens * Kin * 2) + round256((size_t)E * 8);
 }
 
 moe_status moe_wgrad(const void* grad, const void* input, int32_t input_per_pair, int64_t T,
@@ -598,6 +599,8 @@ moe_status moe_wgrad(const void* grad, const void* input, int32_t input_per_pair
     if (st != MOE_OK) return st;
     g.grad_s = grad_s;
     g.input_s = input_s;
+    g.ranges = reinterpret_cast<int32_t*>(ws + round256((size_t)cap_tokens * N * 2) +
+                                          round256((size_t)cap_tokens * Kin * 2));
   }
   st = cuda_status(moe_launch::wgrad(g, stream_of(ctx)), "moe_wgrad");
   rec(ctx, 1, 2);

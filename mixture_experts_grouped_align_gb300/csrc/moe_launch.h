@@ -150,6 +150,7 @@ struct Wgrad {
   const void* grad_s;
   const void* input_s;
   int64_t cap;
+  int32_t* ranges;  // [E][2] first, end alignment block of each expert (slot feed scratch)
 };
 cudaError_t wgrad(const Wgrad& g, cudaStream_t stream);
 

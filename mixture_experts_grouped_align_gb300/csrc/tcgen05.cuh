@@ -202,6 +202,29 @@ MOE_DEV void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
+// mma_commit onto the mbarrier at the same shared-memory offset in every CTA of the cluster
+// in cta_mask.
+MOE_DEV void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- clusters
+
+MOE_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster (warp-converged): release this CTA's prior
+// shared-memory writes (mbarrier inits included) to the cluster, then wait for the others.
+MOE_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Byte offset of 16-byte chunk c (0..7) of row r inside a tile of 128-byte rows stored in
 // 128-byte swizzle atoms.
 MOE_DEV uint32_t sw128_offset(int r, int c) {

@@ -56,6 +56,56 @@ MOE_DEV void load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
       : "memory");
 }
 
+// load_2d into the same shared-memory offset of every CTA of the cluster in cta_mask; each
+// destination's mbarrier at the offset of `bar` receives the box's bytes.
+MOE_DEV void load_2d_multicast(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, uint64_t* bar,
+                               uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_addr(bar)), "h"(cta_mask)
+      : "memory");
+}
+
+// L2 cache policies for the copies below: lines that should leave L2 first (data written
+// once and not read again soon) or last (data read again by other tiles).
+MOE_DEV uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+MOE_DEV uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// load_2d with an L2 cache policy for the lines it reads.
+MOE_DEV void load_2d_hint(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, uint64_t* bar,
+                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+// load_2d_multicast with an L2 cache policy.
+MOE_DEV void load_2d_multicast_hint(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, uint64_t* bar,
+                                    uint16_t cta_mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_addr(bar)), "h"(cta_mask), "l"(policy)
+      : "memory");
+}
+// store_2d with an L2 cache policy for the lines it writes.
+MOE_DEV void store_2d_hint(const CUtensorMap* map, int32_t x, int32_t y, uint32_t src, uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "l"(policy)
+               : "memory");
+}
+
 // Stores the box at (x, y) of the tensor from shared memory at src (bulk-group completion).
 MOE_DEV void store_2d(const CUtensorMap* map, int32_t x, int32_t y, uint32_t src) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(

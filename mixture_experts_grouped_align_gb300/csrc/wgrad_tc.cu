@@ -17,7 +17,13 @@
 //   slot feed (grad and input already copied into slot order): one thread loads a stage as
 //     2 + BN/64 TMA boxes of 64 slots x 128 bytes, which land in exactly the atom layout;
 //     warps 4-11 (two per TMEM lane quarter, one half of the columns each) drain the
-//     accumulators through swizzled 32 x 32 staging boxes that leave by TMA stores.
+//     accumulators through swizzled 32 x 32 staging boxes, read back row-contiguous for
+//     whole-line stores (marked to leave L2 first).  The experts' slot ranges come from a
+//     small kernel (global memory), which leaves shared memory to four 48 KB stages.
+//     Launched in clusters of C CTAs that take the C N tiles of one (expert, Kin tile): the
+//     input boxes, the same for all of them, are loaded once per cluster and multicast
+//     (each CTA issues its share), and every CTA's MMA commit frees the stage in all of
+//     them, which halves (C = 4) the operand bytes the L2 serves per output.
 // Warp 0 owns TMEM (two 128 x 256 fp32 accumulators) and issues the MMAs.  Both feeds run
 // the same MMAs on the same stages in the same order, so they give identical bits.
 // Every mbarrier wait is bounded; a wait that runs out sets MOE_ERR_TIMEOUT and every
@@ -45,29 +51,29 @@ constexpr int kMaxStages = 4;
 
 constexpr int kStageLd = 36;                 // gather feed: staging row stride (floats), conflict-free
 constexpr int kStage = 4 * 32 * kStageLd;    // floats of its epilogue staging (4 warps)
-constexpr int kBox = 32 * 128;               // slot feed: one 32 x 32 fp32 store box (bytes)
+constexpr int kBox = 32 * 128;               // slot feed: one 32 x 32 fp32 staging box (bytes)
 constexpr int kSlotEpiWarps = 8;
 
 struct WLayout {
-  int a, b, slot, nslots, stg, zero, bars, eb, total;
+  int a, b, slot, nslots, stg, bars, eb, total;
 };
 
 // Stages (A = 2 MN atom columns (128 n) | B = BN/64 atom columns) | epilogue staging (slot
-// feed: two store boxes per epilogue warp and one zero box) | barriers | expert block
-// ranges (8 KB).  Offsets from a 1024-byte aligned base.
+// feed: one box per epilogue warp) | barriers | gather feed: expert block ranges (8 KB).
+// Offsets from a 1024-byte aligned base.
 __host__ __device__ inline WLayout wlayout(int BN, bool slot_feed) {
   WLayout L;
   L.a = 0;
   L.b = 2 * kAtomCol;
   L.slot = L.b + (BN / 64) * kAtomCol;
-  const int staging = slot_feed ? (2 * kSlotEpiWarps + 1) * kBox : kStage * 4;
-  int n = (227 * 1024 - 1024 - 256 - 8 * 1024 - staging) / L.slot;
+  const int staging = slot_feed ? kSlotEpiWarps * kBox : kStage * 4;
+  const int ranges = slot_feed ? 0 : 8 * 1024;
+  int n = (227 * 1024 - 1024 - 256 - ranges - staging) / L.slot;
   L.nslots = n > kMaxStages ? kMaxStages : n;
   L.stg = L.nslots * L.slot;
-  L.zero = L.stg + 2 * kSlotEpiWarps * kBox;
   L.bars = L.stg + staging;
   L.eb = L.bars + 256;
-  L.total = L.eb + 8 * 1024 + 1024;
+  L.total = L.eb + ranges + 1024;
   return L;
 }
 
@@ -76,13 +82,22 @@ struct WArgs {
   int BN;          // Kin columns per tile (multiple of 64, <= 256)
   int n_tiles;     // N / 128
   int c_tiles;     // Kin / BN
-  int nt_fast;     // 1: N tiles vary fastest within an expert (every grad column live at once)
-  int64_t tiles;   // E * n_tiles * c_tiles
+  int groups;      // n_tiles / C: the cluster's C CTAs take N tiles C g .. C g + C - 1
+  int nt_fast;     // 1: N tile groups vary fastest within an expert (every grad column live at once)
+  int64_t tiles;   // E * groups * c_tiles (one per cluster)
 };
 
 // Byte offset of (token t, 16-byte chunk c of a row of 64 MN elements) in an atom column.
 __device__ __forceinline__ uint32_t mn_offset(int t, int c) {
   return (uint32_t)((t >> 3) * kAtom + (t & 7) * 128 + ((c ^ (t & 7)) << 4));
+}
+
+// 16-byte global store with an L2 cache policy.
+__device__ __forceinline__ void st_global_v4_hint(float* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                  uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d),
+               "l"(policy)
+               : "memory");
 }
 
 struct TileInfo {
@@ -91,37 +106,43 @@ struct TileInfo {
   int64_t slot_beg, slot_end;  // the expert's token slots
 };
 
-// Tile t -> expert, N tile, Kin tile and the expert's slot range (from the per-expert
-// block ranges the thread block built in shared memory).  Within an expert the tile index
-// whose operand is narrower over all tiles varies fastest, so that the tiles running at
-// once share the wider operand's columns and their rows stay small in L2.
-__device__ __forceinline__ TileInfo tile_info(const WArgs& wa, int64_t t, const int* eb) {
+// Cluster tile t -> expert, this CTA's N tile, Kin tile and the expert's slot range (from
+// the per-expert block ranges the thread block built in shared memory).  Within an expert
+// the tile index whose operand is narrower over all tiles varies fastest, so that the
+// tiles running at once share the wider operand's columns and their rows stay small in L2.
+__device__ __forceinline__ TileInfo tile_info(const WArgs& wa, int64_t t, const int* eb, int C, int rank) {
   const Wgrad& a = wa.g;
   TileInfo ti;
-  const int64_t per_e = (int64_t)wa.n_tiles * wa.c_tiles;
+  const int64_t per_e = (int64_t)wa.groups * wa.c_tiles;
   ti.e = t / per_e;
   const int rem = (int)(t - ti.e * per_e);
+  int grp;
   if (wa.nt_fast) {
-    ti.ct = rem / wa.n_tiles;
-    ti.nt = rem - ti.ct * wa.n_tiles;
+    ti.ct = rem / wa.groups;
+    grp = rem - ti.ct * wa.groups;
   } else {
-    ti.nt = rem / wa.c_tiles;
-    ti.ct = rem - ti.nt * wa.c_tiles;
+    grp = rem / wa.c_tiles;
+    ti.ct = rem - grp * wa.c_tiles;
   }
+  ti.nt = grp * C + rank;
   ti.slot_beg = (int64_t)eb[2 * ti.e] * a.bm;
   ti.slot_end = (int64_t)eb[2 * ti.e + 1] * a.bm;
   return ti;
 }
 
-template <bool SLOT>
+template <bool SLOT, int C>
 __global__ void __launch_bounds__(kThreads, 1)
-    wgrad_tc_kernel(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_i,
-                    const __grid_constant__ CUtensorMap tm_d, WArgs wa) {
+    wgrad_tc_kernel(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_i, WArgs wa) {
   const Wgrad& a = wa.g;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  static_assert(C == 1 || SLOT, "clusters share the slot feed's boxes");
   const int BN = wa.BN;
   const WLayout L = wlayout(BN, SLOT);
+  // this CTA's cluster (C consecutive blocks) and its rank in it; the loops walk cluster tiles
+  const int rank = C > 1 ? (int)tc::cluster_ctarank() : 0;
+  const int64_t cid = blockIdx.x / C, ncl = gridDim.x / C;
+  const uint16_t cmask = (uint16_t)((1u << C) - 1u);
   const int S = L.nslots;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kMaxStages;
@@ -130,28 +151,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = tempty + 2;
   uint32_t* taddr_s = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(taddr_s + 1);
-  int* eb = reinterpret_cast<int*>(smem + L.eb);  // [E][2]: first, end block
+  // [E][2]: first, end block of every expert (slot feed: computed before the launch)
+  int* eb = SLOT ? a.ranges : reinterpret_cast<int*>(smem + L.eb);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nblocks = *a.ntpp / a.bm;
-  for (int i = tid; i < 2 * a.E; i += kThreads) eb[i] = 0;
-  if (SLOT) {  // the zero box that the stores of an expert with no pair read
-    for (int i = tid; i < kBox / 16; i += kThreads)
-      *reinterpret_cast<uint4*>(smem + L.zero + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
-    tc::fence_proxy_async_smem();
-  }
-  __syncthreads();
-  for (int b = tid; b < nblocks; b += kThreads) {  // used blocks: ascending expert ids
-    const int e = a.expert_ids[b];
-    if (e < 0 || e >= a.E) continue;
-    if (b == 0 || a.expert_ids[b - 1] != e) eb[2 * e] = b;
-    if (b == nblocks - 1 || a.expert_ids[b + 1] != e) eb[2 * e + 1] = b + 1;
+  if (!SLOT) {
+    const int nblocks = *a.ntpp / a.bm;
+    for (int i = tid; i < 2 * a.E; i += kThreads) eb[i] = 0;
+    __syncthreads();
+    for (int b = tid; b < nblocks; b += kThreads) {  // used blocks: ascending expert ids
+      const int e = a.expert_ids[b];
+      if (e < 0 || e >= a.E) continue;
+      if (b == 0 || a.expert_ids[b - 1] != e) eb[2 * e] = b;
+      if (b == nblocks - 1 || a.expert_ids[b + 1] != e) eb[2 * e + 1] = b + 1;
+    }
   }
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       // gather feed: one completion arrival per producer thread; slot feed: the TMA thread
       tc::mbar_init(&full[s], SLOT ? 1 : kNumProd);
-      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&empty[s], C);  // the MMA commit of every CTA of the cluster
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&tfull[i], 1);
@@ -167,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc::tc_fence_before();
   __syncthreads();
+  if (C > 1) tc::cluster_sync();  // every CTA's barriers exist before a peer signals them
   tc::tc_fence_after();
   const uint32_t taddr = *taddr_s;
   const uint32_t smem_s = tc::smem_addr(smem);
@@ -199,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     TileInfo ti{};
     auto seek = [&]() {  // the first tile from tt on with a stage (an expert with pairs)
       for (; tt < wa.tiles; tt += gridDim.x) {
-        ti = tile_info(wa, tt, eb);
+        ti = tile_info(wa, tt, eb, 1, 0);
         nst = (ti.slot_end - ti.slot_beg + kTok - 1) / kTok;
         if (nst > 0) return;
       }
@@ -246,9 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma::prefetch_map(&tm_g);
       tma::prefetch_map(&tm_i);
       const uint32_t stage_tx = (uint32_t)(2 + BN / 64) * kAtomCol;
+      // the operand rows are read again by the expert's other tiles: kept in L2 over the dW
+      // lines, which the stores mark to leave first
+      const uint64_t keep = tma::policy_evict_last();
       uint32_t it = 0;
-      for (int64_t tt = blockIdx.x; tt < wa.tiles && !*abort_flag; tt += gridDim.x) {
-        const TileInfo ti = tile_info(wa, tt, eb);
+      for (int64_t tt = cid; tt < wa.tiles && !*abort_flag; tt += ncl) {
+        const TileInfo ti = tile_info(wa, tt, eb, C, rank);
         const int64_t nst = (ti.slot_end - ti.slot_beg) / kTok;  // block_m is a multiple of kTok
         const int32_t xg = (int32_t)((int64_t)ti.nt * kTM * 2), xi = (int32_t)((int64_t)ti.ct * BN * 2);
         bool ok = true;
@@ -262,9 +285,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int32_t y = (int32_t)(ti.slot_beg + st * kTok);
           tma::mbar_arrive_expect_tx(&full[slot], stage_tx);
           // 64 slots x 64 bf16 per box, 128-byte swizzled: one MN atom column
-          tma::load_2d(sl + L.a, &tm_g, xg, y, &full[slot]);
-          tma::load_2d(sl + L.a + kAtomCol, &tm_g, xg + 128, y, &full[slot]);
-          for (int j = 0; j < BN / 64; ++j) tma::load_2d(sl + L.b + j * kAtomCol, &tm_i, xi + 128 * j, y, &full[slot]);
+          tma::load_2d_hint(sl + L.a, &tm_g, xg, y, &full[slot], keep);
+          tma::load_2d_hint(sl + L.a + kAtomCol, &tm_g, xg + 128, y, &full[slot], keep);
+          // input boxes: this CTA's share, into every CTA of the cluster
+          for (int j = rank; j < BN / 64; j += C) {
+            if (C > 1)
+              tma::load_2d_multicast_hint(sl + L.b + j * kAtomCol, &tm_i, xi + 128 * j, y, &full[slot], cmask, keep);
+            else
+              tma::load_2d_hint(sl + L.b + j * kAtomCol, &tm_i, xi + 128 * j, y, &full[slot], keep);
+          }
           ++it;
         }
         if (!ok) {
@@ -274,10 +303,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Leaving early: the loads already issued still land in this block's shared memory,
-      // so wait for the last armed phase of every slot before exiting.
-      if (*abort_flag)
+      // so wait for the last armed phase of every slot before exiting.  In a cluster, the
+      // normal end waits instead until every CTA's MMAs have released this CTA's last
+      // stages, so that no peer's commit arrives after this CTA is gone.
+      if (*abort_flag) {
         for (uint32_t j = it > (uint32_t)S ? it - S : 0; j < it; ++j)
           if (!tc::mbar_wait(&full[j % S], (j / S) & 1)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
+      } else if (C > 1) {
+        for (uint32_t j = it > (uint32_t)S ? it - S : 0; j < it; ++j)
+          if (!tc::mbar_wait(&empty[j % S], (j / S) & 1)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
+      }
     }
     __syncwarp();
   } else if (warp == 0) {
@@ -285,8 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_f16(kTM, BN, 1) | (1u << 15) | (1u << 16);
       uint32_t it = 0, acc_it = 0;
-      for (int64_t tt = blockIdx.x; tt < wa.tiles && !*abort_flag; tt += gridDim.x) {
-        const TileInfo ti = tile_info(wa, tt, eb);
+      for (int64_t tt = cid; tt < wa.tiles && !*abort_flag; tt += ncl) {
+        const TileInfo ti = tile_info(wa, tt, eb, C, rank);
         const int64_t nst = (ti.slot_end - ti.slot_beg + kTok - 1) / kTok;
         if (nst == 0) continue;  // the epilogue writes zeros itself
         const uint32_t acc = acc_it & 1;
@@ -315,7 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_f16_ss(d_tmem, tc::sdesc_sw128_mn(a_s + k4 * 2 * kAtom, kAtomCol, kAtom),
                            tc::sdesc_sw128_mn(b_s + k4 * 2 * kAtom, kAtomCol, kAtom), idesc,
                            (st | k4) != 0);
-          tc::mma_commit(&empty[slot]);
+          if (C > 1)
+            tc::mma_commit_multicast(&empty[slot], cmask);  // the stage is free in every CTA
+          else
+            tc::mma_commit(&empty[slot]);
           ++it;
         }
         if (!ok) break;
@@ -335,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rr = lane >> 3, cc = (lane & 7) * 4;  // store phase: row rr + 4i, columns cc..cc+3
     uint32_t acc_it = 0;
     for (int64_t tt = blockIdx.x; tt < wa.tiles && !*abort_flag; tt += gridDim.x) {
-      const TileInfo ti = tile_info(wa, tt, eb);
+      const TileInfo ti = tile_info(wa, tt, eb, 1, 0);
       float* tile = a.dW + ((ti.e * a.N) + (int64_t)ti.nt * kTM + quarter * 32) * (int64_t)a.Kin +
                     (int64_t)ti.ct * BN;
       if (ti.slot_end == ti.slot_beg) {  // an expert with no pair: dW[e] = 0
@@ -377,20 +415,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ epilogue (slot feed)
     // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (= its 32 dW rows) and half (w - 4) / 4 of
     // the tile's columns, 32 at a time: registers -> a 128-byte swizzled 32 x 32 box in
-    // shared memory (two per warp, alternating) -> one TMA store.
+    // shared memory -> read back four rows at a time, each row's 128 bytes by eight lanes,
+    // and stored as whole lines.
     const int ew = warp - kEpiWarp0, quarter = warp & 3, half = ew >> 2;
     const int cols = BN / 2;
-    const uint32_t stg0 = smem_s + L.stg + ew * 2 * kBox;
-    uint32_t nstore = 0, acc_it = 0;
-    for (int64_t tt = blockIdx.x; tt < wa.tiles && !*abort_flag; tt += gridDim.x) {
-      const TileInfo ti = tile_info(wa, tt, eb);
-      const int32_t row0 = (int32_t)(ti.e * a.N + (int64_t)ti.nt * kTM + quarter * 32);
-      const int32_t col0 = ti.ct * BN + half * cols;
+    const uint32_t box = smem_s + L.stg + ew * kBox;
+    const uint64_t stream_out = tma::policy_evict_first();  // dW is not read again here
+    const int cc = lane & 7, r0 = lane >> 3;                 // store phase: rows r0 + 4 i, chunk cc
+    uint32_t acc_it = 0;
+    for (int64_t tt = cid; tt < wa.tiles && !*abort_flag; tt += ncl) {
+      const TileInfo ti = tile_info(wa, tt, eb, C, rank);
+      float* tile = a.dW + (ti.e * a.N + (int64_t)ti.nt * kTM + quarter * 32) * (int64_t)a.Kin +
+                    (int64_t)ti.ct * BN + half * cols;
       if (ti.slot_end == ti.slot_beg) {  // an expert with no pair: dW[e] = 0
-        if (lane == 0) {
-          for (int c = 0; c < cols; c += 32) tma::store_2d(&tm_d, (col0 + c) * 4, row0, smem_s + L.zero);
-          tma::bulk_commit();
-        }
+        for (int c = 0; c < cols; c += 32)
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            st_global_v4_hint(tile + (int64_t)(r0 + 4 * i) * a.Kin + c + 4 * cc, 0u, 0u, 0u, 0u, stream_out);
         continue;
       }
       const uint32_t acc = acc_it & 1;
@@ -405,33 +446,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[32];
         tc::tmem_ld32(tb + c, v);
         tc::tmem_ld_wait();
-        // the store that last read this box (two stores ago) has finished reading it
-        if (lane == 0) tma::bulk_wait_read_1();
-        __syncwarp();
-        const uint32_t box = stg0 + (nstore & 1) * kBox;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(box + lane * 128 + ((q ^ (lane & 7)) << 4)),
                        "r"(v[4 * q]), "r"(v[4 * q + 1]), "r"(v[4 * q + 2]), "r"(v[4 * q + 3])
                        : "memory");
-        tc::fence_proxy_async_smem();  // these writes, for the TMA engine
         __syncwarp();
-        if (lane == 0) {
-          tma::store_2d(&tm_d, (col0 + c) * 4, row0, box);
-          tma::bulk_commit();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = r0 + 4 * i;
+          uint32_t w0, w1, w2, w3;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                       : "r"(box + r * 128 + ((cc ^ (r & 7)) << 4))
+                       : "memory");
+          st_global_v4_hint(tile + (int64_t)r * a.Kin + c + 4 * cc, w0, w1, w2, w3, stream_out);
         }
-        ++nstore;
+        __syncwarp();
       }
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&tempty[acc]);
       ++acc_it;
     }
-    if (lane == 0) tma::bulk_wait_all();
-    __syncwarp();
   }
   tc::tc_fence_before();
   __syncthreads();
+  if (C > 1) tc::cluster_sync();  // no CTA leaves while a peer may still signal it
   if (warp == 0) {
     tc::tc_fence_after();
     tc::tmem_dealloc(taddr, kTmemCols);
@@ -439,6 +480,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 int sm_count_w() { return moe_launch::sm_count_current(); }
+
+// ranges[e] = (first, end) alignment block of expert e, (0, 0) for an expert with no block:
+// one block of threads, the same rule the gather-feed kernel applies in shared memory.
+__global__ void expert_ranges_kernel(const int32_t* __restrict__ expert_ids, const int32_t* __restrict__ ntpp, int bm,
+                                     int E, int32_t* __restrict__ ranges) {
+  const int nblocks = *ntpp / bm;
+  for (int i = threadIdx.x; i < 2 * E; i += blockDim.x) ranges[i] = 0;
+  __syncthreads();
+  for (int b = threadIdx.x; b < nblocks; b += blockDim.x) {  // used blocks: ascending expert ids
+    const int e = expert_ids[b];
+    if (e < 0 || e >= E) continue;
+    if (b == 0 || expert_ids[b - 1] != e) ranges[2 * e] = b;
+    if (b == nblocks - 1 || expert_ids[b + 1] != e) ranges[2 * e + 1] = b + 1;
+  }
+}
+
+cudaError_t expert_ranges(const Wgrad& g, cudaStream_t stream) {
+  if (g.ranges == nullptr) return cudaErrorInvalidValue;
+  expert_ranges_kernel<<<1, 1024, 0, stream>>>(g.expert_ids, g.ntpp, g.bm, g.E, g.ranges);
+  return cudaGetLastError();
+}
 
 }  // namespace
 
@@ -455,9 +517,46 @@ int wgrad_tc_tile(const Wgrad& g) {
 
 bool wgrad_tc_slot_feed(const Wgrad& g) {
   // whole 64-slot stages never cross into the next expert's slots; TMA row coordinates
-  // (slots, and dW rows e * N + n) are 32-bit
-  return wgrad_tc_tile(g) > 0 && g.bm % kTok == 0 && g.cap < ((int64_t)1 << 31) &&
-         (int64_t)g.E * g.N < ((int64_t)1 << 31) && (int64_t)g.Kin * 4 < ((int64_t)1 << 31);
+  // (slots) are 32-bit
+  return wgrad_tc_tile(g) > 0 && g.bm % kTok == 0 && g.cap < ((int64_t)1 << 31);
+}
+
+// The slot-fed kernel in clusters of C CTAs: persistent, as many whole clusters as fit on
+// the GPU at once (at most one per cluster tile).  *no_fit when no cluster of C fits.
+template <int C>
+cudaError_t launch_slot(const CUtensorMap& mg, const CUtensorMap& mi, WArgs wa, int smem,
+                        cudaStream_t stream, bool* no_fit) {
+  auto kern = wgrad_tc_kernel<true, C>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  wa.groups = wa.n_tiles / C;
+  wa.tiles = (int64_t)wa.g.E * wa.groups * wa.c_tiles;
+  int64_t nclusters = sm_count_w() / C;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  if (C > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)(nclusters * C));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      *no_fit = true;
+      return cudaSuccess;
+    }
+    nclusters = n;
+  }
+  if (wa.tiles < nclusters) nclusters = wa.tiles;
+  if (nclusters <= 0) return cudaSuccess;
+  cfg.gridDim = dim3((unsigned)(nclusters * C));
+  return cudaLaunchKernelEx(&cfg, kern, mg, mi, wa);
 }
 
 cudaError_t wgrad_tc(const Wgrad& g, cudaStream_t stream) {
@@ -467,31 +566,42 @@ cudaError_t wgrad_tc(const Wgrad& g, cudaStream_t stream) {
   if (wa.BN == 0) return cudaErrorInvalidValue;
   wa.n_tiles = g.N / kTM;
   wa.c_tiles = g.Kin / wa.BN;
+  wa.groups = wa.n_tiles;
   wa.nt_fast = g.N <= g.Kin ? 1 : 0;
   wa.tiles = (int64_t)g.E * wa.n_tiles * wa.c_tiles;
   const bool slot = g.grad_s != nullptr && g.input_s != nullptr;
   if (slot && !wgrad_tc_slot_feed(g)) return cudaErrorInvalidValue;
   const WLayout L = wlayout(wa.BN, slot);
+  CUtensorMap mg{}, mi{};
+  if (slot) {
+    // slot-ordered rows: boxes of 64 slots x 128 bytes, 128-byte swizzle (one MN atom column)
+    if (!tma::encode_2d_u8(&mg, g.grad_s, (uint64_t)g.N * 2, (uint64_t)g.cap, (uint64_t)g.N * 2, 128, kTok, true) ||
+        !tma::encode_2d_u8(&mi, g.input_s, (uint64_t)g.Kin * 2, (uint64_t)g.cap, (uint64_t)g.Kin * 2, 128, kTok,
+                           true))
+      return cudaErrorInvalidValue;
+    cudaError_t rerr = expert_ranges(g, stream);
+    if (rerr != cudaSuccess) return rerr;
+    // the largest cluster that divides the N tiles and fits
+    bool no_fit = false;
+    if (wa.n_tiles % 4 == 0) {
+      cudaError_t err = launch_slot<4>(mg, mi, wa, L.total, stream, &no_fit);
+      if (err != cudaSuccess || !no_fit) return err == cudaSuccess ? cudaGetLastError() : err;
+    }
+    no_fit = false;
+    if (wa.n_tiles % 2 == 0) {
+      cudaError_t err = launch_slot<2>(mg, mi, wa, L.total, stream, &no_fit);
+      if (err != cudaSuccess || !no_fit) return err == cudaSuccess ? cudaGetLastError() : err;
+    }
+    cudaError_t err = launch_slot<1>(mg, mi, wa, L.total, stream, &no_fit);
+    return err == cudaSuccess ? cudaGetLastError() : err;
+  }
   int64_t grid = sm_count_w();
   if (wa.tiles < grid) grid = wa.tiles;
   if (grid <= 0) return cudaSuccess;
-  CUtensorMap mg{}, mi{}, md{};
-  if (slot) {
-    // slot-ordered rows: boxes of 64 slots x 128 bytes, 128-byte swizzle (one MN atom
-    // column); dW rows of Kin fp32, stored 32 rows x 128 bytes per box
-    if (!tma::encode_2d_u8(&mg, g.grad_s, (uint64_t)g.N * 2, (uint64_t)g.cap, (uint64_t)g.N * 2, 128, kTok, true) ||
-        !tma::encode_2d_u8(&mi, g.input_s, (uint64_t)g.Kin * 2, (uint64_t)g.cap, (uint64_t)g.Kin * 2, 128, kTok,
-                           true) ||
-        !tma::encode_2d_u8(&md, g.dW, (uint64_t)g.Kin * 4, (uint64_t)g.E * g.N, (uint64_t)g.Kin * 4, 128, 32, true))
-      return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(wgrad_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-    if (err != cudaSuccess) return err;
-    wgrad_tc_kernel<true><<<(unsigned)grid, kThreads, L.total, stream>>>(mg, mi, md, wa);
-  } else {
-    cudaError_t err = cudaFuncSetAttribute(wgrad_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-    if (err != cudaSuccess) return err;
-    wgrad_tc_kernel<false><<<(unsigned)grid, kThreads, L.total, stream>>>(mg, mi, md, wa);
-  }
+  cudaError_t err =
+      cudaFuncSetAttribute(wgrad_tc_kernel<false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  if (err != cudaSuccess) return err;
+  wgrad_tc_kernel<false, 1><<<(unsigned)grid, kThreads, L.total, stream>>>(mg, mi, wa);
   return cudaGetLastError();
 }
 

@@ -52,9 +52,10 @@ int main(void) {
                 (size_t)round_up(64 * 2880 * 2, 256);
   CHECK(ws == want, "workspace %zu, want %zu", ws, want);
 
-  /* wgrad's slot-ordered copies: [cap, N] + [cap, Kin] bf16, deterministic mode only */
+  /* wgrad's slot-ordered copies [cap, N] + [cap, Kin] bf16 and expert ranges [E, 2] int32 */
   CHECK(moe_wgrad_workspace_size(256, 4096, 7168, 128, 98048, 0) ==
-            (size_t)round_up(98048LL * 4096 * 2, 256) + (size_t)round_up(98048LL * 7168 * 2, 256),
+            (size_t)round_up(98048LL * 4096 * 2, 256) + (size_t)round_up(98048LL * 7168 * 2, 256) +
+                (size_t)round_up(256 * 8, 256),
         "wgrad workspace %zu", moe_wgrad_workspace_size(256, 4096, 7168, 128, 98048, 0));
   CHECK(moe_wgrad_workspace_size(256, 4096, 7168, 128, 98048, 1) == 0, "accumulate mode needs no workspace");
 

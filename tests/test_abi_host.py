@@ -172,12 +172,15 @@ def test_grouped_gemm_workspace_size(lib):
 
 
 def test_wgrad_workspace_size(lib):
-    """Slot-ordered copies of grad [cap, N] and input [cap, Kin] bf16, each rounded up to 256
-    bytes, for the deterministic tensor-core wgrad; 0 wherever that kernel cannot read them."""
+    """Slot-ordered copies of grad [cap, N] and input [cap, Kin] bf16 and the experts' block
+    ranges [E, 2] int32, each rounded up to 256 bytes, for the deterministic tensor-core
+    wgrad; 0 wherever that kernel cannot read them."""
     r = lambda v: (v + 255) // 256 * 256
     cap = 98048                                     # 65536 pairs over 256 experts, block 128
-    assert moe.moe_wgrad_workspace_size(256, 4096, 7168, 128, cap, 0) == r(cap * 4096 * 2) + r(cap * 7168 * 2)
-    assert moe.moe_wgrad_workspace_size(256, 7168, 2048, 64, cap, 0) == r(cap * 7168 * 2) + r(cap * 2048 * 2)
+    assert moe.moe_wgrad_workspace_size(256, 4096, 7168, 128, cap, 0) == \
+        r(cap * 4096 * 2) + r(cap * 7168 * 2) + r(256 * 8)
+    assert moe.moe_wgrad_workspace_size(256, 7168, 2048, 64, cap, 0) == \
+        r(cap * 7168 * 2) + r(cap * 2048 * 2) + r(256 * 8)
     assert moe.moe_wgrad_workspace_size(256, 4096, 7168, 128, cap, 1) == 0   # accumulate mode
     assert moe.moe_wgrad_workspace_size(256, 4096, 7168, 16, cap, 0) == 0    # stages would cross experts
     assert moe.moe_wgrad_workspace_size(256, 64, 7168, 128, cap, 0) == 0     # N not a multiple of 128

@@ -92,11 +92,13 @@ def test_wgrad_small(moe, mode, per_pair, bm):
 
 @pytest.mark.parametrize("per_pair", [False, True])
 @pytest.mark.parametrize("bm", [128, 64])
-@pytest.mark.parametrize("N,Kin", [(128, 192), (256, 448), (384, 256)])
+@pytest.mark.parametrize("N,Kin", [(128, 192), (256, 448), (384, 256), (512, 320), (1024, 768)])
 def test_wgrad_slot_feed(moe, per_pair, bm, N, Kin):
     """The slot-ordered feed (workspace given): against the oracle, and bit-identical to the
     gather feed on the same inputs (the same MMAs over the same stages in the same order).
-    Kin = 192 and 448 take 192- and 64-column tiles; N = 256 <= Kin and N = 384 > Kin walk
+    The N tiles (1, 2, 3, 4, 8) run without clusters, in pairs and in fours; Kin = 192, 448,
+    320 and 768 take 192-, 64-, 64- and 256-column tiles (one input box, which one CTA of a
+    cluster loads for all four, up to four boxes, one per CTA); N <= Kin and N > Kin walk
     the tiles of an expert in the two orders."""
     rng = np.random.default_rng(17)
     T, E, k = 333, 7, 3
