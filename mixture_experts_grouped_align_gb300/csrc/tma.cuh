@@ -122,6 +122,13 @@ MOE_DEV void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;
 // Waits until every committed bulk store of this thread has completed.
 MOE_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Starts bringing the box at (x, y) of the tensor into L2 (no shared memory, no completion).
+MOE_DEV void prefetch_2d_l2(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 MOE_DEV void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -274,6 +274,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileInfo ti = tile_info(wa, tt, eb, C, rank);
         const int64_t nst = (ti.slot_end - ti.slot_beg) / kTok;  // block_m is a multiple of kTok
         const int32_t xg = (int32_t)((int64_t)ti.nt * kTM * 2), xi = (int32_t)((int64_t)ti.ct * BN * 2);
+        // the first stages of this CTA's next tile, into L2 while this one streams: the ring
+        // then starts the next tile on L2 hits instead of HBM round trips
+        if (tt + ncl < wa.tiles) {
+          const TileInfo tn = tile_info(wa, tt + ncl, eb, C, rank);
+          const int64_t pst = (tn.slot_end - tn.slot_beg) / kTok;
+          const int32_t pg = (int32_t)((int64_t)tn.nt * kTM * 2), pi = (int32_t)((int64_t)tn.ct * BN * 2);
+          for (int64_t st = 0; st < pst && st < kMaxStages; ++st) {
+            const int32_t y = (int32_t)(tn.slot_beg + st * kTok);
+            tma::prefetch_2d_l2(&tm_g, pg, y);
+            tma::prefetch_2d_l2(&tm_g, pg + 128, y);
+            for (int j = rank; j < BN / 64; j += C) tma::prefetch_2d_l2(&tm_i, pi + 128 * j, y);
+          }
+        }
         bool ok = true;
         for (int64_t st = 0; st < nst; ++st) {
           const int slot = it % S;
