@@ -29,8 +29,13 @@ std::atomic<int64_t> g_debug_stall_ns{0};
 
 int64_t debug_stall_ns() { return g_debug_stall_ns.load(std::memory_order_relaxed); }
 
-// The wait limit and stall flag every GroupedGemm of a call carries.
+// The wait limit and stall flag every GroupedGemm and Wgrad of a call carries.
 void apply_debug_stall(GroupedGemm& g) {
+  const int64_t ns = debug_stall_ns();
+  g.wait_ns = ns > 0 ? ns : 0;
+  g.stall = ns > 0 ? 1 : 0;
+}
+void apply_debug_stall(Wgrad& g) {
   const int64_t ns = debug_stall_ns();
   g.wait_ns = ns > 0 ? ns : 0;
   g.stall = ns > 0 ? 1 : 0;
@@ -580,6 +585,7 @@ moe_status moe_wgrad(const void* grad, const void* input, int32_t input_per_pair
   g.sorted = sorted_token_ids; g.expert_ids = expert_ids; g.ntpp = num_tokens_post_padded;
   g.bm = block_m; g.cap_blocks = cap_blocks; g.dW = dW; g.mode = mode; g.status = status_of(ctx);
   g.cap = cap_tokens;
+  moe_launch::apply_debug_stall(g);
   rec(ctx, 0, 2);
   // With a workspace: grad and input copied into slot order first, then the tensor-memory
   // kernel loads whole 64-slot stages by TMA (the same MMAs in the same order: same bits).

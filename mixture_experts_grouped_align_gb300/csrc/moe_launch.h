@@ -151,8 +151,11 @@ struct Wgrad {
   const void* input_s;
   int64_t cap;
   int32_t* ranges;  // [E][2] first, end alignment block of each expert (slot feed scratch)
+  int64_t wait_ns;  // limit of every wait of the tensor-memory kernel (0: the default)
+  int stall;        // failure-detection self-test: its copy and MMA roles off
 };
 cudaError_t wgrad(const Wgrad& g, cudaStream_t stream);
+void apply_debug_stall(Wgrad& g);
 
 // ---- weight gradient on the tensor-memory path (wgrad_tc.cu)
 int wgrad_tc_tile(const Wgrad& g);

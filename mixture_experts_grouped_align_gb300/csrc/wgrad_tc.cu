@@ -190,8 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t taddr = *taddr_s;
   const uint32_t smem_s = tc::smem_addr(smem);
+  // the limit of every wait (a caller's short limit only in the stalled self-test)
+  const uint64_t wb = a.wait_ns > 0 ? (uint64_t)a.wait_ns : tc::kWaitNs;
 
-  if (!SLOT && warp >= 8) {
+  if (!SLOT && warp >= 8 && !a.stall) {
     // ------------------------------------------------------------------ gather feed
     const int pt = tid - kProd0;
     const int t = pt >> 2, sub = pt & 3;  // token row of the stage, chunk phase
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (tt < wa.tiles) p_next = pair_at();
       const int slot = it % S;
-      if (!tc::mbar_wait(&empty[slot], ((it / S) & 1) ^ 1)) {
+      if (!tc::mbar_wait(&empty[slot], ((it / S) & 1) ^ 1, wb)) {
         moe::set_status(a.status, MOE_ERR_TIMEOUT);
         *abort_flag = 1;
         break;
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++it;
     }
     cp_async_wait_all();
-  } else if (SLOT && warp == 1) {
+  } else if (SLOT && warp == 1 && !a.stall) {
     // ------------------------------------------------------------------ slot feed (TMA)
     if (lane == 0) {
       tma::prefetch_map(&tm_g);
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int64_t st = 0; st < nst; ++st) {
           const int slot = it % S;
-          if (!tc::mbar_wait(&empty[slot], ((it / S) & 1) ^ 1)) {
+          if (!tc::mbar_wait(&empty[slot], ((it / S) & 1) ^ 1, wb)) {
             ok = false;
             break;
           }
@@ -321,14 +323,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // stages, so that no peer's commit arrives after this CTA is gone.
       if (*abort_flag) {
         for (uint32_t j = it > (uint32_t)S ? it - S : 0; j < it; ++j)
-          if (!tc::mbar_wait(&full[j % S], (j / S) & 1)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
+          if (!tc::mbar_wait(&full[j % S], (j / S) & 1, wb)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
       } else if (C > 1) {
         for (uint32_t j = it > (uint32_t)S ? it - S : 0; j < it; ++j)
-          if (!tc::mbar_wait(&empty[j % S], (j / S) & 1)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
+          if (!tc::mbar_wait(&empty[j % S], (j / S) & 1, wb)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
       }
     }
     __syncwarp();
-  } else if (warp == 0) {
+  } else if (warp == 0 && !a.stall) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_f16(kTM, BN, 1) | (1u << 15) | (1u << 16);
@@ -338,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t nst = (ti.slot_end - ti.slot_beg + kTok - 1) / kTok;
         if (nst == 0) continue;  // the epilogue writes zeros itself
         const uint32_t acc = acc_it & 1;
-        if (!tc::mbar_wait(&tempty[acc], ((acc_it >> 1) & 1) ^ 1)) {
+        if (!tc::mbar_wait(&tempty[acc], ((acc_it >> 1) & 1) ^ 1, wb)) {
           moe::set_status(a.status, MOE_ERR_TIMEOUT);
           *abort_flag = 1;
           break;
@@ -348,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int64_t st = 0; st < nst; ++st) {
           const int slot = it % S;
-          if (!tc::mbar_wait(&full[slot], (it / S) & 1)) {
+          if (!tc::mbar_wait(&full[slot], (it / S) & 1, wb)) {
             moe::set_status(a.status, MOE_ERR_TIMEOUT);
             *abort_flag = 1;
             ok = false;
@@ -374,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++acc_it;
       }
       tc::mma_commit(drain);
-      if (!tc::mbar_wait(drain, 0)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
+      if (!tc::mbar_wait(drain, 0, wb)) moe::set_status(a.status, MOE_ERR_TIMEOUT);
     }
     __syncwarp();
   } else if (!SLOT && warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
@@ -396,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const uint32_t acc = acc_it & 1;
-      if (!tc::mbar_wait(&tfull[acc], (acc_it >> 1) & 1)) {
+      if (!tc::mbar_wait(&tfull[acc], (acc_it >> 1) & 1, wb)) {
         moe::set_status(a.status, MOE_ERR_TIMEOUT);
         *abort_flag = 1;
         break;
@@ -448,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const uint32_t acc = acc_it & 1;
-      if (!tc::mbar_wait(&tfull[acc], (acc_it >> 1) & 1)) {
+      if (!tc::mbar_wait(&tfull[acc], (acc_it >> 1) & 1, wb)) {
         moe::set_status(a.status, MOE_ERR_TIMEOUT);
         *abort_flag = 1;
         break;
