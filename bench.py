@@ -84,7 +84,7 @@ L2_FLUSHED = {"tiny", "decode_bf16_M1"}
 DEFAULT_STEPS = {"decode_mxfp4": (2000, 50), "decode_bf16": (4000, 100),
                  "prefill_mxfp4": (10, 3), "tiny": (4000, 100), "mxfp8_wgrad": (3, 3),
                  "pertoken_fp8": (20, 3), "mxfp8_layer": (5, 3)}
-ORACLE_SAMPLE = {"decode_mxfp4": 8, "decode_bf16": 28, "prefill_mxfp4": 4, "tiny": 64,
+ORACLE_SAMPLE = {"decode_mxfp4": 8, "decode_bf16": 28, "prefill_mxfp4": 24, "tiny": 64,
                  "mxfp8_wgrad": 512, "pertoken_fp8": 8192, "mxfp8_layer": 4096}
 # The per-token FP8 grouped GEMM workload: the GEMM1 shape of the MXFP8 workload (256 experts,
 # K = 7168 -> N = 4096, T = 8192 tokens at top-8, Zipf(1.1) routing), rows grouped by expert.
