@@ -21,6 +21,11 @@ MOE_DEV void cp_async16z(uint32_t dst, const void* src, bool valid) {
 MOE_DEV void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
 }
+// 4 bytes, or 4 zero bytes when !valid (source size 0: nothing is read).
+MOE_DEV void cp_async4z(uint32_t dst, const void* src, bool valid) {
+  const int sz = valid ? 4 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(sz) : "memory");
+}
 MOE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 // Waits until at most N of this thread's committed groups are still in flight.
 template <int N>

@@ -9,9 +9,11 @@
 // decoded: the products of codes and power-of-two scales are exact and accumulate in f32.
 //
 // Per thread block (one per SM, 512 threads), persistent over (alignment block, N tile):
-//   warp 0      allocates the 512 TMEM columns (a 128 x BN f32 accumulator in columns
-//               0..255, the scale factors of the stages in 256..511) and, on one lane,
-//               issues the MMAs (M = 128, N = BN, K = 32) of each 128-wide K stage;
+//   warp 0      allocates the 512 TMEM columns (128 x BN f32 accumulators from column 0:
+//               one of BN = 256, or two alternating ones of BN <= 224 so that the epilogue
+//               of a tile overlaps the MMAs of the next; the scale factors of the stages in
+//               448..511) and, on one lane, issues the MMAs (M = 128, N = BN, K = 32) of
+//               each 128-wide K stage;
 //   warps 8-15  copy each stage: one thread loads the BN weight rows of 128 bytes with a
 //               TMA box into a 128-byte-swizzled K-major tile (completing on the stage's
 //               barrier); all copy the 128 gathered activation rows into the same layout
@@ -24,6 +26,9 @@
 //               (mx_quant.cuh: 32 features per E8M0 scale, all in the thread's registers).
 // SwiGLU tiles hold 128 features: weight rows 0..127 of the B tile are their gate rows and
 // 128..255 their up rows (two TMA boxes), so gate and up of a feature share a TMEM lane.
+// A last 224-wide tile may reach past N: its extra weight rows are read (the next expert's,
+// or zeros past the tensor), their scale words are zero-filled, and their outputs are not
+// stored.
 // Tiles past num_tokens_post_padded or of the -1 sentinel are skipped by every role before
 // anything is read (second review of the same page).  Expert offsets are 64-bit (Notes).
 // Every mbarrier wait is bounded; one that runs out sets MOE_ERR_TIMEOUT, every role leaves
@@ -55,7 +60,7 @@ constexpr int kBM = 128, kBK = 128;        // tile rows, K elements (bytes) per 
 constexpr int kProd0 = 256, kNumProd = 256;
 constexpr int kEpiWarp0 = 4;
 constexpr int kTmemCols = 512;
-constexpr int kSfCol0 = 256;               // first TMEM column of the scale regions
+constexpr int kSfCol0 = 448;               // first TMEM column of the scale regions (4 x 16)
 constexpr int kStages = 4;
 constexpr int kLag = 2;                    // stages between a stage's copies and its hand-over
 
@@ -88,6 +93,7 @@ __device__ __forceinline__ uint32_t sfb_col(int s) { return kSfCol0 + 16 * s + 8
 struct MArgs {
   GroupedGemm g;
   int BN;
+  int nacc;        // accumulators in TMEM: 2 (alternating, BN <= 224) or 1 (BN = 256)
   int n_tiles;
   int64_t tiles;
 };
@@ -122,9 +128,9 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
   const MLayout L = mlayout(BN);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
-  uint64_t* tempty = tfull + 1;
-  uint64_t* drain = tempty + 1;
+  uint64_t* tfull = empty + kStages;  // [2]
+  uint64_t* tempty = tfull + 2;       // [2]
+  uint64_t* drain = tempty + 2;
   uint64_t* gb_full = drain + 1;  // [2] B scale group landed (every B-scale thread's copies)
   uint64_t* tma_full = gb_full + 2;  // [kStages] the stage's weight box landed
   uint32_t* taddr_s = reinterpret_cast<uint32_t*>(tma_full + kStages);
@@ -137,8 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
       tc::mbar_init(&tma_full[s], 1);          // the weight box
       tc::mbar_init(&empty[s], 1);
     }
-    tc::mbar_init(tfull, 1);
-    tc::mbar_init(tempty, 4);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&tfull[i], 1);
+      tc::mbar_init(&tempty[i], 4);
+    }
     tc::mbar_init(drain, 1);
     for (int i = 0; i < 2; ++i) tc::mbar_init(&gb_full[i], kNumProd / 2);
     *abort_flag = 0;
@@ -254,9 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
             if (wp < 4) {
               if (sfsrc) cp_async16(smem_s + L.ga + gsel * kBM * 16 + (q * 32 + lane) * 16, sfsrc + kc * 4);
             } else {
-              for (int n = tb; n < BN; n += 128)
-                cp_async16(smem_s + L.gb + gsel * BN * 16 + n * 16,
-                           a.w_scale + b_row<EPI>(a, e, nt, BN, n) * nkb + kc * 4);
+              for (int n = tb; n < BN; n += 128) {
+                const bool live = EPI == EPI_SWIGLU || (int64_t)nt * BN + n < a.Nout;
+                cp_async16z(smem_s + L.gb + gsel * BN * 16 + n * 16,
+                            live ? a.w_scale + b_row<EPI>(a, e, nt, BN, n) * nkb + kc * 4 : a.w_scale, live);
+              }
               cp_async_arrive_noinc(&gb_full[gsel]);
             }
           }
@@ -265,9 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
         } else {
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            if (j < NBW)
-              cp_async4(sl + L.sfb + ((q * NBW + j) * 32 + lane) * 4,
-                        a.w_scale + b_row<EPI>(a, e, nt, BN, 32 * j + lane) * nkb + kc * 4);
+            if (j < NBW) {
+              const bool live = EPI == EPI_SWIGLU || (int64_t)nt * BN + 32 * j + lane < a.Nout;
+              cp_async4z(sl + L.sfb + ((q * NBW + j) * 32 + lane) * 4,
+                         live ? a.w_scale + b_row<EPI>(a, e, nt, BN, 32 * j + lane) * nkb + kc * 4 : a.w_scale,
+                         live);
+            }
         }
         cp_async_commit();
         ++it;
@@ -296,12 +309,15 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
         int64_t blk, e;
         int nt;
         if (!tile_info(ma, t, ntpp, blk, nt, e)) continue;
-        if (!tc::mbar_wait(tempty, (acc_it & 1) ^ 1, wb)) {
+        const uint32_t acc = ma.nacc == 2 ? (acc_it & 1) : 0;
+        const uint32_t use = ma.nacc == 2 ? (acc_it >> 1) : acc_it;  // earlier uses of this accumulator
+        if (!tc::mbar_wait(&tempty[acc], (use & 1) ^ 1, wb)) {
           moe::set_status(a.status, MOE_ERR_TIMEOUT);
           *abort_flag = 1;
           break;
         }
         tc::tc_fence_after();
+        const uint32_t d_tmem = taddr + acc * (uint32_t)BN;
         bool ok = true;
         for (int kc = 0; kc < nk; ++kc) {
           const int s = (int)(it % kStages);
@@ -315,13 +331,13 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
           const uint32_t sl = smem_s + s * L.slot;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            tc::mma_mx8_ss(taddr, tc::sdesc_sw128(sl + L.a + j * 32), tc::sdesc_sw128(sl + L.b + j * 32), idesc[j],
+            tc::mma_mx8_ss(d_tmem, tc::sdesc_sw128(sl + L.a + j * 32), tc::sdesc_sw128(sl + L.b + j * 32), idesc[j],
                            taddr + sfa_col(s), taddr + sfb_col(s), (kc | j) != 0);
           tc::mma_commit(&empty[s]);
           ++it;
         }
         if (!ok) break;
-        tc::mma_commit(tfull);
+        tc::mma_commit(&tfull[acc]);
         ++acc_it;
       }
       tc::mma_commit(drain);
@@ -338,7 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
       int64_t blk, e;
       int nt;
       if (!tile_info(ma, t, ntpp, blk, nt, e)) continue;
-      if (!tc::mbar_wait(tfull, acc_it & 1, wb)) {
+      const uint32_t acc = ma.nacc == 2 ? (acc_it & 1) : 0;
+      const uint32_t use = ma.nacc == 2 ? (acc_it >> 1) : acc_it;
+      if (!tc::mbar_wait(&tfull[acc], use & 1, wb)) {
         moe::set_status(a.status, MOE_ERR_TIMEOUT);
         *abort_flag = 1;
         break;
@@ -346,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
       tc::tc_fence_after();
       const int p = a.sorted[blk * a.bm + r];
       const bool valid = p < a.P;
-      const uint32_t tb = taddr + ((uint32_t)(quarter * 32) << 16);
+      const uint32_t tb = taddr + acc * (uint32_t)BN + ((uint32_t)(quarter * 32) << 16);
       if (EPI == EPI_SWIGLU) {  // 128 features: h = silu(gate) * up, quantised 32 at a time
         const int f0 = nt * 128;
         for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -376,7 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
       } else {
         const int n0 = nt * BN;
         const float wgt = (EPI == EPI_WEIGHTED_F32 && valid) ? a.topk_w[p] : 1.f;
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        // N is a multiple of 128 and n0 of 32: a 32-column chunk is wholly in N or past it
+        const int cols = a.Nout - n0 < BN ? a.Nout - n0 : BN;
+        for (int c0 = 0; c0 < cols; c0 += 32) {
           uint32_t v[32];
           tc::tmem_ld32(tb + c0, v);
           tc::tmem_ld_wait();
@@ -406,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
       }
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tempty);
+      if (lane == 0) tc::mbar_arrive(&tempty[acc]);
       ++acc_it;
     }
   }
@@ -454,8 +474,14 @@ cudaError_t mx8_gemm(const GroupedGemm& g, cudaStream_t stream) {
   MArgs ma;
   ma.g = g;
   const bool sw = g.epi == EPI_SWIGLU;
-  ma.BN = (sw || g.Nout % 256 == 0) ? 256 : 128;
-  ma.n_tiles = sw ? g.Nout / 128 : g.Nout / ma.BN;
+  // SwiGLU: 128 features (gate and up rows) per tile, one accumulator.  The routing-weighted
+  // fp32 epilogue (twice the output bytes of the bf16 one) overlaps the next tile's MMAs:
+  // 224 rows per tile (the last one may reach past N) in two accumulators; measured on the
+  // 7168-wide GEMM2 of the MXFP8 layer, 2.33 -> 2.19 ms.  The bf16 epilogue keeps one
+  // accumulator of 256 rows (224 measured slower there: 2.44 -> 2.71 ms on N = 4096).
+  ma.BN = sw ? 256 : (g.epi == EPI_WEIGHTED_F32 ? 224 : (g.Nout % 256 == 0 ? 256 : 128));
+  ma.nacc = ma.BN <= 224 ? 2 : 1;
+  ma.n_tiles = sw ? g.Nout / 128 : (g.Nout + ma.BN - 1) / ma.BN;
   ma.tiles = g.grid_blocks * ma.n_tiles;
   // weights as E * Nw rows of Kin bytes; boxes of 128 bytes x BN rows in the 128-byte swizzle
   CUtensorMap tmap;
