@@ -555,7 +555,7 @@ def bench_ours(args, rank, world, local_rank):
         "useful_tflops": world * useful_flops(w) * steps / (ms * 1e-3) / 1e12,
         "layer_latency_us": ms_step * 1e3,
         "kernel_ms": {"gemm1_swiglu": g1, "gemm2_weighted": g2, "combine": cb,
-                      "route_align_pad_and_gaps": ms_step - g1 - g2 - cb},
+                      "route_align_pad_x16_and_gaps": ms_step - g1 - g2 - cb},
         "experts_touched": touched,
         "roofline": roofline,
         "step_roofline": {"bytes": step_weight_bytes, "achieved_gbs": step_weight_bytes / (ms_step * 1e-3) / 1e9,

@@ -71,8 +71,9 @@ typedef struct {
   int32_t* dev_status;     /* optional device int32 (set to 0 by the caller); may be NULL   */
   void** events;           /* optional host array of cudaEvent_t recorded on the stream
                               around each kernel of a call (profiling); may be NULL.
-                              moe_forward: [0] before GEMM1, [1] after GEMM1, [2] after
-                              GEMM2, [3] after the combine (needs n_events >= 4);
+                              moe_forward: [0] before GEMM1 (after x's f16 copy), [1]
+                              after GEMM1, [2] after GEMM2, [3] after the combine (needs
+                              n_events >= 4);
                               moe_grouped_gemm, moe_wgrad: [0] before, [1] after.      */
   int32_t n_events;
 } moe_ctx;

@@ -401,7 +401,6 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
       g2.fix_bits = reinterpret_cast<uint32_t*>(fix + f1 + 256);
     }
   }
-  rec(ctx, 0, 4);
   if (fix) {
     st = cuda_status(cudaMemsetAsync(fix, 0, fix_bytes, s), "moe_forward marks");
     if (st != MOE_OK) return st;
@@ -415,6 +414,7 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
     st = cuda_status(moe_launch::bf16_to_f16(x, x16, T_rows * K, status_of(ctx), s), "moe_forward x");
     if (st != MOE_OK) return st;
   }
+  rec(ctx, 0, 4);  // after x's f16 copy: the events bracket the GEMM kernels alone
   st = cuda_status(moe_launch::grouped_gemm(g1, T_rows, s), "moe_forward GEMM1");
   if (st != MOE_OK) return st;
   rec(ctx, 1, 4);

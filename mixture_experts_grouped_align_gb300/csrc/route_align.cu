@@ -5,7 +5,7 @@
 // "tune the Nemotron MTP decode row on S5000 with a checked-in recipe" (torchada PR 115),
 // What it does (moe_align_block_size as the native op feeding the fused-MoE kernel).
 //
-// Design: alignment runs in ONE thread block of 32 warps.  Each warp owns a contiguous
+// Design: for decode sizes alignment runs in ONE thread block of 32 warps.  Each warp owns a contiguous
 // range of pairs; pass 1 builds a private per-warp histogram in shared memory (no
 // atomics: __match_any_sync groups lanes of equal expert and the group leader adds the
 // group size), pass 2 scans the padded counts over experts and the per-warp counts over
@@ -13,7 +13,8 @@
 // ranges and lanes are ranked inside each 32-pair step, the scatter is stable (ascending
 // pair index within an expert) without any order-dependent atomics.  For small T the
 // routing runs in the same block (one launch for the whole decode-size step); larger T
-// routes with a grid of warps first.
+// routes with a grid of warps first, and above 16384 pairs the alignment itself runs on a
+// grid of blocks (align_multi_kernel, below) with the same result.
 #include "moe_common.cuh"
 #include "moe_launch.h"
 
@@ -288,11 +289,147 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(AlignArgs a) {
   }
 }
 
+// The same alignment over many thread blocks, for large pair counts (prefill), without any
+// scratch memory or inter-block communication: block b owns the pairs [b * chunk, (b + 1) *
+// chunk).  Every block counts the whole id array (the expert totals, for the padded
+// offsets) and, separately, the pairs before its own range (its starting rank inside each
+// expert); then it scatters its own range exactly as the single-block kernel does, so the
+// result is the same, bit for bit.  Sentinel slots and block expert ids are spread over
+// all blocks; block 0 writes num_tokens_post_padded and the expert offsets.
+__global__ void __launch_bounds__(kAlignThreads, 1) align_multi_kernel(AlignArgs a) {
+  extern __shared__ int smem_i[];
+  const int E = a.E, bm = a.bm, k = a.k;
+  int* hist = smem_i;                     // [32][E] this block's range, per warp
+  int* all = hist + kAlignWarps * E;      // [E] every pair
+  int* before = all + E;                  // [E] pairs before this block's range
+  int* poff = before + E;                 // [E+1] padded offsets
+  int* scratch = poff + (E + 1);          // [32 + 2]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kAlignWarps * E; i += kAlignThreads) hist[i] = 0;
+  for (int i = tid; i < 2 * E; i += kAlignThreads) all[i] = 0;  // all, before
+  __syncthreads();
+
+  const int P = (int)(a.T * k);
+  const int bchunk = (P + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int bbeg = min(P, (int)blockIdx.x * bchunk), bend = min(P, bbeg + bchunk);
+
+  // totals and this block's starting ranks: one pass over every pair, warp-aggregated
+  for (int base = warp * 32; base < P; base += kAlignThreads) {
+    const int p = base + lane;
+    int e = -1;
+    if (p < P) {
+      e = a.ids[p];
+      if (e < 0 || e >= E) {
+        if (blockIdx.x == 0) moe::set_status(a.status, MOE_ERR_INVALID_EXPERT);
+        e = -1;
+      }
+    }
+    const int key = e >= 0 ? e : (0x40000000 | lane);
+    const unsigned grp = __match_any_sync(kFull, key);
+    if (e >= 0 && lane == __ffs(grp) - 1) atomicAdd(&all[e], __popc(grp));
+    const bool pre = p < bbeg;
+    const unsigned grp_pre = grp & __ballot_sync(kFull, pre);
+    if (e >= 0 && pre && lane == __ffs(grp_pre) - 1) atomicAdd(&before[e], __popc(grp_pre));
+  }
+  // this block's range, per warp (for the stable in-block ranks)
+  const int chunk = (bend - bbeg + kAlignWarps - 1) / kAlignWarps;
+  const int beg = min(bend, bbeg + warp * chunk), end = min(bend, beg + chunk);
+  int* myhist = hist + warp * E;
+  for (int base = beg; base < end; base += 32) {
+    const int p = base + lane;
+    int e = -1;
+    if (p < end) {
+      e = a.ids[p];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const int key = e >= 0 ? e : (0x40000000 | lane);
+    const unsigned grp = __match_any_sync(kFull, key);
+    if (e >= 0 && lane == __ffs(grp) - 1) myhist[e] += __popc(grp);
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // padded offsets over experts; each warp's base = expert offset + earlier blocks' pairs +
+  // earlier warps' pairs of this block
+  const int c = tid < E ? all[tid] : 0;
+  const int padded = (c + bm - 1) / bm * bm;
+  const int off_pad = block_excl_scan(tid < E ? padded : 0, scratch, scratch + 32);
+  const int total_pad = scratch[32];
+  __syncthreads();
+  const int off_cnt = block_excl_scan(c, scratch, scratch + 33);
+  const int total_cnt = scratch[33];
+  if (tid < E) {
+    poff[tid] = off_pad;
+    int run = off_pad + before[tid];
+    for (int w = 0; w < kAlignWarps; ++w) {
+      const int t = hist[w * E + tid];
+      hist[w * E + tid] = run;
+      run += t;
+    }
+    if (blockIdx.x == 0 && a.expert_offsets) a.expert_offsets[tid] = off_cnt;
+  }
+  if (tid == 0) {
+    poff[E] = total_pad;
+    if (blockIdx.x == 0) {
+      *a.ntpp = total_pad;
+      if (a.expert_offsets) a.expert_offsets[E] = total_cnt;
+    }
+  }
+  __syncthreads();
+
+  // stable scatter of this block's range
+  for (int base = beg; base < end; base += 32) {
+    const int p = base + lane;
+    int e = -1;
+    if (p < end) {
+      e = a.ids[p];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const int key = e >= 0 ? e : (0x40000000 | lane);
+    const unsigned grp = __match_any_sync(kFull, key);
+    if (e >= 0) {
+      const int rank = __popc(grp & ((1u << lane) - 1u));
+      a.sorted[myhist[e] + rank] = p;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(grp) - 1) myhist[e] += __popc(grp);
+    __syncwarp();
+  }
+  // sentinel slots and block expert ids, spread over the grid
+  const int64_t gtid = (int64_t)blockIdx.x * kAlignThreads + tid, gstride = (int64_t)gridDim.x * kAlignThreads;
+  for (int64_t s = gtid; s < a.cap; s += gstride) {
+    bool pad = s >= total_pad;
+    if (!pad) {
+      int lo = 0, hi = E;  // last e with poff[e] <= s
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (poff[mid] <= s) lo = mid; else hi = mid;
+      }
+      pad = s >= (int64_t)poff[lo] + all[lo];
+    }
+    if (pad) a.sorted[s] = P;
+  }
+  const int64_t cap_blocks = a.cap / bm;
+  for (int64_t b = gtid; b < cap_blocks; b += gstride) {
+    const int64_t s = b * bm;
+    int eid = -1;
+    if (s < total_pad) {
+      int lo = 0, hi = E;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (poff[mid] <= s) lo = mid; else hi = mid;
+      }
+      eid = lo;
+    }
+    a.expert_ids[b] = eid;
+  }
+}
+
 }  // namespace
 
 namespace moe_launch {
 
-size_t align_smem_bytes(int E) { return sizeof(int) * ((size_t)kAlignWarps * E + 2 * E + 1 + 34); }
+size_t align_smem_bytes(int E) { return sizeof(int) * ((size_t)kAlignWarps * E + 3 * E + 1 + 34); }
 
 cudaError_t align(const float* logits, int32_t* ids, float* w, int64_t T, int k, int E, int bm,
                   int32_t* sorted, int64_t cap, int32_t* expert_ids, int32_t* ntpp,
@@ -312,6 +449,20 @@ cudaError_t align(const float* logits, int32_t* ids, float* w, int64_t T, int k,
     }
   }
   const size_t smem = align_smem_bytes(E);
+  // Above kMultiPairs pairs (prefill) the grid version: one block per 4096 pairs, at most one
+  // per SM.  Both kernels write the same bits, so the choice cannot break padded = unpadded.
+  constexpr int64_t kMultiPairs = 16384;
+  const int64_t P = T * k;
+  if (P > kMultiPairs && !a.route_here) {
+    cudaError_t err = cudaFuncSetAttribute(align_multi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+    if (err != cudaSuccess) return err;
+    int64_t blocks = (P + 4095) / 4096;
+    const int sms = sm_count_current();
+    if (blocks > sms) blocks = sms;
+    align_multi_kernel<<<(unsigned)blocks, kAlignThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+  }
   cudaError_t err = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
   if (err != cudaSuccess) return err;

@@ -134,3 +134,40 @@ def test_capacity_tail_untouched_beyond_cap(moe):
     cap, capb = moe.moe_align_capacity(20, 4, 4)
     assert np.all(r["srt_full"][cap:] == -7)
     assert np.all(r["eid_full"][capb:] == -7)
+
+
+@pytest.mark.parametrize("T,E,k,bm", [
+    (4097, 8, 4, 128),      # 16388 pairs: just past the single-block size, a ragged last range
+    (3000, 1024, 32, 64),   # E = 1024, k = 32: the largest shared-memory histograms
+    (20000, 64, 2, 16),     # small blocks: many block ids, long sentinel tail
+    (65536, 3, 1, 1),       # block_m = 1, a few hot experts
+])
+def test_multi_block_alignment(moe, T, E, k, bm):
+    """Above 16384 pairs the alignment runs on a grid of blocks; its output is the same
+    definition: bit-exact against the oracle over the whole capacity, beyond which nothing is
+    written."""
+    rng = np.random.default_rng(T + E)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32) if E > 64 else \
+        rng.integers(0, E, size=(T, k)).astype(np.int32)
+    if E > 4:
+        ids[rng.random(T) < 0.3] = np.sort(rng.choice(max(E // 4, k), k, replace=False))  # skew to low ids
+    r = gpu_align(moe, T, k, E, bm, ids=ids)
+    check_against_oracle(r, ids, E, bm)
+    assert r["status"] == 0
+    cap, capb = moe.moe_align_capacity(T * k, E, bm)
+    assert np.all(r["srt_full"][cap:] == -7)
+    assert np.all(r["eid_full"][capb:] == -7)
+
+
+def test_multi_block_invalid_expert_id(moe):
+    T, E, k = 9000, 16, 2
+    rng = np.random.default_rng(5)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    ids[4321, 1] = E + 3
+    ids[8999, 0] = -2
+    r = gpu_align(moe, T, k, E, 128, ids=ids)
+    assert r["status"] == -5
+    keep = np.ones(T * k, dtype=bool)
+    keep[[4321 * k + 1, 8999 * k]] = False
+    real = r["sorted"][r["sorted"] < T * k]
+    assert np.array_equal(np.sort(real), np.flatnonzero(keep))
