@@ -77,41 +77,68 @@ __global__ void bf16_to_f16_kernel(const uint4* __restrict__ x, uint4* __restric
 }
 
 // y[s] = f16(x[sorted[s] / k]) for the alignment slots s < num_tokens_post_padded (a slot of
-// the sentinel gets zeros), 8 elements per thread: the token rows in slot order, so that a
-// block of 128 slots is 128 consecutive rows.  |x| > 65504 of a real row is reported.
+// the sentinel gets zeros): the token rows in slot order, so that a block of 128 slots is 128
+// consecutive rows.  One warp per slot row (the pair id read once), four 16-byte chunks in
+// flight per lane.  |x| > 65504 of a real row is reported.
 __global__ void gather_rows_f16_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted,
-                                       const int32_t* __restrict__ ntpp, int64_t P, int k, int64_t per,
-                                       int64_t n8, uint4* __restrict__ y, int32_t* status) {
-  const int64_t lim = (int64_t)*ntpp * per;
+                                       const int32_t* __restrict__ ntpp, int64_t P, int k, int per,
+                                       int64_t slots, uint4* __restrict__ y, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t rows = slots < (int64_t)*ntpp ? slots : (int64_t)*ntpp;
   bool bad = false;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8 && i < lim;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t s = i / per, c = i - s * per;
+  for (int64_t s = warp0; s < rows; s += nwarps) {
     const int p = __ldg(sorted + s);
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (p < P) {
-      v = __ldg(x + (int64_t)(p / k) * per + c);
-      v.x = moe::bf16x2_to_f16x2(v.x, &bad);
-      v.y = moe::bf16x2_to_f16x2(v.y, &bad);
-      v.z = moe::bf16x2_to_f16x2(v.z, &bad);
-      v.w = moe::bf16x2_to_f16x2(v.w, &bad);
+    const uint4* src = x + (int64_t)(p / k) * per;
+    uint4* dst = y + s * per;
+    for (int c0 = lane; c0 < per; c0 += 4 * 32) {
+      uint4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + 32 * j;
+        v[j] = (p < P && c < per) ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + 32 * j;
+        if (c >= per) break;
+        v[j].x = moe::bf16x2_to_f16x2(v[j].x, &bad);
+        v[j].y = moe::bf16x2_to_f16x2(v[j].y, &bad);
+        v[j].z = moe::bf16x2_to_f16x2(v[j].z, &bad);
+        v[j].w = moe::bf16x2_to_f16x2(v[j].w, &bad);
+        dst[c] = v[j];
+      }
     }
-    y[i] = v;
   }
   if (bad) moe::set_status(status, MOE_ERR_RANGE);
 }
 
 // Rows of `per` 16-byte chunks into alignment-slot order: row s <- src row p / div of the
-// pair p in slot s (zeros for the sentinel), one chunk per thread.
+// pair p in slot s (zeros for the sentinel).  One warp per slot row, four chunks in flight
+// per lane.
 __global__ void gather_slot_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ sorted,
-                                        const int32_t* __restrict__ ntpp, int64_t P, int div, int64_t per,
-                                        int64_t n16, uint4* __restrict__ y) {
-  const int64_t lim = (int64_t)*ntpp * per;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16 && i < lim;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t s = i / per, c = i - s * per;
+                                        const int32_t* __restrict__ ntpp, int64_t P, int div, int per,
+                                        int64_t slots, uint4* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t rows = slots < (int64_t)*ntpp ? slots : (int64_t)*ntpp;
+  for (int64_t s = warp0; s < rows; s += nwarps) {
     const int p = __ldg(sorted + s);
-    y[i] = p < P ? __ldg(src + (int64_t)(p / div) * per + c) : make_uint4(0u, 0u, 0u, 0u);
+    const uint4* row = src + (int64_t)(p / div) * per;
+    uint4* dst = y + s * per;
+    for (int c0 = lane; c0 < per; c0 += 4 * 32) {
+      uint4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + 32 * j;
+        v[j] = (p < P && c < per) ? __ldg(row + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (c0 + 32 * j < per) dst[c0 + 32 * j] = v[j];
+    }
   }
 }
 
@@ -142,19 +169,21 @@ namespace moe_launch {
 
 cudaError_t gather_rows_f16(const void* x, const int32_t* sorted, const int32_t* ntpp, int64_t P, int k,
                             int64_t K, int64_t slots, void* y, int32_t* status, cudaStream_t stream) {
-  const int64_t per = K / 8, n8 = slots * per;
-  if (n8 == 0) return cudaSuccess;
-  gather_rows_f16_kernel<<<grid_for(n8, 256), 256, 0, stream>>>((const uint4*)x, sorted, ntpp, P, k, per, n8,
-                                                                 (uint4*)y, status);
+  const int64_t per = K / 8;
+  if (slots == 0 || per == 0) return cudaSuccess;
+  if (per >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+  gather_rows_f16_kernel<<<grid_for(slots * 32, 256), 256, 0, stream>>>((const uint4*)x, sorted, ntpp, P, k,
+                                                                         (int)per, slots, (uint4*)y, status);
   return cudaGetLastError();
 }
 
 cudaError_t gather_slot_rows(const void* src, int64_t row_bytes, const int32_t* sorted, const int32_t* ntpp,
                              int64_t P, int div, int64_t slots, void* y, cudaStream_t stream) {
-  const int64_t per = row_bytes / 16, n16 = slots * per;
-  if (n16 == 0) return cudaSuccess;
-  gather_slot_rows_kernel<<<grid_for(n16, 256), 256, 0, stream>>>((const uint4*)src, sorted, ntpp, P, div, per,
-                                                                  n16, (uint4*)y);
+  const int64_t per = row_bytes / 16;
+  if (slots == 0 || per == 0) return cudaSuccess;
+  if (per >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+  gather_slot_rows_kernel<<<grid_for(slots * 32, 256), 256, 0, stream>>>((const uint4*)src, sorted, ntpp, P, div,
+                                                                         (int)per, slots, (uint4*)y);
   return cudaGetLastError();
 }
 

@@ -313,24 +313,31 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_multi_kernel(AlignArgs
   const int bchunk = (P + (int)gridDim.x - 1) / (int)gridDim.x;
   const int bbeg = min(P, (int)blockIdx.x * bchunk), bend = min(P, bbeg + bchunk);
 
-  // totals and this block's starting ranks: one pass over every pair, warp-aggregated
-  for (int base = warp * 32; base < P; base += kAlignThreads) {
-    const int p = base + lane;
-    int e = -1;
-    if (p < P) {
-      e = a.ids[p];
-      if (e < 0 || e >= E) {
-        if (blockIdx.x == 0) moe::set_status(a.status, MOE_ERR_INVALID_EXPERT);
-        e = -1;
-      }
+  // totals and this block's starting ranks: one pass over every pair, eight loads in flight
+  // per thread (the pass is bound by load latency, not by the shared-memory atomics)
+  constexpr int kUnroll = 8;
+  bool bad = false;
+  for (int base = 0; base < P; base += kUnroll * kAlignThreads) {
+    int ev[kUnroll];
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int p = base + j * kAlignThreads + tid;
+      ev[j] = p < P ? __ldg(a.ids + p) : -1;
     }
-    const int key = e >= 0 ? e : (0x40000000 | lane);
-    const unsigned grp = __match_any_sync(kFull, key);
-    if (e >= 0 && lane == __ffs(grp) - 1) atomicAdd(&all[e], __popc(grp));
-    const bool pre = p < bbeg;
-    const unsigned grp_pre = grp & __ballot_sync(kFull, pre);
-    if (e >= 0 && pre && lane == __ffs(grp_pre) - 1) atomicAdd(&before[e], __popc(grp_pre));
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int p = base + j * kAlignThreads + tid;
+      if (p >= P) continue;
+      const int e = ev[j];
+      if (e < 0 || e >= E) {
+        bad = true;
+        continue;
+      }
+      atomicAdd(&all[e], 1);
+      if (p < bbeg) atomicAdd(&before[e], 1);
+    }
   }
+  if (bad && blockIdx.x == 0) moe::set_status(a.status, MOE_ERR_INVALID_EXPERT);
   // this block's range, per warp (for the stable in-block ranks)
   const int chunk = (bend - bbeg + kAlignWarps - 1) / kAlignWarps;
   const int beg = min(bend, bbeg + warp * chunk), end = min(bend, beg + chunk);
