@@ -37,15 +37,18 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE layer useful TFLOP/s & tokens/s; % of GB300 block-scaled TC / HBM roofline"
 L2_BYTES = 129 * 1024 * 1024
 
-# DRAM traffic (read + write bytes) of one launch of the dominant kernel, from an ncu
-# capture of the same command, valid while the kernel source hashes the same; otherwise
-# reported as null.
+# DRAM traffic (read + write bytes) of one launch of the dominant kernel (for the weight
+# gradient: every launch of one moe_wgrad call), from an ncu capture of the same command,
+# valid while the kernel source hashes the same; otherwise reported as null.
 TRAFFIC = {
     "decode_gemm.cu:gemm1@decode_mxfp4": {
         "src": "1d10e33c80844cd4", "bytes": 997873920 + 4255232},
     # both launches of the call: the main pass and the (empty) exact-scale pass
     "prefill_ts.cu:gemm1@prefill_mxfp4": {
-        "src": "22f52e91b9b3601a", "bytes": 2601815296 + 1444242688 + 68352},
+        "src": "40b9e45121f051d6", "bytes": 2599493120 + 1443217152 + 68608},
+    # the dW1 call: the two slot-order copies, the expert ranges and the tensor-core kernel
+    "wgrad_tc.cu:wgrad_dW1@mxfp8_wgrad": {
+        "src": "76867c344737658b", "bytes": 37354372864},
 }
 
 
@@ -676,8 +679,10 @@ def bench_mxfp8_wgrad(args, rank, world, local_rank):
     dom = int(np.argmax(kms))
     if dom >= 2:
         achieved = dw_bytes[dom] / (kms[dom] * 1e-3) / 1e9
+        tr = TRAFFIC.get(f"wgrad_tc.cu:{names[dom]}@mxfp8_wgrad")
+        traffic = tr["bytes"] if tr and tr.get("src") == src_hash("wgrad_tc.cu", "elementwise.cu") else None
         roofline = {"bound": "hbm", "kernel": f"wgrad ({names[dom]})", "achieved": achieved, "peak": hbm,
-                    "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                    "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                     "algorithmic_bytes": dw_bytes[dom], "peak_source": f"{src} (hbm_gbs)"}
     else:
         # E4M3 x E4M3 block-scaled MMA: the measured bf16 peak times the nominal 2x of fp8
