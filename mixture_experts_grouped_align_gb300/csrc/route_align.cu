@@ -122,18 +122,49 @@ __device__ void softmax_topk(float* __restrict__ w, int k) {
   for (int j = 0; j < k; ++j) w[j] = __double2float_rn(ex[j] / s);
 }
 
+// The same softmax with a warp per token: lane j computes the j-th exponential, and every
+// lane forms the float64 sum from the shuffled terms in exactly softmax_topk's order, so the
+// bits are the same.  For a handful of tokens this replaces k dependent float64
+// exponentials on one lane (float64 is slow on this part) by one per lane; for more tokens
+// the warps' mostly idle float64 instructions crowd the SM's float64 pipe (measured: a
+// 64-token step's alignment 28.7 -> 41.7 us), so the thread-per-token form stays there.
+__device__ void softmax_topk_warp(float* __restrict__ w, int k, int lane) {
+  const double m = (double)w[0];
+  const double ex = lane < k ? exp((double)w[lane] - m) : 0.0;
+  double s;
+  if (k < 8) {
+    s = 0.0;
+    for (int j = 0; j < k; ++j) s += __shfl_sync(kFull, ex, j);
+  } else {
+    double r[8];
+    for (int i = 0; i < 8; ++i) r[i] = __shfl_sync(kFull, ex, i);
+    int j = 8;
+    for (; j + 8 <= k; j += 8)
+      for (int i = 0; i < 8; ++i) r[i] += __shfl_sync(kFull, ex, j + i);
+    s = ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
+    for (; j < k; ++j) s += __shfl_sync(kFull, ex, j);
+  }
+  if (lane < k) w[lane] = __double2float_rn(ex / s);
+  __syncwarp();
+}
+
 // Routes tokens t0 .. t0 + n - 1 (n <= blockDim.x) with the whole thread block: a warp
-// per token selects the top-k, then (after a block barrier) a thread per token computes
-// its softmax, so both phases use every warp of the block.
+// per token selects the top-k; then, for at most 8 tokens (one-token decode steps), the same
+// warp computes the token's softmax, else (after a block barrier) a thread per token does.
 __device__ void route_block(const float* __restrict__ logits, int64_t t0, int n, int E, int k,
                             int32_t* __restrict__ ids, float* __restrict__ w) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const bool warp_soft = n <= 8 && n <= nw;
   for (int i = warp; i < n; i += nw) {
     const int64_t t = t0 + i;
     select_topk_any(logits + t * E, E, k, ids + t * k, w + t * k, lane);
+    if (warp_soft) {
+      __syncwarp();  // the chosen logits, written by lanes 0..k-1
+      softmax_topk_warp(w + t * k, k, lane);
+    }
   }
   __syncthreads();
-  if ((int)threadIdx.x < n) softmax_topk(w + (t0 + threadIdx.x) * k, k);
+  if (!warp_soft && (int)threadIdx.x < n) softmax_topk(w + (t0 + threadIdx.x) * k, k);
   __syncthreads();
 }
 
