@@ -69,10 +69,12 @@ constexpr int kLag = 2;                    // stages between a stage's copies an
 // 512 the scale words instead arrive four stages at a time, 16 bytes per row, into two group
 // buffers (A [128 rows][16 B], B [BN rows][16 B]): far fewer, larger copies.
 struct MLayout {
-  int a, b, sfa, sfb, slot, ga, gb, bars, total;
+  int a, b, sfa, sfb, slot, ga, gb, bars, stg, total;
 };
 
-__host__ __device__ inline MLayout mlayout(int BN) {
+// `staged`: the fp32 routing-weighted epilogue also takes a 32 x 32 fp32 box per epilogue
+// warp, through which its rows leave as whole 128-byte lines.
+__host__ __device__ inline MLayout mlayout(int BN, bool staged) {
   MLayout L;
   L.a = 0;
   L.b = kBM * kBK;
@@ -82,7 +84,8 @@ __host__ __device__ inline MLayout mlayout(int BN) {
   L.ga = kStages * L.slot;
   L.gb = L.ga + 2 * kBM * 16;
   L.bars = L.gb + 2 * BN * 16;
-  L.total = L.bars + 256 + 1024;
+  L.stg = L.bars + 256;
+  L.total = L.stg + (staged ? 4 * 32 * 128 : 0) + 1024;
   return L;
 }
 
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int BN = ma.BN, NBW = BN / 32;  // B scale words per lane
-  const MLayout L = mlayout(BN);
+  const MLayout L = mlayout(BN, EPI == EPI_WEIGHTED_F32);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;  // [2]
@@ -400,19 +403,46 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
           uint32_t v[32];
           tc::tmem_ld32(tb + c0, v);
           tc::tmem_ld_wait();
-          if (valid) {
+          if (EPI == EPI_WEIGHTED_F32) {
+            // this lane's row of the chunk into the box (16-byte chunks swizzled by row), then
+            // four rows per instruction out of it: eight lanes store a row's 128 bytes
+            const uint32_t box = smem_s + L.stg + quarter * 32 * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float o4[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                o4[i] = __uint_as_float(v[4 * j + i]);
+                if (bias) o4[i] += moe::bf16_bits_to_f32(bias[e * a.Nw + n0 + c0 + 4 * j + i]);
+                o4[i] *= wgt;
+              }
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(box + lane * 128 + ((j ^ (lane & 7)) << 4)),
+                           "f"(o4[0]), "f"(o4[1]), "f"(o4[2]), "f"(o4[3])
+                           : "memory");
+            }
+            __syncwarp();
+            const int cc = lane & 7;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = (lane >> 3) + 4 * i;
+              const int pr = __shfl_sync(0xffffffffu, p, rr);
+              float4 w4;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(w4.x), "=f"(w4.y), "=f"(w4.z), "=f"(w4.w)
+                           : "r"(box + rr * 128 + ((cc ^ (rr & 7)) << 4))
+                           : "memory");
+              if (pr < a.P)
+                *reinterpret_cast<float4*>(static_cast<float*>(a.out) + (int64_t)pr * a.Nout + n0 + c0 + 4 * cc) = w4;
+            }
+            __syncwarp();
+          } else if (valid) {
             float o[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               o[j] = __uint_as_float(v[j]);
               if (bias) o[j] += moe::bf16_bits_to_f32(bias[e * a.Nw + n0 + c0 + j]);
             }
-            if (EPI == EPI_WEIGHTED_F32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + (int64_t)p * a.Nout + n0 + c0);
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                dst[j] = make_float4(o[4 * j] * wgt, o[4 * j + 1] * wgt, o[4 * j + 2] * wgt, o[4 * j + 3] * wgt);
-            } else {
+            {
               uint32_t pk[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j)
@@ -442,7 +472,7 @@ int sm_count_mx8() { return moe_launch::sm_count_current(); }
 
 template <int EPI>
 cudaError_t launch_mx8(const MArgs& ma, const CUtensorMap& tmap, cudaStream_t stream) {
-  const MLayout L = mlayout(ma.BN);
+  const MLayout L = mlayout(ma.BN, EPI == EPI_WEIGHTED_F32);
   cudaError_t err = cudaFuncSetAttribute(mx8_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
   int64_t grid = sm_count_mx8();
