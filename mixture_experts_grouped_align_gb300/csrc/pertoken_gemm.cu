@@ -11,8 +11,9 @@
 // Per thread block (one per SM, 512 threads), persistent over (row block, N tile):
 //   all threads first turn the group sizes into the running row offsets O_e and the running
 //   counts of 128-row blocks, so that tile t's expert is a binary search away;
-//   warp 0      allocates the TMEM accumulator (128 x BN f32) and, on one lane, issues the
-//               MMAs (M = 128, N = BN, K = 32; four per 128-wide K stage);
+//   warp 0      allocates two TMEM accumulators (128 x BN f32 each, used in turn so that
+//               a tile's epilogue overlaps the next tile's MMAs) and, on one lane, issues
+//               the MMAs (M = 128, N = BN, K = 32; four per 128-wide K stage);
 //   warps 8-15  copy each stage: one thread loads the BN weight rows of 128 bytes with a TMA
 //               box into a 128-byte-swizzled K-major tile; all copy the block's activation
 //               rows (contiguous: one expert's rows are consecutive) with cp.async into the
@@ -38,7 +39,7 @@ constexpr int kThreads = 512;
 constexpr int kBM = 128, kBK = 128;        // tile rows, K elements (bytes) per stage
 constexpr int kProd0 = 256, kNumProd = 256;
 constexpr int kEpiWarp0 = 4;
-constexpr int kTmemCols = 256;
+constexpr int kTmemCols = 512;               // two accumulators of up to 256 columns
 constexpr int kStages = 4;
 constexpr int kLag = 2;                    // stages between a stage's copies and its hand-over
 constexpr int kMaxE = 1024;
@@ -119,9 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1) pertoken_gemm_kernel(const __grid
   int32_t* boff = reinterpret_cast<int32_t*>(roff + (kMaxE + 1));  // [E + 1] block offsets
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
-  uint64_t* tempty = tfull + 1;
-  uint64_t* drain = tempty + 1;
+  uint64_t* tfull = empty + kStages;  // [2]
+  uint64_t* tempty = tfull + 2;       // [2]
+  uint64_t* drain = tempty + 2;
   uint32_t* taddr_s = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(taddr_s + 1);
 
@@ -131,8 +132,10 @@ __global__ void __launch_bounds__(kThreads, 1) pertoken_gemm_kernel(const __grid
       tc::mbar_init(&full[s], kNumProd / 32 + 1);  // producer warps + the weight box
       tc::mbar_init(&empty[s], 1);
     }
-    tc::mbar_init(tfull, 1);
-    tc::mbar_init(tempty, 4);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&tfull[i], 1);
+      tc::mbar_init(&tempty[i], 4);
+    }
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
     tc::mbar_fence_init();
@@ -254,7 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) pertoken_gemm_kernel(const __grid
       for (int64_t t = blockIdx.x; t < pa.tiles && !*abort_flag; t += gridDim.x) {
         Tile tl;
         if (!tile_of(pa, t, roff, boff, nblocks, tl)) break;
-        if (!tc::mbar_wait(tempty, (acc_it & 1) ^ 1)) {
+        const uint32_t acc = acc_it & 1;
+        if (!tc::mbar_wait(&tempty[acc], ((acc_it >> 1) & 1) ^ 1)) {
           moe::set_status(pa.status, MOE_ERR_TIMEOUT);
           *abort_flag = 1;
           break;
@@ -273,13 +277,13 @@ __global__ void __launch_bounds__(kThreads, 1) pertoken_gemm_kernel(const __grid
           const uint32_t sl = smem_s + s * L.slot;
 #pragma unroll
           for (int j = 0; j < kBK / 32; ++j)
-            mma_f8_ss(taddr, tc::sdesc_sw128(sl + L.a + j * 32), tc::sdesc_sw128(sl + L.b + j * 32), idesc,
+            mma_f8_ss(taddr + acc * 256, tc::sdesc_sw128(sl + L.a + j * 32), tc::sdesc_sw128(sl + L.b + j * 32), idesc,
                       (kc | j) != 0);
           tc::mma_commit(&empty[s]);
           ++it;
         }
         if (!ok) break;
-        tc::mma_commit(tfull);
+        tc::mma_commit(&tfull[acc]);
         ++acc_it;
       }
       tc::mma_commit(drain);
@@ -298,14 +302,15 @@ __global__ void __launch_bounds__(kThreads, 1) pertoken_gemm_kernel(const __grid
       const bool valid = row < tl.r1;
       const float sa = valid ? pa.a_scale[row] : 0.f;
       const float sw = pa.w_scale[tl.e];
-      if (!tc::mbar_wait(tfull, acc_it & 1)) {
+      const uint32_t acc = acc_it & 1;
+      if (!tc::mbar_wait(&tfull[acc], (acc_it >> 1) & 1)) {
         moe::set_status(pa.status, MOE_ERR_TIMEOUT);
         *abort_flag = 1;
         break;
       }
       tc::tc_fence_after();
       const int n0 = tl.nt * BN;
-      const uint32_t tb = taddr + ((uint32_t)(quarter * 32) << 16);
+      const uint32_t tb = taddr + acc * 256 + ((uint32_t)(quarter * 32) << 16);
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t v[32];
         tc::tmem_ld32(tb + c0, v);
@@ -328,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) pertoken_gemm_kernel(const __grid
       }
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tempty);
+      if (lane == 0) tc::mbar_arrive(&tempty[acc]);
       ++acc_it;
     }
   }
