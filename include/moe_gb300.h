@@ -274,10 +274,12 @@ size_t moe_grouped_gemm_workspace_size(moe_quant quant, int64_t T, int32_t k, in
  *    or NULL.  out: [T*k, N] bf16, indexed by pair.
  * N must be a multiple of 16 and Kin of 32.
  * Kernels: MXFP8 above 256 token rows runs the block-scaled tensor-core kernel (K and N
- * multiples of 128); W4A16 above 256 rows runs the tcgen05 kernel with decoded weights in
- * tensor memory when ctx->workspace holds moe_grouped_gemm_workspace_size() bytes (block_m
- * 128, Kin a multiple of 64; |A| <= 65504, else MOE_ERR_RANGE in dev_status);
- * every other call runs the weight-streaming kernel, which needs no workspace.  The kernel
+ * multiples of 128); bf16 above 256 rows the same tcgen05 kernel with bf16 operands (block_m
+ * 128, K a multiple of 64, N of 128); W4A16 above 256 rows runs the tcgen05 kernel with
+ * decoded weights in tensor memory when ctx->workspace holds
+ * moe_grouped_gemm_workspace_size() bytes (block_m 128, Kin a multiple of 64; |A| <= 65504,
+ * else MOE_ERR_RANGE in dev_status); every other call runs the weight-streaming kernel,
+ * which needs no workspace.  The kernel
  * choice depends on T only through the bucket value 256, and each kernel reduces K in one
  * fixed order. */
 moe_status moe_grouped_gemm(moe_quant quant, int32_t E, int32_t N, int32_t Kin,

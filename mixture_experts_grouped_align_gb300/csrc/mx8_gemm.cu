@@ -1,4 +1,6 @@
-// Grouped expert GEMM on MXFP8 operands with the block-scaled tensor-core MMA.
+// Grouped expert GEMM on MXFP8 operands with the block-scaled tensor-core MMA (and, with
+// the template flag BF, on bf16 operands with the plain kind::f16 MMA and no scale factors:
+// the same tiles, copies and epilogues, a bf16 h for SwiGLU).
 //
 // out[p, n] = bf16( sum_k A[row(p), k] * sa[row(p), k / 32] * W[e, n, k] * sw[e, n, k / 32]
 //                   + bias[e, n] ): E4M3 activations and weights, one E8M0 scale per 32
@@ -122,7 +124,8 @@ __device__ __forceinline__ int64_t b_row(const GroupedGemm& a, int64_t e, int nt
   return e * a.Nw + (int64_t)nt * BN + n;
 }
 
-template <int EPI>
+// BF: bf16 weights and activations (kind::f16, no scale factors); otherwise MXFP8.
+template <int EPI, bool BF>
 __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, MArgs ma) {
   const GroupedGemm& a = ma.g;
   extern __shared__ uint8_t smem_raw[];
@@ -164,7 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
   tc::tc_fence_after();
   const uint32_t taddr = *taddr_s;
   const int ntpp = *a.ntpp;
-  const int Kin = a.Kin, nk = Kin / kBK, nkb = Kin / 32;
+  // bytes of an operand row (a stage takes 128 of them: 128 E4M3 or 64 bf16 elements)
+  const int64_t rbytes = BF ? (int64_t)a.Kin * 2 : (int64_t)a.Kin;
+  const int nk = (int)(rbytes / kBK), nkb = a.Kin / 32;
   const uint32_t smem_s = tc::smem_addr(smem);
   // the limit of every wait (a caller's short limit only in the stalled self-test)
   const uint64_t wb = a.wait_ns > 0 ? (uint64_t)a.wait_ns : tc::kWaitNs;
@@ -179,14 +184,16 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
     int npend = 0;
     // scale words by groups of four stages (16-byte rows) when Kin % 512 == 0: a tile's stage
     // count is then a multiple of four, so stage it belongs to group it / 4
-    const bool grouped = (nkb % 16) == 0;
+    const bool grouped = !BF && (nkb % 16) == 0;
     const int tb = pt - 128;  // B-scale copier index (warps 12-15)
     // hand stage h over to the MMA: its copies (this thread's own) have landed
     auto hand_over = [&](uint32_t h) -> bool {
       const int hs = (int)(h % kStages);
       const uint8_t* sl = smem + hs * L.slot;
       tc::fence_proxy_async_smem();
-      if (wp < 4) {
+      if (BF) {
+        // no scale factors: the landed copies are all the stage needs
+      } else if (wp < 4) {
         const uint32_t wv = grouped
             ? *reinterpret_cast<const uint32_t*>(smem + L.ga + ((h >> 2) & 1) * kBM * 16 + (q * 32 + lane) * 16 + (h & 3) * 4)
             : *reinterpret_cast<const uint32_t*>(sl + L.sfa + (q * 32 + lane) * 4);
@@ -210,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
         }
         tc::tmem_st8(taddr + ((uint32_t)(q * 32) << 16) + sfb_col(hs), v);
       }
-      tc::tmem_st_wait();
+      if (!BF) tc::tmem_st_wait();
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&full[hs]);
@@ -224,10 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int p = a.sorted[blk * a.bm + r0 + 32 * i];
-        aptr[i] = p < a.P ? abase + act_row(a, p) * Kin + c16 * 16 : nullptr;
+        aptr[i] = p < a.P ? abase + act_row(a, p) * rbytes + c16 * 16 : nullptr;
       }
       const uint8_t* sfsrc = nullptr;  // A: this lane's row (B rows: b_row below)
-      if (wp < 4) {
+      if (!BF && wp < 4) {
         const int p = a.sorted[blk * a.bm + q * 32 + lane];
         if (p < a.P) sfsrc = a.act_scale + act_row(a, p) * nkb;
       }
@@ -259,7 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           if (aptr[i]) cp_async16(sl + L.a + tc::sw128_offset(r0 + 32 * i, c16), aptr[i] + kc * kBK);
-        if (grouped) {
+        if (BF) {
+          // bf16: no scale words
+        } else if (grouped) {
           if ((kc & 3) == 0) {  // this group's four stages of scale words, 16 bytes per row
             const uint32_t gsel = (it >> 2) & 1;
             if (wp < 4) {
@@ -307,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
       uint32_t idesc[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) idesc[j] = tc::idesc_mx8(kBM, BN, j, j);
+      const uint32_t idesc_bf = tc::idesc_f16(kBM, BN, 1);
       uint32_t it = 0, acc_it = 0;
       for (int64_t t = blockIdx.x; t < ma.tiles && !*abort_flag; t += gridDim.x) {
         int64_t blk, e;
@@ -334,6 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
           const uint32_t sl = smem_s + s * L.slot;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
+            if (BF)  // 16 bf16 of K per MMA: 32 bytes of the 128-byte rows, like 32 E4M3
+              tc::mma_f16_ss(d_tmem, tc::sdesc_sw128(sl + L.a + j * 32), tc::sdesc_sw128(sl + L.b + j * 32),
+                             idesc_bf, (kc | j) != 0);
+            else
             tc::mma_mx8_ss(d_tmem, tc::sdesc_sw128(sl + L.a + j * 32), tc::sdesc_sw128(sl + L.b + j * 32), idesc[j],
                            taddr + sfa_col(s), taddr + sfb_col(s), (kc | j) != 0);
           tc::mma_commit(&empty[s]);
@@ -385,6 +399,16 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
                 up += moe::bf16_bits_to_f32(bias[e * a.Nw + a.Nout + f0 + c0 + j]);
               }
               h[j] = moe::silu(gt) * up;
+            }
+            if (BF) {  // bf16 weights: h in bf16 (RNE)
+              uint32_t pk[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                pk[j] = (uint32_t)moe::f32_to_bf16_bits(h[2 * j]) | ((uint32_t)moe::f32_to_bf16_bits(h[2 * j + 1]) << 16);
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + (int64_t)p * a.Nout + f0 + c0);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+              continue;
             }
             uint32_t code[8], sc;
             mxq::quant32(h, code, sc);
@@ -470,15 +494,16 @@ __global__ void __launch_bounds__(kThreads, 1) mx8_gemm_kernel(const __grid_cons
 
 int sm_count_mx8() { return moe_launch::sm_count_current(); }
 
-template <int EPI>
+template <int EPI, bool BF>
 cudaError_t launch_mx8(const MArgs& ma, const CUtensorMap& tmap, cudaStream_t stream) {
   const MLayout L = mlayout(ma.BN, EPI == EPI_WEIGHTED_F32);
-  cudaError_t err = cudaFuncSetAttribute(mx8_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  cudaError_t err =
+      cudaFuncSetAttribute(mx8_gemm_kernel<EPI, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
   int64_t grid = sm_count_mx8();
   if (ma.tiles < grid) grid = ma.tiles;
   if (grid <= 0) return cudaSuccess;
-  mx8_gemm_kernel<EPI><<<(unsigned)grid, kThreads, L.total, stream>>>(tmap, ma);
+  mx8_gemm_kernel<EPI, BF><<<(unsigned)grid, kThreads, L.total, stream>>>(tmap, ma);
   return cudaGetLastError();
 }
 
@@ -487,15 +512,23 @@ cudaError_t launch_mx8(const MArgs& ma, const CUtensorMap& tmap, cudaStream_t st
 namespace moe_launch {
 
 bool mx8_supported(const GroupedGemm& g) {
-  if (g.wfmt != WF_MXFP8 || g.act_scale == nullptr) return false;
-  if (g.epi != EPI_PLAIN_BF16 && g.epi != EPI_WEIGHTED_F32 && !(g.epi == EPI_SWIGLU && g.out_scale)) return false;
+  const bool bf = g.wfmt == WF_BF16;
+  if (bf) {
+    // bf16 weights and activations: SwiGLU writes bf16 h (no quantiser)
+    if (g.act_fmt != ACT_BF16) return false;
+    if (g.epi != EPI_PLAIN_BF16 && g.epi != EPI_WEIGHTED_F32 && g.epi != EPI_SWIGLU) return false;
+  } else {
+    if (g.wfmt != WF_MXFP8 || g.act_scale == nullptr) return false;
+    if (g.epi != EPI_PLAIN_BF16 && g.epi != EPI_WEIGHTED_F32 && !(g.epi == EPI_SWIGLU && g.out_scale)) return false;
+  }
   if (g.act_by_slot || g.out_by_slot) return false;
-  if (g.bm != kBM || g.Kin <= 0 || g.Kin % kBK != 0) return false;
+  const int64_t rbytes = bf ? (int64_t)g.Kin * 2 : (int64_t)g.Kin;
+  if (g.bm != kBM || g.Kin <= 0 || rbytes % kBK != 0) return false;
   if (g.Nout % 128 != 0) return false;
   if ((int64_t)g.E * g.Nw >= ((int64_t)1 << 31)) return false;  // TMA row coordinates are 32-bit
   // 16-byte copies of activation and weight rows, 4-byte copies of scale words
   const uintptr_t al16 = reinterpret_cast<uintptr_t>(g.act) | reinterpret_cast<uintptr_t>(g.w);
-  const uintptr_t al4 = reinterpret_cast<uintptr_t>(g.act_scale) | reinterpret_cast<uintptr_t>(g.w_scale);
+  const uintptr_t al4 = bf ? 0 : (reinterpret_cast<uintptr_t>(g.act_scale) | reinterpret_cast<uintptr_t>(g.w_scale));
   return (al16 & 15) == 0 && (al4 & 3) == 0;
 }
 
@@ -513,14 +546,21 @@ cudaError_t mx8_gemm(const GroupedGemm& g, cudaStream_t stream) {
   ma.nacc = ma.BN <= 224 ? 2 : 1;
   ma.n_tiles = sw ? g.Nout / 128 : (g.Nout + ma.BN - 1) / ma.BN;
   ma.tiles = g.grid_blocks * ma.n_tiles;
-  // weights as E * Nw rows of Kin bytes; boxes of 128 bytes x BN rows in the 128-byte swizzle
+  // weights as E * Nw rows of Kin (E4M3) or 2 Kin (bf16) bytes; boxes of 128 bytes x BN rows
+  // in the 128-byte swizzle
+  const bool bf = g.wfmt == WF_BF16;
+  const uint64_t rbytes = bf ? (uint64_t)g.Kin * 2 : (uint64_t)g.Kin;
   CUtensorMap tmap;
-  if (!tma::encode_2d_u8(&tmap, g.w, (uint64_t)g.Kin, (uint64_t)g.E * g.Nw, (uint64_t)g.Kin, kBK,
-                         sw ? 128 : ma.BN, true))
+  if (!tma::encode_2d_u8(&tmap, g.w, rbytes, (uint64_t)g.E * g.Nw, rbytes, kBK, sw ? 128 : ma.BN, true))
     return cudaErrorInvalidValue;
-  if (g.epi == EPI_SWIGLU) return launch_mx8<EPI_SWIGLU>(ma, tmap, stream);
-  if (g.epi == EPI_WEIGHTED_F32) return launch_mx8<EPI_WEIGHTED_F32>(ma, tmap, stream);
-  return launch_mx8<EPI_PLAIN_BF16>(ma, tmap, stream);
+  if (bf) {
+    if (g.epi == EPI_SWIGLU) return launch_mx8<EPI_SWIGLU, true>(ma, tmap, stream);
+    if (g.epi == EPI_WEIGHTED_F32) return launch_mx8<EPI_WEIGHTED_F32, true>(ma, tmap, stream);
+    return launch_mx8<EPI_PLAIN_BF16, true>(ma, tmap, stream);
+  }
+  if (g.epi == EPI_SWIGLU) return launch_mx8<EPI_SWIGLU, false>(ma, tmap, stream);
+  if (g.epi == EPI_WEIGHTED_F32) return launch_mx8<EPI_WEIGHTED_F32, false>(ma, tmap, stream);
+  return launch_mx8<EPI_PLAIN_BF16, false>(ma, tmap, stream);
 }
 
 }  // namespace moe_launch

@@ -111,6 +111,18 @@ def test_few_experts_fill_whole_blocks_on_the_decode_path(moe, T, E, k):
     assert_close_bf16(bf16_to_np(yp), oracle_y(lay, w, T), what=f"dense blocks T={T} E={E}")
 
 
+@pytest.mark.parametrize("T", [300, 1001])
+def test_bf16_layer_above_256_rows(moe, T):
+    """bf16 weights above 256 rows (no padding in this mode): both GEMMs on the tcgen05
+    kernel with bf16 operands (I and K multiples of 128), h in bf16."""
+    w = synth.Workload("bf16_prefill", T=T, K=512, I=384, E=16, k=4, quant="bf16", seed=21, bias=True)
+    lay = synth.make_layer(w)
+    L = device_layer(moe, lay, w, T, pad=False)
+    y, rows = run(moe, L, lay, T)
+    assert rows == T
+    assert_close_bf16(bf16_to_np(y), oracle_y(lay, w, T), what=f"bf16 layer T={T}")
+
+
 def test_prefill_full_size_padded_vs_unpadded_and_sampled_oracle(moe):
     w = synth.prefill_workload()
     lay = synth.make_layer(w)

@@ -91,6 +91,23 @@ def test_w4a16_and_bf16_small(moe, T, quant):
     assert_close_bf16(bf16_to_np(out), ref, what=quant)
 
 
+@pytest.mark.parametrize("T,per_pair,bias", [(300, False, True), (700, True, False), (257, False, False)])
+def test_bf16_above_threshold_tensor_path(moe, T, per_pair, bias):
+    """bf16 above 256 rows with N a multiple of 128 and K of 64: the tcgen05 kernel (bf16
+    operands, kind::f16, no scale factors), 224- or 256-wide tiles; the oracle on the
+    decoded operands."""
+    rng = np.random.default_rng(40 + T)
+    E, k, N, Kin = 9, 2, 384, 320
+    ids = random_ids(rng, T, E, k)
+    a = synth.to_bf16_bits(rng.standard_normal((T * k if per_pair else T, Kin)))
+    w = synth.gen_bf16_weight(rng, E, N, Kin, 0.05)
+    b = synth.to_bf16_bits(rng.standard_normal((E, N)) * 0.1) if bias else None
+    out = gemm_dev(moe, "bf16", E, N, Kin, dev(a), None, per_pair, dev(w), None, None if b is None else dev(b), ids)
+    Wd = lambda e: (ofmt.bf16_decode(w[e]), None if b is None else ofmt.bf16_decode(b[e]))
+    ref = olayer.grouped_gemm(ofmt.bf16_decode(a), ids, Wd, per_pair)
+    assert_close_bf16(bf16_to_np(out), ref, what=f"bf16 T={T}")
+
+
 def test_w4a16_weight_streaming_is_exact_for_any_scale(moe):
     """bf16 activations up to 256 rows run the weight-streaming kernel, which multiplies each
     32-block's f32 partial sum by its scale: a scale of 2^-30 on nonzero codes (outside what
