@@ -52,6 +52,51 @@ TRAFFIC = {
 }
 
 
+def e2e_pipelined(L, T, xh, lh, yh, x, lg, y, stream, n):
+    """n layer steps with the inputs copied in from pinned host memory and the output copied
+    out every step, overlapped: inputs of step i + 1 (copy-in stream) and the output of step
+    i - 1 (copy-out stream) move while step i computes; two device buffers of each.  Returns
+    the milliseconds from before the first copy to after the last output copy."""
+    import torch
+
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    xd = [torch.empty_like(x), torch.empty_like(x)]
+    ld = [torch.empty_like(lg), torch.empty_like(lg)]
+    yd = [torch.empty_like(y), torch.empty_like(y)]
+    ev = lambda: torch.cuda.Event()
+    ready, done, out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+
+    def run(count):
+        for i in range(count):
+            b = i % 2
+            with torch.cuda.stream(cin):
+                if i >= 2:
+                    cin.wait_event(done[b])       # step i - 2 has read this input buffer
+                xd[b].copy_(xh, non_blocking=True)
+                ld[b].copy_(lh, non_blocking=True)
+                ready[b].record(cin)
+            stream.wait_event(ready[b])
+            if i >= 2:
+                stream.wait_event(out[b])         # step i - 2's output has left this buffer
+            L.step(xd[b], ld[b], T, yd[b])
+            done[b].record(stream)
+            with torch.cuda.stream(cout):
+                cout.wait_event(done[b])
+                yh.copy_(yd[b], non_blocking=True)
+                out[b].record(cout)
+        stream.wait_stream(cout)
+
+    run(3)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    cin.wait_stream(stream)
+    run(n)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -484,31 +529,16 @@ def bench_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {int(L.status[0])}")
     ms = max_over_ranks(ms, world, dev)
 
-    # end to end: pinned host inputs in, output back out, inside the timed region
+    # end to end: pinned host inputs in, output back out, inside the timed region.  As a
+    # serving loop would run it: the next step's inputs go up on a copy stream and the last
+    # step's output comes down on another while this step computes (two buffers each).
     xh = torch.empty_like(x, device="cpu").pin_memory()
     xh.copy_(x.cpu())
     lh = torch.empty_like(lg, device="cpu").pin_memory()
     lh.copy_(lg.cpu())
     yh = torch.empty_like(y, device="cpu").pin_memory()
-    xd = torch.empty_like(x)
-    ld = torch.empty_like(lg)
     e2e_steps = max(1, min(steps, 500))
-    for _ in range(3):
-        xd.copy_(xh, non_blocking=True); ld.copy_(lh, non_blocking=True)
-        L.step(xd, ld, T, y); yh.copy_(y, non_blocking=True)
-    torch.cuda.synchronize()
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        xd.copy_(xh, non_blocking=True)
-        ld.copy_(lh, non_blocking=True)
-        L.step(xd, ld, T, y)
-        yh.copy_(y, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = e2e_pipelined(L, T, xh, lh, yh, x, lg, y, stream, e2e_steps)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     if rank != 0:
