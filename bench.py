@@ -547,8 +547,15 @@ def bench_ours(args, rank, world, local_rank):
     dominant = "gemm1" if g1 >= g2 else "gemm2"
     dom_bytes, dom_ms = (gemm1_bytes, g1) if dominant == "gemm1" else (gemm2_bytes, g2)
     tensor_path = rows > 256  # row counts above the bucket value 256 run the tcgen05 kernels
-    # the W4A16 layer above 256 rows runs the kernel with the decoded weights in tensor memory
-    kernel_file = ("prefill_ts.cu" if w.quant == "mxfp4" else "prefill_gemm.cu") if tensor_path else "decode_gemm.cu"
+    # the W4A16 layer above 256 rows runs the kernel with the decoded weights in tensor memory;
+    # up to 256 rows the MXFP4 SwiGLU layer runs the block-scaled kernel that reads the E2M1
+    # codes as stored (K and I multiples of 64, at most 3072), other layers weight streaming
+    block_scaled = (not tensor_path and w.quant == "mxfp4" and w.activation == "swiglu"
+                    and w.K % 64 == 0 and w.I % 64 == 0 and w.K <= 3072 and w.I <= 3072)
+    if tensor_path:
+        kernel_file = "prefill_ts.cu" if w.quant == "mxfp4" else "prefill_gemm.cu"
+    else:
+        kernel_file = "decode_tc.cu" if block_scaled else "decode_gemm.cu"
     kernel_name = kernel_file[:-3] + f" ({dominant})"
     key = f"{kernel_file}:{dominant}@{w.name}"
     tr = TRAFFIC.get(key)
@@ -579,7 +586,9 @@ def bench_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": ("f16 tcgen05 mma -> f32" if tensor_path else "f16 mma -> f32") if w.quant != "bf16" else "bf16 mma -> f32",
+        "dtype": ("f16 tcgen05 mma -> f32" if tensor_path else
+                  ("e2m1 x e4m3 planes, block-scaled tcgen05 mma -> f32" if block_scaled else "f16 mma -> f32"))
+                 if w.quant != "bf16" else "bf16 mma -> f32",
         "data": "synthetic (seeded PCG64 inputs, random-init weights)",
         "config": layer_config(w, rows, world, flush),
         "timing": ("replays of one CUDA graph of the whole step (every kernel of the step runs each replay); "
@@ -991,7 +1000,7 @@ def launches_per_step(w, rows):
     n = 3  # GEMM1, GEMM2, combine
     n += 1  # align (routing fused for rows <= 512)
     if w.quant == "mxfp4":
-        n += 1  # x -> f16 (or gathered into slot order)
+        n += 1  # x -> f16 (or gathered into slot order; or, up to 256 rows, x planes + unit list)
     if rows > 512:
         n += 1  # separate routing kernel
     if w.quant == "mxfp4":

@@ -240,8 +240,10 @@ size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t 
   const int64_t P = T_rows * k;
   int64_t rows_h, rows_x;
   forward_scratch_rows(T_rows, k, cap_tokens, &rows_h, &rows_x);
+  // up to 256 rows: the planes of x and h and the unit list of the block-scaled MXFP4 kernel
+  const size_t dt = T_rows <= moe_launch::kPrefillRowsAbove ? moe_launch::decode_tc_workspace_bytes(T_rows, k, K, I) : 0;
   return round256((size_t)rows_h * I * 2) + round256((size_t)P * K * 4) + round256((size_t)rows_x * K * 2) +
-         forward_fix_bytes(T_rows, k, K, I, cap_tokens);
+         forward_fix_bytes(T_rows, k, K, I, cap_tokens) + dt;
 }
 
 // The MXFP8 layer: GEMM1 + SwiGLU, h quantised to MXFP8 (E4M3 codes and one E8M0 scale per
@@ -400,6 +402,26 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
       g2.fix_count = reinterpret_cast<int32_t*>(fix + f1);
       g2.fix_bits = reinterpret_cast<uint32_t*>(fix + f1 + 256);
     }
+  }
+  // Up to 256 rows, MXFP4 with SwiGLU: the block-scaled kernel reads the E2M1 codes as they
+  // are stored, with x and h split into E4M3 planes
+  if (fp4 && !relu2 && !g1.act_by_slot && T_rows <= moe_launch::kPrefillRowsAbove &&
+      moe_launch::decode_tc_supported(g1, g2)) {
+    const size_t off = round256((size_t)rows_h * I * 2) + round256((size_t)P * K * 4) +
+                       round256((size_t)rows_x * K * 2) + forward_fix_bytes(T_rows, k, K, I, cap_tokens);
+    const moe_launch::DecodeTcBufs b = moe_launch::decode_tc_carve(ws + off, T_rows, k, K, I);
+    st = cuda_status(moe_launch::decode_tc_prep(g1, x, T_rows, b, s), "moe_forward x planes");
+    if (st != MOE_OK) return st;
+    rec(ctx, 0, 4);
+    st = cuda_status(moe_launch::decode_tc_gemm(g1, b, s), "moe_forward GEMM1");
+    if (st != MOE_OK) return st;
+    rec(ctx, 1, 4);
+    st = cuda_status(moe_launch::decode_tc_gemm(g2, b, s), "moe_forward GEMM2");
+    if (st != MOE_OK) return st;
+    rec(ctx, 2, 4);
+    st = cuda_status(moe_launch::combine(o, T_real, k, K, y, s), "moe_forward combine");
+    rec(ctx, 3, 4);
+    return st;
   }
   if (fix) {
     st = cuda_status(cudaMemsetAsync(fix, 0, fix_bytes, s), "moe_forward marks");

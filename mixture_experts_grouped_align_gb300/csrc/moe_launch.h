@@ -93,6 +93,26 @@ size_t decode_gemm_smem_bytes(const GroupedGemm& g);
 cudaError_t decode_gemm(const GroupedGemm& g, cudaStream_t stream);
 
 
+// ---- the MXFP4 layer of up to 256 rows on the block-scaled MMA (decode_tc.cu): x split into
+// two E4M3 planes and h into three, one E8M0 scale per 32 elements; GEMM1 writes h's planes
+struct DecodeTcBufs {
+  uint8_t* xq;       // [T_rows, 2, kp(K)] x planes
+  uint8_t* xs;       // [T_rows, sb(K)] x scales
+  uint8_t* hq;       // [P, 3, kp(I)] h planes
+  uint8_t* hs;       // [P, sb(I)] h scales
+  int4* items;       // [P] (alignment block, 16-slot tile, slots to its last pair + 1, expert)
+  int32_t* n_items;
+};
+// Whether GEMM1 (SwiGLU, MXFP4 weights) and GEMM2 (routing-weighted) of a layer fit the kernel.
+bool decode_tc_supported(const GroupedGemm& g1, const GroupedGemm& g2);
+size_t decode_tc_workspace_bytes(int64_t T_rows, int k, int K, int I);
+DecodeTcBufs decode_tc_carve(void* ws, int64_t T_rows, int k, int K, int I);
+// x (bf16 [T_rows, K]) -> planes, and the units' items (g1's alignment).
+cudaError_t decode_tc_prep(const GroupedGemm& g1, const void* x, int64_t T_rows, const DecodeTcBufs& b,
+                           cudaStream_t stream);
+// GEMM1 (g.epi EPI_SWIGLU: x planes -> h planes) or GEMM2 (EPI_WEIGHTED_F32: h planes -> o).
+cudaError_t decode_tc_gemm(const GroupedGemm& g, const DecodeTcBufs& b, cudaStream_t stream);
+
 // ---- grouped GEMMs on the tensor-memory (prefill) path (prefill_gemm.cu)
 int prefill_tile_n(const GroupedGemm& g);
 bool prefill_supported(const GroupedGemm& g);

@@ -95,6 +95,16 @@ MOE_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// 32 lanes x 16 columns -> 16 registers per thread.
+MOE_DEV void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
 MOE_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Registers -> TMEM: thread i writes lane i of the warp's 32-lane quarter, columns c..c+3
@@ -165,6 +175,10 @@ MOE_DEV void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint3
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+
+// Operand type codes of kind::f8f6f4 / mxf8f6f4 (A in bits 7-9, B in bits 10-12 of the
+// instruction descriptor).
+constexpr uint32_t kTypeE4M3 = 0u, kTypeE2M1 = 5u;
 
 // Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale: E4M3 A and B, both
 // K-major, f32 accumulator, UE8M0 scale factors; the scale-factor ids pick the byte of
