@@ -622,15 +622,13 @@ size_t r256(size_t v) { return (v + 255) / 256 * 256; }
 
 constexpr int kSmemMax = 227 * 1024;
 
-// Stage slots: up to kLag + 1 (kLag stages in flight, one for the MMA; with fewer slots the
-// producers wait for the MMA earlier).  The copies go through L1 (8-byte cp.async.ca), so the
-// layout is kept within a 164 KB shared-memory carve-out when three slots or more fit there,
-// which leaves L1 92 KB for the bytes in flight.
+// Stage slots: up to kLag + 2 (kLag stages in flight, two for the MMA: a stage handed over is
+// reused two stages later, which hides the MMA's completion).  The copies go through L1
+// (8-byte cp.async.ca): the carve-out below leaves L1 whatever shared memory does not take.
 int dt_stages(int planes, int Kin) {
   const DtLayout L0 = dt_layout(0, planes, Kin, dt_sb(Kin));
-  const int l1_friendly = (164 * 1024 - 1024 - L0.total) / (L0.slot + 16);
-  int s = l1_friendly >= 3 ? l1_friendly : (kSmemMax - 1024 - L0.total) / (L0.slot + 16);
-  return s < kLag + 1 ? s : kLag + 1;
+  const int s = (kSmemMax - 1024 - L0.total) / (L0.slot + 16);
+  return s < kLag + 2 ? s : kLag + 2;
 }
 
 template <int EPI>
