@@ -41,8 +41,8 @@ L2_BYTES = 129 * 1024 * 1024
 # gradient: every launch of one moe_wgrad call), from an ncu capture of the same command,
 # valid while the kernel source hashes the same; otherwise reported as null.
 TRAFFIC = {
-    "decode_gemm.cu:gemm1@decode_mxfp4": {
-        "src": "1d10e33c80844cd4", "bytes": 997873920 + 4255232},
+    "decode_tc.cu:gemm1@decode_mxfp4": {
+        "src": "ff39a1c5ced13485", "bytes": 997686528 + 4828672},
     # both launches of the call: the main pass and the (empty) exact-scale pass
     "prefill_ts.cu:gemm1@prefill_mxfp4": {
         "src": "40b9e45121f051d6", "bytes": 2599493120 + 1443217152 + 68608},
