@@ -71,9 +71,9 @@ typedef struct {
   int32_t* dev_status;     /* optional device int32 (set to 0 by the caller); may be NULL   */
   void** events;           /* optional host array of cudaEvent_t recorded on the stream
                               around each kernel of a call (profiling); may be NULL.
-                              moe_forward: [0] before GEMM1 (after x's f16 copy), [1]
-                              after GEMM1, [2] after GEMM2, [3] after the combine (needs
-                              n_events >= 4);
+                              moe_forward: [0] before GEMM1 (after x's f16 copy or
+                              planes), [1] after GEMM1, [2] after GEMM2, [3] after the
+                              combine (needs n_events >= 4);
                               moe_grouped_gemm, moe_wgrad: [0] before, [1] after.      */
   int32_t n_events;
 } moe_ctx;
@@ -177,7 +177,11 @@ typedef struct {
  * T_rows*k and rows_x = T_rows up to 256 rows; above that h and x may be kept in
  * alignment-slot order and rows_h = rows_x = cap_tokens, and two small regions (one bit per
  * output tile of each GEMM) follow, which mark tiles whose weight scales need the exact
- * second pass.  Returns 0 for a negative argument. */
+ * second pass.  Up to 256 rows five more regions follow, for the block-scaled MXFP4 kernels:
+ * x as two E4M3 planes [T_rows, 2, kp(K)] and their E8M0 scales [T_rows, sb(K)], h as three
+ * planes [T_rows*k, 3, kp(I)] and scales [T_rows*k, sb(I)], and a unit list
+ * [T_rows*k + 1, 16 bytes], where kp(n) = 128 * ceil(n / 128) and sb(n) = 16 * ceil(ceil(n /
+ * 128) / 4).  Returns 0 for a negative argument. */
 size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t I, int64_t cap_tokens);
 
 /* One MoE expert layer over the alignment of moe_align: both grouped GEMMs run as single
@@ -198,9 +202,14 @@ size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t 
  * nonzero blocks span more than 36 octaves of scale is reported (MOE_ERR_RANGE).
  *
  *   gu = x_t . W1[e]^T + b1[e];  h = silu(gu[:I]) * gu[I:]  (SwiGLU) or
- *        h = max(gu, 0)^2  (relu^2; a NaN stays NaN)  (fp32, then stored as the MMA
- *        operand type of GEMM2: f16 RNE for MXFP4 weights -- |h| or |x| > 65504 sets
- *        MOE_ERR_RANGE -- and bf16 RNE for bf16 weights)
+ *        h = max(gu, 0)^2  (relu^2; a NaN stays NaN)  (fp32, then rounded to the operand
+ *        type of GEMM2: f16 RNE for MXFP4 weights -- |h| > 65504 sets MOE_ERR_RANGE, and so
+ *        does |x| > 65504 where x is converted to f16: above 256 rows and for relu^2 -- and
+ *        bf16 RNE for bf16 weights).  Up to 256 rows the MXFP4 SwiGLU layer (K and I
+ *        multiples of 64, at most 3072) runs the block-scaled kernels: x and the f16 h enter
+ *        the MMA as two and three E4M3 planes under one E8M0 scale per 32 elements, which
+ *        sum to each value exactly for elements no more than 2^9 (x) or 2^6 (h) below their
+ *        block's largest, and within 2^-17 of that largest for the rest
  *   o_tj = w[t,j] * (h . W2[e]^T + b2[e])                    (fp32)
  *   y_t  = sum_{j=0..k-1} o_tj, in order of j, rounded to bf16 RNE.
  * x: [T_rows, K] bf16 (BF16 and MXFP4_W4A16 modes).  topk_w [T_rows, k]; the alignment
