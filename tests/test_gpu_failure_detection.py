@@ -57,10 +57,12 @@ def _oracle(lay, w):
     return layer.moe_layer(x, ids, wt, W)
 
 
-@pytest.mark.parametrize("quant", ["mxfp4", "mxfp8"])
+@pytest.mark.parametrize("quant", ["mxfp4", "mxfp4_decode", "mxfp8"])
 def test_stalled_waits_time_out_and_the_context_recovers(moe, quant):
     if quant == "mxfp4":   # prefill_ts kernels (W4A16, decoded weights in tensor memory)
         w = synth.scaled(synth.TINY, T=300, bias=True)
+    elif quant == "mxfp4_decode":  # decode_tc kernels (64 rows: E2M1 codes on the block-scaled MMA)
+        w = synth.scaled(synth.TINY, T=64, bias=True)
     else:                  # mx8_gemm kernels (block-scaled MXFP8)
         w = synth.Workload("stall_mxfp8", T=300, K=512, I=512, E=8, k=2, quant="mxfp8", seed=7,
                            weight_std=0.05, bias=True)
