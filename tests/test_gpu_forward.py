@@ -325,3 +325,25 @@ def test_relu2_graph_replay_equals_eager(moe):
         assert int(Lg.status[0]) == 0
         ye, _ = run(moe, Le, lay, T)
         assert torch.equal(yg.view(torch.int16), ye.view(torch.int16)), f"T={T}"
+
+
+@pytest.mark.parametrize("block_m", [8, 32, 64, 256])
+def test_mxfp4_small_batch_across_block_sizes(moe, block_m):
+    """Up to 256 rows the MXFP4 SwiGLU layer runs the block-scaled kernels for alignment blocks
+    of at most 128 slots (8-slot units: one or several per block) and the weight-streaming
+    kernels above; each matches the oracle, and padded and unpadded rows stay bit-identical."""
+    from mixture_experts_grouped_align_gb300.runner import DeviceLayer
+    w = synth.Workload("block_sizes", T=61, K=512, I=384, E=8, k=3, quant="mxfp4", seed=31,
+                       scale_exp=(-5, -1), bias=True)
+    lay = synth.make_layer(w)
+
+    def layer(pad):
+        return DeviceLayer(w.quant, w.E, w.K, w.I, w.k, dev(lay["w1"]), dev(lay["w1_scale"]),
+                           dev(lay["b1"]), dev(lay["w2"]), dev(lay["w2_scale"]), dev(lay["b2"]),
+                           max_rows=w.T, pad=pad, block_m=block_m)
+
+    y_pad, rows = run(moe, layer(True), lay, w.T)
+    y_raw, _ = run(moe, layer(False), lay, w.T)
+    assert rows == obucket.bucket(w.T)
+    assert torch.equal(y_pad.view(torch.int16), y_raw.view(torch.int16))
+    assert_close_bf16(bf16_to_np(y_raw), oracle_y(lay, w, w.T), what=f"block_m={block_m}")
