@@ -267,9 +267,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           y[j] = (int32_t)(pv[j] < a.P ? (a.act_per_pair ? (int64_t)pv[j] : (int64_t)(pv[j] / a.k)) : rows_total);
       }
       bool ok = true;
-      // the token tile is read by every feature tile of its block: keep it in L2 ahead of the
-      // weight codes, which each tile reads once
-      const uint64_t pol_keep = tma::policy_evict_last(), pol_once = tma::policy_evict_first();
       for (int kc = 0; kc < nk; ++kc) {
         if (kc % kGroup == 0) {  // raw codes of stages kc .. kc + 3: 128 bytes of every row
           const int rs = (int)(gi % kRawSlots);
@@ -281,8 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma::mbar_arrive_expect_tx(&raw_full[rs], raw_bytes);
 #pragma unroll
             for (int m = 0; m < kMats; ++m)
-              tma::load_2d_hint(rsl + m * kTM * 128, &tmap_w, (kc / kGroup) * 128,
-                                (int32_t)tile_wrow<SW>(a, e, mt, m, 0), &raw_full[rs], pol_once);
+              tma::load_2d(rsl + m * kTM * 128, &tmap_w, (kc / kGroup) * 128, (int32_t)tile_wrow<SW>(a, e, mt, m, 0),
+                           &raw_full[rs]);
           }
           ++gi;
         }
@@ -294,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) tma::mbar_arrive_expect_tx(&ld_full[s], stage_bytes);
         __syncwarp();
         if (a.act_by_slot) {  // the block's 128 slot rows: one box
-          if (lane == 0) tma::load_2d_hint(sl, &tmap_x, kc * 128, (int32_t)(blk * a.bm), &ld_full[s], pol_keep);
+          if (lane == 0) tma::load_2d(sl, &tmap_x, kc * 128, (int32_t)(blk * a.bm), &ld_full[s]);
         } else {  // rows 4 lane .. 4 lane + 3 of the token tile: every lane issues its own gather
           tma_gather4(sl + lane * 512, &tmap_x, kc * 128, y[0], y[1], y[2], y[3], &ld_full[s]);
         }
