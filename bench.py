@@ -587,7 +587,7 @@ def bench_ours(args, rank, world, local_rank):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": ("f16 tcgen05 mma -> f32" if tensor_path else
-                  ("e2m1 x e4m3 planes, block-scaled tcgen05 mma -> f32" if block_scaled else "f16 mma -> f32"))
+                  ("e2m1 x e2m1 digit planes, block-scaled tcgen05 mma -> f32" if block_scaled else "f16 mma -> f32"))
                  if w.quant != "bf16" else "bf16 mma -> f32",
         "data": "synthetic (seeded PCG64 inputs, random-init weights)",
         "config": layer_config(w, rows, world, flush),

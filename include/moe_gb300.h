@@ -178,10 +178,10 @@ typedef struct {
  * alignment-slot order and rows_h = rows_x = cap_tokens, and two small regions (one bit per
  * output tile of each GEMM) follow, which mark tiles whose weight scales need the exact
  * second pass.  Up to 256 rows five more regions follow, for the block-scaled MXFP4 kernels:
- * x as two E4M3 planes [T_rows, 2, kp(K)] and their E8M0 scales [T_rows, sb(K)], h as three
- * planes [T_rows*k, 3, kp(I)] and scales [T_rows*k, sb(I)], and a unit list
- * [T_rows*k + 1, 16 bytes], where kp(n) = 128 * ceil(n / 128) and sb(n) = 16 * ceil(ceil(n /
- * 128) / 4).  Returns 0 for a negative argument. */
+ * x as eight E2M1 digit planes [T_rows, 8, kq(K)] bytes (two codes a byte) and their E8M0
+ * scales [T_rows, sb(K)], h as eight planes [T_rows*k, 8, kq(I)] and scales [T_rows*k,
+ * sb(I)], and a unit list [T_rows*k + 1, 16 bytes], where kq(n) = 64 * ceil(n / 128) and
+ * sb(n) = 16 * ceil(ceil(n / 128) / 4).  Returns 0 for a negative argument. */
 size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t I, int64_t cap_tokens);
 
 /* One MoE expert layer over the alignment of moe_align: both grouped GEMMs run as single
@@ -206,10 +206,11 @@ size_t moe_forward_workspace_size(int64_t T_rows, int32_t k, int32_t K, int32_t 
  *        type of GEMM2: f16 RNE for MXFP4 weights -- |h| > 65504 sets MOE_ERR_RANGE, and so
  *        does |x| > 65504 where x is converted to f16: above 256 rows and for relu^2 -- and
  *        bf16 RNE for bf16 weights).  Up to 256 rows the MXFP4 SwiGLU layer (K and I
- *        multiples of 64, at most 3072) runs the block-scaled kernels: x and the f16 h enter
- *        the MMA as two and three E4M3 planes under one E8M0 scale per 32 elements, which
- *        sum to each value exactly for elements no more than 2^9 (x) or 2^6 (h) below their
- *        block's largest, and within 2^-17 of that largest for the rest
+ *        multiples of 64, 256..3072) runs the block-scaled kernels: x and the f16 h enter
+ *        the MMA as eight E2M1 digit planes (base-4 digits under one E8M0 scale per 32
+ *        elements and plane), which sum to each value exactly for elements no more than
+ *        2^8 (x) or 2^5 (h) below their block's largest, and within 2^-16 of that largest
+ *        for the rest
  *   o_tj = w[t,j] * (h . W2[e]^T + b2[e])                    (fp32)
  *   y_t  = sum_{j=0..k-1} o_tj, in order of j, rounded to bf16 RNE.
  * x: [T_rows, K] bf16 (BF16 and MXFP4_W4A16 modes).  topk_w [T_rows, k]; the alignment
@@ -229,8 +230,8 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
                        const int32_t* expert_offsets, int32_t block_m, int64_t cap_tokens,
                        void* y, const moe_ctx* ctx);
 
-/* Size of the fixed device scratch array used by moe_forward_no_alloc (8 MiB). */
-#define MOE_NO_ALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+/* Size of the fixed device scratch array used by moe_forward_no_alloc (16 MiB). */
+#define MOE_NO_ALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 
 /* moe_forward without a caller workspace; the pages have no counterpart to this call.
  *

@@ -17,10 +17,6 @@ MOE_DEV void cp_async16z(uint32_t dst, const void* src, bool valid) {
   const int sz = valid ? 16 : 0;
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz) : "memory");
 }
-// 8 bytes (.ca); both addresses 8-byte aligned.
-MOE_DEV void cp_async8(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src) : "memory");
-}
 // 4 bytes (.ca); both addresses 4-byte aligned.
 MOE_DEV void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
@@ -29,11 +25,6 @@ MOE_DEV void cp_async4(uint32_t dst, const void* src) {
 MOE_DEV void cp_async4z(uint32_t dst, const void* src, bool valid) {
   const int sz = valid ? 4 : 0;
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(sz) : "memory");
-}
-// Bulk prefetch of `bytes` (a multiple of 16, address 16-byte aligned) from global memory
-// into L2; nothing lands in shared memory and no completion is tracked.
-MOE_DEV void prefetch_l2_bulk(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 MOE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 // Waits until at most N of this thread's committed groups are still in flight.

@@ -404,7 +404,7 @@ moe_status moe_forward(const moe_weights* W, const void* x, const uint8_t* x_sca
     }
   }
   // Up to 256 rows, MXFP4 with SwiGLU: the block-scaled kernel reads the E2M1 codes as they
-  // are stored, with x and h split into E4M3 planes
+  // are stored, with x and h split into E2M1 digit planes
   if (fp4 && !relu2 && !g1.act_by_slot && T_rows <= moe_launch::kPrefillRowsAbove &&
       moe_launch::decode_tc_supported(g1, g2)) {
     const size_t off = round256((size_t)rows_h * I * 2) + round256((size_t)P * K * 4) +

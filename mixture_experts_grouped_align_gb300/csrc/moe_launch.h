@@ -93,12 +93,13 @@ size_t decode_gemm_smem_bytes(const GroupedGemm& g);
 cudaError_t decode_gemm(const GroupedGemm& g, cudaStream_t stream);
 
 
-// ---- the MXFP4 layer of up to 256 rows on the block-scaled MMA (decode_tc.cu): x split into
-// two E4M3 planes and h into three, one E8M0 scale per 32 elements; GEMM1 writes h's planes
+// ---- the MXFP4 layer of up to 256 rows on the block-scaled MMA (decode_tc.cu): x and h split
+// into eight E2M1 digit planes each, one E8M0 scale per 32 elements (plane 0's; plane j's is
+// 2j less); GEMM1 writes h's planes.  kq(n) = 64 * ceil(n / 128) bytes a plane row.
 struct DecodeTcBufs {
-  uint8_t* xq;       // [T_rows, 2, kp(K)] x planes
+  uint8_t* xq;       // [T_rows, 8, kq(K)] x planes, two codes a byte
   uint8_t* xs;       // [T_rows, sb(K)] x scales
-  uint8_t* hq;       // [P, 3, kp(I)] h planes
+  uint8_t* hq;       // [P, 8, kq(I)] h planes
   uint8_t* hs;       // [P, sb(I)] h scales
   int4* items;       // [P] (alignment block, 8-slot tile, slots to its last pair + 1, expert)
   int32_t* n_items;

@@ -95,16 +95,6 @@ MOE_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
-// 32 lanes x 16 columns -> 16 registers per thread.
-MOE_DEV void tmem_ld16(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
 MOE_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Registers -> TMEM: thread i writes lane i of the warp's 32-lane quarter, columns c..c+3
@@ -176,10 +166,6 @@ MOE_DEV void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint3
       : "memory");
 }
 
-// Operand type codes of kind::f8f6f4 / mxf8f6f4 (A in bits 7-9, B in bits 10-12 of the
-// instruction descriptor).
-constexpr uint32_t kTypeE4M3 = 0u, kTypeE2M1 = 5u;
-
 // Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale: E4M3 A and B, both
 // K-major, f32 accumulator, UE8M0 scale factors; the scale-factor ids pick the byte of
 // the 32-bit TMEM scale words this MMA uses (B in bits 4-5, A in bits 29-30), N >> 3 in
@@ -202,6 +188,35 @@ MOE_DEV void mma_mx8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint3
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of tcgen05.mma.kind::mxf4.block_scale: E2M1 A and B (type code 1
+// in bits 7-9 and 10-12), both K-major and packed two codes a byte, f32 accumulator, UE8M0
+// scale factors (bit 23).  Each MMA covers K = 64, i.e. two 32-element scale blocks, whose
+// factors are bytes sf_id and sf_id + 1 (sf_id 0 or 2) of the rows' TMEM scale words.
+MOE_DEV uint32_t idesc_mxf4(int M, int N, uint32_t sf_id_a, uint32_t sf_id_b) {
+  uint32_t d = 0;
+  d |= (sf_id_b & 3u) << 4;
+  d |= 1u << 7;
+  d |= 1u << 10;
+  d |= (uint32_t)(N >> 3) << 17;
+  d |= 1u << 23;
+  d |= (uint32_t)(M >> 4) << 24;
+  d |= (sf_id_a & 3u) << 29;
+  return d;
+}
+
+// D[tmem] (+)= (A . SFA)[smem] . (B . SFB)[smem]^T for packed E2M1 A and B, one E8M0 scale
+// per 32 K elements of every row, read from TMEM; issued by one thread.
+MOE_DEV void mma_mxf4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t sfa_tmem,
+                         uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");

@@ -39,33 +39,6 @@ inline bool encode_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uin
   return r == CUDA_SUCCESS;
 }
 
-// E2M1 (4-bit) weight rows of kin elements (kin / 2 bytes, a multiple of 32, base 32-byte
-// aligned) viewed as [rows][kin / 128 stages][128 elements]: boxes of 128 elements x one
-// stage x box_rows rows land in shared memory in the padded 4-bit layout of the block-scaled
-// MMA (each 16 elements in the low 8 bytes of a 16-byte chunk), 128-byte swizzled.  The
-// transaction count of a box is its global bytes (64 a row).  Returns false when the driver
-// entry point is missing or the encoding is rejected.
-inline bool encode_e2m1_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t kin, uint32_t box_rows) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }();
-  if (encode == nullptr || kin < 128) return false;
-  const cuuint64_t dims[3] = {128, kin / 128, rows};
-  const cuuint64_t strides[2] = {64, kin / 2};
-  const cuuint32_t box[3] = {128, 1, box_rows};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides, box,
-                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 // Arrives on the mbarrier and adds `bytes` to the transaction count its phase waits for.
 MOE_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_addr(bar)),
@@ -80,15 +53,6 @@ MOE_DEV void load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_addr(bar))
-      : "memory");
-}
-
-// Loads the box at (x, y, z) of a 3-D tensor map into shared memory at dst.
-MOE_DEV void load_3d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(tc::smem_addr(bar))
       : "memory");
 }
 

@@ -46,13 +46,13 @@ int main(void) {
   CHECK(strlen(moe_last_error()) > 0, "no error text after a failed call");
 
   /* workspace of the 64-token decode layer: h f16 [P, I] + o fp32 [P, K] + x f16 [T, K], then
-   * x planes [T, 2, 2944] + x scales [T, 96] + h planes [P, 3, 2944] + h scales [P, 96] + the
-   * unit list [P + 1, 16] of the block-scaled kernel */
+   * x digit planes [T, 8, 1472] + x scales [T, 96] + h planes [P, 8, 1472] + h scales [P, 96] +
+   * the unit list [P + 1, 16] of the block-scaled kernel */
   CHECK(moe_align_capacity(256, 128, 128, &ct, &cb) == MOE_OK, "capacity");
   size_t ws = moe_forward_workspace_size(64, 4, 2880, 2880, ct);
   size_t want = (size_t)round_up(256 * 2880 * 2, 256) + (size_t)round_up(256 * 2880 * 4, 256) +
-                (size_t)round_up(64 * 2880 * 2, 256) + (size_t)round_up(64 * 2 * 2944, 256) +
-                (size_t)round_up(64 * 96, 256) + (size_t)round_up(256 * 3 * 2944, 256) +
+                (size_t)round_up(64 * 2880 * 2, 256) + (size_t)round_up(64 * 8 * 1472, 256) +
+                (size_t)round_up(64 * 96, 256) + (size_t)round_up(256 * 8 * 1472, 256) +
                 (size_t)round_up(256 * 96, 256) + (size_t)round_up(257 * 16, 256);
   CHECK(ws == want, "workspace %zu, want %zu", ws, want);
 

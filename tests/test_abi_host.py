@@ -71,8 +71,8 @@ def test_workspace_size(lib):
     cap, _ = moe.moe_align_capacity(256, 128, 128)
     n = moe.moe_forward_workspace_size(64, 4, 2880, 2880, cap)
     P = 256  # up to 256 rows: h and x in pair / token order
-    kp, sb = 23 * 128, 96  # K and I of 2880: 23 stages of 128; 23 scale words, 16-byte rows
-    planes = r(64 * 2 * kp) + r(64 * sb) + r(P * 3 * kp) + r(P * sb) + r((P + 1) * 16)
+    kq, sb = 23 * 64, 96  # K and I of 2880: 23 words of 128 K, 64 bytes each; 16-byte scale rows
+    planes = r(64 * 8 * kq) + r(64 * sb) + r(P * 8 * kq) + r(P * sb) + r((P + 1) * 16)
     assert n == r(P * 2880 * 2) + r(P * 2880 * 4) + r(64 * 2880 * 2) + planes
     cap, _ = moe.moe_align_capacity(4 * 1000, 128, 128)
     n = moe.moe_forward_workspace_size(1000, 4, 2880, 2880, cap)
