@@ -19,11 +19,11 @@
 // for every bf16 element no more than 2^8 below its block's largest and every f16 element
 // no more than 2^5 below it (their ulps are multiples of u); a smaller element is rounded to
 // a multiple of u, an error below 2^-16 of the largest.  Digit plane j of token t is B row
-// 8 t + j of an 8-token unit, so one MMA of N = 64 columns gives every plane's partial sum,
-// and the epilogue adds the planes in a fixed order.
+// 8 t + j of a unit's token tile (4 or 8 slots), so one MMA of N = 32 or 64 columns gives
+// every plane's partial sum, and the epilogue adds the planes in a fixed order.
 //
 // One launch covers every expert (the aiter page, Summary: all expert GEMMs in one launch).
-// A unit is (alignment block, 8-slot token tile, 128 weight rows); only tiles that hold a
+// A unit is (alignment block, token tile, 128 weight rows); only tiles that hold a
 // pair become units (a block past num_tokens_post_padded or with the -1 expert sentinel is
 // never read: the page's second review, sentinel handling), and each CTA takes a contiguous
 // range of units.  Roles: one thread issues the TMA boxes of stages of two 256-K sub-tiles
@@ -43,14 +43,10 @@ constexpr int kThreads = 192;           // warps 0-3 epilogue, 4 TMA producer, 5
 constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kSub = 2;                 // 256-K sub-tiles per stage (one handshake each)
-constexpr int kTok = 8;                 // token rows (slots) per unit
 constexpr int kPlanes = 8;              // E2M1 digit planes per activation row
-constexpr int kTilesPerBallot = 32 / kTok;
 constexpr int kRowsA = 128;             // weight rows per unit (MMA M)
 constexpr int kBoxRowsA = 64;           // weight rows per TMA box
-constexpr int kBRows = kTok * kPlanes;  // B rows per sub-tile (MMA N)
 constexpr int kAStage = kRowsA * 128;   // 256 K of 128 rows: two codes a byte
-constexpr int kBStage = kBRows * 128;
 constexpr int kMaxWords = 24;           // 128-K scale words per unit: Kin <= 3072
 constexpr int kMaxStages = 6;
 constexpr uint32_t kTmemCols = 512;
@@ -58,8 +54,17 @@ constexpr uint32_t kScaleCol0 = 128;    // accumulators at columns 0 and 64
 constexpr uint32_t kScaleBufCols = 8 * kMaxWords;  // per buffer: 4 A + 4 B columns a scale word
 constexpr unsigned kFull = 0xffffffffu;
 
-static_assert(kBRows == 64 && kBRows % 16 == 0, "MMA N of M = 128 is a multiple of 16");
-static_assert((kAStage + kBStage) % 1024 == 0, "MMA slots must keep the 1024-byte swizzle atoms aligned");
+// A unit's token tile: TOK slots (4 or 8), whose digit-plane rows are the MMA's N = 8 TOK
+// B rows, 128 bytes each per sub-tile.
+template <int TOK>
+struct TokTile {
+  static constexpr int kTok = TOK;
+  static constexpr int kTilesPerBallot = 32 / TOK;
+  static constexpr int kBRows = TOK * kPlanes;
+  static constexpr int kBStage = kBRows * 128;
+  static_assert(kBRows == 32 || kBRows == 64, "one or two 32-column TMEM loads; MMA N of M = 128 a multiple of 16");
+  static_assert((kAStage + kBStage) % 1024 == 0, "MMA slots must keep the 1024-byte swizzle atoms aligned");
+};
 static_assert(kScaleCol0 + 2 * kScaleBufCols <= kTmemCols, "tensor memory columns");
 
 // Splits this lane's value v, one of the 32 elements of a scale block held by the warp (one
@@ -131,13 +136,15 @@ struct PrepArgs {
 
 constexpr int kPrepThreads = 1024;
 
-// Block 0 lists the units' (alignment block, token tile) items; the other blocks split the
-// rows of x into eight digit planes.
+// Block 0 lists the units' (alignment block, TOK-slot token tile) items; the other blocks
+// split the rows of x into eight digit planes.
+template <int TOK>
 __global__ void __launch_bounds__(kPrepThreads) dt_prep_kernel(PrepArgs pa) {
+  constexpr int kTok = TokTile<TOK>::kTok, kTilesPerBallot = TokTile<TOK>::kTilesPerBallot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (blockIdx.x == 0) {
     // rounds of 128 alignment blocks, four per warp, every slot load of a round in flight at
-    // once; a block of at most 128 slots is read by one ballot per 32 slots (four tiles each)
+    // once; a block of at most 128 slots is read by one ballot per 32 slots (32 / TOK tiles each)
     __shared__ int wcount[32];
     __shared__ int base_s;
     if (tid == 0) base_s = 0;
@@ -240,17 +247,17 @@ struct DtLayout {
   int mring, sub, slot, stg, ex, bars, total;
 };
 // `stages` ring slots of kSub sub-tiles (each an A tile of 128 weight rows and the B tile of
-// 8 tokens x 8 planes, 128 bytes a row), per epilogue warp a staging area for a unit's
-// scales (its 32 weight rows' scale bytes, then kTok token scale rows), the SwiGLU exchange
+// tok tokens x 8 planes, 128 bytes a row), per epilogue warp a staging area for a unit's
+// scales (its 32 weight rows' scale bytes, then tok token scale rows), the SwiGLU exchange
 // of up values, barriers.
-__host__ __device__ inline DtLayout dt_layout(int stages, int Kin, int sb_tok) {
+__host__ __device__ inline DtLayout dt_layout(int stages, int Kin, int sb_tok, int tok) {
   DtLayout L;
   L.mring = 0;
-  L.sub = kAStage + kBStage;
+  L.sub = kAStage + tok * kPlanes * 128;
   L.slot = kSub * L.sub;
   L.stg = L.mring + stages * L.slot;
-  L.ex = L.stg + 4 * (Kin + kTok * sb_tok);
-  L.bars = L.ex + 2 * 2 * kTok * 32 * 4;
+  L.ex = L.stg + 4 * (Kin + tok * sb_tok);
+  L.bars = L.ex + 2 * 2 * tok * 32 * 4;
   L.total = L.bars + 8 * (2 * stages + 11) + 8;  // barriers, TMEM address, abort flag
   return L;
 }
@@ -287,8 +294,9 @@ MOE_DEV uint32_t plane_scales(uint32_t v, int p) {
 // in its own shared area with 16-byte loads, then every lane writes its row's A words and
 // the B words of B rows lane and 32 + lane (B row 8 t + j: token t, digit plane j) into the
 // warp's lane quarter.
-template <int EPI>
+template <int EPI, int TOK>
 MOE_DEV void write_scales(const DtArgs& d, uint8_t* stg, uint32_t taddr, int q, int lane, int64_t u, uint32_t buf) {
+  constexpr int kTok = TokTile<TOK>::kTok, kBRows = TokTile<TOK>::kBRows;
   const GroupedGemm& a = d.g;
   const int64_t ii = u / d.n_rt;
   const int rt = (int)(u - ii * d.n_rt);
@@ -314,7 +322,7 @@ MOE_DEV void write_scales(const DtArgs& d, uint8_t* stg, uint32_t taddr, int q, 
   const uint8_t* ra = stg + lane * kb;
   const uint32_t ca = taddr + lane_base + scale_col_a(buf), cb = taddr + lane_base + scale_col_b(buf);
   const uint8_t* rb0 = stb + (lane >> 3) * d.sb_tok;
-  const uint8_t* rb1 = stb + (4 + (lane >> 3)) * d.sb_tok;
+  const uint8_t* rb1 = stb + (kBRows > 32 ? 4 + (lane >> 3) : 0) * d.sb_tok;
   const int pl = lane & 7;
   for (int w = 0; w < d.nwords; ++w) {
     const int o = 4 * w;
@@ -323,7 +331,7 @@ MOE_DEV void write_scales(const DtArgs& d, uint8_t* stg, uint32_t taddr, int q, 
     if (o + 4 <= kb) wa |= (uint32_t)*reinterpret_cast<const uint16_t*>(ra + o + 2) << 16;
     tc::tmem_st4(ca + 4 * w, wa, wa, wa, wa);
     const uint32_t v0 = plane_scales(*reinterpret_cast<const uint32_t*>(rb0 + o), pl);
-    const uint32_t v1 = plane_scales(*reinterpret_cast<const uint32_t*>(rb1 + o), pl);
+    const uint32_t v1 = kBRows > 32 ? plane_scales(*reinterpret_cast<const uint32_t*>(rb1 + o), pl) : 0u;
     tc::tmem_st4(cb + 4 * w, v0, v1, 0u, 0u);
   }
   tc::tmem_st_wait();
@@ -331,13 +339,14 @@ MOE_DEV void write_scales(const DtArgs& d, uint8_t* stg, uint32_t taddr, int q, 
   __syncwarp();  // the staging area is read before the next unit's loads refill it
 }
 
-template <int EPI>
+template <int EPI, int TOK>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, DtArgs d) {
+  constexpr int kTok = TokTile<TOK>::kTok, kBRows = TokTile<TOK>::kBRows;
   const GroupedGemm& a = d.g;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const DtLayout L = dt_layout(d.stages, a.Kin, d.sb_tok);
+  const DtLayout L = dt_layout(d.stages, a.Kin, d.sb_tok, TOK);
   const int S = d.stages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);  // [S] MMA slot filled
   uint64_t* empty = full + S;                                   // [S] MMA slot read
@@ -530,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* stg = smem + L.stg + q * (a.Kin + kTok * d.sb_tok);
     // the scale factors of the first two units; each later unit's once the unit two before
     // it (same buffer) has been drained
-    for (int64_t u = u0; u < u0 + 2 && u < u1; ++u) write_scales<EPI>(d, stg, taddr, q, lane, u, (uint32_t)(u - u0) & 1);
+    for (int64_t u = u0; u < u0 + 2 && u < u1; ++u) write_scales<EPI, TOK>(d, stg, taddr, q, lane, u, (uint32_t)(u - u0) & 1);
     if (lane == 0)
       for (int64_t u = u0; u < u0 + 2 && u < u1; ++u) tc::mbar_arrive(&sready[(u - u0) & 1]);
     for (int64_t u = u0; u < u1; ++u) {
@@ -549,15 +558,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::tc_fence_after();
       // columns 8 t + j: token t's digit plane j
-      uint32_t r[2][32];
+      uint32_t r[kBRows / 32][32];
       tc::tmem_ld32(taddr + lane_base + buf * 64, r[0]);
-      tc::tmem_ld32(taddr + lane_base + buf * 64 + 32, r[1]);
+      if (kBRows > 32) tc::tmem_ld32(taddr + lane_base + buf * 64 + 32, r[kBRows / 32 - 1]);
       tc::tmem_ld_wait();
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&tempty[buf]);
       if (u + 2 < u1) {
-        write_scales<EPI>(d, stg, taddr, q, lane, u + 2, buf);
+        write_scales<EPI, TOK>(d, stg, taddr, q, lane, u + 2, buf);
         if (lane == 0) tc::mbar_arrive(&sready[buf]);
       }
       // the planes' partial sums, least significant first
@@ -643,18 +652,26 @@ size_t r256(size_t v) { return (v + 255) / 256 * 256; }
 constexpr int kSmemMax = 227 * 1024;
 
 // Ring slots: as many as fit, up to kMaxStages.
-int dt_stages(int Kin) {
-  const DtLayout L0 = dt_layout(0, Kin, dt_sb(Kin));
+int dt_stages(int Kin, int tok) {
+  const DtLayout L0 = dt_layout(0, Kin, dt_sb(Kin), tok);
   const int s = (kSmemMax - 1024 - L0.total) / (L0.slot + 16);
   return s < kMaxStages ? s : kMaxStages;
 }
 
-template <int EPI>
+// Slots per token tile.  A tile of 4 slots halves the B rows of a stage, which lets a fifth
+// ring slot (of 40 KB) fit beside the others; but an expert with more than 4 pairs in an
+// alignment block then streams its weights once per tile.  With at most 3 pairs per expert
+// on average (the decode regime) the deeper ring wins (GEMM1 of the 64-token decode layer:
+// 0.205 -> 0.190 ms); denser batches keep 8-slot tiles.
+int dt_tok(const GroupedGemm& g) { return g.P <= 3 * (int64_t)g.E ? 4 : 8; }
+
+template <int EPI, int TOK>
 cudaError_t launch_dt(const CUtensorMap& ma, const CUtensorMap& mb, const DtArgs& d, cudaStream_t stream) {
-  const int smem = dt_layout(d.stages, d.g.Kin, d.sb_tok).total + 1024;
-  cudaError_t err = cudaFuncSetAttribute(decode_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = dt_layout(d.stages, d.g.Kin, d.sb_tok, TOK).total + 1024;
+  cudaError_t err =
+      cudaFuncSetAttribute(decode_tc_kernel<EPI, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  decode_tc_kernel<EPI><<<(unsigned)moe_launch::sm_count_current(), kThreads, smem, stream>>>(ma, mb, d);
+  decode_tc_kernel<EPI, TOK><<<(unsigned)moe_launch::sm_count_current(), kThreads, smem, stream>>>(ma, mb, d);
   return cudaGetLastError();
 }
 
@@ -670,15 +687,17 @@ bool decode_tc_supported(const GroupedGemm& g1, const GroupedGemm& g2) {
     if (epi == EPI_SWIGLU ? (g.Nout % 64 != 0 || g.Nw != 2 * (int64_t)g.Nout)
                           : (g.Nout % 32 != 0 || g.Nw != (int64_t)g.Nout))
       return false;
-    if (g.bm % kTok != 0 || g.bm > 128) return false;
+    if (g.bm % 8 != 0 || g.bm > 128) return false;
     // TMA boxes of the weight rows: a 16-byte aligned base, rows of at least one box (128
     // bytes) and at least two boxes of rows, row coordinates below 2^31
     if (reinterpret_cast<uintptr_t>(g.w) % 16 != 0 || g.Kin < 256 || (int64_t)g.E * g.Nw < 2 * kBoxRowsA ||
         (int64_t)g.E * g.Nw >= (int64_t)1 << 31)
       return false;
-    return dt_stages(g.Kin) >= 2;
+    return dt_stages(g.Kin, 8) >= 2;
   };
-  return ok(g1, EPI_SWIGLU) && ok(g2, EPI_WEIGHTED_F32) && g2.Kin == g1.Nout && g1.P == g2.P;
+  // both GEMMs read the one unit list: the same token tiles
+  return ok(g1, EPI_SWIGLU) && ok(g2, EPI_WEIGHTED_F32) && g2.Kin == g1.Nout && g1.P == g2.P &&
+         dt_tok(g1) == dt_tok(g2);
 }
 
 size_t decode_tc_workspace_bytes(int64_t T_rows, int k, int K, int I) {
@@ -728,7 +747,10 @@ cudaError_t decode_tc_prep(const GroupedGemm& g1, const void* x, int64_t T_rows,
   int64_t blocks = (warps + kPrepThreads / 32 - 1) / (kPrepThreads / 32);
   const int64_t cap = 2 * (int64_t)sm_count_current();
   if (blocks > cap) blocks = cap;
-  dt_prep_kernel<<<(unsigned)(1 + blocks), kPrepThreads, 0, stream>>>(pa);
+  if (dt_tok(g1) == 4)
+    dt_prep_kernel<4><<<(unsigned)(1 + blocks), kPrepThreads, 0, stream>>>(pa);
+  else
+    dt_prep_kernel<8><<<(unsigned)(1 + blocks), kPrepThreads, 0, stream>>>(pa);
   return cudaGetLastError();
 }
 
@@ -740,7 +762,8 @@ cudaError_t decode_tc_gemm(const GroupedGemm& g, const DecodeTcBufs& b, cudaStre
   d.n_items = b.n_items;
   d.nsub = (g.Kin + 255) / 256;
   d.nwords = dt_nwords(g.Kin);
-  d.stages = dt_stages(g.Kin);
+  const int tok = dt_tok(g);
+  d.stages = dt_stages(g.Kin, tok);
   // weight rows of Kin / 2 bytes (boxes of 128 bytes x 64 rows) and digit-plane rows of the
   // activations, eight per token row (boxes of 128 bytes x 8 rows), both 128-byte swizzled
   const int64_t act_rows = g.act_per_pair ? g.P : g.P / g.k;
@@ -759,11 +782,12 @@ cudaError_t decode_tc_gemm(const GroupedGemm& g, const DecodeTcBufs& b, cudaStre
     d.hkq = dt_kq(g.Nout);
     d.hsb = dt_sb(g.Nout);
     d.n_rt = g.Nout / 64;
-    return launch_dt<EPI_SWIGLU>(ma, mb, d, stream);
+    return tok == 4 ? launch_dt<EPI_SWIGLU, 4>(ma, mb, d, stream) : launch_dt<EPI_SWIGLU, 8>(ma, mb, d, stream);
   }
   d.bsc = b.hs;
   d.n_rt = (g.Nout + 127) / 128;
-  return launch_dt<EPI_WEIGHTED_F32>(ma, mb, d, stream);
+  return tok == 4 ? launch_dt<EPI_WEIGHTED_F32, 4>(ma, mb, d, stream)
+                  : launch_dt<EPI_WEIGHTED_F32, 8>(ma, mb, d, stream);
 }
 
 }  // namespace moe_launch

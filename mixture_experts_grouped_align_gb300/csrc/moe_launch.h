@@ -101,7 +101,7 @@ struct DecodeTcBufs {
   uint8_t* xs;       // [T_rows, sb(K)] x scales
   uint8_t* hq;       // [P, 8, kq(I)] h planes
   uint8_t* hs;       // [P, sb(I)] h scales
-  int4* items;       // [P] (alignment block, 8-slot tile, slots to its last pair + 1, expert)
+  int4* items;       // [P] (alignment block, 4- or 8-slot tile, slots to its last pair + 1, expert)
   int32_t* n_items;
 };
 // Whether GEMM1 (SwiGLU, MXFP4 weights) and GEMM2 (routing-weighted) of a layer fit the kernel.
