@@ -42,7 +42,7 @@ L2_BYTES = 129 * 1024 * 1024
 # valid while the kernel source hashes the same; otherwise reported as null.
 TRAFFIC = {
     "decode_tc.cu:gemm1@decode_mxfp4": {
-        "src": "00223a33b36f7063", "bytes": 998126848 + 5301504},
+        "src": "dfafccfa25145f06", "bytes": 1024535552 + 5261568},
     # both launches of the call: the main pass and the (empty) exact-scale pass
     "prefill_ts.cu:gemm1@prefill_mxfp4": {
         "src": "40b9e45121f051d6", "bytes": 2599493120 + 1443217152 + 68608},
