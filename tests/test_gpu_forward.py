@@ -330,8 +330,9 @@ def test_relu2_graph_replay_equals_eager(moe):
 @pytest.mark.parametrize("block_m", [8, 32, 64, 256])
 def test_mxfp4_small_batch_across_block_sizes(moe, block_m):
     """Up to 256 rows the MXFP4 SwiGLU layer runs the block-scaled kernels for alignment blocks
-    of at most 128 slots (8-slot units: one or several per block) and the weight-streaming
-    kernels above; each matches the oracle, and padded and unpadded rows stay bit-identical."""
+    of at most 128 slots (4- or 8-slot token tiles: one or several per block) and the
+    weight-streaming kernels above; each matches the oracle, and padded and unpadded rows
+    stay bit-identical."""
     from mixture_experts_grouped_align_gb300.runner import DeviceLayer
     w = synth.Workload("block_sizes", T=61, K=512, I=384, E=8, k=3, quant="mxfp4", seed=31,
                        scale_exp=(-5, -1), bias=True)
@@ -347,3 +348,31 @@ def test_mxfp4_small_batch_across_block_sizes(moe, block_m):
     assert rows == obucket.bucket(w.T)
     assert torch.equal(y_pad.view(torch.int16), y_raw.view(torch.int16))
     assert_close_bf16(bf16_to_np(y_raw), oracle_y(lay, w, w.T), what=f"block_m={block_m}")
+
+
+@pytest.mark.parametrize("T,E,k,block_m", [(40, 32, 2, 16), (40, 8, 4, 32)])  # 4- / 8-slot tiles
+def test_decode_digit_planes_carry_large_and_wide_range_activations(moe, T, E, k, block_m):
+    """The block-scaled decode path carries x as E2M1 digit planes under one scale per 32
+    elements, so it takes activations far above the f16 range (here up to ~2^19, the
+    weights' scales lowered by 2^-17 to match), blocks whose elements lie 2^10 and 2^30
+    below the block's first one, an all-zero block and a block of magnitude ~2^-123 (below
+    the planes' scale floor): no range error, and the oracle's result within the bar."""
+    from mixture_experts_grouped_align_gb300.runner import DeviceLayer
+    w = synth.Workload("digit_planes", T=T, K=512, I=256, E=E, k=k, quant="mxfp4", seed=41,
+                       scale_exp=(-6, -2), bias=True)
+    lay = synth.make_layer(w)
+    rng = np.random.default_rng(41)
+    xf = rng.standard_normal((T, w.K)).astype(np.float32) * np.float32(2.0 ** 17)
+    blocks = xf.reshape(T, w.K // 32, 32)
+    blocks[:, 1, 1:] *= np.float32(2.0 ** -10)
+    blocks[:, 2, 1:] *= np.float32(2.0 ** -30)
+    blocks[:, 3, :] = 0.0
+    blocks[:, 4, :] *= np.float32(2.0 ** -140)
+    lay["x"] = synth.to_bf16_bits(xf)
+    assert np.abs(ofmt.bf16_decode(lay["x"])).max() > 65504
+    lay["w1_scale"] = (lay["w1_scale"].astype(np.int32) - 17).astype(np.uint8)
+    L = DeviceLayer(w.quant, w.E, w.K, w.I, w.k, dev(lay["w1"]), dev(lay["w1_scale"]), dev(lay["b1"]),
+                    dev(lay["w2"]), dev(lay["w2_scale"]), dev(lay["b2"]), max_rows=T, pad=False,
+                    block_m=block_m)
+    y, _ = run(moe, L, lay, T)
+    assert_close_bf16(bf16_to_np(y), oracle_y(lay, w, T), what=f"digit planes E={E} k={k}")
